@@ -1,0 +1,148 @@
+/*
+ * fa_decode.h -- C ABI of the GB300 (sm_103a) split-K paged decode attention
+ * library (libfa_decode.so).
+ *
+ * The operation (FlashAttention-4-style decode forward, as documented by the
+ * Modular MAX pages "FA4Config" (struct), "fa4_splitk_combine_write" and
+ * "fa4_lse_combine_write"):
+ *
+ *   For every sequence b, query token t < num_q and query head h, with kv head
+ *   k = h / (num_q_heads / num_kv_heads) (GQA head fusion; FA4Config, field
+ *   `group`, method BM_eff) and visible keys j < L_b - num_q + t + 1 (the
+ *   num_q new tokens are the last positions of the cache):
+ *     s_j = scale * q[b,t,h,:] . K_j[:qk_depth]
+ *     out[b,t,h,:] = softmax_j(s_j) V_j        (bf16, round-to-nearest-even)
+ *     lse[b,t,h]   = ln sum_j exp(s_j)          (fp32; -inf when no key is visible)
+ *   K_j / V_j are rows of a block-indirected paged cache (FA4Config, method
+ *   v_row_major): page page_table[b][j / page_size], row j % page_size.
+ *
+ *   The key axis of each (sequence, kv head) is split over `splitk` CTAs of
+ *   one thread-block cluster (FA4Config, field splitk_partitions and method
+ *   with_splitk). Each CTA runs an online softmax in exp2 form over its key
+ *   tiles and keeps (max, sum) in raw score units; the partial results are
+ *   merged by the log-sum-exp combine of the fa4_splitk_combine_write page
+ *   (Gmax = max_p max_p, Gsum = sum_p sum_p exp2((max_p - Gmax) c),
+ *   w_p = sum_p exp2((max_p - Gmax) c) / Gsum, O = sum_p w_p O_p with
+ *   c = scale * log2 e), done as a reduce-scatter over distributed shared
+ *   memory in which every CTA owns one band of output columns, casts it to
+ *   bf16 and stores it with TMA.
+ *
+ * Conventions for every function:
+ *   - Return 0 (FA_OK) on success or a negative FA_ERR_* code; the message of
+ *     the last failure on the calling host thread is fa_decode_last_error().
+ *   - Device pointers are plain CUDA device addresses owned by the caller.
+ *     The library never frees or retains them past the call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     fa_decode_run only enqueues work: it does not synchronise, allocate
+ *     device memory or copy to the host.
+ *   - A handle may be used from one host thread at a time.
+ */
+#ifndef FA_DECODE_H
+#define FA_DECODE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_OK 0
+#define FA_ERR_INVALID_ARG (-1)  /* null / misaligned pointer, bad size or shape */
+#define FA_ERR_UNSUPPORTED (-2)  /* valid but not built: depth pair, row count, splitk, device */
+#define FA_ERR_CUDA (-3)         /* a CUDA runtime or driver call failed */
+#define FA_ERR_DEVICE (-4)       /* the device reported a fault through the status word */
+
+/* Bits of the device status word (fa_decode_check). */
+#define FA_STATUS_TIMEOUT 1u     /* a bounded device wait gave up; results are invalid */
+#define FA_STATUS_BAD_PAGE 2u    /* a page id was outside [0, num_pages) or a length exceeded
+                                    max_pages_per_seq * page_size; those rows read zeros */
+
+typedef struct fa_decode* fa_decode_t;
+
+/*
+ * Create a decode plan (FA4Config constructor and with_num_q / with_splitk
+ * reconstructors: fixed geometry for one shape family).
+ *
+ *   out          receives the handle (caller frees it with fa_decode_destroy)
+ *   num_q_heads  Hq >= 1
+ *   num_kv_heads Hkv >= 1, Hq % Hkv == 0; group g = Hq / Hkv
+ *   qk_depth     Dk: Q and K row width (MLA: nope + rope, e.g. 576)
+ *   nope_depth   -1 (no rope part) or 1..qk_depth; layout information only
+ *   ov_depth     Dv: V / output row width
+ *   page_size    PS: rows per cache page, a multiple of 8
+ *   num_q        T: query tokens per sequence (T > 1 masks causally at the tail)
+ *   splitk       P: CTAs per (sequence, kv head): 1, 2, 4, 8 or 16, with
+ *                ov_depth / P a multiple of 8; 0 picks P per sequence from its
+ *                length at run time (1 if L <= 1024, 2 if L <= 4096, else 4)
+ *
+ * Built shapes: (Dk, Dv) in {(64,64), (128,128), (576,512)}; T * g <= 16
+ * rows per CTA, or T == 1 with g a multiple of 16. Other shapes return
+ * FA_ERR_UNSUPPORTED. Needs a current CUDA device of compute capability 10.3
+ * (GB300). Allocates one small device status word.
+ */
+int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk_depth,
+                     int nope_depth, int ov_depth, int page_size, int num_q, int splitk);
+
+/*
+ * Enqueue one decode forward on `stream`.
+ *
+ *   q           bf16 [batch][num_q][num_q_heads][qk_depth], contiguous, 16-byte aligned
+ *   k_pages     bf16 [num_pages][num_kv_heads][page_size][qk_depth], 16-byte aligned
+ *   v_pages     bf16 [num_pages][num_kv_heads][page_size][ov_depth], 16-byte aligned;
+ *               NULL or equal to k_pages selects the MLA latent layout, in which V
+ *               is the first ov_depth columns of each K row (ov_depth <= qk_depth)
+ *   page_table  int32 [batch][max_pages_per_seq] physical page ids; entries past
+ *               ceil(L_b / page_size) are never read
+ *   seq_lens    int32 [batch] L_b, the KV length including the num_q new tokens
+ *   scale       softmax scale, finite and >= 0
+ *   out         bf16 [batch][num_q][num_q_heads][ov_depth], 16-byte aligned
+ *   lse         fp32 [batch][num_q][num_q_heads] or NULL
+ *   stream      cudaStream_t as void*
+ *   batch       B >= 0 (0 enqueues nothing)
+ *   max_pages_per_seq  row stride of page_table, >= 1
+ *   num_pages   pages in k_pages / v_pages, >= 1 (bounds of the TMA views)
+ *
+ * The last three arguments are not in the pages' kernel signature: the grid,
+ * the page-table stride and the extent of the cache views cannot be derived
+ * from the others. Invalid page ids and over-long sequences are detected on the
+ * device, read as zeros and reported by fa_decode_check; they never fault.
+ */
+int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void* v_pages,
+                  const int32_t* page_table, const int32_t* seq_lens, float scale,
+                  void* out, float* lse, void* stream,
+                  int batch, int max_pages_per_seq, int num_pages);
+
+/*
+ * Wait for `stream`, then read and clear the handle's device status word.
+ * *status_out (may be NULL) receives the FA_STATUS_* bits raised by runs since
+ * the last check. Returns FA_ERR_DEVICE when any bit was set, else FA_OK.
+ */
+int fa_decode_check(fa_decode_t h, void* stream, uint32_t* status_out);
+
+/*
+ * Test hooks. flags: FA_DEBUG_SKIP_LOADS makes the load warp issue no copies,
+ * so the first bounded wait of every CTA runs out; wait_limit_ns bounds every
+ * device wait (0 restores the default of one second). Normal runs never need
+ * this call.
+ */
+#define FA_DEBUG_SKIP_LOADS 1u
+int fa_decode_set_debug(fa_decode_t h, uint32_t flags, int64_t wait_limit_ns);
+
+/*
+ * Describe the plan: kernel path, CTAs per cluster, keys per tile, pipeline
+ * stages and dynamic shared memory, as one line of text in buf (size bytes).
+ * FA4Config, method description.
+ */
+int fa_decode_describe(fa_decode_t h, char* buf, int size);
+
+/* Destroy a handle (NULL is a no-op). Frees the status word. */
+int fa_decode_destroy(fa_decode_t h);
+
+/* Message of the last failure on this host thread ("" if none). */
+const char* fa_decode_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_DECODE_H */

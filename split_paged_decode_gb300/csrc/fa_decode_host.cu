@@ -1,0 +1,444 @@
+// fa_decode_host.cu -- the C ABI of libfa_decode.so: argument validation, the
+// launch plan, TMA tensor-map encoding and the cluster launches.
+//
+// The plan mirrors the FA4Config page (Modular MAX docs): a handle fixes the
+// geometry of one shape family the way the FA4Config constructor and its
+// with_num_q / with_splitk reconstructors do, `supported()` becomes the
+// FA_ERR_UNSUPPORTED checks below, cluster_size() is the split-K partition
+// count, and description() is fa_decode_describe().
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "fa_decode_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(FA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool is_aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Cache of one encoded tensor map, keyed by what it was encoded from.
+struct MapCache {
+    bool valid = false;
+    const void* ptr = nullptr;
+    uint64_t key0 = 0, key1 = 0, key2 = 0;
+    CUtensorMap map;
+};
+
+// Tensor map over the K (or V) rows of the paged cache: [num_pages*Hkv*PS][depth]
+// bf16, boxes of 64 columns x box_rows rows, 128-byte swizzle, zero fill.
+int encode_cache_map(MapCache& c, const void* base, int depth, int64_t rows, int box_rows)
+{
+    if (c.valid && c.ptr == base && c.key0 == (uint64_t)depth && c.key1 == (uint64_t)rows &&
+        c.key2 == (uint64_t)box_rows)
+        return FA_OK;
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {(cuuint64_t)depth, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)depth * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&c.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        c.valid = false;
+        return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (cache view, depth %d, rows %lld) failed: %d", depth,
+                    (long long)rows, (int)r);
+    }
+    c.valid = true;
+    c.ptr = base;
+    c.key0 = depth;
+    c.key1 = rows;
+    c.key2 = box_rows;
+    return FA_OK;
+}
+
+// Tensor map over the output: 3-D {Dv, Hq, B*T} bf16, box {chunk, heads, tokens}.
+int encode_out_map(MapCache& c, void* out, int dv, int hq, int64_t bt, int chunk, int heads, int tokens)
+{
+    uint64_t k1 = ((uint64_t)hq << 32) | (uint64_t)dv;
+    uint64_t k2 = ((uint64_t)chunk << 40) | ((uint64_t)heads << 20) | (uint64_t)tokens;
+    if (c.valid && c.ptr == out && c.key0 == (uint64_t)bt && c.key1 == k1 && c.key2 == k2) return FA_OK;
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {(cuuint64_t)dv, (cuuint64_t)hq, (cuuint64_t)bt};
+    cuuint64_t strides[2] = {(cuuint64_t)dv * 2, (cuuint64_t)hq * dv * 2};
+    cuuint32_t box[3] = {(cuuint32_t)chunk, (cuuint32_t)heads, (cuuint32_t)tokens};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(&c.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        c.valid = false;
+        return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (output view) failed: %d", (int)r);
+    }
+    c.valid = true;
+    c.ptr = out;
+    c.key0 = bt;
+    c.key1 = k1;
+    c.key2 = k2;
+    return FA_OK;
+}
+
+}  // namespace
+
+struct fa_decode {
+    int hq, hkv, group, dk, nope, dv, page_size, num_q, splitk;
+    int rows, row_blocks, heads_per_cta, tokens_per_cta, rows_capacity;
+    int device;
+    fad::KernelGeometry geo;         // separate V cache
+    fad::KernelGeometry geo_latent;  // V = prefix of the K row
+    bool has_latent;
+    unsigned int* d_status;
+    uint32_t debug_flags;
+    uint64_t wait_limit_ns;
+    MapCache k_map, v_map, out_map[3];
+};
+
+namespace {
+
+int split_list(const fa_decode* h, int* list)
+{
+    if (h->splitk > 0) {
+        list[0] = h->splitk;
+        return 1;
+    }
+    list[0] = 1;
+    list[1] = 2;
+    list[2] = 4;
+    return 3;
+}
+
+int prepare_kernel(const fa_decode* h, const fad::KernelGeometry& g)
+{
+    cudaError_t e = cudaFuncSetAttribute(g.func, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+    int splits[3];
+    int n = split_list(h, splits);
+    for (int i = 0; i < n; ++i) {
+        const int P = splits[i];
+        if (P <= 1) continue;
+        if (P > 8) {
+            e = cudaFuncSetAttribute(g.func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster size)");
+        }
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3(P, 1, 1);
+        cfg.blockDim = dim3(g.threads, 1, 1);
+        cfg.dynamicSmemBytes = g.smem_bytes;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = P;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, g.func, &cfg);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+        if (clusters < 1)
+            return fail(FA_ERR_UNSUPPORTED, "a cluster of %d CTAs with %d bytes of shared memory each cannot be "
+                                            "scheduled on this device", P, g.smem_bytes);
+    }
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_decode_last_error(void) { return g_last_error.c_str(); }
+
+int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth,
+                     int ov_depth, int page_size, int num_q, int splitk)
+{
+    g_last_error.clear();
+    if (!out) return fail(FA_ERR_INVALID_ARG, "out handle pointer is NULL");
+    *out = nullptr;
+    if (num_q_heads < 1 || num_kv_heads < 1)
+        return fail(FA_ERR_INVALID_ARG, "head counts must be >= 1 (got %d q, %d kv)", num_q_heads, num_kv_heads);
+    if (num_q_heads % num_kv_heads)
+        return fail(FA_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                    num_kv_heads);
+    if (qk_depth < 1 || ov_depth < 1) return fail(FA_ERR_INVALID_ARG, "depths must be >= 1");
+    if (!(nope_depth == -1 || (nope_depth >= 1 && nope_depth <= qk_depth)))
+        return fail(FA_ERR_INVALID_ARG, "nope_depth must be -1 or in [1, qk_depth] (got %d)", nope_depth);
+    if (page_size < 1) return fail(FA_ERR_INVALID_ARG, "page_size must be >= 1");
+    if (num_q < 1) return fail(FA_ERR_INVALID_ARG, "num_q must be >= 1");
+    if (!(splitk == 0 || splitk == 1 || splitk == 2 || splitk == 4 || splitk == 8 || splitk == 16))
+        return fail(FA_ERR_INVALID_ARG, "splitk must be 0 (per sequence), 1, 2, 4, 8 or 16 (got %d)", splitk);
+
+    fa_decode tmp;
+    std::memset(&tmp, 0, sizeof tmp);
+    tmp.hq = num_q_heads;
+    tmp.hkv = num_kv_heads;
+    tmp.group = num_q_heads / num_kv_heads;
+    tmp.dk = qk_depth;
+    tmp.nope = nope_depth < 0 ? qk_depth : nope_depth;
+    tmp.dv = ov_depth;
+    tmp.page_size = page_size;
+    tmp.num_q = num_q;
+    tmp.splitk = splitk;
+    tmp.wait_limit_ns = fad::kDefaultWaitLimitNs;
+
+    // Rows of one CTA: the T*g fused GQA rows, or 16-head blocks for wide groups.
+    const int R = num_q * tmp.group;
+    if (R <= 16) {
+        tmp.rows = R;
+        tmp.rows_capacity = R <= 4 ? 4 : (R <= 8 ? 8 : 16);
+        tmp.row_blocks = 1;
+        tmp.heads_per_cta = tmp.group;
+        tmp.tokens_per_cta = num_q;
+    } else if (num_q == 1 && tmp.group % 16 == 0) {
+        tmp.rows = 16;
+        tmp.rows_capacity = 16;
+        tmp.row_blocks = tmp.group / 16;
+        tmp.heads_per_cta = 16;
+        tmp.tokens_per_cta = 1;
+    } else {
+        return fail(FA_ERR_UNSUPPORTED, "num_q * group = %d rows per kv head: built for <= 16, or num_q == 1 "
+                                        "with group a multiple of 16", R);
+    }
+    if (!fad::simt_geometry(qk_depth, ov_depth, false, tmp.rows_capacity, &tmp.geo))
+        return fail(FA_ERR_UNSUPPORTED, "depth pair (qk %d, ov %d) with %d rows per CTA is not built "
+                                        "(built: 64/64, 128/128, 576/512)", qk_depth, ov_depth, tmp.rows_capacity);
+    tmp.has_latent = fad::simt_geometry(qk_depth, ov_depth, true, tmp.rows_capacity, &tmp.geo_latent);
+    const int bn = tmp.geo.keys_per_tile;
+    if (page_size % 8)
+        return fail(FA_ERR_UNSUPPORTED, "page_size %d is not a multiple of 8", page_size);
+    if (!(page_size % bn == 0 || bn % page_size == 0))
+        return fail(FA_ERR_UNSUPPORTED, "page_size %d and the %d-key tile must divide one another", page_size, bn);
+    int splits[3];
+    const int ns = split_list(&tmp, splits);
+    for (int i = 0; i < ns; ++i) {
+        const int bw = ov_depth / splits[i];
+        if (ov_depth % splits[i] || bw % 8)
+            return fail(FA_ERR_UNSUPPORTED, "ov_depth %d split %d ways gives bands that are not a multiple of 8 "
+                                            "columns", ov_depth, splits[i]);
+    }
+
+    // Device: GB300 only (compute capability 10.3).
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+        return fail(FA_ERR_UNSUPPORTED, "device %d has compute capability %d.%d; this library is built for "
+                                        "sm_103a (GB300)", dev, major, minor);
+    tmp.device = dev;
+    int rc = prepare_kernel(&tmp, tmp.geo);
+    if (rc) return rc;
+    if (tmp.has_latent && (rc = prepare_kernel(&tmp, tmp.geo_latent))) return rc;
+
+    e = cudaMalloc(&tmp.d_status, 256);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status word)");
+    e = cudaMemset(tmp.d_status, 0, 256);
+    if (e != cudaSuccess) {
+        cudaFree(tmp.d_status);
+        return cuda_fail(e, "cudaMemset(status word)");
+    }
+    fa_decode* h = new (std::nothrow) fa_decode(tmp);
+    if (!h) {
+        cudaFree(tmp.d_status);
+        return fail(FA_ERR_CUDA, "out of host memory");
+    }
+    *out = h;
+    return FA_OK;
+}
+
+int fa_decode_destroy(fa_decode_t h)
+{
+    if (!h) return FA_OK;
+    cudaError_t e = cudaFree(h->d_status);
+    delete h;
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFree(status word)");
+    return FA_OK;
+}
+
+int fa_decode_set_debug(fa_decode_t h, uint32_t flags, int64_t wait_limit_ns)
+{
+    if (!h) return fail(FA_ERR_INVALID_ARG, "handle is NULL");
+    if (wait_limit_ns < 0) return fail(FA_ERR_INVALID_ARG, "wait_limit_ns must be >= 0");
+    h->debug_flags = flags;
+    h->wait_limit_ns = wait_limit_ns ? (uint64_t)wait_limit_ns : fad::kDefaultWaitLimitNs;
+    return FA_OK;
+}
+
+int fa_decode_check(fa_decode_t h, void* stream, uint32_t* status_out)
+{
+    if (!h) return fail(FA_ERR_INVALID_ARG, "handle is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned int st = 0;
+    e = cudaMemcpy(&st, h->d_status, sizeof st, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+    e = cudaMemset(h->d_status, 0, sizeof st);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    if (status_out) *status_out = st;
+    if (st) {
+        return fail(FA_ERR_DEVICE, "device status 0x%x:%s%s", st, (st & FA_STATUS_TIMEOUT) ? " wait timed out" : "",
+                    (st & FA_STATUS_BAD_PAGE) ? " page id or length out of range" : "");
+    }
+    return FA_OK;
+}
+
+int fa_decode_describe(fa_decode_t h, char* buf, int size)
+{
+    if (!h || !buf || size < 1) return fail(FA_ERR_INVALID_ARG, "handle or buffer is NULL");
+    snprintf(buf, (size_t)size,
+             "path=simt kernel=%s latent_kernel=%s splitk=%d%s threads=%d keys_per_tile=%d stages=%d "
+             "rows=%d rows_capacity=%d row_blocks=%d smem=%d",
+             h->geo.name, h->has_latent ? h->geo_latent.name : "none", h->splitk,
+             h->splitk == 0 ? "(per sequence: 1/2/4)" : "", h->geo.threads, h->geo.keys_per_tile, h->geo.stages,
+             h->rows, h->rows_capacity, h->row_blocks, h->geo.smem_bytes);
+    return FA_OK;
+}
+
+int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void* v_pages,
+                  const int32_t* page_table, const int32_t* seq_lens, float scale, void* out, float* lse,
+                  void* stream, int batch, int max_pages_per_seq, int num_pages)
+{
+    if (!h) return fail(FA_ERR_INVALID_ARG, "handle is NULL");
+    if (batch < 0) return fail(FA_ERR_INVALID_ARG, "batch must be >= 0 (got %d)", batch);
+    if (batch == 0) return FA_OK;
+    if (!q || !k_pages || !page_table || !seq_lens || !out)
+        return fail(FA_ERR_INVALID_ARG, "q, k_pages, page_table, seq_lens and out must not be NULL");
+    if (!is_aligned(q, 16) || !is_aligned(k_pages, 16) || !is_aligned(out, 16) ||
+        (v_pages && !is_aligned(v_pages, 16)))
+        return fail(FA_ERR_INVALID_ARG, "q, k_pages, v_pages and out must be 16-byte aligned");
+    if (!is_aligned(page_table, 4) || !is_aligned(seq_lens, 4) || (lse && !is_aligned(lse, 4)))
+        return fail(FA_ERR_INVALID_ARG, "page_table, seq_lens and lse must be 4-byte aligned");
+    if (max_pages_per_seq < 1 || num_pages < 1)
+        return fail(FA_ERR_INVALID_ARG, "max_pages_per_seq and num_pages must be >= 1");
+    if (!(scale >= 0.f) || scale == INFINITY) return fail(FA_ERR_INVALID_ARG, "scale must be finite and >= 0");
+    if (batch > 65535) return fail(FA_ERR_UNSUPPORTED, "batch %d exceeds 65535 sequences per call", batch);
+    const int64_t cache_rows = (int64_t)num_pages * h->hkv * h->page_size;
+    if (cache_rows + 256 > INT32_MAX)
+        return fail(FA_ERR_UNSUPPORTED, "cache of %lld rows exceeds the 2^31 TMA row coordinate range",
+                    (long long)cache_rows);
+
+    const bool latent = (v_pages == nullptr || v_pages == k_pages);
+    if (latent && h->dv > h->dk)
+        return fail(FA_ERR_INVALID_ARG, "latent layout (v_pages NULL or == k_pages) needs ov_depth <= qk_depth");
+    const fad::KernelGeometry& g = (latent && h->has_latent) ? h->geo_latent : h->geo;
+    const int bn = g.keys_per_tile;
+    const int box_rows = h->page_size < bn ? h->page_size : bn;
+
+    int rc = encode_cache_map(h->k_map, k_pages, h->dk, cache_rows, box_rows);
+    if (rc) return rc;
+    if (latent && g.func == h->geo.func) {
+        // V = K row prefix through the separate-V kernel (e.g. qk == ov): same rows, V width.
+        rc = encode_cache_map(h->v_map, k_pages, h->dk, cache_rows, box_rows);
+    } else if (!latent) {
+        rc = encode_cache_map(h->v_map, v_pages, h->dv, cache_rows, box_rows);
+    }
+    if (rc) return rc;
+
+    fad::DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.tm_k = h->k_map.map;
+    if (!(latent && g.func != h->geo.func)) p.tm_v = h->v_map.map;
+    p.q = static_cast<const uint16_t*>(q);
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.lse = lse;
+    p.status = h->d_status;
+    p.batch = batch;
+    p.num_q = h->num_q;
+    p.num_q_heads = h->hq;
+    p.num_kv_heads = h->hkv;
+    p.group = h->group;
+    p.qk_depth = h->dk;
+    p.ov_depth = h->dv;
+    p.page_size = h->page_size;
+    p.max_pages = max_pages_per_seq;
+    p.num_pages = num_pages;
+    p.rows = h->rows;
+    p.row_blocks = h->row_blocks;
+    p.heads_per_cta = h->heads_per_cta;
+    p.tokens_per_cta = h->tokens_per_cta;
+    p.box_rows = box_rows;
+    p.oob_row = (int32_t)cache_rows;
+    p.scale = scale;
+    p.scale_log2e = (float)((double)scale * 1.4426950408889634);
+    p.debug_flags = h->debug_flags;
+    p.wait_limit_ns = h->wait_limit_ns;
+    p.auto_split = h->splitk == 0 ? 1 : 0;
+
+    int splits[3];
+    const int ns = split_list(h, splits);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int i = 0; i < ns; ++i) {
+        const int P = splits[i];
+        p.splitk = P;
+        p.band_cols = h->dv / P;
+        p.out_chunk_cols = p.band_cols < 256 ? p.band_cols : 256;
+        rc = encode_out_map(h->out_map[i], out, h->dv, h->hq, (int64_t)batch * h->num_q, p.out_chunk_cols,
+                            h->heads_per_cta, h->tokens_per_cta);
+        if (rc) return rc;
+        p.tm_out = h->out_map[i].map;
+
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3(P, h->hkv * h->row_blocks, batch);
+        cfg.blockDim = dim3(g.threads, 1, 1);
+        cfg.dynamicSmemBytes = g.smem_bytes;
+        cfg.stream = s;
+        if (P > 1) {
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = P;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+        }
+        void* args[1] = {&p};
+        cudaError_t e = cudaLaunchKernelExC(&cfg, g.func, args);
+        if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    }
+    return FA_OK;
+}
+
+}  // extern "C"

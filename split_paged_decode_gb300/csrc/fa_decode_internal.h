@@ -1,0 +1,67 @@
+// fa_decode_internal.h -- types shared by the host planner and the kernels of
+// libfa_decode.so (not installed; the public interface is include/fa_decode.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fa_decode.h"
+
+namespace fad {
+
+constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // one second
+constexpr int kMaxSplit = 16;
+
+// Per-sequence split rule for splitk == 0: short sequences keep one CTA per
+// (sequence, kv head), longer ones spread over 2 or 4.
+__host__ __device__ inline int auto_split_for_len(int len)
+{
+    return len <= 1024 ? 1 : (len <= 4096 ? 2 : 4);
+}
+
+// Everything a decode kernel needs, passed by value as a __grid_constant__
+// parameter block (the tensor maps must live in parameter, constant or global
+// memory for TMA to read them).
+struct DecodeParams {
+    CUtensorMap tm_k;    // K rows: [num_pages*Hkv*PS][Dk] bf16, box {64, box_rows}, 128B swizzle
+    CUtensorMap tm_v;    // V rows: [num_pages*Hkv*PS][Dv] (unused for the latent layout)
+    CUtensorMap tm_out;  // out: 3-D {Dv, Hq, B*T} bf16, box {band_cols, heads_per_cta, tokens_per_cta}
+    const uint16_t* q;   // bf16 bits [B][T][Hq][Dk]
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    float* lse;
+    unsigned int* status;
+    int batch, num_q, num_q_heads, num_kv_heads, group;
+    int qk_depth, ov_depth, page_size, max_pages, num_pages;
+    int rows;            // real query rows per CTA (T*g, or heads_per_cta when row-blocked)
+    int row_blocks;      // CTAs along grid y per kv head
+    int heads_per_cta;   // heads covered by one CTA (g, or the row-block size)
+    int tokens_per_cta;  // tokens covered by one CTA (T, or 1 when row-blocked)
+    int splitk;          // cluster size P of this launch
+    int auto_split;      // 1: a cluster works on sequence b only if auto_split_for_len(L_b) == P
+    int box_rows;        // key rows per K/V TMA box: min(page_size, keys per tile)
+    int band_cols;       // output columns owned by one cluster rank: Dv / P
+    int out_chunk_cols;  // columns per output TMA store box: min(band_cols, 256)
+    int32_t oob_row;     // a row coordinate past the end of the cache views (zero fill)
+    float scale, scale_log2e;
+    uint32_t debug_flags;
+    uint64_t wait_limit_ns;
+};
+
+// Geometry of one compiled kernel variant, for planning and validation.
+struct KernelGeometry {
+    const void* func;    // the __global__ function
+    int threads;
+    int keys_per_tile;   // BN
+    int stages;
+    int rows_capacity;   // RB: query rows one CTA holds
+    int smem_bytes;
+    const char* name;
+};
+
+// Kernel variants of the SIMT (warp-level FMA) path. Returns false when no
+// variant exists for (qk, ov, latent, rows_capacity).
+bool simt_geometry(int qk_depth, int ov_depth, bool latent, int rows_capacity, KernelGeometry* g);
+
+}  // namespace fad

@@ -1,0 +1,416 @@
+// kernel_simt.cu -- the warp-level FMA decode kernel (sm_103a).
+//
+// One CTA = one cluster rank p of one (sequence, kv head[, row block]).
+// Warp roles:
+//   warps 0..3  compute: S = Q K^T over a tile of BN keys, online softmax in
+//               exp2 form with the running (max, sum) in raw score units,
+//               correction of O when the max moves, O += P V;
+//   warp 4      load: walks the page table and issues TMA tile loads of K and
+//               V (128-byte swizzled, one box per 64 columns and per page
+//               segment) into a STAGES-deep shared-memory ring guarded by
+//               full / empty mbarriers.
+// After the key loop the CTA stages its normalised partial O and (max, sum),
+// and the cluster merges them (splitk_combine.cuh).
+//
+// Geometry follows the FA4Config page (Modular MAX docs): GQA rows of one kv
+// head fused into one tile (field group, method BM_eff), paged K/V addressed
+// as block_idx * stride rows (method v_row_major), the split-K cluster
+// (field splitk_partitions, methods cluster_size and with_splitk), and for
+// the latent layout K_nope and V sharing one shared-memory stage (field
+// use_shared_kv, method shared_kv_cols).
+#include "fa_decode_internal.h"
+#include "splitk_combine.cuh"
+
+namespace fad {
+
+template <int DK, int DV, int BN, int STAGES, int RB, bool LATENT>
+struct SimtCfg {
+    static constexpr int NCW = 4;                   // compute warps
+    static constexpr int NCT = NCW * 32;            // compute threads
+    static constexpr int THREADS = NCT + 32;        // + one load warp
+    static constexpr int KBOX = DK / 64;            // 64-column TMA boxes per K row
+    static constexpr int VBOX = DV / 64;
+    static constexpr int K_BYTES = KBOX * BN * 128;
+    static constexpr int V_BYTES = LATENT ? 0 : VBOX * BN * 128;
+    static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
+    static constexpr int OFF_Q = STAGES * STAGE_BYTES;            // float [RB][DK]
+    static constexpr int OFF_S = OFF_Q + RB * DK * 4;             // float [RB][BN]
+    static constexpr int OFF_ALPHA = OFF_S + RB * BN * 4;         // float [RB]
+    static constexpr int OFF_MAXSUM = OFF_ALPHA + ((RB * 4 + 15) / 16) * 16;  // float2 [RB]
+    static constexpr int OFF_STAGE = OFF_MAXSUM + RB * 8;         // float [RB][DV]
+    static constexpr int OFF_OUT = OFF_STAGE + RB * DV * 4;       // bf16 [RB][DV]
+    static constexpr int OFF_BAR = OFF_OUT + RB * DV * 2;         // full[S], empty[S], publish
+    static constexpr int OFF_FLAG = OFF_BAR + (2 * STAGES + 1) * 8;  // abort flag, consumed count
+    static constexpr int SMEM_BYTES = OFF_FLAG + 16 + 1024;       // + alignment slack
+
+    // QK^T mapping: thread -> (key kk = t % BN, row group rg = t / BN)
+    static constexpr int QK_GROUPS = NCT / BN;
+    static constexpr int QK_ROWS = (RB + QK_GROUPS - 1) / QK_GROUPS;
+    // PV mapping: thread -> (4-column chunks, row lane)
+    static constexpr int NCH = DV / 4;
+    static constexpr int PV_ROW_LANES = NCH >= NCT ? 1 : NCT / NCH;
+    static constexpr int PV_CHUNKS = NCH >= NCT ? NCH / NCT : 1;
+    static constexpr int PV_ROWS = (RB + PV_ROW_LANES - 1) / PV_ROW_LANES;
+    // softmax mapping: warp w owns rows w, w + NCW, ...
+    static constexpr int SM_ROWS = (RB + NCW - 1) / NCW;
+
+    static_assert(DK % 64 == 0 && DV % 64 == 0, "depths are whole 64-column boxes");
+    static_assert(NCT % BN == 0 && BN % 32 == 0, "tile of keys must divide the compute threads");
+    static_assert(NCH % NCT == 0 || NCT % NCH == 0, "column chunks must tile the threads");
+    static_assert(!LATENT || DV <= DK, "latent V is a prefix of the K row");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
+};
+
+// Byte offset of element (row, col) inside a K or V tile held as 64-column,
+// 128-byte-swizzled TMA boxes: box-major, then key row, 16-byte unit XOR row.
+__device__ __forceinline__ uint32_t swz_offset(int row, int col, int bn)
+{
+    const int box = col >> 6;
+    const int unit = (col & 63) >> 3;
+    return (uint32_t)((box * bn + row) * 128 + ((unit ^ (row & 7)) << 4) + (col & 7) * 2);
+}
+
+template <int DK, int DV, int BN, int STAGES, int RB, bool LATENT>
+__global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREADS, 1)
+    simt_decode_kernel(const __grid_constant__ DecodeParams p)
+{
+    using C = SimtCfg<DK, DV, BN, STAGES, RB, LATENT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int P = p.splitk;
+    const int rank = (int)blockIdx.x;  // cluster dims are (P, 1, 1) and gridDim.x == P
+    const int kvh = (int)blockIdx.y / p.row_blocks;
+    const int row_block = (int)blockIdx.y % p.row_blocks;
+    const int b = (int)blockIdx.z;
+
+    int L = p.seq_lens[b];
+    if (L < 0) {
+        if (tid == 0 && rank == 0) atomicOr(p.status, FA_STATUS_BAD_PAGE);
+        L = 0;
+    }
+    // Ragged batches launch once per cluster size; a cluster keeps only the
+    // sequences whose length asks for its size (uniform across the cluster).
+    if (p.auto_split && auto_split_for_len(L) != P) return;
+
+    float* q_s = reinterpret_cast<float*>(smem + C::OFF_Q);
+    float* s_s = reinterpret_cast<float*>(smem + C::OFF_S);
+    float* alpha_s = reinterpret_cast<float*>(smem + C::OFF_ALPHA);
+    float2* maxsum_s = reinterpret_cast<float2*>(smem + C::OFF_MAXSUM);
+    float* stage_s = reinterpret_cast<float*>(smem + C::OFF_STAGE);
+    uint16_t* out_s = reinterpret_cast<uint16_t*>(smem + C::OFF_OUT);
+    const uint32_t full_bar = sbase + C::OFF_BAR;
+    const uint32_t empty_bar = full_bar + 8 * STAGES;
+    const uint32_t publish_bar = full_bar + 16 * STAGES;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
+    volatile int* consumed_s = abort_flag + 1;  // tiles the compute warps finished waiting for
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar + 8 * s, 1);
+            mbar_init(empty_bar + 8 * s, C::NCW);
+        }
+        mbar_init(publish_bar, P);
+        *abort_flag = 0;
+        *consumed_s = 0;
+        fence_mbarrier_init_cluster();
+    }
+    if (warp == C::NCW && lane == 0) {
+        tma_prefetch_map(&p.tm_k);
+        if (!LATENT) tma_prefetch_map(&p.tm_v);
+    }
+
+    // Q rows of this CTA -> fp32 in shared memory (rows >= p.rows are zero).
+    // Row r is token r / heads_per_cta, head kvh*g + row_block*heads_per_cta + r % heads_per_cta.
+    if (warp < C::NCW) {
+        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
+        for (int idx = tid; idx < RB * DK / 2; idx += C::NCT) {
+            const int r = idx / (DK / 2);
+            const int d2 = idx % (DK / 2);
+            float2 v = make_float2(0.f, 0.f);
+            if (r < p.rows) {
+                const int t = r / p.heads_per_cta;
+                const int h = kvh * p.group + row_block * p.heads_per_cta + r % p.heads_per_cta;
+                v = bf16x2_to_float2(q32[(((int64_t)b * p.num_q + t) * p.num_q_heads + h) * (DK / 2) + d2]);
+            }
+            q_s[r * DK + 2 * d2] = v.x;
+            q_s[r * DK + 2 * d2 + 1] = v.y;
+        }
+    }
+    __syncthreads();
+    if (P > 1) cluster_sync_all();  // every rank's publish barrier is initialised
+
+    // This rank's share of the key tiles: whole BN-key tiles split evenly,
+    // the remainder going to the low ranks (an empty share is allowed).
+    const int n_tiles = (L + BN - 1) / BN;
+    const int base = n_tiles / P, rem = n_tiles % P;
+    const int tile_begin = rank * base + min(rank, rem);
+    const int tile_count = base + (rank < rem ? 1 : 0);
+
+    // Running softmax state (owned by the softmax lanes) and the O accumulator.
+    float m_run[C::SM_ROWS], l_run[C::SM_ROWS];
+#pragma unroll
+    for (int k = 0; k < C::SM_ROWS; ++k) {
+        m_run[k] = -INFINITY;
+        l_run[k] = 0.f;
+    }
+    float acc[C::PV_ROWS][C::PV_CHUNKS][4];
+#pragma unroll
+    for (int k = 0; k < C::PV_ROWS; ++k)
+#pragma unroll
+        for (int ch = 0; ch < C::PV_CHUNKS; ++ch)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[k][ch][e] = 0.f;
+
+    int issued = 0;  // tiles whose loads the load lane has issued
+    if (warp == C::NCW) {
+        // ------------------------------------------------------------ load warp
+        if (lane == 0 && !(p.debug_flags & FA_DEBUG_SKIP_LOADS)) {
+            const uint64_t policy = l2_policy_evict_first();
+            const int segs = BN / p.box_rows;
+            for (int i = 0; i < tile_count; ++i) {
+                const int s = i % STAGES;
+                if (i >= STAGES &&
+                    !mbar_wait(empty_bar + 8 * s, ((i / STAGES) & 1) ^ 1, abort_flag, p.status, p.wait_limit_ns))
+                    break;
+                mbar_arrive_expect_tx(full_bar + 8 * s, C::STAGE_BYTES);
+                issued = i + 1;
+                const int key0 = (tile_begin + i) * BN;
+                const uint32_t dst = sbase + s * C::STAGE_BYTES;
+                for (int seg = 0; seg < segs; ++seg) {
+                    const int key = key0 + seg * p.box_rows;
+                    int32_t row = p.oob_row;  // zero fill past the sequence or on a bad page
+                    if (key < L) {
+                        const int slot = key / p.page_size;
+                        const int phys = slot < p.max_pages ? p.page_table[(int64_t)b * p.max_pages + slot] : -1;
+                        if (phys >= 0 && phys < p.num_pages)
+                            row = (phys * p.num_kv_heads + kvh) * p.page_size + key % p.page_size;
+                        else
+                            atomicOr(p.status, FA_STATUS_BAD_PAGE);
+                    }
+                    const uint32_t seg_off = seg * p.box_rows * 128;
+#pragma unroll
+                    for (int c = 0; c < C::KBOX; ++c)
+                        tma_load_2d(dst + c * BN * 128 + seg_off, &p.tm_k, c * 64, row, full_bar + 8 * s, policy);
+                    if (!LATENT) {
+#pragma unroll
+                        for (int c = 0; c < C::VBOX; ++c)
+                            tma_load_2d(dst + C::K_BYTES + c * BN * 128 + seg_off, &p.tm_v, c * 64, row,
+                                        full_bar + 8 * s, policy);
+                    }
+                }
+            }
+        }
+    } else {
+        // --------------------------------------------------------- compute warps
+        const int kk = tid % BN;           // QK^T: this thread's key within the tile
+        const int rg = tid / BN;           // ... and its row group
+        const int pv_lane = tid % (C::NCH >= C::NCT ? C::NCT : C::NCH);
+        const int pv_row0 = tid / (C::NCH >= C::NCT ? C::NCT : C::NCH);
+        const float c2 = p.scale_log2e;
+
+        for (int i = 0; i < tile_count; ++i) {
+            const int s = i % STAGES;
+            mbar_wait(full_bar + 8 * s, (i / STAGES) & 1, abort_flag, p.status, p.wait_limit_ns);
+            named_barrier_sync(1, C::NCT);  // also: previous tile's P V reads are done
+            if (*abort_flag) break;         // uniform: read after the barrier
+            if (tid == 0) *consumed_s = i + 1;
+            const uint8_t* kt = smem + s * C::STAGE_BYTES;
+            const uint8_t* vt = LATENT ? kt : kt + C::K_BYTES;
+            const int key0 = (tile_begin + i) * BN;
+
+            // ---- S = Q K^T for key kk, rows rg + QK_GROUPS * k (raw units, masked)
+            {
+                float sacc[C::QK_ROWS];
+#pragma unroll
+                for (int k = 0; k < C::QK_ROWS; ++k) sacc[k] = 0.f;
+#pragma unroll 2
+                for (int cc = 0; cc < DK / 8; ++cc) {
+                    const uint4 kw = *reinterpret_cast<const uint4*>(kt + swz_offset(kk, cc * 8, BN));
+                    const float2 k01 = bf16x2_to_float2(kw.x), k23 = bf16x2_to_float2(kw.y);
+                    const float2 k45 = bf16x2_to_float2(kw.z), k67 = bf16x2_to_float2(kw.w);
+#pragma unroll
+                    for (int k = 0; k < C::QK_ROWS; ++k) {
+                        const int r = rg + C::QK_GROUPS * k;
+                        if (C::QK_ROWS * C::QK_GROUPS > RB && r >= RB) continue;
+                        const float4 qa = *reinterpret_cast<const float4*>(q_s + r * DK + cc * 8);
+                        const float4 qb = *reinterpret_cast<const float4*>(q_s + r * DK + cc * 8 + 4);
+                        float a = sacc[k];
+                        a = fmaf(qa.x, k01.x, a);
+                        a = fmaf(qa.y, k01.y, a);
+                        a = fmaf(qa.z, k23.x, a);
+                        a = fmaf(qa.w, k23.y, a);
+                        a = fmaf(qb.x, k45.x, a);
+                        a = fmaf(qb.y, k45.y, a);
+                        a = fmaf(qb.z, k67.x, a);
+                        a = fmaf(qb.w, k67.y, a);
+                        sacc[k] = a;
+                    }
+                }
+                const int key = key0 + kk;
+#pragma unroll
+                for (int k = 0; k < C::QK_ROWS; ++k) {
+                    const int r = rg + C::QK_GROUPS * k;
+                    if (r >= RB) continue;
+                    const int t = r / p.heads_per_cta;
+                    const int n_vis = L - p.num_q + t + 1;  // causal at the cache tail
+                    s_s[r * BN + kk] = (r < p.rows && key < n_vis) ? sacc[k] : -INFINITY;
+                }
+            }
+            named_barrier_sync(1, C::NCT);
+
+            // ---- online softmax per row (warp-owned rows), exp2 form
+#pragma unroll
+            for (int k = 0; k < C::SM_ROWS; ++k) {
+                const int r = warp + C::NCW * k;
+                if (r >= RB) continue;
+                float v[BN / 32];
+                float tmax = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < BN / 32; ++j) {
+                    v[j] = s_s[r * BN + lane + 32 * j];
+                    tmax = fmaxf(tmax, v[j]);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+                const float m_new = fmaxf(m_run[k], tmax);
+                float alpha = 1.f, psum = 0.f;
+                if (m_new != -INFINITY) {
+                    alpha = (m_run[k] == -INFINITY) ? 0.f : ex2_approx((m_run[k] - m_new) * c2);
+#pragma unroll
+                    for (int j = 0; j < BN / 32; ++j) {
+                        const float pj = (v[j] == -INFINITY) ? 0.f : ex2_approx((v[j] - m_new) * c2);
+                        psum += pj;
+                        s_s[r * BN + lane + 32 * j] = pj;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < BN / 32; ++j) s_s[r * BN + lane + 32 * j] = 0.f;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+                l_run[k] = l_run[k] * alpha + psum;
+                m_run[k] = m_new;
+                if (lane == 0) alpha_s[r] = alpha;
+            }
+            named_barrier_sync(1, C::NCT);
+
+            // ---- correction and O += P V for rows pv_row0 + PV_ROW_LANES * k
+#pragma unroll
+            for (int k = 0; k < C::PV_ROWS; ++k) {
+                const int r = pv_row0 + C::PV_ROW_LANES * k;
+                if (r >= RB) continue;
+                const float a = alpha_s[r];
+#pragma unroll
+                for (int ch = 0; ch < C::PV_CHUNKS; ++ch)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[k][ch][e] *= a;
+            }
+#pragma unroll 2
+            for (int j = 0; j < BN; ++j) {
+                float pr[C::PV_ROWS];
+#pragma unroll
+                for (int k = 0; k < C::PV_ROWS; ++k) {
+                    const int r = pv_row0 + C::PV_ROW_LANES * k;
+                    pr[k] = (r < RB) ? s_s[r * BN + j] : 0.f;
+                }
+#pragma unroll
+                for (int ch = 0; ch < C::PV_CHUNKS; ++ch) {
+                    const int col = (pv_lane + ch * C::NCT) * 4;
+                    const uint2 vw = *reinterpret_cast<const uint2*>(vt + swz_offset(j, col, BN));
+                    const float2 v01 = bf16x2_to_float2(vw.x), v23 = bf16x2_to_float2(vw.y);
+#pragma unroll
+                    for (int k = 0; k < C::PV_ROWS; ++k) {
+                        acc[k][ch][0] = fmaf(pr[k], v01.x, acc[k][ch][0]);
+                        acc[k][ch][1] = fmaf(pr[k], v01.y, acc[k][ch][1]);
+                        acc[k][ch][2] = fmaf(pr[k], v23.x, acc[k][ch][2]);
+                        acc[k][ch][3] = fmaf(pr[k], v23.y, acc[k][ch][3]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar + 8 * s);  // this warp is done with the stage
+        }
+
+        // ---- stage the normalised partial O and (max, sum)
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < C::SM_ROWS; ++k) {
+                const int r = warp + C::NCW * k;
+                if (r < RB) maxsum_s[r] = make_float2(m_run[k], l_run[k]);
+            }
+        }
+        named_barrier_sync(1, C::NCT);
+        const int BW = p.band_cols;
+#pragma unroll
+        for (int k = 0; k < C::PV_ROWS; ++k) {
+            const int r = pv_row0 + C::PV_ROW_LANES * k;
+            if (r >= RB) continue;
+            const float l = maxsum_s[r].y;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+            for (int ch = 0; ch < C::PV_CHUNKS; ++ch) {
+                const int col = (pv_lane + ch * C::NCT) * 4;
+                const int q = col / BW, j = col % BW;
+                *reinterpret_cast<float4*>(stage_s + (q * RB + r) * BW + j) =
+                    make_float4(acc[k][ch][0] * inv, acc[k][ch][1] * inv, acc[k][ch][2] * inv,
+                                acc[k][ch][3] * inv);
+            }
+        }
+    }
+
+    __syncthreads();  // staging complete (all warps; the load warp is idle here)
+    if (warp < C::NCW) {
+        splitk_merge_and_store<RB>(p, P, rank, b, kvh, row_block, stage_s, maxsum_s, out_s, publish_bar,
+                                   abort_flag, tid, C::NCT, 1);
+    } else if (lane == 0 && *abort_flag) {
+        // Gave up early: let copies already issued, but never consumed, land
+        // before the CTA exits (each wait again bounded).
+        volatile int keep_waiting = 0;
+        for (int i = *consumed_s; i < issued; ++i)
+            mbar_wait(full_bar + 8 * (i % STAGES), (i / STAGES) & 1, &keep_waiting, p.status, p.wait_limit_ns);
+    }
+    __syncwarp();
+    if (P > 1) cluster_sync_all();  // peers may still read this CTA's staged bands until here
+}
+
+// ---------------------------------------------------------------------------
+// Variants and their geometry
+// ---------------------------------------------------------------------------
+template <int DK, int DV, int BN, int STAGES, int RB, bool LATENT>
+static bool fill_geometry(KernelGeometry* g, const char* name)
+{
+    using C = SimtCfg<DK, DV, BN, STAGES, RB, LATENT>;
+    g->func = reinterpret_cast<const void*>(&simt_decode_kernel<DK, DV, BN, STAGES, RB, LATENT>);
+    g->threads = C::THREADS;
+    g->keys_per_tile = BN;
+    g->stages = STAGES;
+    g->rows_capacity = RB;
+    g->smem_bytes = C::SMEM_BYTES;
+    g->name = name;
+    return true;
+}
+
+bool simt_geometry(int qk, int ov, bool latent, int rb, KernelGeometry* g)
+{
+#define FAD_SIMT(DK, DV, BN, ST, RB, LAT, SUFFIX)                                              \
+    if (qk == DK && ov == DV && latent == LAT && rb == RB)                                      \
+        return fill_geometry<DK, DV, BN, ST, RB, LAT>(                                          \
+            g, "simt_d" #DK "_v" #DV "_bn" #BN "_s" #ST "_r" #RB SUFFIX);
+    FAD_SIMT(64, 64, 64, 4, 4, false, "")
+    FAD_SIMT(64, 64, 64, 4, 8, false, "")
+    FAD_SIMT(64, 64, 64, 4, 16, false, "")
+    FAD_SIMT(128, 128, 64, 4, 4, false, "")
+    FAD_SIMT(128, 128, 64, 4, 8, false, "")
+    FAD_SIMT(128, 128, 64, 4, 16, false, "")
+    FAD_SIMT(576, 512, 32, 3, 16, true, "_latent")
+    FAD_SIMT(576, 512, 32, 2, 16, false, "")
+#undef FAD_SIMT
+    return false;
+}
+
+}  // namespace fad

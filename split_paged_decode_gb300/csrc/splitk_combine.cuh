@@ -1,0 +1,118 @@
+// splitk_combine.cuh -- the cluster split-K epilogue shared by every decode
+// kernel: publish this CTA's partial result, merge all partitions' results
+// for this CTA's band of output columns over distributed shared memory, cast
+// to bf16 and TMA-store the band.
+//
+// Follows the fa4_splitk_combine_write page (Modular MAX docs): pass 2 is a
+// reduce-scatter in which cluster rank p owns the output column band
+// [p * Dv / P, (p + 1) * Dv / P); it reads every rank's (max, sum) and every
+// rank's normalised partial O for its band, forms
+//   Gmax = max_q max_q,  Gsum = sum_q sum_q * exp2((max_q - Gmax) * c),
+//   w_q  = sum_q * exp2((max_q - Gmax) * c) / Gsum,  O = sum_q w_q * O_q,
+// (c = scale * log2 e; the sum_q factor cancels each partial's own
+// normalisation) and stores its band. One publish barrier (an mbarrier that
+// every rank arrives on remotely, released at cluster scope) makes the staged
+// partials visible before the remote reads; no second cluster barrier is
+// needed because the bf16 band is packed into a buffer no peer reads, and the
+// kernel's terminal cluster barrier keeps every rank's staged bands alive
+// until all ranks have finished reading them.
+#pragma once
+
+#include "device_common.cuh"
+
+namespace fad {
+
+// Layout contract with the kernels:
+//   stage_s  float [P][RB][BW]: rank-local normalised partial O, band-major
+//            (element (r, col) at ((col / BW) * RB + r) * BW + col % BW)
+//   maxsum_s float2 [RB]: (max in raw q.k units, sum of exp2((s - max) * c));
+//            an empty partition holds (-inf, 0)
+//   out_s    bf16 [BW / OC][RB][OC]: this rank's packed band in store boxes of
+//            OC = min(BW, 256) columns, rows r = t * heads + hh
+// Rows >= p.rows are padding: they are merged (harmlessly) but never stored.
+//
+// Called by `nthreads` threads with ids `tid` in [0, nthreads), after a CTA-wide
+// barrier that follows the staging writes. Thread tid 0 of the calling group
+// publishes. `bar_id` names a hardware barrier private to the group.
+template <int RB>
+__device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, int P, int rank, int b,
+                                                       int kvh, int row_block, const float* stage_s,
+                                                       const float2* maxsum_s, uint16_t* out_s,
+                                                       uint32_t publish_bar, volatile int* abort_flag,
+                                                       int tid, int nthreads, uint32_t bar_id)
+{
+    const int BW = p.band_cols;
+    const float c = p.scale_log2e;
+    const uint32_t stage_base = smem_addr(stage_s);
+    const uint32_t maxsum_base = smem_addr(maxsum_s);
+
+    if (P > 1) {
+        if (tid == 0) {
+            // Round 1: every rank tells every rank (itself included) that its
+            // stage is complete. The preceding CTA barrier orders the other
+            // threads' staging writes before this release.
+            for (int q = 0; q < P; ++q) mbar_arrive_cluster(map_shared_rank(publish_bar, q));
+        }
+        mbar_wait<true>(publish_bar, 0, abort_flag, p.status, p.wait_limit_ns);
+    }
+
+    const int chunks = BW / 4;
+    for (int it = tid; it < RB * chunks; it += nthreads) {
+        const int r = it / chunks;
+        const int j = (it % chunks) * 4;
+        float mq[kMaxSplit], wq[kMaxSplit];
+        float gmax = -INFINITY;
+        for (int q = 0; q < P; ++q) {
+            float2 ms = (P > 1) ? ld_dsmem_f2(map_shared_rank(maxsum_base + 8u * r, q)) : maxsum_s[r];
+            mq[q] = ms.x;
+            wq[q] = ms.y;
+            if (ms.y > 0.f) gmax = fmaxf(gmax, ms.x);
+        }
+        float gsum = 0.f;
+        for (int q = 0; q < P; ++q) {
+            float w = 0.f;
+            if (wq[q] > 0.f) w = wq[q] * ex2_approx((mq[q] - gmax) * c);
+            wq[q] = w;
+            gsum += w;
+        }
+        const float inv = gsum > 0.f ? 1.f / gsum : 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint32_t off = 4u * ((uint32_t)(rank * RB + r) * BW + j);
+        for (int q = 0; q < P; ++q) {
+            if (wq[q] <= 0.f) continue;
+            float4 v = (P > 1) ? ld_dsmem_f4(map_shared_rank(stage_base + off, q))
+                               : *reinterpret_cast<const float4*>(stage_s + (rank * RB + r) * BW + j);
+            const float w = wq[q] * inv;
+            o.x = fmaf(w, v.x, o.x);
+            o.y = fmaf(w, v.y, o.y);
+            o.z = fmaf(w, v.z, o.z);
+            o.w = fmaf(w, v.w, o.w);
+        }
+        uint2 packed = make_uint2(float2_to_bf16x2(o.x, o.y), float2_to_bf16x2(o.z, o.w));
+        const int OC = p.out_chunk_cols;
+        *reinterpret_cast<uint2*>(out_s + ((j / OC) * RB + r) * OC + j % OC) = packed;
+
+        if (rank == 0 && j == 0 && r < p.rows && p.lse != nullptr) {
+            const int t = r / p.heads_per_cta;
+            const int h = kvh * p.group + row_block * p.heads_per_cta + r % p.heads_per_cta;
+            // natural-log LSE of the scaled scores: scale * Gmax + ln(Gsum)
+            const float lse = gsum > 0.f ? p.scale * gmax + lg2_approx(gsum) * 0.6931471805599453f
+                                         : -INFINITY;
+            p.lse[((int64_t)b * p.num_q + t) * p.num_q_heads + h] = lse;
+        }
+    }
+
+    // bf16 band complete in shared memory -> one TMA store of the band.
+    fence_proxy_async_smem();
+    named_barrier_sync(bar_id, nthreads);
+    if (tid == 0) {
+        const int OC = p.out_chunk_cols;
+        for (int c0 = 0; c0 < BW; c0 += OC)
+            tma_store_3d(&p.tm_out, smem_addr(out_s + (c0 / OC) * RB * OC), rank * BW + c0,
+                         kvh * p.group + row_block * p.heads_per_cta, b * p.num_q);
+        tma_store_commit();
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    }
+}
+
+}  // namespace fad

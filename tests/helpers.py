@@ -1,0 +1,98 @@
+"""Shared test helpers: run the library on a seeded workload, run the oracle on
+the same inputs, and compare element by element with the stated tolerance."""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+
+import oracle
+import split_paged_decode_gb300 as spd
+from split_paged_decode_gb300.workloads import DecodeInputs, bf16_bits
+
+# Tolerances of the decode output (bf16) and of the fp32 log-sum-exp.
+OUT_ATOL = 1e-2
+OUT_RTOL = 1e-2
+LSE_ATOL = 1e-3
+
+
+def oracle_threads() -> int:
+    return max(1, min(64, os.cpu_count() or 1))
+
+
+def run_oracle(inp: DecodeInputs, rows=None):
+    w = inp.workload
+    v = None if inp.v_pages is None else bf16_bits(inp.v_pages)
+    return oracle.decode(bf16_bits(inp.q), bf16_bits(inp.k_pages), v, inp.page_table.numpy(),
+                         inp.seq_lens.numpy(), inp.scale, ov_depth=w.ov_depth, rows=rows,
+                         threads=oracle_threads())
+
+
+class DeviceCall:
+    """Device copies of one input set plus a handle, for repeated runs."""
+
+    def __init__(self, inp: DecodeInputs, splitk: int | None = None, device="cuda"):
+        w = inp.workload
+        self.inp = inp
+        self.q = inp.q.to(device)
+        self.k = inp.k_pages.to(device)
+        self.v = None if inp.v_pages is None else inp.v_pages.to(device)
+        self.pt = inp.page_table.to(device)
+        self.lens = inp.seq_lens.to(device)
+        self.out = torch.full((w.batch, w.num_q, w.num_q_heads, w.ov_depth), float("nan"),
+                              dtype=torch.bfloat16, device=device)
+        self.lse = torch.full((w.batch, w.num_q, w.num_q_heads), float("nan"), dtype=torch.float32,
+                              device=device)
+        P = w.splitk if splitk is None else splitk
+        self.h = spd.fa_decode_create(w.num_q_heads, w.num_kv_heads, w.qk_depth, w.nope_depth,
+                                      w.ov_depth, w.page_size, w.num_q, P)
+
+    def run(self, stream=None):
+        spd.fa_decode_run(self.h, self.q, self.k, self.v, self.pt, self.lens, self.inp.scale, self.out,
+                          self.lse, stream=stream)
+
+    def status(self) -> int:
+        return spd.fa_decode_check(self.h)
+
+    def close(self):
+        if self.h:
+            spd.fa_decode_destroy(self.h)
+            self.h = 0
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
+
+
+def compare(out, lse, ref_out, ref_lse, what=""):
+    """Element-wise bound |out-ref| <= atol + rtol*|ref|, |lse-ref| <= 1e-3 (-inf must match)."""
+    out = np.asarray(out, np.float64)
+    lse = np.asarray(lse, np.float64)
+    assert np.all(np.isfinite(out)), f"{what}: non-finite outputs"
+    err = np.abs(out - ref_out)
+    bound = OUT_ATOL + OUT_RTOL * np.abs(ref_out)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outputs out of tolerance; "
+                           f"worst excess {np.max(err - bound):.3e} at {np.unravel_index(np.argmax(err - bound), err.shape)}")
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(lse), fin), f"{what}: lse finiteness differs"
+    assert np.all(lse[~fin] == ref_lse[~fin]), f"{what}: lse of rows without keys must be -inf"
+    lerr = np.abs(lse[fin] - ref_lse[fin])
+    assert lerr.size == 0 or lerr.max() <= LSE_ATOL, f"{what}: lse error {lerr.max():.3e}"
+
+
+def check_against_oracle(call: DeviceCall, rows=None, what=""):
+    """Compare the device result with the oracle on all rows, or on rows [(b,t,h), ...]."""
+    out = call.out.float().cpu().numpy()
+    lse = call.lse.cpu().numpy()
+    if rows is None:
+        ref_out, ref_lse = run_oracle(call.inp)
+        compare(out, lse, ref_out, ref_lse, what)
+    else:
+        rows = np.asarray(rows, np.int32).reshape(-1, 3)
+        ref_out, ref_lse = run_oracle(call.inp, rows=rows)
+        compare(out[rows[:, 0], rows[:, 1], rows[:, 2]], lse[rows[:, 0], rows[:, 1], rows[:, 2]],
+                ref_out, ref_lse, what)

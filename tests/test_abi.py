@@ -1,0 +1,102 @@
+"""The C ABI on the CPU: the library loads, exports what the header declares,
+and rejects bad arguments on the host (no GPU needed, no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import split_paged_decode_gb300 as spd
+from split_paged_decode_gb300 import build as spd_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    spd_build.build_library()
+    return spd.load_library()
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(fa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(spd.EXPORTED) <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_binding_names_match_header():
+    assert set(declared_functions()) == set(spd.EXPORTED)
+
+
+def _create(lib, *args):
+    h = ctypes.c_void_p()
+    rc = lib.fa_decode_create(ctypes.byref(h), *args)
+    return rc, h
+
+
+@pytest.mark.parametrize("args", [
+    (0, 1, 128, -1, 128, 128, 1, 1),      # no heads
+    (32, 6, 128, -1, 128, 128, 1, 1),     # heads not divisible
+    (32, 8, 128, 200, 128, 128, 1, 1),    # nope > qk
+    (32, 8, 128, -1, 128, 0, 1, 1),       # page size
+    (32, 8, 128, -1, 128, 128, 0, 1),     # num_q
+    (32, 8, 128, -1, 128, 128, 1, 3),     # splitk not a power of two
+    (32, 8, 128, -1, 128, 128, 1, 32),    # splitk too large
+])
+def test_create_rejects_invalid_arguments(lib, args):
+    rc, h = _create(lib, *args)
+    assert rc == spd.FA_ERR_INVALID_ARG
+    assert not h.value
+    assert lib.fa_decode_last_error().decode()
+
+
+@pytest.mark.parametrize("args", [
+    (32, 8, 96, -1, 96, 128, 1, 1),       # depth pair not built
+    (32, 8, 128, -1, 128, 20, 1, 1),      # page size not a multiple of 8
+    (32, 8, 128, -1, 128, 96, 1, 1),      # page size and tile do not divide
+    (4, 1, 64, -1, 64, 64, 1, 16),        # 64 / 16 = 4-column bands
+    (40, 2, 128, -1, 128, 64, 1, 1),      # 20 rows, group not a multiple of 16
+    (32, 8, 128, -1, 128, 64, 8, 1),      # 32 rows with num_q > 1
+])
+def test_create_rejects_unsupported_shapes(lib, args):
+    rc, h = _create(lib, *args)
+    assert rc == spd.FA_ERR_UNSUPPORTED, lib.fa_decode_last_error()
+    assert not h.value
+
+
+def test_null_handle_calls_fail_cleanly(lib):
+    assert lib.fa_decode_run(None, None, None, None, None, None, 1.0, None, None, None, 1, 1, 1) \
+        == spd.FA_ERR_INVALID_ARG
+    assert lib.fa_decode_check(None, None, None) == spd.FA_ERR_INVALID_ARG
+    assert lib.fa_decode_set_debug(None, 0, 0) == spd.FA_ERR_INVALID_ARG
+    assert lib.fa_decode_describe(None, None, 0) == spd.FA_ERR_INVALID_ARG
+    assert lib.fa_decode_destroy(None) == spd.FA_OK
+
+
+def test_valid_create_without_gpu_reports_cuda_error(lib):
+    """On a machine without a GB300 a valid shape fails at the device query."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc, h = _create(lib, 32, 8, 128, -1, 128, 128, 1, 4)
+    assert rc in (spd.FA_ERR_CUDA, spd.FA_ERR_UNSUPPORTED)
+    assert not h.value
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(FileNotFoundError):
+        spd.load_library(str(tmp_path / "libfa_decode.so"))

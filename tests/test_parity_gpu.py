@@ -1,0 +1,222 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Bound: |out - ref| <= 1e-2 + 1e-2 |ref| element-wise on the bf16 output and
+|lse - ref| <= 1e-3 on the fp32 log-sum-exp; page gathering, the single-key
+case and page permutations are checked bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import split_paged_decode_gb300 as spd
+from split_paged_decode_gb300.workloads import WORKLOADS, DecodeWorkload, generate
+
+from helpers import DeviceCall, check_against_oracle, compare, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from split_paged_decode_gb300 import build
+
+    build.build_library()
+    spd.load_library()
+
+
+def wl(**kw):
+    base = dict(name="case", batch=3, num_q=1, num_q_heads=8, num_kv_heads=2, qk_depth=128, ov_depth=128,
+                page_size=64, splitk=2, seq_len_lo=1, seq_len_hi=700, seed=100)
+    base.update(kw)
+    return DecodeWorkload(**base)
+
+
+def run_and_check(w, seq_lens=None, rows=None, what=None):
+    inp = generate(w, seq_lens=seq_lens)
+    with DeviceCall(inp) as call:
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, rows=rows, what=what or w.name)
+        return call.out.cpu(), call.lse.cpu()
+
+
+# --- small shapes: several tiles, ragged tails, empty partitions -----------------------
+
+@pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
+def test_gqa_d128_splits(P):
+    run_and_check(wl(splitk=P, seed=10 + P), what=f"d128 P{P}")
+
+
+@pytest.mark.parametrize("ps", [8, 16, 32, 64, 128, 256])
+def test_page_sizes(ps):
+    run_and_check(wl(page_size=ps, splitk=4, seed=20), what=f"ps{ps}")
+
+
+@pytest.mark.parametrize("g,T", [(1, 1), (2, 1), (4, 1), (8, 1), (16, 1), (4, 2), (4, 4), (2, 8), (1, 16)])
+def test_rows_per_cta(g, T):
+    run_and_check(wl(num_q_heads=2 * g, num_kv_heads=2, num_q=T, seed=30 + g * T), what=f"g{g} T{T}")
+
+
+@pytest.mark.parametrize("P", [1, 2, 4, 8])
+def test_d64(P):
+    run_and_check(wl(qk_depth=64, ov_depth=64, splitk=P, seed=40 + P), what=f"d64 P{P}")
+
+
+@pytest.mark.parametrize("P", [1, 2, 4])
+def test_latent_small(P):
+    w = wl(num_q_heads=32, num_kv_heads=1, qk_depth=576, nope_depth=512, ov_depth=512, latent=True,
+           splitk=P, batch=2, seq_len_hi=300, scale=1.0 / np.sqrt(192.0), seed=50 + P)
+    run_and_check(w, what=f"latent P{P}")
+
+
+def test_latent_explicit_v_cache():
+    """(576, 512) with a separate V cache uses the separate-V kernel."""
+    w = wl(num_q_heads=16, num_kv_heads=1, qk_depth=576, nope_depth=512, ov_depth=512, latent=False,
+           splitk=2, batch=2, seq_len_hi=200, seed=55)
+    run_and_check(w, what="576/512 explicit V")
+
+
+def test_v_equal_k_pointer_means_v_is_k_prefix():
+    w = wl(splitk=2, seed=56)
+    inp = generate(w)
+    with DeviceCall(inp) as call:
+        call.v = call.k  # same pointer: V rows are the K rows
+        call.run()
+        assert call.status() == 0
+        inp.v_pages = None  # the oracle's latent layout with ov == qk
+        check_against_oracle(call, what="v is k")
+
+
+def test_causal_short_sequences_and_empty():
+    """Lengths 0, 1, below num_q and at tile edges; rows with no visible key give 0 / -inf."""
+    w = wl(num_q=4, num_q_heads=8, num_kv_heads=2, batch=8, splitk=4, seed=60)
+    run_and_check(w, seq_lens=[0, 1, 2, 3, 4, 63, 64, 65], what="short/empty")
+
+
+def test_ragged_auto_split():
+    w = wl(batch=12, num_q=4, splitk=0, seq_len_lo=1, seq_len_hi=9000, page_size=64, seed=61)
+    run_and_check(w, seq_lens=[1, 5, 1024, 1025, 4096, 4097, 8192, 9000, 64, 65, 2000, 3000],
+                  what="auto split")
+
+
+def test_more_tiles_than_ranks_and_fewer():
+    w = wl(batch=4, splitk=8, seed=62)
+    run_and_check(w, seq_lens=[64, 65, 64 * 8 + 1, 64 * 17 - 3], what="tiles vs ranks")
+
+
+# --- the five workloads at full size -----------------------------------------------------
+
+def _sample_rows(w, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.integers(0, w.batch, n), rng.integers(0, w.num_q, n),
+                     rng.integers(0, w.num_q_heads, n)], 1)
+
+
+@pytest.mark.parametrize("name", ["tiny", "batched_gqa", "long_context", "ragged_speculative", "mla"])
+def test_workload_full_size(name):
+    w = WORKLOADS[name]
+    rows = None
+    if name in ("ragged_speculative", "mla"):
+        rows = _sample_rows(w, 512, 7)
+    run_and_check(w, rows=rows, what=name)
+
+
+# --- bit-exact properties ----------------------------------------------------------------
+
+def test_single_key_is_bit_exact():
+    """One visible key: weight exp2(0) / 1 = 1, so out is that key's V row exactly."""
+    w = wl(batch=4, splitk=2, seed=70)
+    inp = generate(w, seq_lens=[1, 1, 1, 1])
+    with DeviceCall(inp) as call:
+        call.run()
+        assert call.status() == 0
+        out = call.out.cpu()
+        for b in range(4):
+            page = int(inp.page_table[b, 0])
+            for h in range(8):
+                assert torch.equal(out[b, 0, h], inp.v_pages[page, h // 4, 0]), (b, h)
+        ref_out, ref_lse = run_oracle(inp)
+        compare(out.float().numpy(), call.lse.cpu().numpy(), ref_out, ref_lse, "single key")
+
+
+def test_page_permutation_is_bitwise_invariant():
+    w = wl(batch=3, splitk=4, seed=71)
+    inp = generate(w)
+    with DeviceCall(inp) as call:
+        call.run()
+        out1, lse1 = call.out.clone(), call.lse.clone()
+        perm = torch.randperm(inp.num_pages, generator=torch.Generator().manual_seed(5))
+        k2 = torch.empty_like(inp.k_pages)
+        v2 = torch.empty_like(inp.v_pages)
+        k2[perm] = inp.k_pages
+        v2[perm] = inp.v_pages
+        pt = inp.page_table.clone()
+        pt[pt >= 0] = perm[pt[pt >= 0].long()].to(torch.int32)
+        call.k, call.v, call.pt = k2.cuda(), v2.cuda(), pt.cuda()
+        call.run()
+        assert call.status() == 0
+        assert torch.equal(call.out, out1)
+        assert torch.equal(call.lse, lse1)
+
+
+def test_repeated_runs_are_deterministic():
+    inp = generate(wl(splitk=4, seed=72))
+    with DeviceCall(inp) as call:
+        call.run()
+        a = call.out.clone()
+        call.run()
+        assert torch.equal(call.out, a)
+
+
+def test_side_stream():
+    inp = generate(wl(splitk=2, seed=73))
+    s = torch.cuda.Stream()
+    with DeviceCall(inp) as call:
+        with torch.cuda.stream(s):
+            call.run(stream=s)
+        s.synchronize()
+        assert spd.fa_decode_check(call.h, s) == 0
+        check_against_oracle(call, what="side stream")
+
+
+# --- failure reporting without a fault ---------------------------------------------------
+
+def test_bad_page_id_is_reported_not_faulted():
+    w = wl(batch=3, splitk=2, seed=80)
+    inp = generate(w)
+    bad = inp.page_table.clone()
+    bad[1, 0] = inp.num_pages + 1000  # out of range: read as zeros, flagged
+    with DeviceCall(inp) as call:
+        call.pt = bad.cuda()
+        call.run()
+        st = spd.fa_decode_check(call.h)
+        assert st & spd.FA_STATUS_BAD_PAGE
+        rows = [(b, 0, h) for b in (0, 2) for h in range(8)]  # untouched sequences stay right
+        check_against_oracle(call, rows=rows, what="bad page neighbours")
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """With loads suppressed, every CTA's first wait runs out after the short
+    limit and the kernel returns with FA_STATUS_TIMEOUT; the next run is normal."""
+    inp = generate(wl(batch=2, splitk=2, seed=81))
+    with DeviceCall(inp) as call:
+        spd.fa_decode_set_debug(call.h, spd.FA_DEBUG_SKIP_LOADS, 20_000_000)  # 20 ms
+        call.run()
+        st = spd.fa_decode_check(call.h)
+        assert st & spd.FA_STATUS_TIMEOUT
+        spd.fa_decode_set_debug(call.h, 0, 0)
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what="after timeout")
+
+
+def test_run_rejects_misaligned_pointer():
+    inp = generate(wl(seed=82))
+    with DeviceCall(inp) as call:
+        with pytest.raises(spd.FaDecodeError) as e:
+            spd.fa_decode_run(call.h, call.q.data_ptr() + 2, call.k, call.v, call.pt, call.lens, inp.scale,
+                              call.out, call.lse, batch=3, max_pages_per_seq=call.pt.shape[1],
+                              num_pages=call.k.shape[0])
+        assert e.value.code == spd.FA_ERR_INVALID_ARG
