@@ -33,15 +33,19 @@ struct SimtCfg {
     static constexpr int K_BYTES = KBOX * BN * 128;
     static constexpr int V_BYTES = LATENT ? 0 : VBOX * BN * 128;
     static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
-    static constexpr int OFF_Q = STAGES * STAGE_BYTES;            // float [RB][DK]
-    static constexpr int OFF_S = OFF_Q + RB * DK * 4;             // float [RB][BN]
-    static constexpr int OFF_ALPHA = OFF_S + RB * BN * 4;         // float [RB]
-    static constexpr int OFF_MAXSUM = OFF_ALPHA + ((RB * 4 + 15) / 16) * 16;  // float2 [RB]
-    static constexpr int OFF_STAGE = OFF_MAXSUM + RB * 8;         // float [RB][DV]
-    static constexpr int OFF_OUT = OFF_STAGE + RB * DV * 4;       // bf16 [RB][DV]
-    static constexpr int OFF_BAR = OFF_OUT + RB * DV * 2;         // full[S], empty[S], publish
-    static constexpr int OFF_FLAG = OFF_BAR + (2 * STAGES + 1) * 8;  // abort flag, consumed count
-    static constexpr int SMEM_BYTES = OFF_FLAG + 16 + 1024;       // + alignment slack
+    // Region offsets. Every region starts on 128 bytes; those a TMA copy
+    // touches (the K/V ring and the bf16 output band) start on 1024 bytes.
+    static constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+    static constexpr int OFF_Q = STAGES * STAGE_BYTES;                         // float [RB][DK]
+    static constexpr int OFF_S = align_up(OFF_Q + RB * DK * 4, 128);          // float [RB][BN]
+    static constexpr int OFF_ALPHA = align_up(OFF_S + RB * BN * 4, 128);      // float [RB]
+    static constexpr int OFF_MAXSUM = align_up(OFF_ALPHA + RB * 4, 128);      // float2 [RB]
+    static constexpr int OFF_STAGE = align_up(OFF_MAXSUM + RB * 8, 128);      // float [RB][DV]
+    static constexpr int OFF_OUT = align_up(OFF_STAGE + RB * DV * 4, 1024);   // bf16 [RB][DV]
+    static constexpr int OFF_BAR = align_up(OFF_OUT + RB * DV * 2, 128);      // full[S], empty[S], publish
+    static constexpr int OFF_FLAG = OFF_BAR + (2 * STAGES + 1) * 8;           // abort flag, consumed count
+    static constexpr int SMEM_BYTES = OFF_FLAG + 16 + 1024;                    // + base alignment slack
+    static_assert(STAGE_BYTES % 1024 == 0 && OFF_OUT % 1024 == 0, "TMA regions on 1024 bytes");
 
     // QK^T mapping: thread -> (key kk = t % BN, row group rg = t / BN)
     static constexpr int QK_GROUPS = NCT / BN;
