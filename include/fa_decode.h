@@ -121,11 +121,13 @@ int fa_decode_check(fa_decode_t h, void* stream, uint32_t* status_out);
 
 /*
  * Test hooks. flags: FA_DEBUG_SKIP_LOADS makes the load warp issue no copies,
- * so the first bounded wait of every CTA runs out; wait_limit_ns bounds every
- * device wait (0 restores the default of one second). Normal runs never need
- * this call.
+ * so the first bounded wait of every CTA runs out; FA_DEBUG_FORCE_SIMT selects
+ * the FMA kernel on shapes the tensor-core kernel would take (to compare the
+ * two on one input); wait_limit_ns bounds every device wait (0 restores the
+ * default of one second). Normal runs never need this call.
  */
 #define FA_DEBUG_SKIP_LOADS 1u
+#define FA_DEBUG_FORCE_SIMT 2u   /* run the warp-level FMA kernel even where the tcgen05 one applies */
 int fa_decode_set_debug(fa_decode_t h, uint32_t flags, int64_t wait_limit_ns);
 
 /*

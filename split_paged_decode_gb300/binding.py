@@ -21,6 +21,7 @@ FA_ERR_DEVICE = -4
 FA_STATUS_TIMEOUT = 1
 FA_STATUS_BAD_PAGE = 2
 FA_DEBUG_SKIP_LOADS = 1
+FA_DEBUG_FORCE_SIMT = 2
 
 # Every symbol include/fa_decode.h declares.
 EXPORTED = ("fa_decode_create", "fa_decode_run", "fa_decode_check", "fa_decode_set_debug",

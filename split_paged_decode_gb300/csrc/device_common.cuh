@@ -210,6 +210,23 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Barrier over `threads` threads that also ORs a predicate across them: every
+// participant receives the same answer, so a decision taken on it is uniform
+// even when the inputs were read at different times.
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t threads, bool pred)
+{
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"((uint32_t)pred), "r"(id), "r"(threads)
+        : "memory");
+    return out != 0;
+}
+
 // ---------------------------------------------------------------------------
 // MUFU transcendental instructions (hardware approximations, ~2^-22 rel. error)
 // ---------------------------------------------------------------------------

@@ -125,9 +125,10 @@ struct fa_decode {
     int hq, hkv, group, dk, nope, dv, page_size, num_q, splitk;
     int rows, row_blocks, heads_per_cta, tokens_per_cta, rows_capacity;
     int device;
-    fad::KernelGeometry geo;         // separate V cache
-    fad::KernelGeometry geo_latent;  // V = prefix of the K row
-    bool has_latent;
+    fad::KernelGeometry geo;         // SIMT kernel, separate V cache (or V = K rows)
+    fad::KernelGeometry geo_latent;  // SIMT kernel, V = prefix of the K row
+    fad::KernelGeometry geo_tc;      // tcgen05 kernel
+    bool has_simt, has_latent, has_tc;
     unsigned int* d_status;
     uint32_t debug_flags;
     uint64_t wait_limit_ns;
@@ -238,15 +239,19 @@ int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk
         return fail(FA_ERR_UNSUPPORTED, "num_q * group = %d rows per kv head: built for <= 16, or num_q == 1 "
                                         "with group a multiple of 16", R);
     }
-    if (!fad::simt_geometry(qk_depth, ov_depth, false, tmp.rows_capacity, &tmp.geo))
-        return fail(FA_ERR_UNSUPPORTED, "depth pair (qk %d, ov %d) with %d rows per CTA is not built "
-                                        "(built: 64/64, 128/128, 576/512)", qk_depth, ov_depth, tmp.rows_capacity);
-    tmp.has_latent = fad::simt_geometry(qk_depth, ov_depth, true, tmp.rows_capacity, &tmp.geo_latent);
-    const int bn = tmp.geo.keys_per_tile;
     if (page_size % 8)
         return fail(FA_ERR_UNSUPPORTED, "page_size %d is not a multiple of 8", page_size);
-    if (!(page_size % bn == 0 || bn % page_size == 0))
-        return fail(FA_ERR_UNSUPPORTED, "page_size %d and the %d-key tile must divide one another", page_size, bn);
+    auto page_fits = [&](int bn) { return page_size % bn == 0 || bn % page_size == 0; };
+    tmp.has_simt = fad::simt_geometry(qk_depth, ov_depth, false, tmp.rows_capacity, &tmp.geo) &&
+                   page_fits(tmp.geo.keys_per_tile);
+    tmp.has_latent = tmp.has_simt && fad::simt_geometry(qk_depth, ov_depth, true, tmp.rows_capacity,
+                                                        &tmp.geo_latent);
+    tmp.has_tc = tmp.row_blocks == 1 && fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlots, &tmp.geo_tc) &&
+                 page_fits(tmp.geo_tc.keys_per_tile);
+    if (!tmp.has_simt && !tmp.has_tc)
+        return fail(FA_ERR_UNSUPPORTED, "no kernel for (qk %d, ov %d), %d rows per CTA and page_size %d "
+                                        "(built: 64/64, 128/128, 576/512; page size and key tile must divide "
+                                        "one another)", qk_depth, ov_depth, tmp.rows, page_size);
     int splits[3];
     const int ns = split_list(&tmp, splits);
     for (int i = 0; i < ns; ++i) {
@@ -267,9 +272,10 @@ int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk
         return fail(FA_ERR_UNSUPPORTED, "device %d has compute capability %d.%d; this library is built for "
                                         "sm_103a (GB300)", dev, major, minor);
     tmp.device = dev;
-    int rc = prepare_kernel(&tmp, tmp.geo);
-    if (rc) return rc;
+    int rc = FA_OK;
+    if (tmp.has_simt && (rc = prepare_kernel(&tmp, tmp.geo))) return rc;
     if (tmp.has_latent && (rc = prepare_kernel(&tmp, tmp.geo_latent))) return rc;
+    if (tmp.has_tc && (rc = prepare_kernel(&tmp, tmp.geo_tc))) return rc;
 
     e = cudaMalloc(&tmp.d_status, 256);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status word)");
@@ -327,12 +333,13 @@ int fa_decode_check(fa_decode_t h, void* stream, uint32_t* status_out)
 int fa_decode_describe(fa_decode_t h, char* buf, int size)
 {
     if (!h || !buf || size < 1) return fail(FA_ERR_INVALID_ARG, "handle or buffer is NULL");
+    const fad::KernelGeometry& g = h->has_tc ? h->geo_tc : h->geo;
     snprintf(buf, (size_t)size,
-             "path=simt kernel=%s latent_kernel=%s splitk=%d%s threads=%d keys_per_tile=%d stages=%d "
-             "rows=%d rows_capacity=%d row_blocks=%d smem=%d",
-             h->geo.name, h->has_latent ? h->geo_latent.name : "none", h->splitk,
-             h->splitk == 0 ? "(per sequence: 1/2/4)" : "", h->geo.threads, h->geo.keys_per_tile, h->geo.stages,
-             h->rows, h->rows_capacity, h->row_blocks, h->geo.smem_bytes);
+             "path=%s kernel=%s simt_kernel=%s latent_kernel=%s splitk=%d%s threads=%d keys_per_tile=%d "
+             "stages=%d rows=%d rows_capacity=%d row_blocks=%d smem=%d",
+             h->has_tc ? "tcgen05" : "simt", g.name, h->has_simt ? h->geo.name : "none",
+             h->has_latent ? h->geo_latent.name : "none", h->splitk, h->splitk == 0 ? "(per sequence: 1/2/4)" : "",
+             g.threads, g.keys_per_tile, g.stages, h->rows, h->rows_capacity, h->row_blocks, g.smem_bytes);
     return FA_OK;
 }
 
@@ -362,14 +369,20 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     const bool latent = (v_pages == nullptr || v_pages == k_pages);
     if (latent && h->dv > h->dk)
         return fail(FA_ERR_INVALID_ARG, "latent layout (v_pages NULL or == k_pages) needs ov_depth <= qk_depth");
-    const fad::KernelGeometry& g = (latent && h->has_latent) ? h->geo_latent : h->geo;
+    // Kernel choice: the latent-layout SIMT kernel for the MLA latent cache,
+    // else the tcgen05 kernel where it applies, else the SIMT kernel.
+    const bool use_latent = latent && h->has_latent;
+    const bool use_tc = !use_latent && h->has_tc && !(h->debug_flags & FA_DEBUG_FORCE_SIMT && h->has_simt);
+    if (!use_latent && !use_tc && !h->has_simt)
+        return fail(FA_ERR_UNSUPPORTED, "no kernel for this call (latent layout %d)", (int)latent);
+    const fad::KernelGeometry& g = use_latent ? h->geo_latent : (use_tc ? h->geo_tc : h->geo);
     const int bn = g.keys_per_tile;
     const int box_rows = h->page_size < bn ? h->page_size : bn;
 
     int rc = encode_cache_map(h->k_map, k_pages, h->dk, cache_rows, box_rows);
     if (rc) return rc;
-    if (latent && g.func == h->geo.func) {
-        // V = K row prefix through the separate-V kernel (e.g. qk == ov): same rows, V width.
+    if (latent && !use_latent) {
+        // V = K row prefix through a separate-V kernel (e.g. qk == ov): same rows, V width.
         rc = encode_cache_map(h->v_map, k_pages, h->dk, cache_rows, box_rows);
     } else if (!latent) {
         rc = encode_cache_map(h->v_map, v_pages, h->dv, cache_rows, box_rows);
@@ -379,7 +392,7 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     fad::DecodeParams p;
     std::memset(&p, 0, sizeof p);
     p.tm_k = h->k_map.map;
-    if (!(latent && g.func != h->geo.func)) p.tm_v = h->v_map.map;
+    if (!use_latent) p.tm_v = h->v_map.map;
     p.q = static_cast<const uint16_t*>(q);
     p.page_table = page_table;
     p.seq_lens = seq_lens;

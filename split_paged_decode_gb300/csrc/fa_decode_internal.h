@@ -64,4 +64,9 @@ struct KernelGeometry {
 // variant exists for (qk, ov, latent, rows_capacity).
 bool simt_geometry(int qk_depth, int ov_depth, bool latent, int rows_capacity, KernelGeometry* g);
 
+// Kernel variants of the tcgen05 path (head dim 128, <= 16 rows per CTA) with
+// a ring of `nslot` 32 KB K/V tile slots.
+bool tc_geometry(int qk_depth, int ov_depth, int rows, int nslot, KernelGeometry* g);
+constexpr int kTcSlots = 3;
+
 }  // namespace fad

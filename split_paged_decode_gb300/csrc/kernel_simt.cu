@@ -220,8 +220,9 @@ __global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREA
         for (int i = 0; i < tile_count; ++i) {
             const int s = i % STAGES;
             mbar_wait(full_bar + 8 * s, (i / STAGES) & 1, abort_flag, p.status, p.wait_limit_ns);
-            named_barrier_sync(1, C::NCT);  // also: previous tile's P V reads are done
-            if (*abort_flag) break;         // uniform: read after the barrier
+            // Also orders the previous tile's P V reads before this tile's S writes.
+            // The abort decision is reduced over the compute threads, so it is uniform.
+            if (named_barrier_or(1, C::NCT, *abort_flag != 0)) break;
             if (tid == 0) *consumed_s = i + 1;
             const uint8_t* kt = smem + s * C::STAGE_BYTES;
             const uint8_t* vt = LATENT ? kt : kt + C::K_BYTES;
@@ -314,8 +315,9 @@ __global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREA
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[k][ch][e] *= a;
             }
+            const int j_end = min(BN, L - key0);  // rows past L_b never enter P V
 #pragma unroll 2
-            for (int j = 0; j < BN; ++j) {
+            for (int j = 0; j < j_end; ++j) {
                 float pr[C::PV_ROWS];
 #pragma unroll
                 for (int k = 0; k < C::PV_ROWS; ++k) {

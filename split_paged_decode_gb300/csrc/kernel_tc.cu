@@ -1,0 +1,505 @@
+// kernel_tc.cu -- the tcgen05 (5th-generation tensor core) decode kernel for
+// GQA rows of head dimension 128 (sm_103a).
+//
+// The T*g <= 16 query rows of one kv head are too few to fill an MMA M
+// dimension, so both products are issued transposed, with the keys (resp.
+// the value columns) on M = 128 and the query rows on N = 16:
+//   S^T [128 keys x 16 rows]  = K_tile [128 x 128] . Q^T          (A, B K-major)
+//   O^T [128 dv x 16 rows]    = V_tile^T [128 dv x 128 keys] . P^T (A MN-major)
+// with fp32 accumulators in tensor memory. This keeps the tile dense on the
+// tensor pipe while HBM stays the bound.
+//
+// Warp roles (one CTA = one cluster rank of one (sequence, kv head)):
+//   warp 0     load: page-table walk, TMA loads of 128-key K and V tiles
+//              (two 64-column 128-byte-swizzled boxes each) into a ring of
+//              NSLOT 32 KB slots, items in the order K0 V0 K1 V1 ...
+//   warp 1     MMA: allocates 64 TMEM columns (S x2, O x2), issues
+//              S_i = K_i Q^T, then O_{i-1} = V_{i-1}^T P_{i-1}^T, committing
+//              to mbarriers; the slot of a tile is released by the commit of
+//              the MMA that read it.
+//   warps 2-5  softmax + correction (thread = TMEM lane = key for S, = value
+//              column for O): online softmax in exp2 form with the running
+//              max in raw score units, P^T to shared memory as bf16, and the
+//              correction O <- O * alpha + O_tile in registers; then the
+//              split-K epilogue (splitk_combine.cuh).
+//
+// Geometry and vocabulary follow the FA4Config page (Modular MAX docs):
+// TMEM_S / TMEM_O / TMEM_P column maps, num_kv_stages, GQA fusion (field
+// group), split-K clusters (splitk_partitions, with_splitk); the TMEM
+// visibility rule of the fa4_lse_combine_write page (wait for the MMA's
+// barrier, then tcgen05.fence::after_thread_sync, before reading TMEM) is
+// applied to every TMEM read.
+#include "fa_decode_internal.h"
+#include "splitk_combine.cuh"
+#include "tcgen05.cuh"
+
+namespace fad {
+
+template <int NSLOT>
+struct TcCfg {
+    static constexpr int D = 128;       // qk_depth == ov_depth
+    static constexpr int BN = 128;      // keys per tile (M of S^T)
+    static constexpr int NR = 16;       // padded query rows (N of both MMAs)
+    static constexpr int THREADS = 192;
+    static constexpr int WG0 = 2;       // first softmax warp
+    static constexpr int TILE_BYTES = BN * D * 2;        // 32 KB: one K or V tile
+    static constexpr int BOX_BYTES = BN * 128;           // one 64-column box of a tile
+    static constexpr int Q_BYTES = NR * D * 2;           // 4 KB
+    static constexpr int P_BYTES = NR * BN * 2;          // 4 KB
+    static constexpr int TMEM_COLS = 64;
+    static constexpr int TMEM_S0 = 0, TMEM_O0 = 32;      // S[2] at 0/16, O[2] at 32/48
+
+    static constexpr int OFF_RING = 0;                            // NSLOT x 32 KB
+    static constexpr int OFF_Q = NSLOT * TILE_BYTES;              // K-major SW128 [2 boxes][16][128 B]
+    static constexpr int OFF_P = OFF_Q + Q_BYTES;                 // [2 buffers][2 atoms][16][128 B]
+    static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;           // float [2][4][16]
+    static constexpr int OFF_MAXSUM = OFF_RED + 2 * 4 * NR * 4;   // float2 [16]
+    static constexpr int OFF_BAR = OFF_MAXSUM + NR * 8;
+    // barriers: slot_full[NSLOT], slot_empty[NSLOT], s_full[2], s_empty[2],
+    // p_full[2], p_empty[2], o_full[2], o_empty[2], q_full, publish, mma_done
+    static constexpr int NBAR = 2 * NSLOT + 15;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;          // tmem base, abort, consumed
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    // The epilogue reuses the drained ring: f32 stage [P][16][BW] in slot 0,
+    // the bf16 output band in slot 1.
+    static constexpr int OFF_STAGE = 0;
+    static constexpr int OFF_OUT = TILE_BYTES;
+    static_assert(NSLOT >= 2, "ring of at least one K and one V tile");
+    static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms on 1024 bytes");
+};
+
+template <int NSLOT>
+__global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(const __grid_constant__ DecodeParams p)
+{
+    using C = TcCfg<NSLOT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int P = p.splitk;
+    const int rank = (int)blockIdx.x;
+    const int kvh = (int)blockIdx.y;
+    const int b = (int)blockIdx.z;
+
+    int L = p.seq_lens[b];
+    if (L < 0) {
+        if (tid == 0 && rank == 0) atomicOr(p.status, FA_STATUS_BAD_PAGE);
+        L = 0;
+    }
+    if (p.auto_split && auto_split_for_len(L) != P) return;  // uniform across the cluster
+
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    const uint32_t slot_full = bar0, slot_empty = bar0 + 8 * NSLOT;
+    const uint32_t s_full = bar0 + 16 * NSLOT, s_empty = s_full + 16, p_full = s_full + 32, p_empty = s_full + 48;
+    const uint32_t o_full = s_full + 64, o_empty = s_full + 80, q_full = s_full + 96, publish_bar = s_full + 104;
+    const uint32_t mma_done = s_full + 112;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    volatile int* consumed_s = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+    float* red_s = reinterpret_cast<float*>(smem + C::OFF_RED);
+    float2* maxsum_s = reinterpret_cast<float2*>(smem + C::OFF_MAXSUM);
+
+    if (tid == 0) {
+        for (int s = 0; s < NSLOT; ++s) {
+            mbar_init(slot_full + 8 * s, 1);
+            mbar_init(slot_empty + 8 * s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full + 8 * i, 1);
+            mbar_init(s_empty + 8 * i, 4);
+            mbar_init(p_full + 8 * i, 4);
+            mbar_init(p_empty + 8 * i, 1);
+            mbar_init(o_full + 8 * i, 1);
+            mbar_init(o_empty + 8 * i, 4);
+        }
+        mbar_init(q_full, 1);
+        mbar_init(publish_bar, P);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        *consumed_s = 0;
+        fence_mbarrier_init_cluster();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&p.tm_k);
+        tma_prefetch_map(&p.tm_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + C::OFF_MISC, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    if (P > 1) cluster_sync_all();
+
+    const int n_tiles = (L + C::BN - 1) / C::BN;
+    const int base = n_tiles / P, rem = n_tiles % P;
+    const int tile_begin = rank * base + min(rank, rem);
+    const int tile_count = base + (rank < rem ? 1 : 0);
+    const int n_items = 2 * tile_count;
+
+    // Softmax / correction state (warps 2-5).
+    float m_run[C::NR], l_part[C::NR], o_acc[C::NR];
+#pragma unroll
+    for (int r = 0; r < C::NR; ++r) {
+        m_run[r] = -INFINITY;
+        l_part[r] = 0.f;
+        o_acc[r] = 0.f;
+    }
+
+    int issued = 0;
+    if (warp == 0) {
+        // ------------------------------------------------------------------ load warp
+        if (lane == 0 && !(p.debug_flags & FA_DEBUG_SKIP_LOADS)) {
+            const uint64_t policy = l2_policy_evict_first();
+            const int segs = C::BN / p.box_rows;
+            int32_t rows[16];  // row coordinate of every page segment of the current tile
+            for (int j = 0; j < n_items; ++j) {
+                const int slot = j % NSLOT;
+                if (j >= NSLOT &&
+                    !mbar_wait(slot_empty + 8 * slot, ((j / NSLOT) & 1) ^ 1, abort_flag, p.status, p.wait_limit_ns))
+                    break;
+                const int tile = tile_begin + (j >> 1);
+                if ((j & 1) == 0) {
+                    for (int seg = 0; seg < segs; ++seg) {
+                        const int key = tile * C::BN + seg * p.box_rows;
+                        int32_t row = p.oob_row;
+                        if (key < L) {
+                            const int pslot = key / p.page_size;
+                            const int phys =
+                                pslot < p.max_pages ? p.page_table[(int64_t)b * p.max_pages + pslot] : -1;
+                            if (phys >= 0 && phys < p.num_pages)
+                                row = (phys * p.num_kv_heads + kvh) * p.page_size + key % p.page_size;
+                            else
+                                atomicOr(p.status, FA_STATUS_BAD_PAGE);
+                        }
+                        rows[seg] = row;
+                    }
+                }
+                mbar_arrive_expect_tx(slot_full + 8 * slot, C::TILE_BYTES);
+                issued = j + 1;
+                const CUtensorMap* map = (j & 1) ? &p.tm_v : &p.tm_k;
+                const uint32_t dst = sbase + C::OFF_RING + slot * C::TILE_BYTES;
+                for (int seg = 0; seg < segs; ++seg) {
+                    const uint32_t off = seg * p.box_rows * 128;
+                    tma_load_2d(dst + off, map, 0, rows[seg], slot_full + 8 * slot, policy);
+                    tma_load_2d(dst + C::BOX_BYTES + off, map, 64, rows[seg], slot_full + 8 * slot, policy);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------- MMA warp
+        if (lane == 0) {
+            const uint32_t id_s = umma_idesc_bf16_f32(128, C::NR, false, false);
+            const uint32_t id_pv = umma_idesc_bf16_f32(128, C::NR, true, false);
+            const uint32_t q_addr = sbase + C::OFF_Q;
+            bool ok = mbar_wait(q_full, 0, abort_flag, p.status, p.wait_limit_ns);
+
+            auto issue_pv = [&](int t) -> bool {
+                const int j = 2 * t + 1, slot = j % NSLOT;
+                if (!mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns))
+                    return false;
+                *consumed_s = j + 1;
+                if (!mbar_wait(p_full + 8 * (t & 1), (t >> 1) & 1, abort_flag, p.status, p.wait_limit_ns))
+                    return false;
+                if (t >= 2 &&
+                    !mbar_wait(o_empty + 8 * (t & 1), ((t >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns))
+                    return false;
+                tc_fence_after_sync();
+                const uint32_t v_addr = sbase + C::OFF_RING + slot * C::TILE_BYTES;
+                const uint32_t p_addr = sbase + C::OFF_P + (t & 1) * C::P_BYTES;
+                const uint32_t d = tmem + C::TMEM_O0 + 16 * (t & 1);
+#pragma unroll
+                for (int ks = 0; ks < C::BN / 16; ++ks) {
+                    // A = V^T, MN-major: 64-column atoms one box apart (LBO), 8-key groups 1024 B apart (SBO)
+                    const uint64_t a = umma_smem_desc(v_addr + ks * 2048, C::BOX_BYTES, 1024, kLayoutSwizzle128);
+                    // B = P, K-major: 64-key atoms of 16 rows x 128 B
+                    const uint64_t bd = umma_smem_desc(p_addr + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024,
+                                                       kLayoutSwizzle128);
+                    umma_f16_ss(d, a, bd, id_pv, ks > 0);
+                }
+                umma_commit(o_full + 8 * (t & 1));
+                umma_commit(slot_empty + 8 * slot);
+                umma_commit(p_empty + 8 * (t & 1));
+                return true;
+            };
+
+            for (int i = 0; ok && i < tile_count; ++i) {
+                const int j = 2 * i, slot = j % NSLOT;
+                if (!mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns)) break;
+                *consumed_s = j + 1;
+                if (i >= 2 &&
+                    !mbar_wait(s_empty + 8 * (i & 1), ((i >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns))
+                    break;
+                tc_fence_after_sync();
+                const uint32_t k_addr = sbase + C::OFF_RING + slot * C::TILE_BYTES;
+                const uint32_t d = tmem + C::TMEM_S0 + 16 * (i & 1);
+#pragma unroll
+                for (int ks = 0; ks < C::D / 16; ++ks) {
+                    const uint32_t koff = (ks >> 2) * C::BOX_BYTES + (ks & 3) * 32;
+                    const uint64_t a = umma_smem_desc(k_addr + koff, 16, 1024, kLayoutSwizzle128);
+                    const uint64_t bd = umma_smem_desc(q_addr + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024,
+                                                       kLayoutSwizzle128);
+                    umma_f16_ss(d, a, bd, id_s, ks > 0);
+                }
+                umma_commit(s_full + 8 * (i & 1));
+                umma_commit(slot_empty + 8 * slot);
+                if (i >= 1 && !issue_pv(i - 1)) {
+                    ok = false;
+                    break;
+                }
+                if (i == tile_count - 1 && !issue_pv(i)) ok = false;
+            }
+            // Every MMA issued above has completed once this barrier fires.
+            umma_commit(mma_done);
+            volatile int keep_waiting = 0;
+            mbar_wait(mma_done, 0, &keep_waiting, p.status, p.wait_limit_ns);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------- softmax / correction warps
+        const int wt = tid - 32 * C::WG0;             // 0..127
+        const int quad = warp & 3;                    // TMEM lane quadrant of this warp
+        const int my_lane = 32 * quad + lane;         // key (S) or value column (O) of this thread
+        const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
+        const float c2 = p.scale_log2e;
+
+        // Q rows -> K-major 128-byte-swizzled B operand; rows >= p.rows are zero.
+        for (int idx = wt; idx < C::NR * 16; idx += 128) {
+            const int r = idx >> 4, u = idx & 15;  // 16-byte chunk u of row r
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r < p.rows) {
+                const int t = r / p.heads_per_cta;
+                const int h = kvh * p.group + r % p.heads_per_cta;
+                v = reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.num_q + t) * p.num_q_heads + h) * C::D)[u];
+            }
+            *reinterpret_cast<uint4*>(smem + C::OFF_Q + (u >> 3) * 2048 + r * 128 + (((u & 7) ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (wt == 0) mbar_arrive(q_full);
+
+        int row_tok[C::NR];  // visible-key bound of every row (0 for padding rows)
+#pragma unroll
+        for (int r = 0; r < C::NR; ++r) row_tok[r] = r < p.rows ? L - p.num_q + r / p.heads_per_cta + 1 : 0;
+
+        float alpha_prev[C::NR];
+        auto correct = [&](int t, const float (&a)[C::NR]) {
+            mbar_wait(o_full + 8 * (t & 1), (t >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+            tc_fence_after_sync();
+            float ot[16];
+            tmem_ld_32x32b_x16(tmem + lane_addr + C::TMEM_O0 + 16 * (t & 1), ot);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_empty + 8 * (t & 1));
+#pragma unroll
+            for (int r = 0; r < C::NR; ++r) o_acc[r] = fmaf(o_acc[r], a[r], ot[r]);
+        };
+
+        for (int i = 0; i < tile_count; ++i) {
+            mbar_wait(s_full + 8 * (i & 1), (i >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+            tc_fence_after_sync();
+            float s[16];
+            tmem_ld_32x32b_x16(tmem + lane_addr + C::TMEM_S0 + 16 * (i & 1), s);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_empty + 8 * (i & 1));
+
+            const int key0 = (tile_begin + i) * C::BN;
+            const int key = key0 + my_lane;
+#pragma unroll
+            for (int r = 0; r < C::NR; ++r) s[r] = key < row_tok[r] ? s[r] : -INFINITY;
+
+            // Per-row max over this warp's 32 keys (reduce-scatter: lane l ends
+            // with row (l >> 1) & 15), then over the four warps in shared memory.
+            {
+                float v8[8], v4[4], v2[2], v1;
+                const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float send = h16 ? s[k] : s[k + 8];
+                    const float keep = h16 ? s[k + 8] : s[k];
+                    v8[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float send = h8 ? v8[k] : v8[k + 4];
+                    const float keep = h8 ? v8[k + 4] : v8[k];
+                    v4[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+                }
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float send = h4 ? v4[k] : v4[k + 2];
+                    const float keep = h4 ? v4[k + 2] : v4[k];
+                    v2[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+                }
+                {
+                    const float send = h2 ? v2[0] : v2[1];
+                    const float keep = h2 ? v2[1] : v2[0];
+                    v1 = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+                }
+                v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, 1));
+                if ((lane & 1) == 0) red_s[((i & 1) * 4 + quad) * C::NR + ((lane >> 1) & 15)] = v1;
+            }
+            // The abort decision is reduced over the warpgroup, so it is uniform.
+            if (named_barrier_or(1, 128, *abort_flag != 0)) break;
+
+            float alpha[C::NR];
+            {
+                const float4* rq = reinterpret_cast<const float4*>(red_s + (i & 1) * 4 * C::NR);
+#pragma unroll
+                for (int r4 = 0; r4 < C::NR / 4; ++r4) {
+                    float4 a0 = rq[r4], a1 = rq[4 + r4], a2 = rq[8 + r4], a3 = rq[12 + r4];
+                    float tm[4] = {fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x)),
+                                   fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y)),
+                                   fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z)),
+                                   fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w))};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = 4 * r4 + e;
+                        const float m_new = fmaxf(m_run[r], tm[e]);
+                        float a = 1.f, pr = 0.f;
+                        if (m_new != -INFINITY) {
+                            a = (m_run[r] == -INFINITY) ? 0.f : ex2_approx((m_run[r] - m_new) * c2);
+                            pr = (s[r] == -INFINITY) ? 0.f : ex2_approx((s[r] - m_new) * c2);
+                        }
+                        alpha[r] = a;
+                        l_part[r] = fmaf(l_part[r], a, pr);
+                        m_run[r] = m_new;
+                        s[r] = pr;
+                    }
+                }
+            }
+
+            // P (bf16) -> K-major swizzled B operand of O^T = V^T P^T
+            if (i >= 2)
+                mbar_wait(p_empty + 8 * (i & 1), ((i >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+            {
+                uint8_t* pb = smem + C::OFF_P + (i & 1) * C::P_BYTES + (my_lane >> 6) * 2048;
+                const int kk = my_lane & 63;
+#pragma unroll
+                for (int r = 0; r < C::NR; ++r)
+                    *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((((kk >> 3) ^ (r & 7))) << 4) + (kk & 7) * 2) =
+                        __float2bfloat16_rn(s[r]);
+            }
+            // Last tile of the sequence: zero the V rows past L so that unused
+            // cache rows (whatever they hold) meet P = 0 as exact zeros.
+            if (key0 + C::BN > L) {
+                const int j = 2 * i + 1, slot = j % NSLOT;
+                mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns);
+                if (key >= L) {
+                    uint4* vrow0 = reinterpret_cast<uint4*>(smem + C::OFF_RING + slot * C::TILE_BYTES + my_lane * 128);
+                    uint4* vrow1 = reinterpret_cast<uint4*>(smem + C::OFF_RING + slot * C::TILE_BYTES +
+                                                            C::BOX_BYTES + my_lane * 128);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        vrow0[u] = make_uint4(0, 0, 0, 0);
+                        vrow1[u] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full + 8 * (i & 1));
+
+            if (i >= 1) correct(i - 1, alpha_prev);
+#pragma unroll
+            for (int r = 0; r < C::NR; ++r) alpha_prev[r] = alpha[r];
+        }
+        if (tile_count > 0) correct(tile_count - 1, alpha_prev);  // bounded even after an abort
+        tc_fence_before_sync();
+    }
+
+    // All TMEM reads and MMAs are complete (the MMA lane waited for mma_done).
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        volatile int keep_waiting = 0;
+        for (int j = *consumed_s; j < issued; ++j)
+            mbar_wait(slot_full + 8 * (j % NSLOT), (j / NSLOT) & 1, &keep_waiting, p.status, p.wait_limit_ns);
+    }
+
+    if (warp >= C::WG0) {
+        const int wt = tid - 32 * C::WG0;
+        const int quad = warp & 3;
+        const int dv = 32 * quad + lane;
+        // Row sums: per-thread partial sums -> warp reduce-scatter -> four warps.
+        {
+            float v8[8], v4[4], v2[2], v1;
+            const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float send = h16 ? l_part[k] : l_part[k + 8];
+                const float keep = h16 ? l_part[k + 8] : l_part[k];
+                v8[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float send = h8 ? v8[k] : v8[k + 4];
+                const float keep = h8 ? v8[k + 4] : v8[k];
+                v4[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float send = h4 ? v4[k] : v4[k + 2];
+                const float keep = h4 ? v4[k + 2] : v4[k];
+                v2[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+            }
+            {
+                const float send = h2 ? v2[0] : v2[1];
+                const float keep = h2 ? v2[1] : v2[0];
+                v1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+            }
+            v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+            named_barrier_sync(1, 128);  // red_s may still be read by the last tile's max step
+            if ((lane & 1) == 0) red_s[quad * C::NR + ((lane >> 1) & 15)] = v1;
+            named_barrier_sync(1, 128);
+        }
+        float* stage_s = reinterpret_cast<float*>(smem + C::OFF_STAGE);
+        const int BW = p.band_cols;
+        const int q = dv / BW, j = dv % BW;
+#pragma unroll
+        for (int r = 0; r < C::NR; ++r) {
+            const float l = red_s[r] + red_s[C::NR + r] + red_s[2 * C::NR + r] + red_s[3 * C::NR + r];
+            if (wt == 0) maxsum_s[r] = make_float2(m_run[r], l);
+            stage_s[(q * C::NR + r) * BW + j] = l > 0.f ? o_acc[r] / l : 0.f;
+        }
+        named_barrier_sync(1, 128);
+        splitk_merge_and_store<C::NR>(p, P, rank, b, kvh, 0, stage_s, maxsum_s,
+                                      reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), publish_bar, abort_flag, wt,
+                                      128, 1);
+    }
+    __syncwarp();
+    if (P > 1) cluster_sync_all();  // peers may still read this CTA's staged bands until here
+}
+
+bool tc_geometry(int qk, int ov, int rows, int nslot, KernelGeometry* g)
+{
+    if (qk != 128 || ov != 128 || rows > 16) return false;
+#define FAD_TC(NS)                                                                        \
+    if (nslot == NS) {                                                                    \
+        g->func = reinterpret_cast<const void*>(&tc_decode_kernel<NS>);                   \
+        g->threads = TcCfg<NS>::THREADS;                                                  \
+        g->keys_per_tile = TcCfg<NS>::BN;                                                 \
+        g->stages = NS;                                                                   \
+        g->rows_capacity = TcCfg<NS>::NR;                                                 \
+        g->smem_bytes = TcCfg<NS>::SMEM_BYTES;                                            \
+        g->name = "tc_d128_bn128_n16_slots" #NS;                                          \
+        return true;                                                                      \
+    }
+    FAD_TC(2)
+    FAD_TC(3)
+    FAD_TC(4)
+    FAD_TC(6)
+#undef FAD_TC
+    return false;
+}
+
+}  // namespace fad

@@ -32,7 +32,7 @@ def run_oracle(inp: DecodeInputs, rows=None):
 class DeviceCall:
     """Device copies of one input set plus a handle, for repeated runs."""
 
-    def __init__(self, inp: DecodeInputs, splitk: int | None = None, device="cuda"):
+    def __init__(self, inp: DecodeInputs, splitk: int | None = None, device="cuda", path: str = "auto"):
         w = inp.workload
         self.inp = inp
         self.q = inp.q.to(device)
@@ -47,6 +47,11 @@ class DeviceCall:
         P = w.splitk if splitk is None else splitk
         self.h = spd.fa_decode_create(w.num_q_heads, w.num_kv_heads, w.qk_depth, w.nope_depth,
                                       w.ov_depth, w.page_size, w.num_q, P)
+        if path == "simt":
+            spd.fa_decode_set_debug(self.h, spd.FA_DEBUG_FORCE_SIMT, 0)
+
+    def describe(self) -> str:
+        return spd.fa_decode_describe(self.h)
 
     def run(self, stream=None):
         spd.fa_decode_run(self.h, self.q, self.k, self.v, self.pt, self.lens, self.inp.scale, self.out,

@@ -33,9 +33,9 @@ def wl(**kw):
     return DecodeWorkload(**base)
 
 
-def run_and_check(w, seq_lens=None, rows=None, what=None):
+def run_and_check(w, seq_lens=None, rows=None, what=None, path="auto"):
     inp = generate(w, seq_lens=seq_lens)
-    with DeviceCall(inp) as call:
+    with DeviceCall(inp, path=path) as call:
         call.run()
         assert call.status() == 0
         check_against_oracle(call, rows=rows, what=what or w.name)
@@ -44,19 +44,34 @@ def run_and_check(w, seq_lens=None, rows=None, what=None):
 
 # --- small shapes: several tiles, ragged tails, empty partitions -----------------------
 
+PATHS = ["auto", "simt"]  # auto takes the tcgen05 kernel for head dim 128 and <= 16 rows
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
-def test_gqa_d128_splits(P):
-    run_and_check(wl(splitk=P, seed=10 + P), what=f"d128 P{P}")
+def test_gqa_d128_splits(P, path):
+    run_and_check(wl(splitk=P, seed=10 + P), what=f"d128 P{P} {path}", path=path)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("ps", [8, 16, 32, 64, 128, 256])
-def test_page_sizes(ps):
-    run_and_check(wl(page_size=ps, splitk=4, seed=20), what=f"ps{ps}")
+def test_page_sizes(ps, path):
+    run_and_check(wl(page_size=ps, splitk=4, seed=20), what=f"ps{ps} {path}", path=path)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("g,T", [(1, 1), (2, 1), (4, 1), (8, 1), (16, 1), (4, 2), (4, 4), (2, 8), (1, 16)])
-def test_rows_per_cta(g, T):
-    run_and_check(wl(num_q_heads=2 * g, num_kv_heads=2, num_q=T, seed=30 + g * T), what=f"g{g} T{T}")
+def test_rows_per_cta(g, T, path):
+    run_and_check(wl(num_q_heads=2 * g, num_kv_heads=2, num_q=T, seed=30 + g * T), what=f"g{g} T{T} {path}",
+                  path=path)
+
+
+def test_tensor_core_path_is_selected():
+    inp = generate(wl(seed=9))
+    with DeviceCall(inp) as call:
+        assert call.describe().startswith("path=tcgen05"), call.describe()
+    with DeviceCall(generate(wl(qk_depth=64, ov_depth=64, seed=9))) as call:
+        assert call.describe().startswith("path=simt"), call.describe()
 
 
 @pytest.mark.parametrize("P", [1, 2, 4, 8])
@@ -89,21 +104,40 @@ def test_v_equal_k_pointer_means_v_is_k_prefix():
         check_against_oracle(call, what="v is k")
 
 
-def test_causal_short_sequences_and_empty():
+@pytest.mark.parametrize("path", PATHS)
+def test_causal_short_sequences_and_empty(path):
     """Lengths 0, 1, below num_q and at tile edges; rows with no visible key give 0 / -inf."""
-    w = wl(num_q=4, num_q_heads=8, num_kv_heads=2, batch=8, splitk=4, seed=60)
-    run_and_check(w, seq_lens=[0, 1, 2, 3, 4, 63, 64, 65], what="short/empty")
+    w = wl(num_q=4, num_q_heads=8, num_kv_heads=2, batch=10, splitk=4, seed=60)
+    run_and_check(w, seq_lens=[0, 1, 2, 3, 4, 63, 64, 65, 127, 129], what=f"short/empty {path}", path=path)
 
 
-def test_ragged_auto_split():
+@pytest.mark.parametrize("path", PATHS)
+def test_ragged_auto_split(path):
     w = wl(batch=12, num_q=4, splitk=0, seq_len_lo=1, seq_len_hi=9000, page_size=64, seed=61)
     run_and_check(w, seq_lens=[1, 5, 1024, 1025, 4096, 4097, 8192, 9000, 64, 65, 2000, 3000],
-                  what="auto split")
+                  what=f"auto split {path}", path=path)
 
 
-def test_more_tiles_than_ranks_and_fewer():
+@pytest.mark.parametrize("path", PATHS)
+def test_more_tiles_than_ranks_and_fewer(path):
     w = wl(batch=4, splitk=8, seed=62)
-    run_and_check(w, seq_lens=[64, 65, 64 * 8 + 1, 64 * 17 - 3], what="tiles vs ranks")
+    run_and_check(w, seq_lens=[64, 65, 128 * 8 + 1, 128 * 17 - 3], what=f"tiles vs ranks {path}", path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_nonfinite_rows_past_the_sequence_do_not_leak(path):
+    """Rows past L_b in a sequence's last page may hold anything (here NaN / inf):
+    they must not reach the output."""
+    w = wl(batch=3, splitk=2, page_size=64, seed=63)
+    inp = generate(w, seq_lens=[70, 200, 129])
+    for b, L in enumerate([70, 200, 129]):
+        last = int(inp.page_table[b, (L - 1) // 64])
+        inp.k_pages[last, :, L % 64:, :] = float("nan")
+        inp.v_pages[last, :, L % 64:, :] = float("inf")
+    with DeviceCall(inp, path=path) as call:
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what=f"non-finite tails {path}")
 
 
 # --- the five workloads at full size -----------------------------------------------------
@@ -116,11 +150,19 @@ def _sample_rows(w, n, seed):
 
 @pytest.mark.parametrize("name", ["tiny", "batched_gqa", "long_context", "ragged_speculative", "mla"])
 def test_workload_full_size(name):
+    """Each workload at full size in the launch configuration the benchmark times."""
     w = WORKLOADS[name]
     rows = None
     if name in ("ragged_speculative", "mla"):
         rows = _sample_rows(w, 512, 7)
     run_and_check(w, rows=rows, what=name)
+
+
+@pytest.mark.parametrize("name", ["batched_gqa", "long_context", "ragged_speculative"])
+def test_workload_full_size_simt(name):
+    w = WORKLOADS[name]
+    rows = None if name != "ragged_speculative" else _sample_rows(w, 512, 8)
+    run_and_check(w, rows=rows, what=f"{name} simt", path="simt")
 
 
 # --- bit-exact properties ----------------------------------------------------------------
