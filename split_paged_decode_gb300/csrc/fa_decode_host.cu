@@ -127,8 +127,10 @@ struct fa_decode {
     int device;
     fad::KernelGeometry geo;         // SIMT kernel, separate V cache (or V = K rows)
     fad::KernelGeometry geo_latent;  // SIMT kernel, V = prefix of the K row
-    fad::KernelGeometry geo_tc;      // tcgen05 kernel
+    fad::KernelGeometry geo_tc;      // tcgen05 kernel, 3-slot ring (two CTAs per SM)
+    fad::KernelGeometry geo_tc_big;  // tcgen05 kernel, 6-slot ring (one CTA per SM)
     bool has_simt, has_latent, has_tc;
+    int sm_count;
     unsigned int* d_status;
     uint32_t debug_flags;
     uint64_t wait_limit_ns;
@@ -246,7 +248,9 @@ int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk
                    page_fits(tmp.geo.keys_per_tile);
     tmp.has_latent = tmp.has_simt && fad::simt_geometry(qk_depth, ov_depth, true, tmp.rows_capacity,
                                                         &tmp.geo_latent);
-    tmp.has_tc = tmp.row_blocks == 1 && fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlots, &tmp.geo_tc) &&
+    tmp.has_tc = tmp.row_blocks == 1 &&
+                 fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsShared, &tmp.geo_tc) &&
+                 fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsAlone, &tmp.geo_tc_big) &&
                  page_fits(tmp.geo_tc.keys_per_tile);
     if (!tmp.has_simt && !tmp.has_tc)
         return fail(FA_ERR_UNSUPPORTED, "no kernel for (qk %d, ov %d), %d rows per CTA and page_size %d "
@@ -276,6 +280,8 @@ int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk
     if (tmp.has_simt && (rc = prepare_kernel(&tmp, tmp.geo))) return rc;
     if (tmp.has_latent && (rc = prepare_kernel(&tmp, tmp.geo_latent))) return rc;
     if (tmp.has_tc && (rc = prepare_kernel(&tmp, tmp.geo_tc))) return rc;
+    if (tmp.has_tc && (rc = prepare_kernel(&tmp, tmp.geo_tc_big))) return rc;
+    cudaDeviceGetAttribute(&tmp.sm_count, cudaDevAttrMultiProcessorCount, dev);
 
     e = cudaMalloc(&tmp.d_status, 256);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status word)");
@@ -375,7 +381,12 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     const bool use_tc = !use_latent && h->has_tc && !(h->debug_flags & FA_DEBUG_FORCE_SIMT && h->has_simt);
     if (!use_latent && !use_tc && !h->has_simt)
         return fail(FA_ERR_UNSUPPORTED, "no kernel for this call (latent layout %d)", (int)latent);
-    const fad::KernelGeometry& g = use_latent ? h->geo_latent : (use_tc ? h->geo_tc : h->geo);
+    // A grid that fits in one wave gets the deep ring (one CTA per SM); more
+    // CTAs than SMs share SMs two by two with the shallow ring.
+    const int64_t ctas = (int64_t)(h->splitk > 0 ? h->splitk : 4) * h->hkv * h->row_blocks * batch;
+    const bool tc_big = use_tc && h->splitk > 0 && ctas <= h->sm_count;
+    const fad::KernelGeometry& g =
+        use_latent ? h->geo_latent : (use_tc ? (tc_big ? h->geo_tc_big : h->geo_tc) : h->geo);
     const int bn = g.keys_per_tile;
     const int box_rows = h->page_size < bn ? h->page_size : bn;
 

@@ -67,6 +67,7 @@ bool simt_geometry(int qk_depth, int ov_depth, bool latent, int rows_capacity, K
 // Kernel variants of the tcgen05 path (head dim 128, <= 16 rows per CTA) with
 // a ring of `nslot` 32 KB K/V tile slots.
 bool tc_geometry(int qk_depth, int ov_depth, int rows, int nslot, KernelGeometry* g);
-constexpr int kTcSlots = 3;
+constexpr int kTcSlotsShared = 3;  // two CTAs per SM (grids of more than one wave)
+constexpr int kTcSlotsAlone = 6;   // one CTA per SM, 192 KB of loads in flight
 
 }  // namespace fad

@@ -10,9 +10,11 @@
 // tensor pipe while HBM stays the bound.
 //
 // Warp roles (one CTA = one cluster rank of one (sequence, kv head)):
-//   warp 0     load: page-table walk, TMA loads of 128-key K and V tiles
-//              (two 64-column 128-byte-swizzled boxes each) into a ring of
-//              NSLOT 32 KB slots, items in the order K0 V0 K1 V1 ...
+//   warp 0     load: page-table walk (entries fetched three tiles ahead),
+//              TMA loads of 128-key K and V tiles (two 64-column
+//              128-byte-swizzled boxes per page segment, one lane per
+//              segment) into a ring of NSLOT 32 KB slots, in the order the
+//              MMA warp consumes them: K0 K1 V0 K2 V1 ... K_{n-1} V_{n-2} V_{n-1}
 //   warp 1     MMA: allocates 64 TMEM columns (S x2, O x2), issues
 //              S_i = K_i Q^T, then O_{i-1} = V_{i-1}^T P_{i-1}^T, committing
 //              to mbarriers; the slot of a tile is released by the commit of
@@ -58,7 +60,8 @@ struct TcCfg {
     // barriers: slot_full[NSLOT], slot_empty[NSLOT], s_full[2], s_empty[2],
     // p_full[2], p_empty[2], o_full[2], o_empty[2], q_full, publish, mma_done
     static constexpr int NBAR = 2 * NSLOT + 15;
-    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;          // tmem base, abort, consumed
+    static constexpr int OFF_ROWS = OFF_BAR + NBAR * 8;          // int [4 tiles][16 segments]
+    static constexpr int OFF_MISC = OFF_ROWS + 4 * 16 * 4;       // tmem base, abort, consumed
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     // The epilogue reuses the drained ring: f32 stage [P][16][BW] in slot 0,
     // the bf16 output band in slot 1.
@@ -67,6 +70,10 @@ struct TcCfg {
     static_assert(NSLOT >= 2, "ring of at least one K and one V tile");
     static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms on 1024 bytes");
 };
+
+// Position of tile i's K and V in the load sequence K0 K1 V0 K2 V1 ... V_{n-1}.
+__device__ __forceinline__ int k_item(int i) { return i == 0 ? 0 : 2 * i - 1; }
+__device__ __forceinline__ int v_item(int i, int n) { return i == n - 1 ? 2 * n - 1 : 2 * i + 2; }
 
 template <int NSLOT>
 __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(const __grid_constant__ DecodeParams p)
@@ -98,7 +105,6 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
     const uint32_t mma_done = s_full + 112;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-    volatile int* consumed_s = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
     float* red_s = reinterpret_cast<float*>(smem + C::OFF_RED);
     float2* maxsum_s = reinterpret_cast<float2*>(smem + C::OFF_MAXSUM);
 
@@ -119,7 +125,6 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
         mbar_init(publish_bar, P);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
-        *consumed_s = 0;
         fence_mbarrier_init_cluster();
     }
     if (warp == 0 && lane == 0) {
@@ -154,40 +159,56 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
     int issued = 0;
     if (warp == 0) {
         // ------------------------------------------------------------------ load warp
-        if (lane == 0 && !(p.debug_flags & FA_DEBUG_SKIP_LOADS)) {
+        // All 32 lanes run the loop; lane s owns page segment s of every tile.
+        if (!(p.debug_flags & FA_DEBUG_SKIP_LOADS)) {
             const uint64_t policy = l2_policy_evict_first();
-            const int segs = C::BN / p.box_rows;
-            int32_t rows[16];  // row coordinate of every page segment of the current tile
+            const int segs = C::BN / p.box_rows;  // <= 16
+            int32_t* rows_s = reinterpret_cast<int32_t*>(smem + C::OFF_ROWS);
+            // Physical page of this lane's segment of tile t, or kNoSegment /
+            // kPastSequence (zero fill, no error); -1 past the page table.
+            constexpr int kNoSegment = INT32_MIN, kPastSequence = INT32_MIN + 1;
+            auto page_of = [&](int t) -> int {
+                if (lane >= segs || t >= tile_count) return kNoSegment;
+                const int key = (tile_begin + t) * C::BN + lane * p.box_rows;
+                if (key >= L) return kPastSequence;
+                const int pslot = key / p.page_size;
+                if (pslot >= p.max_pages) return -1;
+                return p.page_table[(int64_t)b * p.max_pages + pslot];
+            };
+            int e0 = page_of(0), e1 = page_of(1), e2 = page_of(2);  // three tiles ahead
             for (int j = 0; j < n_items; ++j) {
                 const int slot = j % NSLOT;
-                if (j >= NSLOT &&
-                    !mbar_wait(slot_empty + 8 * slot, ((j / NSLOT) & 1) ^ 1, abort_flag, p.status, p.wait_limit_ns))
-                    break;
-                const int tile = tile_begin + (j >> 1);
-                if ((j & 1) == 0) {
-                    for (int seg = 0; seg < segs; ++seg) {
-                        const int key = tile * C::BN + seg * p.box_rows;
-                        int32_t row = p.oob_row;
-                        if (key < L) {
-                            const int pslot = key / p.page_size;
-                            const int phys =
-                                pslot < p.max_pages ? p.page_table[(int64_t)b * p.max_pages + pslot] : -1;
-                            if (phys >= 0 && phys < p.num_pages)
-                                row = (phys * p.num_kv_heads + kvh) * p.page_size + key % p.page_size;
-                            else
-                                atomicOr(p.status, FA_STATUS_BAD_PAGE);
-                        }
-                        rows[seg] = row;
-                    }
+                const bool is_v = (j == n_items - 1) || (j > 0 && (j & 1) == 0);
+                const int t = is_v ? (j == n_items - 1 ? tile_count - 1 : (j - 2) >> 1) : (j + 1) >> 1;
+                if (j >= NSLOT) {
+                    const bool ok = mbar_wait(slot_empty + 8 * slot, ((j / NSLOT) & 1) ^ 1, abort_flag, p.status,
+                                              p.wait_limit_ns);
+                    if (!__all_sync(0xffffffffu, ok)) break;
                 }
-                mbar_arrive_expect_tx(slot_full + 8 * slot, C::TILE_BYTES);
+                int32_t row;
+                if (!is_v) {
+                    row = p.oob_row;  // zero fill past the sequence or on a bad page
+                    if (e0 >= 0 && e0 < p.num_pages) {
+                        const int key = (tile_begin + t) * C::BN + lane * p.box_rows;
+                        row = (e0 * p.num_kv_heads + kvh) * p.page_size + key % p.page_size;
+                    } else if (e0 != kNoSegment && e0 != kPastSequence) {
+                        atomicOr(p.status, FA_STATUS_BAD_PAGE);
+                    }
+                    if (lane < 16) rows_s[(t & 3) * 16 + lane] = row;
+                    e0 = e1;
+                    e1 = e2;
+                    e2 = page_of(t + 3);
+                } else {
+                    row = lane < 16 ? rows_s[(t & 3) * 16 + lane] : p.oob_row;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(slot_full + 8 * slot, C::TILE_BYTES);
+                __syncwarp();
                 issued = j + 1;
-                const CUtensorMap* map = (j & 1) ? &p.tm_v : &p.tm_k;
-                const uint32_t dst = sbase + C::OFF_RING + slot * C::TILE_BYTES;
-                for (int seg = 0; seg < segs; ++seg) {
-                    const uint32_t off = seg * p.box_rows * 128;
-                    tma_load_2d(dst + off, map, 0, rows[seg], slot_full + 8 * slot, policy);
-                    tma_load_2d(dst + C::BOX_BYTES + off, map, 64, rows[seg], slot_full + 8 * slot, policy);
+                if (lane < segs) {
+                    const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
+                    const uint32_t dst = sbase + C::OFF_RING + slot * C::TILE_BYTES + lane * p.box_rows * 128;
+                    tma_load_2d(dst, map, 0, row, slot_full + 8 * slot, policy);
+                    tma_load_2d(dst + C::BOX_BYTES, map, 64, row, slot_full + 8 * slot, policy);
                 }
             }
         }
@@ -200,10 +221,9 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
             bool ok = mbar_wait(q_full, 0, abort_flag, p.status, p.wait_limit_ns);
 
             auto issue_pv = [&](int t) -> bool {
-                const int j = 2 * t + 1, slot = j % NSLOT;
+                const int j = v_item(t, tile_count), slot = j % NSLOT;
                 if (!mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns))
                     return false;
-                *consumed_s = j + 1;
                 if (!mbar_wait(p_full + 8 * (t & 1), (t >> 1) & 1, abort_flag, p.status, p.wait_limit_ns))
                     return false;
                 if (t >= 2 &&
@@ -229,9 +249,8 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
             };
 
             for (int i = 0; ok && i < tile_count; ++i) {
-                const int j = 2 * i, slot = j % NSLOT;
+                const int j = k_item(i), slot = j % NSLOT;
                 if (!mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns)) break;
-                *consumed_s = j + 1;
                 if (i >= 2 &&
                     !mbar_wait(s_empty + 8 * (i & 1), ((i >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns))
                     break;
@@ -389,7 +408,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
             // Last tile of the sequence: zero the V rows past L so that unused
             // cache rows (whatever they hold) meet P = 0 as exact zeros.
             if (key0 + C::BN > L) {
-                const int j = 2 * i + 1, slot = j % NSLOT;
+                const int j = v_item(i, tile_count), slot = j % NSLOT;
                 mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns);
                 if (key >= L) {
                     uint4* vrow0 = reinterpret_cast<uint4*>(smem + C::OFF_RING + slot * C::TILE_BYTES + my_lane * 128);
@@ -421,8 +440,10 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
     if (warp == 0 && lane == 0 && *abort_flag) {
+        // Gave up early: wait (bounded) until the copies of the last NSLOT
+        // issued items have landed, so none is in flight when the CTA exits.
         volatile int keep_waiting = 0;
-        for (int j = *consumed_s; j < issued; ++j)
+        for (int j = issued > NSLOT ? issued - NSLOT : 0; j < issued; ++j)
             mbar_wait(slot_full + 8 * (j % NSLOT), (j / NSLOT) & 1, &keep_waiting, p.status, p.wait_limit_ns);
     }
 
