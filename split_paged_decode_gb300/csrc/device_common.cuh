@@ -168,8 +168,10 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
+// barrier.cluster.*.aligned: all lanes of the warp together (reconverge first).
 __device__ __forceinline__ void cluster_sync_all()
 {
+    __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -205,8 +207,10 @@ __device__ __forceinline__ float2 ld_dsmem_f2(uint32_t cluster_addr)
 // ---------------------------------------------------------------------------
 // Named barriers over a subset of warps (id 0 is __syncthreads).
 // ---------------------------------------------------------------------------
+// bar.sync is the .aligned form: reconverge the warp first.
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads)
 {
+    __syncwarp();
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 

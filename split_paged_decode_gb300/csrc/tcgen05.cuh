@@ -65,21 +65,28 @@ __device__ __forceinline__ void umma_commit(uint32_t mbar)
                  : "memory");
 }
 
+// The .sync.aligned instructions below must be executed by all 32 lanes of a
+// warp together; every wrapper first reconverges the warp (__syncwarp), since
+// a preceding polling loop or a lane-specific branch may have left it diverged.
+
 // Allocate `ncols` TMEM columns (power of two >= 32); the base address is
 // written to shared memory at `dst`. Executed by one whole warp.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols)
 {
+    __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
                  : "memory");
 }
 
 __device__ __forceinline__ void tmem_relinquish()
 {
+    __syncwarp();
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 {
+    __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
@@ -93,6 +100,7 @@ __device__ __forceinline__ void tc_fence_after_sync() { asm volatile("tcgen05.fe
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, float (&v)[16])
 {
     uint32_t r[16];
+    __syncwarp();
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
