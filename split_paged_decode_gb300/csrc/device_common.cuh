@@ -176,6 +176,21 @@ __device__ __forceinline__ void cluster_sync_all()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Split cluster barrier: arrive early (relaxed: orders nothing but this
+// thread's earlier fence.mbarrier_init), wait later (acquire). Every thread
+// of every CTA in the cluster arrives once before anyone's wait returns.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // Address of the same shared-memory variable in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t map_shared_rank(uint32_t local, uint32_t rank)
 {

@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREA
         }
     }
     __syncthreads();
-    if (P > 1) cluster_sync_all();  // every rank's publish barrier is initialised
+    if (P > 1) cluster_arrive_relaxed();  // waited before the merge publishes to peers
 
     // This rank's share of the key tiles: whole BN-key tiles split evenly,
     // the remainder going to the low ranks (an empty share is allowed).
@@ -357,7 +357,8 @@ __global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREA
             const int r = pv_row0 + C::PV_ROW_LANES * k;
             if (r >= RB) continue;
             const float l = maxsum_s[r].y;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float inv = 0.f;
+            if (l > 0.f) inv = __frcp_rn(l);
 #pragma unroll
             for (int ch = 0; ch < C::PV_CHUNKS; ++ch) {
                 const int col = (pv_lane + ch * C::NCT) * 4;
@@ -370,6 +371,7 @@ __global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREA
     }
 
     __syncthreads();  // staging complete (all warps; the load warp is idle here)
+    if (P > 1) cluster_wait();  // every rank's publish barrier is initialised
     if (warp < C::NCW) {
         splitk_merge_and_store<RB>(p, P, rank, b, kvh, row_block, stage_s, maxsum_s, out_s, publish_bar,
                                    abort_flag, tid, C::NCT, 1);

@@ -15,10 +15,10 @@
 //              128-byte-swizzled boxes per page segment, one lane per
 //              segment) into a ring of NSLOT 32 KB slots, in the order the
 //              MMA warp consumes them: K0 K1 V0 K2 V1 ... K_{n-1} V_{n-2} V_{n-1}
-//   warp 1     MMA: allocates 64 TMEM columns (S x2, O x2), issues
-//              S_i = K_i Q^T, then O_{i-1} = V_{i-1}^T P_{i-1}^T, committing
-//              to mbarriers; the slot of a tile is released by the commit of
-//              the MMA that read it.
+//   warp 1     MMA: allocates 256 TMEM columns (S and O, two buffers of four
+//              accumulators each), issues S_i = K_i Q^T, then
+//              O_{i-1} = V_{i-1}^T P_{i-1}^T, committing to mbarriers; the
+//              slot of a tile is released by the commit of the MMA that read it.
 //   warps 2-5  softmax + correction (thread = TMEM lane = key for S, = value
 //              column for O): online softmax in exp2 form with the running
 //              max in raw score units, P^T to shared memory as bf16, and the
@@ -37,29 +37,37 @@
 
 namespace fad {
 
-template <int NSLOT>
+template <int NSLOT, int NRV>
 struct TcCfg {
     static constexpr int D = 128;       // qk_depth == ov_depth
     static constexpr int BN = 128;      // keys per tile (M of S^T)
     static constexpr int NR = 16;       // padded query rows (N of both MMAs)
+    static_assert(NRV == 4 || NRV == 8 || NRV == 16, "real rows per CTA");
     static constexpr int THREADS = 192;
-    static constexpr int WG0 = 2;       // first softmax warp
+    static constexpr int WG0 = 2;       // first softmax warp (warps 2-5 cover TMEM quadrants 2, 3, 0, 1)
     static constexpr int TILE_BYTES = BN * D * 2;        // 32 KB: one K or V tile
     static constexpr int BOX_BYTES = BN * 128;           // one 64-column box of a tile
     static constexpr int Q_BYTES = NR * D * 2;           // 4 KB
     static constexpr int P_BYTES = NR * BN * 2;          // 4 KB
-    static constexpr int TMEM_COLS = 64;
-    static constexpr int TMEM_S0 = 0, TMEM_O0 = 32;      // S[2] at 0/16, O[2] at 32/48
+    // Each product's 8 K-steps are spread over NACC independent accumulators
+    // (K-step ks accumulates into ks % NACC), so dependent MMAs form chains of
+    // depth 8 / NACC; readers sum the NACC partials. 16 columns per
+    // accumulator (N = 16): S[2 buffers][NACC] then O[2 buffers][NACC].
+    static constexpr int NACC = 4;
+    static constexpr int ACC_COLS = 16;
+    static constexpr int BUF_COLS = NACC * ACC_COLS;              // 64
+    static constexpr int TMEM_S0 = 0, TMEM_O0 = 2 * BUF_COLS;     // 0 / 128
+    static constexpr int TMEM_COLS = 4 * BUF_COLS;                // 256
 
     static constexpr int OFF_RING = 0;                            // NSLOT x 32 KB
     static constexpr int OFF_Q = NSLOT * TILE_BYTES;              // K-major SW128 [2 boxes][16][128 B]
     static constexpr int OFF_P = OFF_Q + Q_BYTES;                 // [2 buffers][2 atoms][16][128 B]
-    static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;           // float [2][4][16]
-    static constexpr int OFF_MAXSUM = OFF_RED + 2 * 4 * NR * 4;   // float2 [16]
+    static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;           // float [2][4][NRV]
+    static constexpr int OFF_MAXSUM = OFF_RED + 2 * 4 * NR * 4;   // float2 [NRV]
     static constexpr int OFF_BAR = OFF_MAXSUM + NR * 8;
     // barriers: slot_full[NSLOT], slot_empty[NSLOT], s_full[2], s_empty[2],
-    // p_full[2], p_empty[2], o_full[2], o_empty[2], q_full, publish, mma_done
-    static constexpr int NBAR = 2 * NSLOT + 15;
+    // p_full[2], p_empty[2], o_full[2], o_empty[2], q_full, publish, mma_done, tmem_ready
+    static constexpr int NBAR = 2 * NSLOT + 16;
     static constexpr int OFF_ROWS = OFF_BAR + NBAR * 8;          // int [4 tiles][16 segments]
     static constexpr int OFF_MISC = OFF_ROWS + 4 * 16 * 4;       // tmem base, abort, consumed
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
@@ -71,14 +79,58 @@ struct TcCfg {
     static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms on 1024 bytes");
 };
 
+// Warp reduce-scatter of N per-row values (max or sum over the warp's 32
+// lanes): recursive halving exchanges half of the remaining rows at each of
+// the first log2(N) steps, then a butterfly finishes. On return v[0] holds
+// the reduction of row `row`; lanes whose low (32 / N) bits are zero hold
+// distinct rows.
+template <bool kMax>
+__device__ __forceinline__ float rs_op(float a, float b) { return kMax ? fmaxf(a, b) : a + b; }
+
+template <int N, int W, bool kMax, int M>
+__device__ __forceinline__ void reduce_scatter_step(float (&v)[M], int lane, int& row)
+{
+    if constexpr (N > 1) {
+        const bool up = (lane & W) != 0;
+#pragma unroll
+        for (int k = 0; k < N / 2; ++k) {
+            const float send = up ? v[k] : v[k + N / 2];
+            const float keep = up ? v[k + N / 2] : v[k];
+            v[k] = rs_op<kMax>(keep, __shfl_xor_sync(0xffffffffu, send, W));
+        }
+        row += up ? N / 2 : 0;
+        reduce_scatter_step<N / 2, W / 2, kMax, M>(v, lane, row);
+    } else {
+#pragma unroll
+        for (int w = W; w >= 1; w >>= 1) v[0] = rs_op<kMax>(v[0], __shfl_xor_sync(0xffffffffu, v[0], w));
+    }
+}
+
+template <int N, bool kMax>
+__device__ __forceinline__ float warp_reduce_scatter(const float (&in)[N], int lane, int& row)
+{
+    float v[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) v[k] = in[k];
+    row = 0;
+    reduce_scatter_step<N, 16, kMax, N>(v, lane, row);
+    return v[0];
+}
+
 // Position of tile i's K and V in the load sequence K0 K1 V0 K2 V1 ... V_{n-1}.
 __device__ __forceinline__ int k_item(int i) { return i == 0 ? 0 : 2 * i - 1; }
 __device__ __forceinline__ int v_item(int i, int n) { return i == n - 1 ? 2 * n - 1 : 2 * i + 2; }
 
-template <int NSLOT>
-__global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(const __grid_constant__ DecodeParams p)
+// Lazy rescaling: the running max of a row moves only when a tile's max
+// exceeds it by more than this many exp2 units, so most tiles skip the
+// correction; P then stays below 2^8, safe in bf16 and fp32.
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int NSLOT, int NRV>
+__global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
+    tc_decode_kernel(const __grid_constant__ DecodeParams p)
 {
-    using C = TcCfg<NSLOT>;
+    using C = TcCfg<NSLOT, NRV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_addr(smem);
@@ -102,7 +154,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
     const uint32_t slot_full = bar0, slot_empty = bar0 + 8 * NSLOT;
     const uint32_t s_full = bar0 + 16 * NSLOT, s_empty = s_full + 16, p_full = s_full + 32, p_empty = s_full + 48;
     const uint32_t o_full = s_full + 64, o_empty = s_full + 80, q_full = s_full + 96, publish_bar = s_full + 104;
-    const uint32_t mma_done = s_full + 112;
+    const uint32_t mma_done = s_full + 112, tmem_ready = s_full + 120;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     float* red_s = reinterpret_cast<float*>(smem + C::OFF_RED);
@@ -124,6 +176,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
         mbar_init(q_full, 1);
         mbar_init(publish_bar, P);
         mbar_init(mma_done, 1);
+        mbar_init(tmem_ready, 1);
         *abort_flag = 0;
         fence_mbarrier_init_cluster();
     }
@@ -131,15 +184,20 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
         tma_prefetch_map(&p.tm_k);
         tma_prefetch_map(&p.tm_v);
     }
+    __syncthreads();  // barriers initialised; the load warp may start at once
+    // Peers arrive on this CTA's publish barrier only after the matching
+    // cluster wait (before the merge), so the prologue does not wait here.
+    if (P > 1) cluster_arrive_relaxed();
+    uint32_t tmem = 0;
     if (warp == 1) {
         tmem_alloc(sbase + C::OFF_MISC, C::TMEM_COLS);
         tmem_relinquish();
+        tc_fence_before_sync();
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem = *tmem_slot;
+        if (lane == 0) mbar_arrive(tmem_ready);
     }
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-    if (P > 1) cluster_sync_all();
 
     const int n_tiles = (L + C::BN - 1) / C::BN;
     const int base = n_tiles / P, rem = n_tiles % P;
@@ -147,10 +205,10 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
     const int tile_count = base + (rank < rem ? 1 : 0);
     const int n_items = 2 * tile_count;
 
-    // Softmax / correction state (warps 2-5).
-    float m_run[C::NR], l_part[C::NR], o_acc[C::NR];
+    // Softmax / correction state (warps 2-5), real rows only.
+    float m_run[NRV], l_part[NRV], o_acc[NRV];
 #pragma unroll
-    for (int r = 0; r < C::NR; ++r) {
+    for (int r = 0; r < NRV; ++r) {
         m_run[r] = -INFINITY;
         l_part[r] = 0.f;
         o_acc[r] = 0.f;
@@ -217,7 +275,14 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
         if (lane == 0) {
             const uint32_t id_s = umma_idesc_bf16_f32(128, C::NR, false, false);
             const uint32_t id_pv = umma_idesc_bf16_f32(128, C::NR, true, false);
-            const uint32_t q_addr = sbase + C::OFF_Q;
+            // Descriptors at offset 0 of each operand region; steps add to the
+            // start-address field (bytes >> 4), which never carries.
+            const uint64_t q_desc0 = umma_smem_desc(sbase + C::OFF_Q, 16, 1024, kLayoutSwizzle128);
+            const uint64_t k_desc0 = umma_smem_desc(sbase + C::OFF_RING, 16, 1024, kLayoutSwizzle128);
+            // A = V^T, MN-major: 64-column atoms one box apart (LBO), 8-key groups 1024 B apart (SBO)
+            const uint64_t v_desc0 = umma_smem_desc(sbase + C::OFF_RING, C::BOX_BYTES, 1024, kLayoutSwizzle128);
+            // B = P, K-major: 64-key atoms of 16 rows x 128 B
+            const uint64_t p_desc0 = umma_smem_desc(sbase + C::OFF_P, 16, 1024, kLayoutSwizzle128);
             bool ok = mbar_wait(q_full, 0, abort_flag, p.status, p.wait_limit_ns);
 
             auto issue_pv = [&](int t) -> bool {
@@ -230,18 +295,13 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
                     !mbar_wait(o_empty + 8 * (t & 1), ((t >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns))
                     return false;
                 tc_fence_after_sync();
-                const uint32_t v_addr = sbase + C::OFF_RING + slot * C::TILE_BYTES;
-                const uint32_t p_addr = sbase + C::OFF_P + (t & 1) * C::P_BYTES;
-                const uint32_t d = tmem + C::TMEM_O0 + 16 * (t & 1);
+                const uint64_t a0 = v_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
+                const uint64_t b0 = p_desc0 + (uint64_t)(((t & 1) * C::P_BYTES) >> 4);
+                const uint32_t d = tmem + C::TMEM_O0 + C::BUF_COLS * (t & 1);
 #pragma unroll
-                for (int ks = 0; ks < C::BN / 16; ++ks) {
-                    // A = V^T, MN-major: 64-column atoms one box apart (LBO), 8-key groups 1024 B apart (SBO)
-                    const uint64_t a = umma_smem_desc(v_addr + ks * 2048, C::BOX_BYTES, 1024, kLayoutSwizzle128);
-                    // B = P, K-major: 64-key atoms of 16 rows x 128 B
-                    const uint64_t bd = umma_smem_desc(p_addr + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024,
-                                                       kLayoutSwizzle128);
-                    umma_f16_ss(d, a, bd, id_pv, ks > 0);
-                }
+                for (int ks = 0; ks < C::BN / 16; ++ks)
+                    umma_f16_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)((ks * 2048) >> 4),
+                                b0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_pv, ks >= C::NACC);
                 umma_commit(o_full + 8 * (t & 1));
                 umma_commit(slot_empty + 8 * slot);
                 umma_commit(p_empty + 8 * (t & 1));
@@ -255,16 +315,13 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
                     !mbar_wait(s_empty + 8 * (i & 1), ((i >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns))
                     break;
                 tc_fence_after_sync();
-                const uint32_t k_addr = sbase + C::OFF_RING + slot * C::TILE_BYTES;
-                const uint32_t d = tmem + C::TMEM_S0 + 16 * (i & 1);
+                const uint64_t a0 = k_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
+                const uint32_t d = tmem + C::TMEM_S0 + C::BUF_COLS * (i & 1);
 #pragma unroll
-                for (int ks = 0; ks < C::D / 16; ++ks) {
-                    const uint32_t koff = (ks >> 2) * C::BOX_BYTES + (ks & 3) * 32;
-                    const uint64_t a = umma_smem_desc(k_addr + koff, 16, 1024, kLayoutSwizzle128);
-                    const uint64_t bd = umma_smem_desc(q_addr + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024,
-                                                       kLayoutSwizzle128);
-                    umma_f16_ss(d, a, bd, id_s, ks > 0);
-                }
+                for (int ks = 0; ks < C::D / 16; ++ks)
+                    umma_f16_ss(d + C::ACC_COLS * (ks % C::NACC),
+                                a0 + (uint64_t)(((ks >> 2) * C::BOX_BYTES + (ks & 3) * 32) >> 4),
+                                q_desc0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_s, ks >= C::NACC);
                 umma_commit(s_full + 8 * (i & 1));
                 umma_commit(slot_empty + 8 * slot);
                 if (i >= 1 && !issue_pv(i - 1)) {
@@ -301,29 +358,40 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
         fence_proxy_async_smem();
         named_barrier_sync(1, 128);
         if (wt == 0) mbar_arrive(q_full);
+        mbar_wait(tmem_ready, 0, abort_flag, p.status, p.wait_limit_ns);
+        tc_fence_after_sync();
+        tmem = *tmem_slot;
 
-        int row_tok[C::NR];  // visible-key bound of every row (0 for padding rows)
+        int row_tok[NRV];  // visible-key bound of every row (0 for padding rows)
 #pragma unroll
-        for (int r = 0; r < C::NR; ++r) row_tok[r] = r < p.rows ? L - p.num_q + r / p.heads_per_cta + 1 : 0;
+        for (int r = 0; r < NRV; ++r) row_tok[r] = r < p.rows ? L - p.num_q + r / p.heads_per_cta + 1 : 0;
 
-        float alpha_prev[C::NR];
-        auto correct = [&](int t, const float (&a)[C::NR]) {
+        float alpha_prev[NRV];
+        bool rescaled_prev = false;
+        auto correct = [&](int t, const float (&a)[NRV], bool rescaled) {
             mbar_wait(o_full + 8 * (t & 1), (t >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
             tc_fence_after_sync();
-            float ot[16];
-            tmem_ld_32x32b_x16(tmem + lane_addr + C::TMEM_O0 + 16 * (t & 1), ot);
+            float ot[NRV];
+            tmem_ld4_sum(tmem + lane_addr + C::TMEM_O0 + C::BUF_COLS * (t & 1), C::ACC_COLS, ot);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_empty + 8 * (t & 1));
+            if (rescaled) {
 #pragma unroll
-            for (int r = 0; r < C::NR; ++r) o_acc[r] = fmaf(o_acc[r], a[r], ot[r]);
+                for (int r = 0; r < NRV; ++r) o_acc[r] = fmaf(o_acc[r], a[r], ot[r]);
+            } else {
+#pragma unroll
+                for (int r = 0; r < NRV; ++r) o_acc[r] += ot[r];
+            }
         };
+        // lanes holding distinct rows after a reduce-scatter of NRV values
+        const bool row_writer = (lane & (32 / NRV - 1)) == 0;
 
         for (int i = 0; i < tile_count; ++i) {
             mbar_wait(s_full + 8 * (i & 1), (i >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
             tc_fence_after_sync();
-            float s[16];
-            tmem_ld_32x32b_x16(tmem + lane_addr + C::TMEM_S0 + 16 * (i & 1), s);
+            float s[NRV];
+            tmem_ld4_sum(tmem + lane_addr + C::TMEM_S0 + C::BUF_COLS * (i & 1), C::ACC_COLS, s);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_empty + 8 * (i & 1));
@@ -331,77 +399,69 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
             const int key0 = (tile_begin + i) * C::BN;
             const int key = key0 + my_lane;
 #pragma unroll
-            for (int r = 0; r < C::NR; ++r) s[r] = key < row_tok[r] ? s[r] : -INFINITY;
+            for (int r = 0; r < NRV; ++r) s[r] = key < row_tok[r] ? s[r] : -INFINITY;
 
-            // Per-row max over this warp's 32 keys (reduce-scatter: lane l ends
-            // with row (l >> 1) & 15), then over the four warps in shared memory.
+            // Per-row max over this warp's 32 keys, then over the four warps.
             {
-                float v8[8], v4[4], v2[2], v1;
-                const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float send = h16 ? s[k] : s[k + 8];
-                    const float keep = h16 ? s[k + 8] : s[k];
-                    v8[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float send = h8 ? v8[k] : v8[k + 4];
-                    const float keep = h8 ? v8[k + 4] : v8[k];
-                    v4[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-                }
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const float send = h4 ? v4[k] : v4[k + 2];
-                    const float keep = h4 ? v4[k + 2] : v4[k];
-                    v2[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-                }
-                {
-                    const float send = h2 ? v2[0] : v2[1];
-                    const float keep = h2 ? v2[1] : v2[0];
-                    v1 = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-                }
-                v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, 1));
-                if ((lane & 1) == 0) red_s[((i & 1) * 4 + quad) * C::NR + ((lane >> 1) & 15)] = v1;
+                int row;
+                const float wmax = warp_reduce_scatter<NRV, true>(s, lane, row);
+                if (row_writer) red_s[((i & 1) * 4 + quad) * NRV + row] = wmax;
             }
             // The abort decision is reduced over the warpgroup, so it is uniform.
             if (named_barrier_or(1, 128, *abort_flag != 0)) break;
 
-            float alpha[C::NR];
+            float tmax[NRV];
             {
-                const float4* rq = reinterpret_cast<const float4*>(red_s + (i & 1) * 4 * C::NR);
+                const float* rq = red_s + (i & 1) * 4 * NRV;
 #pragma unroll
-                for (int r4 = 0; r4 < C::NR / 4; ++r4) {
-                    float4 a0 = rq[r4], a1 = rq[4 + r4], a2 = rq[8 + r4], a3 = rq[12 + r4];
-                    float tm[4] = {fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x)),
-                                   fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y)),
-                                   fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z)),
-                                   fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w))};
+                for (int r4 = 0; r4 < NRV / 4; ++r4) {
+                    const float4 a0 = reinterpret_cast<const float4*>(rq)[r4];
+                    const float4 a1 = reinterpret_cast<const float4*>(rq + NRV)[r4];
+                    const float4 a2 = reinterpret_cast<const float4*>(rq + 2 * NRV)[r4];
+                    const float4 a3 = reinterpret_cast<const float4*>(rq + 3 * NRV)[r4];
+                    tmax[4 * r4 + 0] = fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x));
+                    tmax[4 * r4 + 1] = fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y));
+                    tmax[4 * r4 + 2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
+                    tmax[4 * r4 + 3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
+                }
+            }
+            // Move the running max only where the tile exceeds it by more than
+            // the threshold (every thread sees the same values: uniform branch).
+            bool rescale = false;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r = 4 * r4 + e;
-                        const float m_new = fmaxf(m_run[r], tm[e]);
-                        float a = 1.f, pr = 0.f;
-                        if (m_new != -INFINITY) {
-                            a = (m_run[r] == -INFINITY) ? 0.f : ex2_approx((m_run[r] - m_new) * c2);
-                            pr = (s[r] == -INFINITY) ? 0.f : ex2_approx((s[r] - m_new) * c2);
-                        }
-                        alpha[r] = a;
-                        l_part[r] = fmaf(l_part[r], a, pr);
-                        m_run[r] = m_new;
-                        s[r] = pr;
+            for (int r = 0; r < NRV; ++r)
+                rescale |= (m_run[r] == -INFINITY) ? (tmax[r] != -INFINITY)
+                                                   : ((tmax[r] - m_run[r]) * c2 > kRescaleThreshold);
+            float alpha[NRV];
+            if (rescale) {
+#pragma unroll
+                for (int r = 0; r < NRV; ++r) {
+                    const bool move = (m_run[r] == -INFINITY) ? (tmax[r] != -INFINITY)
+                                                              : ((tmax[r] - m_run[r]) * c2 > kRescaleThreshold);
+                    alpha[r] = 1.f;
+                    if (move) {
+                        alpha[r] = (m_run[r] == -INFINITY) ? 0.f : ex2_approx((m_run[r] - tmax[r]) * c2);
+                        m_run[r] = tmax[r];
+                        l_part[r] *= alpha[r];
                     }
                 }
             }
+#pragma unroll
+            for (int r = 0; r < NRV; ++r) {
+                const float pr = (s[r] == -INFINITY) ? 0.f : ex2_approx((s[r] - m_run[r]) * c2);
+                l_part[r] += pr;
+                s[r] = pr;
+            }
 
-            // P (bf16) -> K-major swizzled B operand of O^T = V^T P^T
+            // P (bf16) -> K-major swizzled B operand of O^T = V^T P^T (rows >= NRV
+            // only feed output columns that are never read).
             if (i >= 2)
                 mbar_wait(p_empty + 8 * (i & 1), ((i >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
             {
                 uint8_t* pb = smem + C::OFF_P + (i & 1) * C::P_BYTES + (my_lane >> 6) * 2048;
                 const int kk = my_lane & 63;
 #pragma unroll
-                for (int r = 0; r < C::NR; ++r)
+                for (int r = 0; r < NRV; ++r)
                     *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((((kk >> 3) ^ (r & 7))) << 4) + (kk & 7) * 2) =
                         __float2bfloat16_rn(s[r]);
             }
@@ -425,11 +485,12 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full + 8 * (i & 1));
 
-            if (i >= 1) correct(i - 1, alpha_prev);
+            if (i >= 1) correct(i - 1, alpha_prev, rescaled_prev);
 #pragma unroll
-            for (int r = 0; r < C::NR; ++r) alpha_prev[r] = alpha[r];
+            for (int r = 0; r < NRV; ++r) alpha_prev[r] = rescale ? alpha[r] : 1.f;
+            rescaled_prev = rescale;
         }
-        if (tile_count > 0) correct(tile_count - 1, alpha_prev);  // bounded even after an abort
+        if (tile_count > 0) correct(tile_count - 1, alpha_prev, rescaled_prev);  // bounded even after an abort
         tc_fence_before_sync();
     }
 
@@ -453,72 +514,55 @@ __global__ void __launch_bounds__(TcCfg<NSLOT>::THREADS, 2) tc_decode_kernel(con
         const int dv = 32 * quad + lane;
         // Row sums: per-thread partial sums -> warp reduce-scatter -> four warps.
         {
-            float v8[8], v4[4], v2[2], v1;
-            const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float send = h16 ? l_part[k] : l_part[k + 8];
-                const float keep = h16 ? l_part[k + 8] : l_part[k];
-                v8[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float send = h8 ? v8[k] : v8[k + 4];
-                const float keep = h8 ? v8[k + 4] : v8[k];
-                v4[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-            }
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const float send = h4 ? v4[k] : v4[k + 2];
-                const float keep = h4 ? v4[k + 2] : v4[k];
-                v2[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-            }
-            {
-                const float send = h2 ? v2[0] : v2[1];
-                const float keep = h2 ? v2[1] : v2[0];
-                v1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-            }
-            v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+            int row;
+            const float wsum = warp_reduce_scatter<NRV, false>(l_part, lane, row);
             named_barrier_sync(1, 128);  // red_s may still be read by the last tile's max step
-            if ((lane & 1) == 0) red_s[quad * C::NR + ((lane >> 1) & 15)] = v1;
+            if ((lane & (32 / NRV - 1)) == 0) red_s[quad * NRV + row] = wsum;
             named_barrier_sync(1, 128);
         }
         float* stage_s = reinterpret_cast<float*>(smem + C::OFF_STAGE);
         const int BW = p.band_cols;
         const int q = dv / BW, j = dv % BW;
 #pragma unroll
-        for (int r = 0; r < C::NR; ++r) {
-            const float l = red_s[r] + red_s[C::NR + r] + red_s[2 * C::NR + r] + red_s[3 * C::NR + r];
+        for (int r = 0; r < NRV; ++r) {
+            const float l = red_s[r] + red_s[NRV + r] + red_s[2 * NRV + r] + red_s[3 * NRV + r];
             if (wt == 0) maxsum_s[r] = make_float2(m_run[r], l);
-            stage_s[(q * C::NR + r) * BW + j] = l > 0.f ? o_acc[r] / l : 0.f;
+            float inv = 0.f;
+            if (l > 0.f) inv = __frcp_rn(l);  // l is the same in every thread: no divergence
+            stage_s[(q * NRV + r) * BW + j] = o_acc[r] * inv;
         }
         named_barrier_sync(1, 128);
-        splitk_merge_and_store<C::NR>(p, P, rank, b, kvh, 0, stage_s, maxsum_s,
+        if (P > 1) cluster_wait();  // every rank's publish barrier is initialised
+        splitk_merge_and_store<NRV>(p, P, rank, b, kvh, 0, stage_s, maxsum_s,
                                       reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), publish_bar, abort_flag, wt,
                                       128, 1);
     }
+    if (P > 1 && warp < C::WG0) cluster_wait();  // pairs with the early arrive
     __syncwarp();
     if (P > 1) cluster_sync_all();  // peers may still read this CTA's staged bands until here
 }
 
 bool tc_geometry(int qk, int ov, int rows, int nslot, KernelGeometry* g)
 {
-    if (qk != 128 || ov != 128 || rows > 16) return false;
-#define FAD_TC(NS)                                                                        \
-    if (nslot == NS) {                                                                    \
-        g->func = reinterpret_cast<const void*>(&tc_decode_kernel<NS>);                   \
-        g->threads = TcCfg<NS>::THREADS;                                                  \
-        g->keys_per_tile = TcCfg<NS>::BN;                                                 \
+    if (qk != 128 || ov != 128 || rows < 1 || rows > 16) return false;
+    const int nrv = rows <= 4 ? 4 : (rows <= 8 ? 8 : 16);
+#define FAD_TC(NS, NRV)                                                                   \
+    if (nslot == NS && nrv == NRV) {                                                      \
+        g->func = reinterpret_cast<const void*>(&tc_decode_kernel<NS, NRV>);              \
+        g->threads = TcCfg<NS, NRV>::THREADS;                                             \
+        g->keys_per_tile = TcCfg<NS, NRV>::BN;                                            \
         g->stages = NS;                                                                   \
-        g->rows_capacity = TcCfg<NS>::NR;                                                 \
-        g->smem_bytes = TcCfg<NS>::SMEM_BYTES;                                            \
-        g->name = "tc_d128_bn128_n16_slots" #NS;                                          \
+        g->rows_capacity = NRV;                                                           \
+        g->smem_bytes = TcCfg<NS, NRV>::SMEM_BYTES;                                       \
+        g->name = "tc_d128_bn128_n16_r" #NRV "_slots" #NS;                                \
         return true;                                                                      \
     }
-    FAD_TC(2)
-    FAD_TC(3)
-    FAD_TC(4)
-    FAD_TC(6)
+    FAD_TC(3, 4)
+    FAD_TC(3, 8)
+    FAD_TC(3, 16)
+    FAD_TC(6, 4)
+    FAD_TC(6, 8)
+    FAD_TC(6, 16)
 #undef FAD_TC
     return false;
 }

@@ -31,9 +31,11 @@ namespace fad {
 //            OC = min(BW, 256) columns, rows r = t * heads + hh
 // Rows >= p.rows are padding: they are merged (harmlessly) but never stored.
 //
-// Called by `nthreads` threads with ids `tid` in [0, nthreads), after a CTA-wide
-// barrier that follows the staging writes. Thread tid 0 of the calling group
-// publishes. `bar_id` names a hardware barrier private to the group.
+// Called by `nthreads` threads with ids `tid` in [0, nthreads), after a
+// barrier of the group that follows the staging writes, and (P > 1) after a
+// cluster barrier wait that guarantees every rank has initialised its
+// publish barrier. Thread tid 0 of the calling group publishes. `bar_id`
+// names a hardware barrier private to the group.
 template <int RB>
 __device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, int P, int rank, int b,
                                                        int kvh, int row_block, const float* stage_s,
@@ -111,7 +113,7 @@ __device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, in
             tma_store_3d(&p.tm_out, smem_addr(out_s + (c0 / OC) * RB * OC), rank * BW + c0,
                          kvh * p.group + row_block * p.heads_per_cta, b * p.num_q);
         tma_store_commit();
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        tma_store_wait_read();  // the band's shared memory may be released once read
     }
 }
 
