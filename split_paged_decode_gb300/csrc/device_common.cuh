@@ -107,6 +107,39 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Shared-memory progress counters published by one warp and read by another.
+__device__ __forceinline__ void st_release_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Bounded wait until the counter at `addr` exceeds `target` (same limit and
+// abort protocol as mbar_wait).
+__device__ __forceinline__ bool counter_wait(uint32_t addr, uint32_t target, volatile int* abort_flag,
+                                             unsigned int* status, uint64_t limit_ns)
+{
+    if (ld_acquire_u32(addr) > target) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (ld_acquire_u32(addr) > target) return true;
+        if ((n & 31u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                *abort_flag = 1;
+                atomicOr(status, FA_STATUS_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor); the tensor maps live in the __grid_constant__
 // kernel parameter block.

@@ -15,11 +15,12 @@
 //              128-byte-swizzled boxes per page segment, one lane per
 //              segment) into a ring of NSLOT 32 KB slots, in the order the
 //              MMA warp consumes them: K0 K1 V0 K2 V1 ... K_{n-1} V_{n-2} V_{n-1}
-//   warp 1     MMA: allocates 256 TMEM columns (S and O, two buffers of four
-//              accumulators each), issues S_i = K_i Q^T, then
-//              O_{i-1} = V_{i-1}^T P_{i-1}^T, committing to mbarriers; the
-//              slot of a tile is released by the commit of the MMA that read it.
-//   warps 2-5  softmax + correction (thread = TMEM lane = key for S, = value
+//   warp 1     MMA S: allocates 256 TMEM columns (S and O, two buffers of four
+//              accumulators each) and issues every S_i = K_i Q^T;
+//   warp 2     MMA O: issues every O_t = V_t^T P_t^T; each MMA warp commits
+//              once per tile;
+//   warps 3-6  softmax + correction; they also release the ring slots once
+//              the MMA that read a slot has completed; (thread = TMEM lane = key for S, = value
 //              column for O): online softmax in exp2 form with the running
 //              max in raw score units, P^T to shared memory as bf16, and the
 //              correction O <- O * alpha + O_tile in registers; then the
@@ -43,8 +44,8 @@ struct TcCfg {
     static constexpr int BN = 128;      // keys per tile (M of S^T)
     static constexpr int NR = 16;       // padded query rows (N of both MMAs)
     static_assert(NRV == 4 || NRV == 8 || NRV == 16, "real rows per CTA");
-    static constexpr int THREADS = 192;
-    static constexpr int WG0 = 2;       // first softmax warp (warps 2-5 cover TMEM quadrants 2, 3, 0, 1)
+    static constexpr int THREADS = 224;
+    static constexpr int WG0 = 3;       // first softmax warp (warps 3-6 cover TMEM quadrants 3, 0, 1, 2)
     static constexpr int TILE_BYTES = BN * D * 2;        // 32 KB: one K or V tile
     static constexpr int BOX_BYTES = BN * 128;           // one 64-column box of a tile
     static constexpr int Q_BYTES = NR * D * 2;           // 4 KB
@@ -66,10 +67,10 @@ struct TcCfg {
     static constexpr int OFF_MAXSUM = OFF_RED + 2 * 4 * NR * 4;   // float2 [NRV]
     static constexpr int OFF_BAR = OFF_MAXSUM + NR * 8;
     // barriers: slot_full[NSLOT], slot_empty[NSLOT], s_full[2], s_empty[2],
-    // p_full[2], p_empty[2], o_full[2], o_empty[2], q_full, publish, mma_done, tmem_ready
+    // p_full[2], (unused)[2], o_full[2], o_empty[2], q_full, publish, mma_done, tmem_ready
     static constexpr int NBAR = 2 * NSLOT + 16;
     static constexpr int OFF_ROWS = OFF_BAR + NBAR * 8;          // int [4 tiles][16 segments]
-    static constexpr int OFF_MISC = OFF_ROWS + 4 * 16 * 4;       // tmem base, abort, consumed
+    static constexpr int OFF_MISC = OFF_ROWS + 4 * 16 * 4;       // tmem base, abort, S issued, O issued
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     // The epilogue reuses the drained ring: f32 stage [P][16][BW] in slot 0,
     // the bf16 output band in slot 1.
@@ -152,11 +153,13 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
 
     const uint32_t bar0 = sbase + C::OFF_BAR;
     const uint32_t slot_full = bar0, slot_empty = bar0 + 8 * NSLOT;
-    const uint32_t s_full = bar0 + 16 * NSLOT, s_empty = s_full + 16, p_full = s_full + 32, p_empty = s_full + 48;
+    const uint32_t s_full = bar0 + 16 * NSLOT, s_empty = s_full + 16, p_full = s_full + 32;
     const uint32_t o_full = s_full + 64, o_empty = s_full + 80, q_full = s_full + 96, publish_bar = s_full + 104;
     const uint32_t mma_done = s_full + 112, tmem_ready = s_full + 120;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    // Progress of the two MMA warps (products issued), for the ring-order rule.
+    const uint32_t s_issued = sbase + C::OFF_MISC + 8, o_issued = sbase + C::OFF_MISC + 12;
     float* red_s = reinterpret_cast<float*>(smem + C::OFF_RED);
     float2* maxsum_s = reinterpret_cast<float2*>(smem + C::OFF_MAXSUM);
 
@@ -169,15 +172,16 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
             mbar_init(s_full + 8 * i, 1);
             mbar_init(s_empty + 8 * i, 4);
             mbar_init(p_full + 8 * i, 4);
-            mbar_init(p_empty + 8 * i, 1);
             mbar_init(o_full + 8 * i, 1);
             mbar_init(o_empty + 8 * i, 4);
         }
         mbar_init(q_full, 1);
         mbar_init(publish_bar, P);
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, 2);
         mbar_init(tmem_ready, 1);
         *abort_flag = 0;
+        *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 8) = 0;
+        *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 12) = 0;
         fence_mbarrier_init_cluster();
     }
     if (warp == 0 && lane == 0) {
@@ -270,67 +274,82 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------- MMA warp
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------ MMA warps
+        // One warp issues tcgen05.mma only every ~60 cycles, so the products go
+        // to two warps: warp 1 issues every S_i = K_i Q^T, warp 2 every
+        // O_t = V_t^T P_t^T, each with one commit per tile. The softmax warps
+        // release the ring slots and observe the P buffers' reuse themselves.
+        //
+        // Ring-order rule: a slot's full barrier is waited on for an item only
+        // after the item that held the slot before has been consumed (a parity
+        // wait on a barrier whose previous phase has not completed would alias
+        // with that phase). When the previous item belongs to the other warp,
+        // its published progress counter is waited on first.
         if (lane == 0) {
-            const uint32_t id_s = umma_idesc_bf16_f32(128, C::NR, false, false);
-            const uint32_t id_pv = umma_idesc_bf16_f32(128, C::NR, true, false);
-            // Descriptors at offset 0 of each operand region; steps add to the
-            // start-address field (bytes >> 4), which never carries.
-            const uint64_t q_desc0 = umma_smem_desc(sbase + C::OFF_Q, 16, 1024, kLayoutSwizzle128);
-            const uint64_t k_desc0 = umma_smem_desc(sbase + C::OFF_RING, 16, 1024, kLayoutSwizzle128);
-            // A = V^T, MN-major: 64-column atoms one box apart (LBO), 8-key groups 1024 B apart (SBO)
-            const uint64_t v_desc0 = umma_smem_desc(sbase + C::OFF_RING, C::BOX_BYTES, 1024, kLayoutSwizzle128);
-            // B = P, K-major: 64-key atoms of 16 rows x 128 B
-            const uint64_t p_desc0 = umma_smem_desc(sbase + C::OFF_P, 16, 1024, kLayoutSwizzle128);
-            bool ok = mbar_wait(q_full, 0, abort_flag, p.status, p.wait_limit_ns);
-
-            auto issue_pv = [&](int t) -> bool {
-                const int j = v_item(t, tile_count), slot = j % NSLOT;
-                if (!mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns))
-                    return false;
-                if (!mbar_wait(p_full + 8 * (t & 1), (t >> 1) & 1, abort_flag, p.status, p.wait_limit_ns))
-                    return false;
-                if (t >= 2 &&
-                    !mbar_wait(o_empty + 8 * (t & 1), ((t >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns))
-                    return false;
-                tc_fence_after_sync();
-                const uint64_t a0 = v_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
-                const uint64_t b0 = p_desc0 + (uint64_t)(((t & 1) * C::P_BYTES) >> 4);
-                const uint32_t d = tmem + C::TMEM_O0 + C::BUF_COLS * (t & 1);
-#pragma unroll
-                for (int ks = 0; ks < C::BN / 16; ++ks)
-                    umma_f16_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)((ks * 2048) >> 4),
-                                b0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_pv, ks >= C::NACC);
-                umma_commit(o_full + 8 * (t & 1));
-                umma_commit(slot_empty + 8 * slot);
-                umma_commit(p_empty + 8 * (t & 1));
-                return true;
+            auto prev_consumed = [&](int item) -> bool {  // wait until `item` has been consumed
+                if (item < 0) return true;
+                const bool is_v = (item == n_items - 1) || (item > 0 && (item & 1) == 0);
+                const int t = is_v ? (item == n_items - 1 ? tile_count - 1 : (item - 2) >> 1) : (item + 1) >> 1;
+                return counter_wait(is_v ? o_issued : s_issued, (uint32_t)t, abort_flag, p.status, p.wait_limit_ns);
             };
-
-            for (int i = 0; ok && i < tile_count; ++i) {
-                const int j = k_item(i), slot = j % NSLOT;
-                if (!mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns)) break;
-                if (i >= 2 &&
-                    !mbar_wait(s_empty + 8 * (i & 1), ((i >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns))
-                    break;
-                tc_fence_after_sync();
-                const uint64_t a0 = k_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
-                const uint32_t d = tmem + C::TMEM_S0 + C::BUF_COLS * (i & 1);
+            if (warp == 1) {
+                const uint32_t id_s = umma_idesc_bf16_f32(128, C::NR, false, false);
+                const uint64_t q_desc0 = umma_smem_desc(sbase + C::OFF_Q, 16, 1024, kLayoutSwizzle128);
+                const uint64_t k_desc0 = umma_smem_desc(sbase + C::OFF_RING, 16, 1024, kLayoutSwizzle128);
+                bool ok = mbar_wait(q_full, 0, abort_flag, p.status, p.wait_limit_ns);
+                for (int i = 0; ok && i < tile_count; ++i) {
+                    const int j = k_item(i), slot = j % NSLOT;
+                    if (!prev_consumed(j - NSLOT)) break;
+                    if (!mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns))
+                        break;
+                    if (i >= 2 &&
+                        !mbar_wait(s_empty + 8 * (i & 1), ((i >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns))
+                        break;
+                    tc_fence_after_sync();
+                    const uint64_t a0 = k_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
+                    const uint32_t d = tmem + C::TMEM_S0 + C::BUF_COLS * (i & 1);
 #pragma unroll
-                for (int ks = 0; ks < C::D / 16; ++ks)
-                    umma_f16_ss(d + C::ACC_COLS * (ks % C::NACC),
-                                a0 + (uint64_t)(((ks >> 2) * C::BOX_BYTES + (ks & 3) * 32) >> 4),
-                                q_desc0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_s, ks >= C::NACC);
-                umma_commit(s_full + 8 * (i & 1));
-                umma_commit(slot_empty + 8 * slot);
-                if (i >= 1 && !issue_pv(i - 1)) {
-                    ok = false;
-                    break;
+                    for (int ks = 0; ks < C::D / 16; ++ks)
+                        umma_f16_ss(d + C::ACC_COLS * (ks % C::NACC),
+                                    a0 + (uint64_t)(((ks >> 2) * C::BOX_BYTES + (ks & 3) * 32) >> 4),
+                                    q_desc0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_s,
+                                    ks >= C::NACC);
+                    umma_commit(s_full + 8 * (i & 1));
+                    st_release_u32(s_issued, (uint32_t)(i + 1));
                 }
-                if (i == tile_count - 1 && !issue_pv(i)) ok = false;
+            } else {
+                const uint32_t id_pv = umma_idesc_bf16_f32(128, C::NR, true, false);
+                // A = V^T, MN-major: 64-column atoms one box apart (LBO), 8-key groups 1024 B apart (SBO)
+                const uint64_t v_desc0 = umma_smem_desc(sbase + C::OFF_RING, C::BOX_BYTES, 1024, kLayoutSwizzle128);
+                // B = P, K-major: 64-key atoms of 16 rows x 128 B
+                const uint64_t p_desc0 = umma_smem_desc(sbase + C::OFF_P, 16, 1024, kLayoutSwizzle128);
+                mbar_wait(tmem_ready, 0, abort_flag, p.status, p.wait_limit_ns);
+                tc_fence_after_sync();
+                tmem = *tmem_slot;
+                for (int t = 0; t < tile_count; ++t) {
+                    const int j = v_item(t, tile_count), slot = j % NSLOT;
+                    if (!prev_consumed(j - NSLOT)) break;
+                    if (!mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns))
+                        break;
+                    if (!mbar_wait(p_full + 8 * (t & 1), (t >> 1) & 1, abort_flag, p.status, p.wait_limit_ns)) break;
+                    if (t >= 2 &&
+                        !mbar_wait(o_empty + 8 * (t & 1), ((t >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns))
+                        break;
+                    tc_fence_after_sync();
+                    const uint64_t a0 = v_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
+                    const uint64_t b0 = p_desc0 + (uint64_t)(((t & 1) * C::P_BYTES) >> 4);
+                    const uint32_t d = tmem + C::TMEM_O0 + C::BUF_COLS * (t & 1);
+#pragma unroll
+                    for (int ks = 0; ks < C::BN / 16; ++ks)
+                        umma_f16_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)((ks * 2048) >> 4),
+                                    b0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_pv, ks >= C::NACC);
+                    umma_commit(o_full + 8 * (t & 1));
+                    st_release_u32(o_issued, (uint32_t)(t + 1));
+                }
             }
-            // Every MMA issued above has completed once this barrier fires.
+            // mma_done expects one commit from each MMA warp: it fires once every
+            // MMA of both warps has completed.
             umma_commit(mma_done);
             volatile int keep_waiting = 0;
             mbar_wait(mma_done, 0, &keep_waiting, p.status, p.wait_limit_ns);
@@ -376,6 +395,9 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_empty + 8 * (t & 1));
+            // O_t has completed: V_t's ring slot is free, and so (for tile t + 2)
+            // is the P buffer it read.
+            if (wt == 0) mbar_arrive(slot_empty + 8 * (v_item(t, tile_count) % NSLOT));
             if (rescaled) {
 #pragma unroll
                 for (int r = 0; r < NRV; ++r) o_acc[r] = fmaf(o_acc[r], a[r], ot[r]);
@@ -386,6 +408,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
         };
         // lanes holding distinct rows after a reduce-scatter of NRV values
         const bool row_writer = (lane & (32 / NRV - 1)) == 0;
+        bool seen_abort = false;  // sticky: this thread has seen the abort flag
 
         for (int i = 0; i < tile_count; ++i) {
             mbar_wait(s_full + 8 * (i & 1), (i >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
@@ -395,23 +418,36 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_empty + 8 * (i & 1));
+            // S_i has completed, so no MMA reads K_i any more: free its ring slot.
+            if (wt == 0) mbar_arrive(slot_empty + 8 * (k_item(i) % NSLOT));
 
             const int key0 = (tile_begin + i) * C::BN;
             const int key = key0 + my_lane;
 #pragma unroll
             for (int r = 0; r < NRV; ++r) s[r] = key < row_tok[r] ? s[r] : -INFINITY;
 
-            // Per-row max over this warp's 32 keys, then over the four warps.
-            {
-                int row;
-                const float wmax = warp_reduce_scatter<NRV, true>(s, lane, row);
-                if (row_writer) red_s[((i & 1) * 4 + quad) * NRV + row] = wmax;
-            }
-            // The abort decision is reduced over the warpgroup, so it is uniform.
-            if (named_barrier_or(1, 128, *abort_flag != 0)) break;
-
-            float tmax[NRV];
-            {
+            // Lazy rescale: a row's running max moves only when some score
+            // exceeds it by more than the threshold. In the common case a single
+            // reducing barrier confirms that no thread needs it; otherwise the
+            // tile max is exchanged and the rows that exceed are moved.
+            bool need = false;
+#pragma unroll
+            for (int r = 0; r < NRV; ++r)
+                need |= (s[r] != -INFINITY) &&
+                        (m_run[r] == -INFINITY || (s[r] - m_run[r]) * c2 > kRescaleThreshold);
+            seen_abort |= (*abort_flag != 0);
+            bool rescale = false;
+            float alpha[NRV];
+            if (named_barrier_or(1, 128, need || seen_abort)) {
+                {
+                    int row;
+                    const float wmax = warp_reduce_scatter<NRV, true>(s, lane, row);
+                    if (row_writer) red_s[((i & 1) * 4 + quad) * NRV + row] = wmax;
+                }
+                seen_abort |= (*abort_flag != 0);
+                // The abort decision is reduced over the warpgroup, so it is uniform.
+                if (named_barrier_or(1, 128, seen_abort)) break;
+                float tmax[NRV];
                 const float* rq = red_s + (i & 1) * 4 * NRV;
 #pragma unroll
                 for (int r4 = 0; r4 < NRV / 4; ++r4) {
@@ -424,16 +460,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
                     tmax[4 * r4 + 2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
                     tmax[4 * r4 + 3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
                 }
-            }
-            // Move the running max only where the tile exceeds it by more than
-            // the threshold (every thread sees the same values: uniform branch).
-            bool rescale = false;
-#pragma unroll
-            for (int r = 0; r < NRV; ++r)
-                rescale |= (m_run[r] == -INFINITY) ? (tmax[r] != -INFINITY)
-                                                   : ((tmax[r] - m_run[r]) * c2 > kRescaleThreshold);
-            float alpha[NRV];
-            if (rescale) {
+                rescale = true;
 #pragma unroll
                 for (int r = 0; r < NRV; ++r) {
                     const bool move = (m_run[r] == -INFINITY) ? (tmax[r] != -INFINITY)
@@ -454,9 +481,8 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
             }
 
             // P (bf16) -> K-major swizzled B operand of O^T = V^T P^T (rows >= NRV
-            // only feed output columns that are never read).
-            if (i >= 2)
-                mbar_wait(p_empty + 8 * (i & 1), ((i >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+            // only feed output columns that are never read). Buffer i & 1 was
+            // last read by O_{i-2}, whose completion correct(i - 2) observed.
             {
                 uint8_t* pb = smem + C::OFF_P + (i & 1) * C::P_BYTES + (my_lane >> 6) * 2048;
                 const int kk = my_lane & 63;
