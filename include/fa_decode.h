@@ -137,6 +137,41 @@ int fa_decode_set_debug(fa_decode_t h, uint32_t flags, int64_t wait_limit_ns);
  */
 int fa_decode_describe(fa_decode_t h, char* buf, int size);
 
+/*
+ * fa_decode_run_noalloc -- one decode forward that allocates no device memory.
+ *
+ * The pages have no counterpart for this call; it exists for callers that
+ * cannot call cudaMalloc: code whose device memory must all come from its own
+ * pool or arena (a serving runtime that reserves the GPU up front, a process
+ * under a hard device-memory budget), and latency-critical paths that cannot
+ * afford the implicit synchronisation of an allocation. fa_decode_create
+ * allocates a device status word per handle; this entry point uses instead a
+ * status word in a fixed array that the library declares statically on the
+ * device: FA_NOALLOC_STATUS_SLOTS words (256 bytes), held by every GPU that
+ * loads the library until the process exits.
+ *
+ * Arguments: those of fa_decode_create (the plan is built on the host for this
+ * call only), then those of fa_decode_run, then
+ *   status_slot  which word of the static array this call reports into, in
+ *                [0, FA_NOALLOC_STATUS_SLOTS); anything else is rejected with
+ *                FA_ERR_INVALID_ARG. The word is cleared on `stream` before the
+ *                launch, since the array keeps what the previous call left.
+ *                Calls that use the same slot and overlap on the GPU race on it.
+ *   status_out   NULL: the call only enqueues work (as fa_decode_run does).
+ *                Otherwise the call waits for `stream`, stores the FA_STATUS_*
+ *                bits in *status_out and returns FA_ERR_DEVICE if any is set.
+ *
+ * The first call on each device looks up the array's device address there
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * The call itself makes no device allocation and frees nothing.
+ */
+#define FA_NOALLOC_STATUS_SLOTS 64
+int fa_decode_run_noalloc(int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth, int ov_depth,
+                          int page_size, int num_q, int splitk, const void* q, const void* k_pages,
+                          const void* v_pages, const int32_t* page_table, const int32_t* seq_lens, float scale,
+                          void* out, float* lse, void* stream, int batch, int max_pages_per_seq, int num_pages,
+                          int status_slot, uint32_t* status_out);
+
 /* Destroy a handle (NULL is a no-op). Frees the status word. */
 int fa_decode_destroy(fa_decode_t h);
 

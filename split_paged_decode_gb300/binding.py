@@ -22,10 +22,11 @@ FA_STATUS_TIMEOUT = 1
 FA_STATUS_BAD_PAGE = 2
 FA_DEBUG_SKIP_LOADS = 1
 FA_DEBUG_FORCE_SIMT = 2
+FA_NOALLOC_STATUS_SLOTS = 64
 
 # Every symbol include/fa_decode.h declares.
 EXPORTED = ("fa_decode_create", "fa_decode_run", "fa_decode_check", "fa_decode_set_debug",
-            "fa_decode_describe", "fa_decode_destroy", "fa_decode_last_error")
+            "fa_decode_describe", "fa_decode_run_noalloc", "fa_decode_destroy", "fa_decode_last_error")
 
 
 class FaDecodeError(RuntimeError):
@@ -59,6 +60,9 @@ def load_library(path: str | None = None):
     lib.fa_decode_set_debug.restype = i32
     lib.fa_decode_describe.argtypes = [vp, ctypes.c_char_p, i32]
     lib.fa_decode_describe.restype = i32
+    lib.fa_decode_run_noalloc.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                          ctypes.c_float, vp, vp, vp, i32, i32, i32, i32, ctypes.POINTER(u32)]
+    lib.fa_decode_run_noalloc.restype = i32
     lib.fa_decode_destroy.argtypes = [vp]
     lib.fa_decode_destroy.restype = i32
     lib.fa_decode_last_error.argtypes = []
@@ -136,6 +140,31 @@ def fa_decode_describe(h: int) -> str:
     buf = ctypes.create_string_buffer(512)
     _check(load_library().fa_decode_describe(h, buf, len(buf)))
     return buf.value.decode()
+
+
+def fa_decode_run_noalloc(num_q_heads: int, num_kv_heads: int, qk_depth: int, nope_depth: int, ov_depth: int,
+                          page_size: int, num_q: int, splitk: int, q, k_pages, v_pages, page_table, seq_lens,
+                          scale: float, out, lse, stream=None, batch: int | None = None,
+                          max_pages_per_seq: int | None = None, num_pages: int | None = None,
+                          status_slot: int = 0, wait: bool = True) -> int | None:
+    """One decode forward without any device allocation (see include/fa_decode.h).
+
+    For callers that cannot allocate device memory. With wait=True the call
+    synchronises the stream and returns the status bits (raising FaDecodeError
+    if any is set); with wait=False it only enqueues and returns None.
+    """
+    if batch is None:
+        batch = int(q.shape[0])
+    if max_pages_per_seq is None:
+        max_pages_per_seq = int(page_table.shape[1])
+    if num_pages is None:
+        num_pages = int(k_pages.shape[0])
+    st = ctypes.c_uint32(0)
+    _check(load_library().fa_decode_run_noalloc(
+        num_q_heads, num_kv_heads, qk_depth, nope_depth, ov_depth, page_size, num_q, splitk, _addr(q),
+        _addr(k_pages), _addr(v_pages), _addr(page_table), _addr(seq_lens), float(scale), _addr(out), _addr(lse),
+        _stream(stream), batch, max_pages_per_seq, num_pages, status_slot, ctypes.byref(st) if wait else None))
+    return int(st.value) if wait else None
 
 
 def fa_decode_destroy(h: int) -> None:

@@ -187,16 +187,12 @@ int prepare_kernel(const fa_decode* h, const fad::KernelGeometry& g)
 
 }  // namespace
 
-extern "C" {
-
-const char* fa_decode_last_error(void) { return g_last_error.c_str(); }
-
-int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth,
-                     int ov_depth, int page_size, int num_q, int splitk)
+// Validation, kernel choice and per-kernel attributes of a plan (the
+// FA4Config constructor and supported() checks). Allocates nothing; the
+// caller provides the status word.
+static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth, int ov_depth,
+                       int page_size, int num_q, int splitk)
 {
-    g_last_error.clear();
-    if (!out) return fail(FA_ERR_INVALID_ARG, "out handle pointer is NULL");
-    *out = nullptr;
     if (num_q_heads < 1 || num_kv_heads < 1)
         return fail(FA_ERR_INVALID_ARG, "head counts must be >= 1 (got %d q, %d kv)", num_q_heads, num_kv_heads);
     if (num_q_heads % num_kv_heads)
@@ -210,7 +206,6 @@ int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk
     if (!(splitk == 0 || splitk == 1 || splitk == 2 || splitk == 4 || splitk == 8 || splitk == 16))
         return fail(FA_ERR_INVALID_ARG, "splitk must be 0 (per sequence), 1, 2, 4, 8 or 16 (got %d)", splitk);
 
-    fa_decode tmp;
     std::memset(&tmp, 0, sizeof tmp);
     tmp.hq = num_q_heads;
     tmp.hkv = num_kv_heads;
@@ -282,8 +277,52 @@ int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk
     if (tmp.has_tc && (rc = prepare_kernel(&tmp, tmp.geo_tc))) return rc;
     if (tmp.has_tc && (rc = prepare_kernel(&tmp, tmp.geo_tc_big))) return rc;
     cudaDeviceGetAttribute(&tmp.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    return FA_OK;
+}
 
-    e = cudaMalloc(&tmp.d_status, 256);
+// Device memory for callers that cannot allocate (fa_decode_run_noalloc):
+// status words in a file-scope device array, so no call ever needs
+// cudaMalloc. Every GPU that loads this library holds the array until the
+// process exits. On the host the name g_noalloc_status only stands for the
+// symbol: its device address comes from cudaGetSymbolAddress, taken once per
+// device with that device current.
+static __device__ __align__(256) unsigned int g_noalloc_status[FA_NOALLOC_STATUS_SLOTS];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+unsigned int* g_noalloc_addr[kMaxDevices] = {};
+
+int noalloc_status_base(int dev, unsigned int** out)
+{
+    if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void* ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_status);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static status array)");
+        g_noalloc_addr[dev] = static_cast<unsigned int*>(ptr);
+    }
+    *out = g_noalloc_addr[dev];
+    return FA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+const char* fa_decode_last_error(void) { return g_last_error.c_str(); }
+
+int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth,
+                     int ov_depth, int page_size, int num_q, int splitk)
+{
+    g_last_error.clear();
+    if (!out) return fail(FA_ERR_INVALID_ARG, "out handle pointer is NULL");
+    *out = nullptr;
+    fa_decode tmp;
+    int rc = plan_decode(tmp, num_q_heads, num_kv_heads, qk_depth, nope_depth, ov_depth, page_size, num_q, splitk);
+    if (rc) return rc;
+
+    cudaError_t e = cudaMalloc(&tmp.d_status, 256);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status word)");
     e = cudaMemset(tmp.d_status, 0, 256);
     if (e != cudaSuccess) {
@@ -462,6 +501,44 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
         cudaError_t e = cudaLaunchKernelExC(&cfg, g.func, args);
         if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     }
+    return FA_OK;
+}
+
+int fa_decode_run_noalloc(int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth, int ov_depth,
+                          int page_size, int num_q, int splitk, const void* q, const void* k_pages,
+                          const void* v_pages, const int32_t* page_table, const int32_t* seq_lens, float scale,
+                          void* out, float* lse, void* stream, int batch, int max_pages_per_seq, int num_pages,
+                          int status_slot, uint32_t* status_out)
+{
+    g_last_error.clear();
+    if (status_slot < 0 || status_slot >= FA_NOALLOC_STATUS_SLOTS)
+        return fail(FA_ERR_INVALID_ARG, "status_slot %d is outside the %d status words of the static array",
+                    status_slot, FA_NOALLOC_STATUS_SLOTS);
+    // The plan lives on this stack frame; its tensor maps are encoded on the host.
+    fa_decode plan;
+    int rc = plan_decode(plan, num_q_heads, num_kv_heads, qk_depth, nope_depth, ov_depth, page_size, num_q, splitk);
+    if (rc) return rc;
+    unsigned int* base = nullptr;
+    if ((rc = noalloc_status_base(plan.device, &base))) return rc;
+    plan.d_status = base + status_slot;
+    // The array keeps whatever the previous call on this slot left: clear the
+    // word this call reports into, in stream order before the launch.
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(plan.d_status, 0, sizeof(unsigned int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the static status word");
+    if ((rc = fa_decode_run(&plan, q, k_pages, v_pages, page_table, seq_lens, scale, out, lse, stream, batch,
+                            max_pages_per_seq, num_pages)))
+        return rc;
+    if (!status_out) return FA_OK;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned int st = 0;
+    e = cudaMemcpy(&st, plan.d_status, sizeof st, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the static status word");
+    *status_out = st;
+    if (st)
+        return fail(FA_ERR_DEVICE, "device status 0x%x:%s%s", st, (st & FA_STATUS_TIMEOUT) ? " wait timed out" : "",
+                    (st & FA_STATUS_BAD_PAGE) ? " page id or length out of range" : "");
     return FA_OK;
 }
 
