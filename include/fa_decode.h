@@ -123,12 +123,38 @@ int fa_decode_check(fa_decode_t h, void* stream, uint32_t* status_out);
  * Test hooks. flags: FA_DEBUG_SKIP_LOADS makes the load warp issue no copies,
  * so the first bounded wait of every CTA runs out; FA_DEBUG_FORCE_SIMT selects
  * the FMA kernel on shapes the tensor-core kernel would take (to compare the
- * two on one input); wait_limit_ns bounds every device wait (0 restores the
- * default of one second). Normal runs never need this call.
+ * two on one input); FA_DEBUG_TWO_CLUSTERS launches the tensor-core kernel of
+ * a fixed split with at most two clusters, each working through its share of
+ * the (sequence, kv head) units in turn, so that small inputs exercise the
+ * multi-unit schedule that large batches get; wait_limit_ns bounds every
+ * device wait (0 restores the default of one second). Normal runs never need
+ * this call.
  */
 #define FA_DEBUG_SKIP_LOADS 1u
 #define FA_DEBUG_FORCE_SIMT 2u   /* run the warp-level FMA kernel even where the tcgen05 one applies */
+#define FA_DEBUG_TWO_CLUSTERS 4u /* at most two clusters on the tensor-core path with a fixed split */
 int fa_decode_set_debug(fa_decode_t h, uint32_t flags, int64_t wait_limit_ns);
+
+/*
+ * Per-CTA timeline trace, a profiling aid with no counterpart on the pages.
+ * With a buffer set, each CTA of the tcgen05 kernel writes
+ * FA_TRACE_WORDS_PER_CTA 64-bit words at buf + FA_TRACE_WORDS_PER_CTA * c,
+ * c = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z) of the
+ * launch (the last one when a call makes several), holding %globaltimer
+ * readings in nanoseconds; 0 = event not reached:
+ *   [0] kernel entry  [1] first copy issued  [2] first S product observed
+ *   [3] exit
+ *   [4 + 8k + e] for the k-th unit (sequence, kv head) the CTA works on, k < 7:
+ *     e = 0 unit start (softmax warps), 1 its first S product observed,
+ *     2 its last O product folded in, 3 partial staged for the merge,
+ *     4 merge started, 5 merge done, 6 number of tiles of this rank (a count,
+ *     not a time), 7 the unit's first copy issued.
+ * CTAs past n_words / FA_TRACE_WORDS_PER_CTA record nothing. The caller owns
+ * the buffer (device memory, 8-byte aligned) and clears it; buf NULL turns
+ * tracing off. The FMA kernel records nothing.
+ */
+#define FA_TRACE_WORDS_PER_CTA 64
+int fa_decode_set_trace(fa_decode_t h, uint64_t* buf, int64_t n_words);
 
 /*
  * Describe the plan: kernel path, CTAs per cluster, keys per tile, pipeline

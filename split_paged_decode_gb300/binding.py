@@ -22,11 +22,14 @@ FA_STATUS_TIMEOUT = 1
 FA_STATUS_BAD_PAGE = 2
 FA_DEBUG_SKIP_LOADS = 1
 FA_DEBUG_FORCE_SIMT = 2
+FA_DEBUG_TWO_CLUSTERS = 4
+FA_TRACE_WORDS_PER_CTA = 64
 FA_NOALLOC_STATUS_SLOTS = 64
 
 # Every symbol include/fa_decode.h declares.
 EXPORTED = ("fa_decode_create", "fa_decode_run", "fa_decode_check", "fa_decode_set_debug",
-            "fa_decode_describe", "fa_decode_run_noalloc", "fa_decode_destroy", "fa_decode_last_error")
+            "fa_decode_set_trace", "fa_decode_describe", "fa_decode_run_noalloc", "fa_decode_destroy",
+            "fa_decode_last_error")
 
 
 class FaDecodeError(RuntimeError):
@@ -58,6 +61,8 @@ def load_library(path: str | None = None):
     lib.fa_decode_check.restype = i32
     lib.fa_decode_set_debug.argtypes = [vp, u32, i64]
     lib.fa_decode_set_debug.restype = i32
+    lib.fa_decode_set_trace.argtypes = [vp, vp, i64]
+    lib.fa_decode_set_trace.restype = i32
     lib.fa_decode_describe.argtypes = [vp, ctypes.c_char_p, i32]
     lib.fa_decode_describe.restype = i32
     lib.fa_decode_run_noalloc.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
@@ -134,6 +139,15 @@ def fa_decode_check(h: int, stream=None) -> int:
 
 def fa_decode_set_debug(h: int, flags: int, wait_limit_ns: int = 0) -> None:
     _check(load_library().fa_decode_set_debug(h, flags, wait_limit_ns))
+
+
+def fa_decode_set_trace(h: int, buf=None) -> None:
+    """Record a per-CTA timeline into `buf` (a device int64 tensor, zeroed by the
+    caller; FA_TRACE_WORDS_PER_CTA words per CTA) on later runs; None stops it."""
+    if buf is None:
+        _check(load_library().fa_decode_set_trace(h, None, 0))
+    else:
+        _check(load_library().fa_decode_set_trace(h, _addr(buf), buf.numel()))
 
 
 def fa_decode_describe(h: int) -> str:

@@ -224,6 +224,38 @@ __device__ __forceinline__ void cluster_wait()
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
+// Remote arrive without release semantics: signals progress only (it orders
+// none of this thread's memory accesses for the peer).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// Asynchronous store into a (peer or own) CTA's shared memory at a
+// shared::cluster address; its bytes count as completed transactions on the
+// mbarrier at `cluster_bar` (in the destination CTA), so a thread that sees
+// that barrier's phase complete sees the data. No release fence is involved.
+__device__ __forceinline__ void st_async_f4(uint32_t cluster_addr, float a, float b, float c, float d,
+                                            uint32_t cluster_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     cluster_addr),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_f2(uint32_t cluster_addr, float a, float b, uint32_t cluster_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                     cluster_addr),
+                 "f"(a), "f"(b), "r"(cluster_bar)
+                 : "memory");
+}
+
+// Orders this thread's prior accesses, and those it has acquired from other
+// threads, before its later ones at cluster scope.
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
 // Address of the same shared-memory variable in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t map_shared_rank(uint32_t local, uint32_t rank)
 {

@@ -128,12 +128,15 @@ struct fa_decode {
     fad::KernelGeometry geo;         // SIMT kernel, separate V cache (or V = K rows)
     fad::KernelGeometry geo_latent;  // SIMT kernel, V = prefix of the K row
     fad::KernelGeometry geo_tc;      // tcgen05 kernel, 3-slot ring (two CTAs per SM)
-    fad::KernelGeometry geo_tc_big;  // tcgen05 kernel, 6-slot ring (one CTA per SM)
+    fad::KernelGeometry geo_tc_big;  // tcgen05 kernel, 6-slot ring (one CTA per SM, several units per cluster)
     bool has_simt, has_latent, has_tc;
     int sm_count;
+    int tc_big_clusters;             // clusters of geo_tc_big (fixed split) resident at once
     unsigned int* d_status;
     uint32_t debug_flags;
     uint64_t wait_limit_ns;
+    uint64_t* trace;
+    int64_t trace_words;
     MapCache k_map, v_map, out_map[3];
 };
 
@@ -182,6 +185,34 @@ int prepare_kernel(const fa_decode* h, const fad::KernelGeometry& g)
             return fail(FA_ERR_UNSUPPORTED, "a cluster of %d CTAs with %d bytes of shared memory each cannot be "
                                             "scheduled on this device", P, g.smem_bytes);
     }
+    return FA_OK;
+}
+
+// Clusters of P CTAs of kernel g that the device holds at once.
+int resident_clusters(const fa_decode* h, const fad::KernelGeometry& g, int P, int* out)
+{
+    cudaError_t e;
+    if (P <= 1) {
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, g.func, g.threads, g.smem_bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        *out = per_sm * h->sm_count;
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3(P, 1, 1);
+        cfg.blockDim = dim3(g.threads, 1, 1);
+        cfg.dynamicSmemBytes = g.smem_bytes;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = P;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(out, g.func, &cfg);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+    }
+    if (*out < 1) return fail(FA_ERR_UNSUPPORTED, "kernel %s fits no cluster of %d CTAs", g.name, P);
     return FA_OK;
 }
 
@@ -277,6 +308,8 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
     if (tmp.has_tc && (rc = prepare_kernel(&tmp, tmp.geo_tc))) return rc;
     if (tmp.has_tc && (rc = prepare_kernel(&tmp, tmp.geo_tc_big))) return rc;
     cudaDeviceGetAttribute(&tmp.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (tmp.has_tc && splitk > 0 && (rc = resident_clusters(&tmp, tmp.geo_tc_big, splitk, &tmp.tc_big_clusters)))
+        return rc;
     return FA_OK;
 }
 
@@ -356,6 +389,16 @@ int fa_decode_set_debug(fa_decode_t h, uint32_t flags, int64_t wait_limit_ns)
     return FA_OK;
 }
 
+int fa_decode_set_trace(fa_decode_t h, uint64_t* buf, int64_t n_words)
+{
+    if (!h) return fail(FA_ERR_INVALID_ARG, "handle is NULL");
+    if (buf && (n_words < 0 || !is_aligned(buf, 8)))
+        return fail(FA_ERR_INVALID_ARG, "trace buffer must be 8-byte aligned with n_words >= 0");
+    h->trace = buf;
+    h->trace_words = buf ? n_words : 0;
+    return FA_OK;
+}
+
 int fa_decode_check(fa_decode_t h, void* stream, uint32_t* status_out)
 {
     if (!h) return fail(FA_ERR_INVALID_ARG, "handle is NULL");
@@ -420,10 +463,22 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     const bool use_tc = !use_latent && h->has_tc && !(h->debug_flags & FA_DEBUG_FORCE_SIMT && h->has_simt);
     if (!use_latent && !use_tc && !h->has_simt)
         return fail(FA_ERR_UNSUPPORTED, "no kernel for this call (latent layout %d)", (int)latent);
-    // A grid that fits in one wave gets the deep ring (one CTA per SM); more
-    // CTAs than SMs share SMs two by two with the shallow ring.
-    const int64_t ctas = (int64_t)(h->splitk > 0 ? h->splitk : 4) * h->hkv * h->row_blocks * batch;
-    const bool tc_big = use_tc && h->splitk > 0 && ctas <= h->sm_count;
+    // A fixed split takes the deep ring (one CTA per SM); when there are more
+    // (sequence, kv head) units than clusters fit on the device at once, the
+    // resident clusters work through the units in turn. The per-sequence
+    // split (three launches) shares SMs two by two with the shallow ring.
+    const bool tc_big = use_tc && h->splitk > 0;
+    const int64_t units = (int64_t)h->hkv * batch;
+    int64_t clusters = units;
+    if (tc_big) {
+        const int64_t most = (h->debug_flags & FA_DEBUG_TWO_CLUSTERS) ? 2 : h->tc_big_clusters;
+        if (clusters > most) {
+            // As many rounds as the resident clusters need, spread evenly: the
+            // fewest clusters that still finish in that many rounds.
+            const int64_t rounds = (units + most - 1) / most;
+            clusters = (units + rounds - 1) / rounds;
+        }
+    }
     const fad::KernelGeometry& g =
         use_latent ? h->geo_latent : (use_tc ? (tc_big ? h->geo_tc_big : h->geo_tc) : h->geo);
     const int bn = g.keys_per_tile;
@@ -469,6 +524,8 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     p.debug_flags = h->debug_flags;
     p.wait_limit_ns = h->wait_limit_ns;
     p.auto_split = h->splitk == 0 ? 1 : 0;
+    p.trace = reinterpret_cast<unsigned long long*>(h->trace);
+    p.trace_ctas = h->trace_words / FA_TRACE_WORDS_PER_CTA;
 
     int splits[3];
     const int ns = split_list(h, splits);
@@ -485,7 +542,9 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
 
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
-        cfg.gridDim = dim3(P, h->hkv * h->row_blocks, batch);
+        // Cluster c (= blockIdx.y + gridDim.y * blockIdx.z) takes units
+        // c, c + G, ... of u = b * Hkv + kvh; with G = units that is one unit each.
+        cfg.gridDim = clusters == units ? dim3(P, h->hkv * h->row_blocks, batch) : dim3(P, (unsigned)clusters, 1);
         cfg.blockDim = dim3(g.threads, 1, 1);
         cfg.dynamicSmemBytes = g.smem_bytes;
         cfg.stream = s;

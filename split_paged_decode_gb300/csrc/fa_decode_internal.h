@@ -47,6 +47,8 @@ struct DecodeParams {
     float scale, scale_log2e;
     uint32_t debug_flags;
     uint64_t wait_limit_ns;
+    unsigned long long* trace;  // per-CTA timeline (FA_TRACE_WORDS_PER_CTA words each) or NULL
+    int64_t trace_ctas;         // CTAs the trace buffer holds
 };
 
 // Geometry of one compiled kernel variant, for planning and validation.

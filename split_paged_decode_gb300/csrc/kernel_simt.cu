@@ -373,8 +373,8 @@ __global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREA
     __syncthreads();  // staging complete (all warps; the load warp is idle here)
     if (P > 1) cluster_wait();  // every rank's publish barrier is initialised
     if (warp < C::NCW) {
-        splitk_merge_and_store<RB>(p, P, rank, b, kvh, row_block, stage_s, maxsum_s, out_s, publish_bar,
-                                   abort_flag, tid, C::NCT, 1);
+        splitk_merge_and_store<RB>(p, P, rank, b, kvh, row_block, stage_s, maxsum_s, out_s, publish_bar, 0,
+                                   0, abort_flag, tid, C::NCT, 1);
     } else if (lane == 0 && *abort_flag) {
         // Gave up early: let copies already issued, but never consumed, land
         // before the CTA exits (each wait again bounded).

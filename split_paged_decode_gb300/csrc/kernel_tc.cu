@@ -40,12 +40,19 @@ namespace fad {
 
 template <int NSLOT, int NRV>
 struct TcCfg {
+    // The deep-ring variant (one CTA per SM) works through several
+    // (sequence, kv head) units per cluster; it keeps dedicated Q, stage and
+    // output buffers so that a unit's epilogue overlaps the next unit's
+    // loads. The shallow-ring variant (two CTAs per SM) takes one unit per
+    // cluster and stages its epilogue in the drained ring.
+    static constexpr bool MULTI = NSLOT > kTcSlotsShared;
     static constexpr int D = 128;       // qk_depth == ov_depth
     static constexpr int BN = 128;      // keys per tile (M of S^T)
     static constexpr int NR = 16;       // padded query rows (N of both MMAs)
     static_assert(NRV == 4 || NRV == 8 || NRV == 16, "real rows per CTA");
-    static constexpr int THREADS = 224;
     static constexpr int WG0 = 3;       // first softmax warp (warps 3-6 cover TMEM quadrants 3, 0, 1, 2)
+    static constexpr int EPI = 7;       // the multi-unit variant's epilogue warp
+    static constexpr int THREADS = MULTI ? 256 : 224;
     static constexpr int TILE_BYTES = BN * D * 2;        // 32 KB: one K or V tile
     static constexpr int BOX_BYTES = BN * 128;           // one 64-column box of a tile
     static constexpr int Q_BYTES = NR * D * 2;           // 4 KB
@@ -60,25 +67,70 @@ struct TcCfg {
     static constexpr int TMEM_S0 = 0, TMEM_O0 = 2 * BUF_COLS;     // 0 / 128
     static constexpr int TMEM_COLS = 4 * BUF_COLS;                // 256
 
+    static constexpr int Q_BUFS = MULTI ? 2 : 1;                  // by unit parity
     static constexpr int OFF_RING = 0;                            // NSLOT x 32 KB
-    static constexpr int OFF_Q = NSLOT * TILE_BYTES;              // K-major SW128 [2 boxes][16][128 B]
-    static constexpr int OFF_P = OFF_Q + Q_BYTES;                 // [2 buffers][2 atoms][16][128 B]
+    static constexpr int OFF_Q = NSLOT * TILE_BYTES;              // K-major SW128 [Q_BUFS][2 boxes][16][128 B]
+    static constexpr int OFF_P = OFF_Q + Q_BUFS * Q_BYTES;        // [2 buffers][2 atoms][16][128 B]
     static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;           // float [2][4][NRV]
     static constexpr int OFF_MAXSUM = OFF_RED + 2 * 4 * NR * 4;   // float2 [NRV]
     static constexpr int OFF_BAR = OFF_MAXSUM + NR * 8;
     // barriers: slot_full[NSLOT], slot_empty[NSLOT], s_full[2], s_empty[2],
-    // p_full[2], (unused)[2], o_full[2], o_empty[2], q_full, publish, mma_done, tmem_ready
-    static constexpr int NBAR = 2 * NSLOT + 16;
+    // p_full[2], o_full[2], o_empty[2], q_full[2], q_empty[2], publish,
+    // mma_done, tmem_ready, recv_full[2], recv_free[2], (spare)
+    static constexpr int NBAR = 2 * NSLOT + 22;
     static constexpr int OFF_ROWS = OFF_BAR + NBAR * 8;          // int [4 tiles][16 segments]
-    static constexpr int OFF_MISC = OFF_ROWS + 4 * 16 * 4;       // tmem base, abort, S issued, O issued
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-    // The epilogue reuses the drained ring: f32 stage [P][16][BW] in slot 0,
-    // the bf16 output band in slot 1.
+    static constexpr int OFF_MISC = OFF_ROWS + 4 * 16 * 4;       // tmem base, abort, S next item, O next item
+    static constexpr int MISC_END = OFF_MISC + 16;
+    // Epilogue buffers. Single-unit variant: f32 stage [P][NRV][Dv / P] in the
+    // drained ring (slot 0) that peers pull from, bf16 output band in slot 1.
+    // Multi-unit variant: receive buffers that peers push into (one or two,
+    // by unit, as space allows: float [P][Dv / P][NRV] + float2 [P][NRV]),
+    // the combine weights float [P][NRV] and the output band.
+    static constexpr int OUT_BYTES = NRV * D * 2;
+    static constexpr int RECV_BUFS = NRV <= 8 ? 2 : 1;
+    static constexpr int RECV_O_BYTES = NRV * D * 4;
+    static constexpr int RECV_BYTES = RECV_O_BYTES + kMaxSplit * NRV * 8;
+    static constexpr int OFF_RECV = (MISC_END + 127) / 128 * 128;
+    static constexpr int OFF_WTAB = OFF_RECV + RECV_BUFS * RECV_BYTES;
     static constexpr int OFF_STAGE = 0;
-    static constexpr int OFF_OUT = TILE_BYTES;
+    static constexpr int OFF_OUT = MULTI ? (OFF_WTAB + kMaxSplit * NRV * 4 + 127) / 128 * 128 : TILE_BYTES;
+    static constexpr int SMEM_BYTES = (MULTI ? OFF_OUT + OUT_BYTES : MISC_END) + 1024;
     static_assert(NSLOT >= 2, "ring of at least one K and one V tile");
     static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms on 1024 bytes");
+    static_assert(OFF_OUT % 128 == 0, "TMA store source on 128 bytes");
+    // 227 KB of dynamic shared memory per CTA; two CTAs of the shallow ring
+    // share an SM's 228 KB, each with 1 KB reserved by the system.
+    static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
+    static_assert(MULTI || 2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs per SM");
 };
+
+// One unit of work: the query rows of kv head `kvh` of sequence `b`, units
+// numbered u = b * Hkv + kvh. Cluster c of G takes units c, c + G, c + 2G, ...
+struct Unit {
+    int u, b, kvh, L;
+};
+
+// Advances w.u to this cluster's next unit that this launch handles (with
+// the per-sequence split rule, sequences of another split are skipped) and
+// fills in the rest; false when none is left. Every role of the CTA walks
+// the same sequence of units.
+__device__ __forceinline__ bool next_unit(const DecodeParams& p, int stride, int n_units, Unit& w, bool report)
+{
+    for (; w.u < n_units; w.u += stride) {
+        const int b = w.u / p.num_kv_heads;
+        int L = p.seq_lens[b];
+        if (L < 0) {
+            if (report) atomicOr(p.status, FA_STATUS_BAD_PAGE);
+            L = 0;
+        }
+        if (p.auto_split && auto_split_for_len(L) != p.splitk) continue;
+        w.b = b;
+        w.kvh = w.u - b * p.num_kv_heads;
+        w.L = L;
+        return true;
+    }
+    return false;
+}
 
 // Warp reduce-scatter of N per-row values (max or sum over the warp's 32
 // lanes): recursive halving exchanges half of the remaining rows at each of
@@ -128,7 +180,7 @@ __device__ __forceinline__ int v_item(int i, int n) { return i == n - 1 ? 2 * n 
 constexpr float kRescaleThreshold = 8.0f;
 
 template <int NSLOT, int NRV>
-__global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
+__global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>::MULTI ? 1 : 2)
     tc_decode_kernel(const __grid_constant__ DecodeParams p)
 {
     using C = TcCfg<NSLOT, NRV>;
@@ -141,25 +193,33 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
     const int lane = tid & 31;
     const int P = p.splitk;
     const int rank = (int)blockIdx.x;
-    const int kvh = (int)blockIdx.y;
-    const int b = (int)blockIdx.z;
+    const int n_units = p.batch * p.num_kv_heads;
+    const int cluster_id = (int)(blockIdx.y + gridDim.y * blockIdx.z);
+    const int n_clusters = (int)(gridDim.y * gridDim.z);
 
-    int L = p.seq_lens[b];
-    if (L < 0) {
-        if (tid == 0 && rank == 0) atomicOr(p.status, FA_STATUS_BAD_PAGE);
-        L = 0;
-    }
-    if (p.auto_split && auto_split_for_len(L) != P) return;  // uniform across the cluster
+    // Optional timeline trace (a profiling aid): one thread writes each event.
+    const int64_t cta_lin = (int64_t)blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+    unsigned long long* const trace =
+        (p.trace != nullptr && cta_lin < p.trace_ctas) ? p.trace + cta_lin * FA_TRACE_WORDS_PER_CTA : nullptr;
+    auto stamp = [&](int slot) {
+        if (trace) trace[slot] = global_timer_ns();
+    };
+    constexpr int kTraceUnits = 7;
+    auto unit_slot = [](int k, int e) { return 4 + 8 * k + e; };
+    if (tid == 0) stamp(0);
 
     const uint32_t bar0 = sbase + C::OFF_BAR;
     const uint32_t slot_full = bar0, slot_empty = bar0 + 8 * NSLOT;
     const uint32_t s_full = bar0 + 16 * NSLOT, s_empty = s_full + 16, p_full = s_full + 32;
-    const uint32_t o_full = s_full + 64, o_empty = s_full + 80, q_full = s_full + 96, publish_bar = s_full + 104;
-    const uint32_t mma_done = s_full + 112, tmem_ready = s_full + 120;
+    const uint32_t o_full = s_full + 48, o_empty = s_full + 64, q_full = s_full + 80, q_empty = s_full + 96;
+    const uint32_t publish_bar = s_full + 112, mma_done = s_full + 120, tmem_ready = s_full + 128;
+    const uint32_t recv_full = s_full + 136, recv_free = s_full + 152;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-    // Progress of the two MMA warps (products issued), for the ring-order rule.
-    const uint32_t s_issued = sbase + C::OFF_MISC + 8, o_issued = sbase + C::OFF_MISC + 12;
+    // Ring-order progress of the two MMA warps: the global index of the next
+    // K (resp. V) item each will consume; every earlier item of its kind has
+    // been consumed.
+    const uint32_t s_next = sbase + C::OFF_MISC + 8, o_next = sbase + C::OFF_MISC + 12;
     float* red_s = reinterpret_cast<float*>(smem + C::OFF_RED);
     float2* maxsum_s = reinterpret_cast<float2*>(smem + C::OFF_MAXSUM);
 
@@ -174,11 +234,18 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
             mbar_init(p_full + 8 * i, 4);
             mbar_init(o_full + 8 * i, 1);
             mbar_init(o_empty + 8 * i, 4);
+            mbar_init(q_full + 8 * i, 4);  // one arrival per softmax warp
+            mbar_init(q_empty + 8 * i, 1);
         }
-        mbar_init(q_full, 1);
         mbar_init(publish_bar, P);
         mbar_init(mma_done, 2);
         mbar_init(tmem_ready, 1);
+        for (int i = 0; i < 2; ++i) {
+            // P > 1: the epilogue warp's expect_tx arrive plus the pushed bytes;
+            // P == 1: the epilogue warp and the four softmax warps arrive.
+            mbar_init(recv_full + 8 * i, P > 1 ? 1 : 5);
+            mbar_init(recv_free + 8 * i, P);  // one arrival per receiving rank
+        }
         *abort_flag = 0;
         *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 8) = 0;
         *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 12) = 0;
@@ -190,7 +257,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
     }
     __syncthreads();  // barriers initialised; the load warp may start at once
     // Peers arrive on this CTA's publish barrier only after the matching
-    // cluster wait (before the merge), so the prologue does not wait here.
+    // cluster wait (before the first merge), so the prologue does not wait here.
     if (P > 1) cluster_arrive_relaxed();
     uint32_t tmem = 0;
     if (warp == 1) {
@@ -203,21 +270,21 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
         if (lane == 0) mbar_arrive(tmem_ready);
     }
 
-    const int n_tiles = (L + C::BN - 1) / C::BN;
-    const int base = n_tiles / P, rem = n_tiles % P;
-    const int tile_begin = rank * base + min(rank, rem);
-    const int tile_count = base + (rank < rem ? 1 : 0);
-    const int n_items = 2 * tile_count;
+    // Tiles [tile_begin, tile_begin + tile_count) of a unit belong to this rank.
+    auto rank_tiles = [&](int L, int& tile_begin, int& tile_count) {
+        const int n_tiles = (L + C::BN - 1) / C::BN;
+        const int base = n_tiles / P, rem = n_tiles % P;
+        tile_begin = rank * base + min(rank, rem);
+        tile_count = base + (rank < rem ? 1 : 0);
+    };
 
-    // Softmax / correction state (warps 2-5), real rows only.
+    // Softmax / correction state (warps 3-6), real rows only.
     float m_run[NRV], l_part[NRV], o_acc[NRV];
-#pragma unroll
-    for (int r = 0; r < NRV; ++r) {
-        m_run[r] = -INFINITY;
-        l_part[r] = 0.f;
-        o_acc[r] = 0.f;
-    }
 
+    // Items (K or V tiles) and tiles are numbered globally over the units of
+    // this cluster, so ring slots, buffers and barrier phases run on across
+    // unit boundaries. Within a unit of n tiles the items come in the order
+    // K0 K1 V0 K2 V1 ... K_{n-1} V_{n-2} V_{n-1}.
     int issued = 0;
     if (warp == 0) {
         // ------------------------------------------------------------------ load warp
@@ -226,52 +293,68 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
             const uint64_t policy = l2_policy_evict_first();
             const int segs = C::BN / p.box_rows;  // <= 16
             int32_t* rows_s = reinterpret_cast<int32_t*>(smem + C::OFF_ROWS);
-            // Physical page of this lane's segment of tile t, or kNoSegment /
-            // kPastSequence (zero fill, no error); -1 past the page table.
             constexpr int kNoSegment = INT32_MIN, kPastSequence = INT32_MIN + 1;
-            auto page_of = [&](int t) -> int {
-                if (lane >= segs || t >= tile_count) return kNoSegment;
-                const int key = (tile_begin + t) * C::BN + lane * p.box_rows;
-                if (key >= L) return kPastSequence;
-                const int pslot = key / p.page_size;
-                if (pslot >= p.max_pages) return -1;
-                return p.page_table[(int64_t)b * p.max_pages + pslot];
-            };
-            int e0 = page_of(0), e1 = page_of(1), e2 = page_of(2);  // three tiles ahead
-            for (int j = 0; j < n_items; ++j) {
-                const int slot = j % NSLOT;
-                const bool is_v = (j == n_items - 1) || (j > 0 && (j & 1) == 0);
-                const int t = is_v ? (j == n_items - 1 ? tile_count - 1 : (j - 2) >> 1) : (j + 1) >> 1;
-                if (j >= NSLOT) {
-                    const bool ok = mbar_wait(slot_empty + 8 * slot, ((j / NSLOT) & 1) ^ 1, abort_flag, p.status,
-                                              p.wait_limit_ns);
-                    if (!__all_sync(0xffffffffu, ok)) break;
-                }
-                int32_t row;
-                if (!is_v) {
-                    row = p.oob_row;  // zero fill past the sequence or on a bad page
-                    if (e0 >= 0 && e0 < p.num_pages) {
-                        const int key = (tile_begin + t) * C::BN + lane * p.box_rows;
-                        row = (e0 * p.num_kv_heads + kvh) * p.page_size + key % p.page_size;
-                    } else if (e0 != kNoSegment && e0 != kPastSequence) {
-                        atomicOr(p.status, FA_STATUS_BAD_PAGE);
+            int J0 = 0, lu = 0;
+            bool ok = true;
+            Unit w{cluster_id, 0, 0, 0};
+            for (; ok && next_unit(p, n_clusters, n_units, w, tid == 0 && rank == 0); w.u += n_clusters, ++lu) {
+                int tile_begin, tile_count;
+                rank_tiles(w.L, tile_begin, tile_count);
+                const int n_items = 2 * tile_count;
+                // Physical page of this lane's segment of tile t, or kNoSegment /
+                // kPastSequence (zero fill, no error); -1 past the page table.
+                auto page_of = [&](int t) -> int {
+                    if (lane >= segs || t >= tile_count) return kNoSegment;
+                    const int key = (tile_begin + t) * C::BN + lane * p.box_rows;
+                    if (key >= w.L) return kPastSequence;
+                    const int pslot = key / p.page_size;
+                    if (pslot >= p.max_pages) return -1;
+                    return p.page_table[(int64_t)w.b * p.max_pages + pslot];
+                };
+                int e0 = page_of(0), e1 = page_of(1), e2 = page_of(2);  // three tiles ahead
+                for (int j = 0; j < n_items; ++j) {
+                    const int jj = J0 + j, slot = jj % NSLOT;
+                    const bool is_v = (j == n_items - 1) || (j > 0 && (j & 1) == 0);
+                    const int t = is_v ? (j == n_items - 1 ? tile_count - 1 : (j - 2) >> 1) : (j + 1) >> 1;
+                    if (jj >= NSLOT) {
+                        const bool got = mbar_wait(slot_empty + 8 * slot, ((jj / NSLOT) & 1) ^ 1, abort_flag,
+                                                   p.status, p.wait_limit_ns);
+                        if (!__all_sync(0xffffffffu, got)) {
+                            ok = false;
+                            break;
+                        }
                     }
-                    if (lane < 16) rows_s[(t & 3) * 16 + lane] = row;
-                    e0 = e1;
-                    e1 = e2;
-                    e2 = page_of(t + 3);
-                } else {
-                    row = lane < 16 ? rows_s[(t & 3) * 16 + lane] : p.oob_row;
+                    int32_t row;
+                    if (!is_v) {
+                        row = p.oob_row;  // zero fill past the sequence or on a bad page
+                        if (e0 >= 0 && e0 < p.num_pages) {
+                            const int key = (tile_begin + t) * C::BN + lane * p.box_rows;
+                            row = (e0 * p.num_kv_heads + w.kvh) * p.page_size + key % p.page_size;
+                        } else if (e0 != kNoSegment && e0 != kPastSequence) {
+                            atomicOr(p.status, FA_STATUS_BAD_PAGE);
+                        }
+                        if (lane < 16) rows_s[(t & 3) * 16 + lane] = row;
+                        e0 = e1;
+                        e1 = e2;
+                        e2 = page_of(t + 3);
+                    } else {
+                        row = lane < 16 ? rows_s[(t & 3) * 16 + lane] : p.oob_row;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(slot_full + 8 * slot, C::TILE_BYTES);
+                    __syncwarp();
+                    issued = jj + 1;
+                    if (lane < segs) {
+                        const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
+                        const uint32_t dst = sbase + C::OFF_RING + slot * C::TILE_BYTES + lane * p.box_rows * 128;
+                        tma_load_2d(dst, map, 0, row, slot_full + 8 * slot, policy);
+                        tma_load_2d(dst + C::BOX_BYTES, map, 64, row, slot_full + 8 * slot, policy);
+                    }
+                    if (lane == 0 && j == 0) {
+                        if (jj == 0) stamp(1);
+                        if (lu < kTraceUnits) stamp(unit_slot(lu, 7));
+                    }
                 }
-                if (lane == 0) mbar_arrive_expect_tx(slot_full + 8 * slot, C::TILE_BYTES);
-                __syncwarp();
-                issued = j + 1;
-                if (lane < segs) {
-                    const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
-                    const uint32_t dst = sbase + C::OFF_RING + slot * C::TILE_BYTES + lane * p.box_rows * 128;
-                    tma_load_2d(dst, map, 0, row, slot_full + 8 * slot, policy);
-                    tma_load_2d(dst + C::BOX_BYTES, map, 64, row, slot_full + 8 * slot, policy);
-                }
+                J0 += n_items;
             }
         }
     } else if (warp == 1 || warp == 2) {
@@ -281,73 +364,90 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
         // O_t = V_t^T P_t^T, each with one commit per tile. The softmax warps
         // release the ring slots and observe the P buffers' reuse themselves.
         //
-        // Ring-order rule: a slot's full barrier is waited on for an item only
-        // after the item that held the slot before has been consumed (a parity
-        // wait on a barrier whose previous phase has not completed would alias
-        // with that phase). When the previous item belongs to the other warp,
-        // its published progress counter is waited on first.
+        // Ring-order rule: a slot's full barrier is waited on for item j only
+        // after item j - NSLOT, which held the slot before, has been consumed
+        // (a parity wait on a barrier whose previous phase has not completed
+        // would alias with that phase). Each warp consumes its own kind in
+        // order, so it waits for the other warp's published next-item index
+        // to pass j - NSLOT.
         if (lane == 0) {
-            auto prev_consumed = [&](int item) -> bool {  // wait until `item` has been consumed
-                if (item < 0) return true;
-                const bool is_v = (item == n_items - 1) || (item > 0 && (item & 1) == 0);
-                const int t = is_v ? (item == n_items - 1 ? tile_count - 1 : (item - 2) >> 1) : (item + 1) >> 1;
-                return counter_wait(is_v ? o_issued : s_issued, (uint32_t)t, abort_flag, p.status, p.wait_limit_ns);
-            };
-            if (warp == 1) {
-                const uint32_t id_s = umma_idesc_bf16_f32(128, C::NR, false, false);
-                const uint64_t q_desc0 = umma_smem_desc(sbase + C::OFF_Q, 16, 1024, kLayoutSwizzle128);
-                const uint64_t k_desc0 = umma_smem_desc(sbase + C::OFF_RING, 16, 1024, kLayoutSwizzle128);
-                bool ok = mbar_wait(q_full, 0, abort_flag, p.status, p.wait_limit_ns);
-                for (int i = 0; ok && i < tile_count; ++i) {
-                    const int j = k_item(i), slot = j % NSLOT;
-                    if (!prev_consumed(j - NSLOT)) break;
-                    if (!mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns))
-                        break;
-                    if (i >= 2 &&
-                        !mbar_wait(s_empty + 8 * (i & 1), ((i >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns))
-                        break;
-                    tc_fence_after_sync();
-                    const uint64_t a0 = k_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
-                    const uint32_t d = tmem + C::TMEM_S0 + C::BUF_COLS * (i & 1);
-#pragma unroll
-                    for (int ks = 0; ks < C::D / 16; ++ks)
-                        umma_f16_ss(d + C::ACC_COLS * (ks % C::NACC),
-                                    a0 + (uint64_t)(((ks >> 2) * C::BOX_BYTES + (ks & 3) * 32) >> 4),
-                                    q_desc0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_s,
-                                    ks >= C::NACC);
-                    umma_commit(s_full + 8 * (i & 1));
-                    st_release_u32(s_issued, (uint32_t)(i + 1));
-                }
-            } else {
-                const uint32_t id_pv = umma_idesc_bf16_f32(128, C::NR, true, false);
-                // A = V^T, MN-major: 64-column atoms one box apart (LBO), 8-key groups 1024 B apart (SBO)
-                const uint64_t v_desc0 = umma_smem_desc(sbase + C::OFF_RING, C::BOX_BYTES, 1024, kLayoutSwizzle128);
-                // B = P, K-major: 64-key atoms of 16 rows x 128 B
-                const uint64_t p_desc0 = umma_smem_desc(sbase + C::OFF_P, 16, 1024, kLayoutSwizzle128);
+            const bool is_s = (warp == 1);
+            const uint32_t other_next = is_s ? o_next : s_next;
+            const uint32_t id_s = umma_idesc_bf16_f32(128, C::NR, false, false);
+            const uint64_t q_desc0 = umma_smem_desc(sbase + C::OFF_Q, 16, 1024, kLayoutSwizzle128);
+            const uint64_t k_desc0 = umma_smem_desc(sbase + C::OFF_RING, 16, 1024, kLayoutSwizzle128);
+            const uint32_t id_pv = umma_idesc_bf16_f32(128, C::NR, true, false);
+            // A = V^T, MN-major: 64-column atoms one box apart (LBO), 8-key groups 1024 B apart (SBO)
+            const uint64_t v_desc0 = umma_smem_desc(sbase + C::OFF_RING, C::BOX_BYTES, 1024, kLayoutSwizzle128);
+            // B = P, K-major: 64-key atoms of 16 rows x 128 B
+            const uint64_t p_desc0 = umma_smem_desc(sbase + C::OFF_P, 16, 1024, kLayoutSwizzle128);
+            if (!is_s) {
                 mbar_wait(tmem_ready, 0, abort_flag, p.status, p.wait_limit_ns);
                 tc_fence_after_sync();
                 tmem = *tmem_slot;
-                for (int t = 0; t < tile_count; ++t) {
-                    const int j = v_item(t, tile_count), slot = j % NSLOT;
-                    if (!prev_consumed(j - NSLOT)) break;
-                    if (!mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns))
-                        break;
-                    if (!mbar_wait(p_full + 8 * (t & 1), (t >> 1) & 1, abort_flag, p.status, p.wait_limit_ns)) break;
-                    if (t >= 2 &&
-                        !mbar_wait(o_empty + 8 * (t & 1), ((t >> 1) - 1) & 1, abort_flag, p.status, p.wait_limit_ns))
-                        break;
-                    tc_fence_after_sync();
-                    const uint64_t a0 = v_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
-                    const uint64_t b0 = p_desc0 + (uint64_t)(((t & 1) * C::P_BYTES) >> 4);
-                    const uint32_t d = tmem + C::TMEM_O0 + C::BUF_COLS * (t & 1);
-#pragma unroll
-                    for (int ks = 0; ks < C::BN / 16; ++ks)
-                        umma_f16_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)((ks * 2048) >> 4),
-                                    b0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_pv, ks >= C::NACC);
-                    umma_commit(o_full + 8 * (t & 1));
-                    st_release_u32(o_issued, (uint32_t)(t + 1));
-                }
             }
+            auto ring_turn = [&](int j) -> bool {  // item j may wait on its slot
+                return j < NSLOT ||
+                       counter_wait(other_next, (uint32_t)(j - NSLOT), abort_flag, p.status, p.wait_limit_ns);
+            };
+            int J0 = 0, gt = 0, lu = 0;
+            bool ok = true;
+            Unit w{cluster_id, 0, 0, 0};
+            for (; ok && next_unit(p, n_clusters, n_units, w, false); w.u += n_clusters, ++lu) {
+                int tile_begin, tile_count;
+                rank_tiles(w.L, tile_begin, tile_count);
+                if (is_s) {
+                    ok = mbar_wait(q_full + 8 * (lu & 1), (lu >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+                    const uint64_t qd = q_desc0 + (uint64_t)(((lu & 1) * C::Q_BYTES) >> 4);
+                    for (int i = 0; ok && i < tile_count; ++i) {
+                        const int gi = gt + i, j = J0 + k_item(i), slot = j % NSLOT;
+                        ok = ring_turn(j) &&
+                             mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns) &&
+                             (gi < 2 || mbar_wait(s_empty + 8 * (gi & 1), ((gi >> 1) - 1) & 1, abort_flag, p.status,
+                                                  p.wait_limit_ns));
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        const uint64_t a0 = k_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
+                        const uint32_t d = tmem + C::TMEM_S0 + C::BUF_COLS * (gi & 1);
+#pragma unroll
+                        for (int ks = 0; ks < C::D / 16; ++ks)
+                            umma_f16_ss(d + C::ACC_COLS * (ks % C::NACC),
+                                        a0 + (uint64_t)(((ks >> 2) * C::BOX_BYTES + (ks & 3) * 32) >> 4),
+                                        qd + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_s,
+                                        ks >= C::NACC);
+                        umma_commit(s_full + 8 * (gi & 1));
+                        st_release_u32(s_next, (uint32_t)(i + 1 < tile_count ? J0 + k_item(i + 1)
+                                                                             : J0 + 2 * tile_count));
+                    }
+                    // Q buffer lu & 1 is read by no further product of this warp.
+                    mbar_arrive(q_empty + 8 * (lu & 1));
+                } else {
+                    for (int t = 0; ok && t < tile_count; ++t) {
+                        const int gi = gt + t, j = J0 + v_item(t, tile_count), slot = j % NSLOT;
+                        ok = ring_turn(j) &&
+                             mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns) &&
+                             mbar_wait(p_full + 8 * (gi & 1), (gi >> 1) & 1, abort_flag, p.status, p.wait_limit_ns) &&
+                             (gi < 2 || mbar_wait(o_empty + 8 * (gi & 1), ((gi >> 1) - 1) & 1, abort_flag, p.status,
+                                                  p.wait_limit_ns));
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        const uint64_t a0 = v_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
+                        const uint64_t b0 = p_desc0 + (uint64_t)(((gi & 1) * C::P_BYTES) >> 4);
+                        const uint32_t d = tmem + C::TMEM_O0 + C::BUF_COLS * (gi & 1);
+#pragma unroll
+                        for (int ks = 0; ks < C::BN / 16; ++ks)
+                            umma_f16_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)((ks * 2048) >> 4),
+                                        b0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_pv,
+                                        ks >= C::NACC);
+                        umma_commit(o_full + 8 * (gi & 1));
+                        st_release_u32(o_next, (uint32_t)(t + 1 < tile_count ? J0 + v_item(t + 1, tile_count)
+                                                                             : J0 + 2 * tile_count));
+                    }
+                }
+                gt += tile_count;
+                J0 += 2 * tile_count;
+            }
+            st_release_u32(is_s ? s_next : o_next, 0xffffffffu);  // nothing more to wait for
             // mma_done expects one commit from each MMA warp: it fires once every
             // MMA of both warps has completed.
             umma_commit(mma_done);
@@ -355,7 +455,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
             mbar_wait(mma_done, 0, &keep_waiting, p.status, p.wait_limit_ns);
         }
         __syncwarp();
-    } else {
+    } else if (warp < C::WG0 + 4) {
         // ------------------------------------------------- softmax / correction warps
         const int wt = tid - 32 * C::WG0;             // 0..127
         const int quad = warp & 3;                    // TMEM lane quadrant of this warp
@@ -363,164 +463,386 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
         const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
         const float c2 = p.scale_log2e;
 
-        // Q rows -> K-major 128-byte-swizzled B operand; rows >= p.rows are zero.
-        for (int idx = wt; idx < C::NR * 16; idx += 128) {
-            const int r = idx >> 4, u = idx & 15;  // 16-byte chunk u of row r
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < p.rows) {
-                const int t = r / p.heads_per_cta;
-                const int h = kvh * p.group + r % p.heads_per_cta;
-                v = reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.num_q + t) * p.num_q_heads + h) * C::D)[u];
+        // Q rows of a unit -> K-major 128-byte-swizzled B operand; rows >= p.rows are zero.
+        auto load_q = [&](const Unit& x, uint4 (&v)[2]) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int idx = wt + 128 * k, r = idx >> 4, u = idx & 15;  // 16-byte chunk u of row r
+                v[k] = make_uint4(0, 0, 0, 0);
+                if (r < p.rows) {
+                    const int t = r / p.heads_per_cta;
+                    const int h = x.kvh * p.group + r % p.heads_per_cta;
+                    v[k] = reinterpret_cast<const uint4*>(
+                        p.q + (((int64_t)x.b * p.num_q + t) * p.num_q_heads + h) * C::D)[u];
+                }
             }
-            *reinterpret_cast<uint4*>(smem + C::OFF_Q + (u >> 3) * 2048 + r * 128 + (((u & 7) ^ (r & 7)) << 4)) = v;
+        };
+        auto store_q = [&](int buf, const uint4 (&v)[2]) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int idx = wt + 128 * k, r = idx >> 4, u = idx & 15;
+                *reinterpret_cast<uint4*>(smem + C::OFF_Q + buf * C::Q_BYTES + (u >> 3) * 2048 + r * 128 +
+                                          (((u & 7) ^ (r & 7)) << 4)) = v[k];
+            }
+        };
+
+        Unit w{cluster_id, 0, 0, 0};
+        bool have = next_unit(p, n_clusters, n_units, w, false);
+        if (have) {
+            uint4 qv[2];
+            load_q(w, qv);
+            store_q(0, qv);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full);
         }
-        fence_proxy_async_smem();
-        named_barrier_sync(1, 128);
-        if (wt == 0) mbar_arrive(q_full);
         mbar_wait(tmem_ready, 0, abort_flag, p.status, p.wait_limit_ns);
         tc_fence_after_sync();
         tmem = *tmem_slot;
 
-        int row_tok[NRV];  // visible-key bound of every row (0 for padding rows)
-#pragma unroll
-        for (int r = 0; r < NRV; ++r) row_tok[r] = r < p.rows ? L - p.num_q + r / p.heads_per_cta + 1 : 0;
-
-        float alpha_prev[NRV];
-        bool rescaled_prev = false;
-        auto correct = [&](int t, const float (&a)[NRV], bool rescaled) {
-            mbar_wait(o_full + 8 * (t & 1), (t >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
-            tc_fence_after_sync();
-            float ot[NRV];
-            tmem_ld4_sum(tmem + lane_addr + C::TMEM_O0 + C::BUF_COLS * (t & 1), C::ACC_COLS, ot);
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(o_empty + 8 * (t & 1));
-            // O_t has completed: V_t's ring slot is free, and so (for tile t + 2)
-            // is the P buffer it read.
-            if (wt == 0) mbar_arrive(slot_empty + 8 * (v_item(t, tile_count) % NSLOT));
-            if (rescaled) {
-#pragma unroll
-                for (int r = 0; r < NRV; ++r) o_acc[r] = fmaf(o_acc[r], a[r], ot[r]);
-            } else {
-#pragma unroll
-                for (int r = 0; r < NRV; ++r) o_acc[r] += ot[r];
-            }
-        };
         // lanes holding distinct rows after a reduce-scatter of NRV values
         const bool row_writer = (lane & (32 / NRV - 1)) == 0;
         bool seen_abort = false;  // sticky: this thread has seen the abort flag
-
-        for (int i = 0; i < tile_count; ++i) {
-            mbar_wait(s_full + 8 * (i & 1), (i >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
-            tc_fence_after_sync();
-            float s[NRV];
-            tmem_ld4_sum(tmem + lane_addr + C::TMEM_S0 + C::BUF_COLS * (i & 1), C::ACC_COLS, s);
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_empty + 8 * (i & 1));
-            // S_i has completed, so no MMA reads K_i any more: free its ring slot.
-            if (wt == 0) mbar_arrive(slot_empty + 8 * (k_item(i) % NSLOT));
-
-            const int key0 = (tile_begin + i) * C::BN;
-            const int key = key0 + my_lane;
-#pragma unroll
-            for (int r = 0; r < NRV; ++r) s[r] = key < row_tok[r] ? s[r] : -INFINITY;
-
-            // Lazy rescale: a row's running max moves only when some score
-            // exceeds it by more than the threshold. In the common case a single
-            // reducing barrier confirms that no thread needs it; otherwise the
-            // tile max is exchanged and the rows that exceed are moved.
-            bool need = false;
-#pragma unroll
-            for (int r = 0; r < NRV; ++r)
-                need |= (s[r] != -INFINITY) &&
-                        (m_run[r] == -INFINITY || (s[r] - m_run[r]) * c2 > kRescaleThreshold);
-            seen_abort |= (*abort_flag != 0);
-            bool rescale = false;
-            float alpha[NRV];
-            if (named_barrier_or(1, 128, need || seen_abort)) {
-                {
-                    int row;
-                    const float wmax = warp_reduce_scatter<NRV, true>(s, lane, row);
-                    if (row_writer) red_s[((i & 1) * 4 + quad) * NRV + row] = wmax;
-                }
-                seen_abort |= (*abort_flag != 0);
-                // The abort decision is reduced over the warpgroup, so it is uniform.
-                if (named_barrier_or(1, 128, seen_abort)) break;
-                float tmax[NRV];
-                const float* rq = red_s + (i & 1) * 4 * NRV;
-#pragma unroll
-                for (int r4 = 0; r4 < NRV / 4; ++r4) {
-                    const float4 a0 = reinterpret_cast<const float4*>(rq)[r4];
-                    const float4 a1 = reinterpret_cast<const float4*>(rq + NRV)[r4];
-                    const float4 a2 = reinterpret_cast<const float4*>(rq + 2 * NRV)[r4];
-                    const float4 a3 = reinterpret_cast<const float4*>(rq + 3 * NRV)[r4];
-                    tmax[4 * r4 + 0] = fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x));
-                    tmax[4 * r4 + 1] = fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y));
-                    tmax[4 * r4 + 2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
-                    tmax[4 * r4 + 3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
-                }
-                rescale = true;
-#pragma unroll
-                for (int r = 0; r < NRV; ++r) {
-                    const bool move = (m_run[r] == -INFINITY) ? (tmax[r] != -INFINITY)
-                                                              : ((tmax[r] - m_run[r]) * c2 > kRescaleThreshold);
-                    alpha[r] = 1.f;
-                    if (move) {
-                        alpha[r] = (m_run[r] == -INFINITY) ? 0.f : ex2_approx((m_run[r] - tmax[r]) * c2);
-                        m_run[r] = tmax[r];
-                        l_part[r] *= alpha[r];
-                    }
-                }
+        bool cluster_waited = false;
+        int J0 = 0, gt = 0, lu = 0;
+        while (have) {
+            const int L = w.L;
+            int tile_begin, tile_count;
+            rank_tiles(L, tile_begin, tile_count);
+            if (wt == 0 && lu < kTraceUnits) {
+                stamp(unit_slot(lu, 0));
+                if (trace) trace[unit_slot(lu, 6)] = (unsigned long long)tile_count;
             }
+            // The next unit of this cluster: its Q rows are fetched now and
+            // stored once the S warp has left the buffer's previous unit (after
+            // this unit's first tile), so the S warp runs straight on into it.
+            Unit nx = w;
+            nx.u += n_clusters;
+            const bool more = C::MULTI && next_unit(p, n_clusters, n_units, nx, false);
+            uint4 qn[2];
+            bool q_pending = more;
+            if (more) load_q(nx, qn);
+            auto put_next_q = [&]() {  // before a fence.proxy.async and the warp's q_full arrive
+                if (lu >= 1)
+                    mbar_wait(q_empty + 8 * ((lu + 1) & 1), ((lu - 1) >> 1) & 1, abort_flag, p.status,
+                              p.wait_limit_ns);
+                store_q((lu + 1) & 1, qn);
+            };
 #pragma unroll
             for (int r = 0; r < NRV; ++r) {
-                const float pr = (s[r] == -INFINITY) ? 0.f : ex2_approx((s[r] - m_run[r]) * c2);
-                l_part[r] += pr;
-                s[r] = pr;
+                m_run[r] = -INFINITY;
+                l_part[r] = 0.f;
+                o_acc[r] = 0.f;
             }
+            int row_tok[NRV];  // visible-key bound of every row (0 for padding rows)
+#pragma unroll
+            for (int r = 0; r < NRV; ++r) row_tok[r] = r < p.rows ? L - p.num_q + r / p.heads_per_cta + 1 : 0;
 
-            // P (bf16) -> K-major swizzled B operand of O^T = V^T P^T (rows >= NRV
-            // only feed output columns that are never read). Buffer i & 1 was
-            // last read by O_{i-2}, whose completion correct(i - 2) observed.
-            {
-                uint8_t* pb = smem + C::OFF_P + (i & 1) * C::P_BYTES + (my_lane >> 6) * 2048;
-                const int kk = my_lane & 63;
+            float alpha_prev[NRV];
+            bool rescaled_prev = false;
+            // O of tile t (global index gi) has completed: fold it into o_acc.
+            auto correct = [&](int t, int gi, const float (&a)[NRV], bool rescaled) {
+                mbar_wait(o_full + 8 * (gi & 1), (gi >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+                tc_fence_after_sync();
+                float ot[NRV];
+                tmem_ld4_sum(tmem + lane_addr + C::TMEM_O0 + C::BUF_COLS * (gi & 1), C::ACC_COLS, ot);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_empty + 8 * (gi & 1));
+                // O_t has completed: V_t's ring slot is free, and so (for tile t + 2)
+                // is the P buffer it read.
+                if (wt == 0) mbar_arrive(slot_empty + 8 * ((J0 + v_item(t, tile_count)) % NSLOT));
+                if (rescaled) {
+#pragma unroll
+                    for (int r = 0; r < NRV; ++r) o_acc[r] = fmaf(o_acc[r], a[r], ot[r]);
+                } else {
+#pragma unroll
+                    for (int r = 0; r < NRV; ++r) o_acc[r] += ot[r];
+                }
+            };
+
+            for (int i = 0; i < tile_count; ++i) {
+                const int gi = gt + i;
+                mbar_wait(s_full + 8 * (gi & 1), (gi >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+                if (wt == 0 && i == 0) {
+                    if (gi == 0) stamp(2);
+                    if (lu < kTraceUnits) stamp(unit_slot(lu, 1));
+                }
+                tc_fence_after_sync();
+                float s[NRV];
+                tmem_ld4_sum(tmem + lane_addr + C::TMEM_S0 + C::BUF_COLS * (gi & 1), C::ACC_COLS, s);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_empty + 8 * (gi & 1));
+                // S_i has completed, so no MMA reads K_i any more: free its ring slot.
+                if (wt == 0) mbar_arrive(slot_empty + 8 * ((J0 + k_item(i)) % NSLOT));
+
+                const int key0 = (tile_begin + i) * C::BN;
+                const int key = key0 + my_lane;
+#pragma unroll
+                for (int r = 0; r < NRV; ++r) s[r] = key < row_tok[r] ? s[r] : -INFINITY;
+
+                // Lazy rescale: a row's running max moves only when some score
+                // exceeds it by more than the threshold. In the common case a single
+                // reducing barrier confirms that no thread needs it; otherwise the
+                // tile max is exchanged and the rows that exceed are moved.
+                bool need = false;
 #pragma unroll
                 for (int r = 0; r < NRV; ++r)
-                    *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((((kk >> 3) ^ (r & 7))) << 4) + (kk & 7) * 2) =
-                        __float2bfloat16_rn(s[r]);
-            }
-            // Last tile of the sequence: zero the V rows past L so that unused
-            // cache rows (whatever they hold) meet P = 0 as exact zeros.
-            if (key0 + C::BN > L) {
-                const int j = v_item(i, tile_count), slot = j % NSLOT;
-                mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns);
-                if (key >= L) {
-                    uint4* vrow0 = reinterpret_cast<uint4*>(smem + C::OFF_RING + slot * C::TILE_BYTES + my_lane * 128);
-                    uint4* vrow1 = reinterpret_cast<uint4*>(smem + C::OFF_RING + slot * C::TILE_BYTES +
-                                                            C::BOX_BYTES + my_lane * 128);
+                    need |= (s[r] != -INFINITY) &&
+                            (m_run[r] == -INFINITY || (s[r] - m_run[r]) * c2 > kRescaleThreshold);
+                seen_abort |= (*abort_flag != 0);
+                bool rescale = false;
+                float alpha[NRV];
+                if (named_barrier_or(1, 128, need || seen_abort)) {
+                    {
+                        int row;
+                        const float wmax = warp_reduce_scatter<NRV, true>(s, lane, row);
+                        if (row_writer) red_s[((gi & 1) * 4 + quad) * NRV + row] = wmax;
+                    }
+                    seen_abort |= (*abort_flag != 0);
+                    // The abort decision is reduced over the warpgroup, so it is uniform.
+                    if (named_barrier_or(1, 128, seen_abort)) {
+                        seen_abort = true;
+                        break;
+                    }
+                    float tmax[NRV];
+                    const float* rq = red_s + (gi & 1) * 4 * NRV;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        vrow0[u] = make_uint4(0, 0, 0, 0);
-                        vrow1[u] = make_uint4(0, 0, 0, 0);
+                    for (int r4 = 0; r4 < NRV / 4; ++r4) {
+                        const float4 a0 = reinterpret_cast<const float4*>(rq)[r4];
+                        const float4 a1 = reinterpret_cast<const float4*>(rq + NRV)[r4];
+                        const float4 a2 = reinterpret_cast<const float4*>(rq + 2 * NRV)[r4];
+                        const float4 a3 = reinterpret_cast<const float4*>(rq + 3 * NRV)[r4];
+                        tmax[4 * r4 + 0] = fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x));
+                        tmax[4 * r4 + 1] = fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y));
+                        tmax[4 * r4 + 2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
+                        tmax[4 * r4 + 3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
+                    }
+                    rescale = true;
+#pragma unroll
+                    for (int r = 0; r < NRV; ++r) {
+                        const bool move = (m_run[r] == -INFINITY) ? (tmax[r] != -INFINITY)
+                                                                  : ((tmax[r] - m_run[r]) * c2 > kRescaleThreshold);
+                        alpha[r] = 1.f;
+                        if (move) {
+                            alpha[r] = (m_run[r] == -INFINITY) ? 0.f : ex2_approx((m_run[r] - tmax[r]) * c2);
+                            m_run[r] = tmax[r];
+                            l_part[r] *= alpha[r];
+                        }
                     }
                 }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full + 8 * (i & 1));
-
-            if (i >= 1) correct(i - 1, alpha_prev, rescaled_prev);
 #pragma unroll
-            for (int r = 0; r < NRV; ++r) alpha_prev[r] = rescale ? alpha[r] : 1.f;
-            rescaled_prev = rescale;
+                for (int r = 0; r < NRV; ++r) {
+                    const float pr = (s[r] == -INFINITY) ? 0.f : ex2_approx((s[r] - m_run[r]) * c2);
+                    l_part[r] += pr;
+                    s[r] = pr;
+                }
+
+                // P (bf16) -> K-major swizzled B operand of O^T = V^T P^T (rows >= NRV
+                // only feed output columns that are never read). Buffer gi & 1 was
+                // last read by O of global tile gi - 2, whose completion the
+                // correction of that tile observed.
+                {
+                    uint8_t* pb = smem + C::OFF_P + (gi & 1) * C::P_BYTES + (my_lane >> 6) * 2048;
+                    const int kk = my_lane & 63;
+#pragma unroll
+                    for (int r = 0; r < NRV; ++r)
+                        *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((((kk >> 3) ^ (r & 7))) << 4) +
+                                                          (kk & 7) * 2) = __float2bfloat16_rn(s[r]);
+                }
+                // Last tile of the sequence: zero the V rows past L so that unused
+                // cache rows (whatever they hold) meet P = 0 as exact zeros.
+                if (key0 + C::BN > L) {
+                    const int j = J0 + v_item(i, tile_count), slot = j % NSLOT;
+                    mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns);
+                    if (key >= L) {
+                        uint4* vrow0 =
+                            reinterpret_cast<uint4*>(smem + C::OFF_RING + slot * C::TILE_BYTES + my_lane * 128);
+                        uint4* vrow1 = reinterpret_cast<uint4*>(smem + C::OFF_RING + slot * C::TILE_BYTES +
+                                                                C::BOX_BYTES + my_lane * 128);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            vrow0[u] = make_uint4(0, 0, 0, 0);
+                            vrow1[u] = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                }
+                const bool q_now = q_pending;  // uniform: the first tile of the unit
+                if (q_now) put_next_q();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(p_full + 8 * (gi & 1));
+                    if (q_now) mbar_arrive(q_full + 8 * ((lu + 1) & 1));
+                }
+                q_pending = false;
+
+                if (i >= 1) correct(i - 1, gi - 1, alpha_prev, rescaled_prev);
+#pragma unroll
+                for (int r = 0; r < NRV; ++r) alpha_prev[r] = rescale ? alpha[r] : 1.f;
+                rescaled_prev = rescale;
+            }
+            // Bounded even after an abort. After an abort the O of the tile
+            // that broke the loop was never issued; the wait gives up at once.
+            if (tile_count > 0) correct(tile_count - 1, gt + tile_count - 1, alpha_prev, rescaled_prev);
+            if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 2));
+            gt += tile_count;
+            J0 += 2 * tile_count;
+            if (q_pending) {  // no tile stored it (no tiles, or an abort in the first)
+                put_next_q();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(q_full + 8 * ((lu + 1) & 1));
+            }
+
+            // ---------------------------------------------------- unit epilogue
+            // Row sums: per-thread partial sums -> warp reduce-scatter -> four warps.
+            {
+                int row;
+                const float wsum = warp_reduce_scatter<NRV, false>(l_part, lane, row);
+                named_barrier_sync(1, 128);  // red_s may still be read by the last tile's max step
+                if (row_writer) red_s[quad * NRV + row] = wsum;
+                named_barrier_sync(1, 128);
+            }
+            const int BW = p.band_cols;
+            const int dv = my_lane;
+            if constexpr (C::MULTI) {
+                // Push this rank's normalised partial into the band owners'
+                // receive buffers (see splitk_merge_pushed) and go on with the
+                // next unit; the epilogue warps merge.
+                const int rb = lu % C::RECV_BUFS, rk = lu / C::RECV_BUFS;
+                // Every receiver has finished with this buffer's previous unit.
+                if (rk >= 1)
+                    mbar_wait<true>(recv_free + 8 * rb, (rk - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+                if (P > 1 && !cluster_waited) {
+                    cluster_wait();  // every rank's barriers are initialised
+                    cluster_waited = true;
+                }
+                float v[NRV], lrow[NRV];
+#pragma unroll
+                for (int r = 0; r < NRV; ++r) {
+                    lrow[r] = red_s[r] + red_s[NRV + r] + red_s[2 * NRV + r] + red_s[3 * NRV + r];
+                    v[r] = lrow[r] > 0.f ? o_acc[r] * __frcp_rn(lrow[r]) : 0.f;  // lrow is uniform
+                }
+                const uint32_t recv0 = sbase + C::OFF_RECV + rb * C::RECV_BYTES;
+                const int q = dv / BW, col = dv % BW;
+                const uint32_t o_dst = recv0 + 4u * (uint32_t)((rank * BW + col) * NRV);
+                if (P > 1) {
+                    const uint32_t bar_q = map_shared_rank(recv_full + 8 * rb, q);
+                    const uint32_t dst_q = map_shared_rank(o_dst, q);
+#pragma unroll
+                    for (int r4 = 0; r4 < NRV / 4; ++r4)
+                        st_async_f4(dst_q + 16 * r4, v[4 * r4], v[4 * r4 + 1], v[4 * r4 + 2], v[4 * r4 + 3], bar_q);
+                    for (int idx = wt; idx < P * NRV; idx += 128) {
+                        const int qq = idx / NRV, rr = idx % NRV;
+                        float mm = 0.f, ll = 0.f;
+#pragma unroll
+                        for (int r = 0; r < NRV; ++r)
+                            if (r == rr) {
+                                mm = m_run[r];
+                                ll = lrow[r];
+                            }
+                        const uint32_t ms_dst = recv0 + C::RECV_O_BYTES + 8u * (uint32_t)(rank * NRV + rr);
+                        st_async_f2(map_shared_rank(ms_dst, qq), mm, ll, map_shared_rank(recv_full + 8 * rb, qq));
+                    }
+                } else {
+                    float* o_loc = reinterpret_cast<float*>(smem + (o_dst - sbase));
+#pragma unroll
+                    for (int r4 = 0; r4 < NRV / 4; ++r4)
+                        reinterpret_cast<float4*>(o_loc)[r4] =
+                            make_float4(v[4 * r4], v[4 * r4 + 1], v[4 * r4 + 2], v[4 * r4 + 3]);
+                    if (wt == 0) {
+                        float2* ms_loc = reinterpret_cast<float2*>(smem + (recv0 - sbase) + C::RECV_O_BYTES);
+#pragma unroll
+                        for (int r = 0; r < NRV; ++r) ms_loc[r] = make_float2(m_run[r], lrow[r]);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(recv_full + 8 * rb);
+                }
+                if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
+            } else {
+                float* stage_s = reinterpret_cast<float*>(smem + C::OFF_STAGE);
+                const int q = dv / BW, jc = dv % BW;
+#pragma unroll
+                for (int r = 0; r < NRV; ++r) {
+                    const float l = red_s[r] + red_s[NRV + r] + red_s[2 * NRV + r] + red_s[3 * NRV + r];
+                    if (wt == 0) maxsum_s[r] = make_float2(m_run[r], l);
+                    float inv = 0.f;
+                    if (l > 0.f) inv = __frcp_rn(l);  // l is the same in every thread: no divergence
+                    stage_s[(q * NRV + r) * BW + jc] = o_acc[r] * inv;
+                }
+                if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
+                named_barrier_sync(1, 128);
+                if (P > 1) {
+                    cluster_wait();  // every rank's publish barrier is initialised
+                    cluster_waited = true;
+                }
+                if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 4));
+                splitk_merge_and_store<NRV>(p, P, rank, w.b, w.kvh, 0, stage_s, maxsum_s,
+                                            reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), publish_bar, 0u, 0u,
+                                            abort_flag, wt, 128, 1);
+                if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 5));
+            }
+            ++lu;
+            // Uniform over the warpgroup: stop after an abort.
+            seen_abort |= (*abort_flag != 0);
+            if (named_barrier_or(1, 128, seen_abort) || !more) break;
+            w = nx;
         }
-        if (tile_count > 0) correct(tile_count - 1, alpha_prev, rescaled_prev);  // bounded even after an abort
+        if (P > 1 && !cluster_waited) cluster_wait();  // pairs with the early arrive
         tc_fence_before_sync();
+    } else {
+        // ------------------------------------------- epilogue warp (multi-unit variant)
+        // Merges each unit's pushed partials and stores the output band while
+        // the softmax warps work on the next unit.
+        bool cluster_waited = false;
+        int lu = 0;
+        Unit w{cluster_id, 0, 0, 0};
+        const uint32_t expect = (uint32_t)pushed_bytes(P, p.band_cols, NRV);
+        for (; next_unit(p, n_clusters, n_units, w, false); w.u += n_clusters, ++lu) {
+            const int rb = lu % C::RECV_BUFS, rk = lu / C::RECV_BUFS;
+            if (P > 1 && !cluster_waited) {
+                cluster_wait();  // every rank's barriers are initialised
+                cluster_waited = true;
+            }
+            // This buffer's previous phase completed (this warp waited for it),
+            // so the arrival belongs to this unit's phase; pushed bytes that
+            // landed earlier are already counted against it.
+            if (lane == 0) {
+                if (P > 1)
+                    mbar_arrive_expect_tx(recv_full + 8 * rb, expect);
+                else
+                    mbar_arrive(recv_full + 8 * rb);
+            }
+            const bool got = mbar_wait<true>(recv_full + 8 * rb, rk & 1, abort_flag, p.status, p.wait_limit_ns);
+            if (!__all_sync(0xffffffffu, got)) break;
+            if (lane == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 4));
+            const uint8_t* recv = smem + C::OFF_RECV + rb * C::RECV_BYTES;
+            splitk_merge_pushed<NRV>(p, P, rank, w.b, w.kvh, reinterpret_cast<const float*>(recv),
+                                     reinterpret_cast<const float2*>(recv + C::RECV_O_BYTES),
+                                     reinterpret_cast<float*>(smem + C::OFF_WTAB),
+                                     reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), lane);
+            // Release the buffer to every sender: all lanes' reads of it are
+            // complete (their results are in the band); one fence orders them
+            // ahead of the senders' next pushes, then relaxed arrives.
+            __syncwarp();
+            if (lane == 0) {
+                if (P > 1) {
+                    fence_acq_rel_cluster();
+                    for (int q = 0; q < P; ++q) mbar_arrive_cluster_relaxed(map_shared_rank(recv_free + 8 * rb, q));
+                } else {
+                    mbar_arrive(recv_free + 8 * rb);
+                }
+            }
+            if (lane == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 5));
+        }
+        if (lane == 0) tma_store_wait_read();  // the last band has been read out of shared memory
+        __syncwarp();
+        if (P > 1 && !cluster_waited) cluster_wait();  // pairs with the early arrive
     }
 
-    // All TMEM reads and MMAs are complete (the MMA lane waited for mma_done).
+    // All TMEM reads and MMAs are complete (the MMA lanes waited for mma_done).
     __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
@@ -533,39 +855,10 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, 2)
         for (int j = issued > NSLOT ? issued - NSLOT : 0; j < issued; ++j)
             mbar_wait(slot_full + 8 * (j % NSLOT), (j / NSLOT) & 1, &keep_waiting, p.status, p.wait_limit_ns);
     }
-
-    if (warp >= C::WG0) {
-        const int wt = tid - 32 * C::WG0;
-        const int quad = warp & 3;
-        const int dv = 32 * quad + lane;
-        // Row sums: per-thread partial sums -> warp reduce-scatter -> four warps.
-        {
-            int row;
-            const float wsum = warp_reduce_scatter<NRV, false>(l_part, lane, row);
-            named_barrier_sync(1, 128);  // red_s may still be read by the last tile's max step
-            if ((lane & (32 / NRV - 1)) == 0) red_s[quad * NRV + row] = wsum;
-            named_barrier_sync(1, 128);
-        }
-        float* stage_s = reinterpret_cast<float*>(smem + C::OFF_STAGE);
-        const int BW = p.band_cols;
-        const int q = dv / BW, j = dv % BW;
-#pragma unroll
-        for (int r = 0; r < NRV; ++r) {
-            const float l = red_s[r] + red_s[NRV + r] + red_s[2 * NRV + r] + red_s[3 * NRV + r];
-            if (wt == 0) maxsum_s[r] = make_float2(m_run[r], l);
-            float inv = 0.f;
-            if (l > 0.f) inv = __frcp_rn(l);  // l is the same in every thread: no divergence
-            stage_s[(q * NRV + r) * BW + j] = o_acc[r] * inv;
-        }
-        named_barrier_sync(1, 128);
-        if (P > 1) cluster_wait();  // every rank's publish barrier is initialised
-        splitk_merge_and_store<NRV>(p, P, rank, b, kvh, 0, stage_s, maxsum_s,
-                                      reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), publish_bar, abort_flag, wt,
-                                      128, 1);
-    }
-    if (P > 1 && warp < C::WG0) cluster_wait();  // pairs with the early arrive
+    if (P > 1 && warp < C::WG0) cluster_wait();  // pairs with the early arrive (the other warps waited above)
     __syncwarp();
     if (P > 1) cluster_sync_all();  // peers may still read this CTA's staged bands until here
+    if (tid == 0) stamp(3);
 }
 
 bool tc_geometry(int qk, int ov, int rows, int nslot, KernelGeometry* g)

@@ -36,11 +36,21 @@ namespace fad {
 // cluster barrier wait that guarantees every rank has initialised its
 // publish barrier. Thread tid 0 of the calling group publishes. `bar_id`
 // names a hardware barrier private to the group.
+//
+// A kernel that merges several units in turn with the same buffers passes
+// the parity of this unit's publish phase and a `stage_free_bar` (count P):
+// once this rank has read every peer's stage (its own included), it arrives
+// on that barrier in every rank, and a rank rewrites its stage for the next
+// unit only after its own barrier has completed the phase. A peer's publish for unit n + 1 then
+// cannot reach a rank before that rank's unit-n phase has completed (it would
+// need that rank's reads of the peer's unit-n stage), so one publish barrier
+// alternates parity safely. stage_free_bar == 0: a single unit, no arrivals.
 template <int RB>
 __device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, int P, int rank, int b,
                                                        int kvh, int row_block, const float* stage_s,
                                                        const float2* maxsum_s, uint16_t* out_s,
-                                                       uint32_t publish_bar, volatile int* abort_flag,
+                                                       uint32_t publish_bar, uint32_t publish_parity,
+                                                       uint32_t stage_free_bar, volatile int* abort_flag,
                                                        int tid, int nthreads, uint32_t bar_id)
 {
     const int BW = p.band_cols;
@@ -55,7 +65,7 @@ __device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, in
             // threads' staging writes before this release.
             for (int q = 0; q < P; ++q) mbar_arrive_cluster(map_shared_rank(publish_bar, q));
         }
-        mbar_wait<true>(publish_bar, 0, abort_flag, p.status, p.wait_limit_ns);
+        mbar_wait<true>(publish_bar, publish_parity, abort_flag, p.status, p.wait_limit_ns);
     }
 
     const int chunks = BW / 4;
@@ -108,12 +118,108 @@ __device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, in
     fence_proxy_async_smem();
     named_barrier_sync(bar_id, nthreads);
     if (tid == 0) {
+        // Every thread's remote reads are complete (their values are in the
+        // band); release the peers' stages for their next unit.
+        if (stage_free_bar != 0) {
+            if (P > 1)
+                for (int q = 0; q < P; ++q) mbar_arrive_cluster(map_shared_rank(stage_free_bar, q));
+            else
+                mbar_arrive(stage_free_bar);
+        }
         const int OC = p.out_chunk_cols;
         for (int c0 = 0; c0 < BW; c0 += OC)
             tma_store_3d(&p.tm_out, smem_addr(out_s + (c0 / OC) * RB * OC), rank * BW + c0,
                          kvh * p.group + row_block * p.heads_per_cta, b * p.num_q);
         tma_store_commit();
         tma_store_wait_read();  // the band's shared memory may be released once read
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Push variant (the multi-unit tcgen05 kernel). Pulling peers' partials with
+// remote loads needs a release at cluster scope on the publishing side, and
+// on a CTA whose loads are streaming such a release waits microseconds for
+// the copies in flight. Here every rank instead pushes, from registers, the
+// columns of its normalised partial O that each band owner needs, plus its
+// per-row (max, sum), into the owner's receive buffer with st.async; the
+// bytes complete on the owner's recv_full barrier, so the owner merges from
+// its own shared memory once that barrier's phase completes.
+//
+// Receive buffer of rank q, one per buffer index:
+//   recv_o  float  [P][BW][RB]: rank p's partial, column c of q's band, row r
+//           at ((p * BW + c) * RB + r)
+//   recv_ms float2 [P][RB]:     rank p's (max, sum) of row r
+// Bytes expected per unit: P * BW * RB * 4 + P * RB * 8.
+// ---------------------------------------------------------------------------
+__host__ __device__ constexpr int pushed_bytes(int P, int BW, int RB) { return P * BW * RB * 4 + P * RB * 8; }
+
+// Merge by one warp (`lane` 0..31) of the partials in this rank's receive
+// buffer, cast, TMA store of the band and lse (rank 0). The caller has waited
+// for the buffer's recv_full phase; it releases the buffer afterwards.
+// `wtab` is float [P][RB] of scratch for the combine weights.
+template <int RB>
+__device__ __forceinline__ void splitk_merge_pushed(const DecodeParams& p, int P, int rank, int b, int kvh,
+                                                    const float* recv_o, const float2* recv_ms, float* wtab,
+                                                    uint16_t* out_s, int lane)
+{
+    const int BW = p.band_cols;
+    const float c = p.scale_log2e;
+    // The previous unit's store of out_s must have read it.
+    if (lane == 0) tma_store_wait_read();
+    __syncwarp();
+    // Per row: Gmax over the partitions that saw keys, Gsum, and the weights
+    // w_q = sum_q * exp2((max_q - Gmax) * c) / Gsum (0 for an empty partition).
+    for (int r = lane; r < RB; r += 32) {
+        float gmax = -INFINITY;
+        for (int q = 0; q < P; ++q) {
+            const float2 ms = recv_ms[q * RB + r];
+            if (ms.y > 0.f) gmax = fmaxf(gmax, ms.x);
+        }
+        float gsum = 0.f;
+        for (int q = 0; q < P; ++q) {
+            const float2 ms = recv_ms[q * RB + r];
+            const float w = ms.y > 0.f ? ms.y * ex2_approx((ms.x - gmax) * c) : 0.f;
+            wtab[q * RB + r] = w;
+            gsum += w;
+        }
+        const float inv = gsum > 0.f ? 1.f / gsum : 0.f;
+        for (int q = 0; q < P; ++q) wtab[q * RB + r] *= inv;
+        if (rank == 0 && r < p.rows && p.lse != nullptr) {
+            const int t = r / p.heads_per_cta;
+            const int h = kvh * p.group + r % p.heads_per_cta;
+            // natural-log LSE of the scaled scores: scale * Gmax + ln(Gsum)
+            p.lse[((int64_t)b * p.num_q + t) * p.num_q_heads + h] =
+                gsum > 0.f ? p.scale * gmax + lg2_approx(gsum) * 0.6931471805599453f : -INFINITY;
+        }
+    }
+    __syncwarp();
+    const int OC = p.out_chunk_cols;
+    for (int col = lane; col < BW; col += 32) {
+        float o[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) o[r] = 0.f;
+        for (int q = 0; q < P; ++q) {
+            const float4* src = reinterpret_cast<const float4*>(recv_o + (q * BW + col) * RB);
+#pragma unroll
+            for (int r4 = 0; r4 < RB / 4; ++r4) {
+                const float4 v = src[r4];
+                o[4 * r4 + 0] = fmaf(wtab[q * RB + 4 * r4 + 0], v.x, o[4 * r4 + 0]);
+                o[4 * r4 + 1] = fmaf(wtab[q * RB + 4 * r4 + 1], v.y, o[4 * r4 + 1]);
+                o[4 * r4 + 2] = fmaf(wtab[q * RB + 4 * r4 + 2], v.z, o[4 * r4 + 2]);
+                o[4 * r4 + 3] = fmaf(wtab[q * RB + 4 * r4 + 3], v.w, o[4 * r4 + 3]);
+            }
+        }
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(out_s) + (col / OC) * RB * OC + col % OC;
+#pragma unroll
+        for (int r = 0; r < RB; ++r) dst[r * OC] = __float2bfloat16_rn(o[r]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        for (int c0 = 0; c0 < BW; c0 += OC)
+            tma_store_3d(&p.tm_out, smem_addr(out_s + (c0 / OC) * RB * OC), rank * BW + c0, kvh * p.group,
+                         b * p.num_q);
+        tma_store_commit();
     }
 }
 

@@ -49,6 +49,8 @@ class DeviceCall:
                                       w.ov_depth, w.page_size, w.num_q, P)
         if path == "simt":
             spd.fa_decode_set_debug(self.h, spd.FA_DEBUG_FORCE_SIMT, 0)
+        elif path == "two_clusters":  # each cluster works through many units in turn
+            spd.fa_decode_set_debug(self.h, spd.FA_DEBUG_TWO_CLUSTERS, 0)
 
     def describe(self) -> str:
         return spd.fa_decode_describe(self.h)

@@ -97,6 +97,13 @@ def test_valid_create_without_gpu_reports_cuda_error(lib):
     assert not h.value
 
 
+def test_trace_hook_rejects_null_handle(lib):
+    """The trace hook (a profiling aid) validates on the host like every call."""
+    assert lib.fa_decode_set_trace(None, None, 0) == spd.FA_ERR_INVALID_ARG
+    with pytest.raises(spd.FaDecodeError):
+        spd.fa_decode_set_trace(0, None)
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(FileNotFoundError):
         spd.load_library(str(tmp_path / "libfa_decode.so"))

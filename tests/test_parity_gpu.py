@@ -140,6 +140,41 @@ def test_nonfinite_rows_past_the_sequence_do_not_leak(path):
         check_against_oracle(call, what=f"non-finite tails {path}")
 
 
+# --- several (sequence, kv head) units per cluster ----------------------------------------
+
+@pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
+def test_multi_unit_schedule(P):
+    """Two clusters work through 2 x 7 units each, with empty sequences, sequences
+    shorter than one tile per rank (ranks without tiles) and tails of every kind."""
+    w = wl(batch=7, num_kv_heads=2, num_q_heads=8, splitk=P, page_size=64, seed=90 + P)
+    lens = [0, 1, 130, 700, 129, 2000, 64]
+    run_and_check(w, seq_lens=lens, what=f"multi-unit P{P}", path="two_clusters")
+
+
+@pytest.mark.parametrize("g,T", [(1, 1), (4, 1), (8, 1), (4, 4), (16, 1)])
+def test_multi_unit_rows(g, T):
+    w = wl(batch=5, num_kv_heads=3, num_q_heads=3 * g, num_q=T, splitk=4, seed=95 + g * T)
+    run_and_check(w, what=f"multi-unit g{g} T{T}", path="two_clusters")
+
+
+def test_multi_unit_matches_one_unit_per_cluster_bitwise():
+    """A unit's arithmetic does not depend on which cluster takes it."""
+    inp = generate(wl(batch=6, splitk=4, seed=97))
+    with DeviceCall(inp) as one, DeviceCall(inp, path="two_clusters") as many:
+        one.run()
+        many.run()
+        assert one.status() == 0 and many.status() == 0
+        assert torch.equal(one.out, many.out)
+        assert torch.equal(one.lse, many.lse)
+
+
+def test_many_units_default_grid():
+    """More units than resident clusters without any debug flag (the batched shape)."""
+    w = wl(batch=40, num_kv_heads=8, num_q_heads=32, splitk=4, page_size=128, seq_len_lo=1, seq_len_hi=3000,
+           seed=98)
+    run_and_check(w, rows=_sample_rows(w, 400, 9), what="many units")
+
+
 # --- the five workloads at full size -----------------------------------------------------
 
 def _sample_rows(w, n, seed):
