@@ -149,6 +149,8 @@ int fa_decode_set_debug(fa_decode_t h, uint32_t flags, int64_t wait_limit_ns);
  *     2 its last O product folded in, 3 partial staged for the merge,
  *     4 merge started, 5 merge done, 6 number of tiles of this rank (a count,
  *     not a time), 7 the unit's first copy issued.
+ *   [60] first unit's Q seen by the S-MMA warp  [61] first K tile landed
+ *   [62] first V tile landed  [63] first unit's Q stored by the softmax warps
  * CTAs past n_words / FA_TRACE_WORDS_PER_CTA record nothing. The caller owns
  * the buffer (device memory, 8-byte aligned) and clears it; buf NULL turns
  * tracing off. The FMA kernel records nothing.

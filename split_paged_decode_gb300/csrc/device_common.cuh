@@ -294,6 +294,14 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Arrive on a named barrier without waiting (a producer's half of a
+// producer / consumer pair of bar.arrive and bar.sync).
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t threads)
+{
+    __syncwarp();
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // Barrier over `threads` threads that also ORs a predicate across them: every
 // participant receives the same answer, so a decision taken on it is uniform
 // even when the inputs were read at different times.

@@ -9,22 +9,26 @@
 // with fp32 accumulators in tensor memory. This keeps the tile dense on the
 // tensor pipe while HBM stays the bound.
 //
-// Warp roles (one CTA = one cluster rank of one (sequence, kv head)):
-//   warp 0     load: page-table walk (entries fetched three tiles ahead),
+// Warp roles (one CTA = one cluster rank; a cluster works on one
+// (sequence, kv head) unit at a time, the deep-ring variant on several in turn):
+//   warp 0     load: page-table walk (warp-wide blocks of entries fetched a
+//              block ahead),
 //              TMA loads of 128-key K and V tiles (two 64-column
 //              128-byte-swizzled boxes per page segment, one lane per
 //              segment) into a ring of NSLOT 32 KB slots, in the order the
-//              MMA warp consumes them: K0 K1 V0 K2 V1 ... K_{n-1} V_{n-2} V_{n-1}
+//              MMA warps consume them (V lagging K by VLAG tiles, see k_item)
 //   warp 1     MMA S: allocates 256 TMEM columns (S and O, two buffers of four
 //              accumulators each) and issues every S_i = K_i Q^T;
-//   warp 2     MMA O: issues every O_t = V_t^T P_t^T; each MMA warp commits
-//              once per tile;
-//   warps 3-6  softmax + correction; they also release the ring slots once
-//              the MMA that read a slot has completed; (thread = TMEM lane = key for S, = value
+//   warp 2     MMA O: issues every O_t = V_t^T P_t^T; each MMA warp commits a
+//              tile's products to the softmax warps and to the ring slot it read;
+//   warps 3-6  softmax + correction (thread = TMEM lane = key for S, = value
 //              column for O): online softmax in exp2 form with the running
 //              max in raw score units, P^T to shared memory as bf16, and the
 //              correction O <- O * alpha + O_tile in registers; then the
-//              split-K epilogue (splitk_combine.cuh).
+//              split-K epilogue (splitk_combine.cuh): in the shallow-ring
+//              variant they merge themselves, in the deep-ring variant they
+//              push their partial to the band owners and go on;
+//   warp 7     (deep ring) epilogue: merges the pushed partials, stores the band.
 //
 // Geometry and vocabulary follow the FA4Config page (Modular MAX docs):
 // TMEM_S / TMEM_O / TMEM_P column maps, num_kv_stages, GQA fusion (field
@@ -46,13 +50,20 @@ struct TcCfg {
     // loads. The shallow-ring variant (two CTAs per SM) takes one unit per
     // cluster and stages its epilogue in the drained ring.
     static constexpr bool MULTI = NSLOT > kTcSlotsShared;
+    // V tiles are issued VLAG tiles after their K (<= 3: rows_s ring). A lag
+    // of 2 was measured slower than 1 on the deep ring: K tiles then wait in
+    // the ring for an S buffer instead.
+    static constexpr int VLAG = 1;
     static constexpr int D = 128;       // qk_depth == ov_depth
     static constexpr int BN = 128;      // keys per tile (M of S^T)
     static constexpr int NR = 16;       // padded query rows (N of both MMAs)
     static_assert(NRV == 4 || NRV == 8 || NRV == 16, "real rows per CTA");
-    static constexpr int WG0 = 3;       // first softmax warp (warps 3-6 cover TMEM quadrants 3, 0, 1, 2)
-    static constexpr int EPI = 7;       // the multi-unit variant's epilogue warp
-    static constexpr int THREADS = MULTI ? 256 : 224;
+    // Softmax warpgroups: two (taking alternate tiles) where the registers of
+    // one CTA per SM allow it, else one.
+    static constexpr int NWG = (MULTI && NRV <= 8) ? 2 : 1;
+    static constexpr int WG0 = 3;       // first softmax warp (warps 3-6, 7-10 each cover TMEM quadrants 3, 0, 1, 2)
+    static constexpr int EPI = WG0 + 4 * NWG;  // the multi-unit variant's epilogue warp
+    static constexpr int THREADS = MULTI ? 32 * (EPI + 1) : 224;
     static constexpr int TILE_BYTES = BN * D * 2;        // 32 KB: one K or V tile
     static constexpr int BOX_BYTES = BN * 128;           // one 64-column box of a tile
     static constexpr int Q_BYTES = NR * D * 2;           // 4 KB
@@ -94,7 +105,11 @@ struct TcCfg {
     static constexpr int OFF_WTAB = OFF_RECV + RECV_BUFS * RECV_BYTES;
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_OUT = MULTI ? (OFF_WTAB + kMaxSplit * NRV * 4 + 127) / 128 * 128 : TILE_BYTES;
-    static constexpr int SMEM_BYTES = (MULTI ? OFF_OUT + OUT_BYTES : MISC_END) + 1024;
+    // Two softmax warpgroups: the second's partial O [128 dv][NRV] and (max, sum) [NRV].
+    static constexpr int XCHG_O_BYTES = NWG == 2 ? D * NRV * 4 : 0;
+    static constexpr int OFF_XCHG = OFF_OUT + OUT_BYTES;
+    static constexpr int END_MULTI = OFF_XCHG + (NWG == 2 ? XCHG_O_BYTES + NRV * 8 : 0);
+    static constexpr int SMEM_BYTES = (MULTI ? END_MULTI : MISC_END) + 1024;
     static_assert(NSLOT >= 2, "ring of at least one K and one V tile");
     static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms on 1024 bytes");
     static_assert(OFF_OUT % 128 == 0, "TMA store source on 128 bytes");
@@ -170,9 +185,32 @@ __device__ __forceinline__ float warp_reduce_scatter(const float (&in)[N], int l
     return v[0];
 }
 
-// Position of tile i's K and V in the load sequence K0 K1 V0 K2 V1 ... V_{n-1}.
-__device__ __forceinline__ int k_item(int i) { return i == 0 ? 0 : 2 * i - 1; }
-__device__ __forceinline__ int v_item(int i, int n) { return i == n - 1 ? 2 * n - 1 : 2 * i + 2; }
+// Load order of a unit's n tiles with V lagging D tiles behind K: K0 .. K_D,
+// then V_t K_{t+D+1} for t = 0 .. n-D-2, then the remaining V in order; for
+// D = 1: K0 K1 V0 K2 V1 ... K_{n-1} V_{n-2} V_{n-1}. A later V spends less
+// time in the ring waiting for its P.
+template <int D>
+__device__ __forceinline__ int k_item(int i) { return i <= D ? i : 2 * i - D; }
+template <int D>
+__device__ __forceinline__ int v_item(int t, int n) { return t <= n - D - 2 ? D + 1 + 2 * t : n + t; }
+// Inverse: the tile and kind of position j.
+template <int D>
+__device__ __forceinline__ void item_at(int j, int n, bool& is_v, int& t)
+{
+    if (j < min(n, D + 1)) {
+        is_v = false;
+        t = j;
+        return;
+    }
+    const int m = j - (D + 1);
+    if (m < 2 * (n - D - 1)) {
+        is_v = (m & 1) == 0;
+        t = is_v ? (m >> 1) : ((m - 1) >> 1) + D + 1;
+    } else {
+        is_v = true;
+        t = j - n;
+    }
+}
 
 // Lazy rescaling: the running max of a row moves only when a tile's max
 // exceeds it by more than this many exp2 units, so most tiles skip the
@@ -207,6 +245,46 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
     constexpr int kTraceUnits = 7;
     auto unit_slot = [](int k, int e) { return 4 + 8 * k + e; };
     if (tid == 0) stamp(0);
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&p.tm_k);
+        tma_prefetch_map(&p.tm_v);
+    }
+
+    // Tiles [tile_begin, tile_begin + tile_count) of a unit belong to this rank.
+    auto rank_tiles = [&](int L, int& tile_begin, int& tile_count) {
+        const int n_tiles = (L + C::BN - 1) / C::BN;
+        const int base = n_tiles / P, rem = n_tiles % P;
+        tile_begin = rank * base + min(rank, rem);
+        tile_count = base + (rank < rem ? 1 : 0);
+    };
+    // Page-table entries reach the load warp in warp-wide blocks: lane l
+    // holds the entry of (tile tb + l / segs, page segment l % segs) of the
+    // block starting at tile tb, fetched one block ahead, and a tile's entries
+    // are shuffled out of it. The first block is fetched before the sequence
+    // length is known, guessing that the sequence fills its page-table row;
+    // the guess is checked once the length has arrived, so the two reads
+    // overlap instead of following one another.
+    const int segs = C::BN / p.box_rows;  // page segments per tile: 1, 2, 4, 8 or 16
+    const int tpb = 32 / segs;            // tiles per block of page entries
+    int spec_begin = -1, spec_count = 0, spec_raw = -1;
+    if (warp == 0 && cluster_id < n_units && p.max_pages <= INT32_MAX / C::BN / p.page_size) {
+        int gb, gc;
+        rank_tiles(p.max_pages * p.page_size, gb, gc);
+        spec_begin = gb;
+        spec_count = gc;
+        const int b0 = cluster_id / p.num_kv_heads;
+        const int t = lane / segs;
+        const int pslot = ((gb + t) * C::BN + (lane % segs) * p.box_rows) / p.page_size;
+        if (t < gc && pslot < p.max_pages) spec_raw = p.page_table[(int64_t)b0 * p.max_pages + pslot];
+    }
+    if (cluster_id >= n_units) return;  // (grids never have more clusters than units)
+    if (p.auto_split) {
+        // A cluster with no unit in this launch (the per-sequence split gives
+        // its sequences to another launch) leaves at once; the decision is the
+        // same in every CTA of the cluster.
+        Unit first{cluster_id, 0, 0, 0};
+        if (!next_unit(p, n_clusters, n_units, first, tid == 0 && rank == 0)) return;
+    }
 
     const uint32_t bar0 = sbase + C::OFF_BAR;
     const uint32_t slot_full = bar0, slot_empty = bar0 + 8 * NSLOT;
@@ -220,7 +298,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
     // K (resp. V) item each will consume; every earlier item of its kind has
     // been consumed.
     const uint32_t s_next = sbase + C::OFF_MISC + 8, o_next = sbase + C::OFF_MISC + 12;
-    float* red_s = reinterpret_cast<float*>(smem + C::OFF_RED);
+    float* red_s = reinterpret_cast<float*>(smem + C::OFF_RED);  // [2][4][NRV]: by tile parity (= warpgroup)
     float2* maxsum_s = reinterpret_cast<float2*>(smem + C::OFF_MAXSUM);
 
     if (tid == 0) {
@@ -251,10 +329,6 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
         *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 12) = 0;
         fence_mbarrier_init_cluster();
     }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&p.tm_k);
-        tma_prefetch_map(&p.tm_v);
-    }
     __syncthreads();  // barriers initialised; the load warp may start at once
     // Peers arrive on this CTA's publish barrier only after the matching
     // cluster wait (before the first merge), so the prologue does not wait here.
@@ -270,14 +344,6 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
         if (lane == 0) mbar_arrive(tmem_ready);
     }
 
-    // Tiles [tile_begin, tile_begin + tile_count) of a unit belong to this rank.
-    auto rank_tiles = [&](int L, int& tile_begin, int& tile_count) {
-        const int n_tiles = (L + C::BN - 1) / C::BN;
-        const int base = n_tiles / P, rem = n_tiles % P;
-        tile_begin = rank * base + min(rank, rem);
-        tile_count = base + (rank < rem ? 1 : 0);
-    };
-
     // Softmax / correction state (warps 3-6), real rows only.
     float m_run[NRV], l_part[NRV], o_acc[NRV];
 
@@ -291,7 +357,6 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
         // All 32 lanes run the loop; lane s owns page segment s of every tile.
         if (!(p.debug_flags & FA_DEBUG_SKIP_LOADS)) {
             const uint64_t policy = l2_policy_evict_first();
-            const int segs = C::BN / p.box_rows;  // <= 16
             int32_t* rows_s = reinterpret_cast<int32_t*>(smem + C::OFF_ROWS);
             constexpr int kNoSegment = INT32_MIN, kPastSequence = INT32_MIN + 1;
             int J0 = 0, lu = 0;
@@ -301,21 +366,28 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                 int tile_begin, tile_count;
                 rank_tiles(w.L, tile_begin, tile_count);
                 const int n_items = 2 * tile_count;
-                // Physical page of this lane's segment of tile t, or kNoSegment /
-                // kPastSequence (zero fill, no error); -1 past the page table.
-                auto page_of = [&](int t) -> int {
-                    if (lane >= segs || t >= tile_count) return kNoSegment;
-                    const int key = (tile_begin + t) * C::BN + lane * p.box_rows;
+                // This lane's entry of the block starting at tile tb: the physical
+                // page, or kNoSegment / kPastSequence (zero fill, no error); -1
+                // past the page table. `raw` >= -1: that entry, already read.
+                auto block_entry = [&](int tb, int raw = -2) -> int {
+                    const int t = tb + lane / segs;
+                    if (t >= tile_count) return kNoSegment;
+                    const int key = (tile_begin + t) * C::BN + (lane % segs) * p.box_rows;
                     if (key >= w.L) return kPastSequence;
                     const int pslot = key / p.page_size;
                     if (pslot >= p.max_pages) return -1;
-                    return p.page_table[(int64_t)w.b * p.max_pages + pslot];
+                    return raw >= -1 ? raw : p.page_table[(int64_t)w.b * p.max_pages + pslot];
                 };
-                int e0 = page_of(0), e1 = page_of(1), e2 = page_of(2);  // three tiles ahead
+                // The guess holds when the unit's first tiles are the guessed ones
+                // (then every entry block_entry needs below was read).
+                const bool guessed =
+                    lu == 0 && w.u == cluster_id && tile_begin == spec_begin && tile_count <= spec_count;
+                int blk_cur = block_entry(0, guessed ? spec_raw : -2), blk_next = block_entry(tpb);
                 for (int j = 0; j < n_items; ++j) {
                     const int jj = J0 + j, slot = jj % NSLOT;
-                    const bool is_v = (j == n_items - 1) || (j > 0 && (j & 1) == 0);
-                    const int t = is_v ? (j == n_items - 1 ? tile_count - 1 : (j - 2) >> 1) : (j + 1) >> 1;
+                    bool is_v;
+                    int t;
+                    item_at<C::VLAG>(j, tile_count, is_v, t);
                     if (jj >= NSLOT) {
                         const bool got = mbar_wait(slot_empty + 8 * slot, ((jj / NSLOT) & 1) ^ 1, abort_flag,
                                                    p.status, p.wait_limit_ns);
@@ -326,17 +398,22 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                     }
                     int32_t row;
                     if (!is_v) {
-                        row = p.oob_row;  // zero fill past the sequence or on a bad page
-                        if (e0 >= 0 && e0 < p.num_pages) {
-                            const int key = (tile_begin + t) * C::BN + lane * p.box_rows;
-                            row = (e0 * p.num_kv_heads + w.kvh) * p.page_size + key % p.page_size;
-                        } else if (e0 != kNoSegment && e0 != kPastSequence) {
-                            atomicOr(p.status, FA_STATUS_BAD_PAGE);
+                        if (t > 0 && (t & (tpb - 1)) == 0) {
+                            // Waits only if the block fetched a block of tiles ago has not arrived.
+                            blk_cur = blk_next;
+                            blk_next = block_entry(t + tpb);
                         }
-                        if (lane < 16) rows_s[(t & 3) * 16 + lane] = row;
-                        e0 = e1;
-                        e1 = e2;
-                        e2 = page_of(t + 3);
+                        const int e = __shfl_sync(0xffffffffu, blk_cur, (t & (tpb - 1)) * segs + (lane & (segs - 1)));
+                        row = p.oob_row;  // zero fill past the sequence or on a bad page
+                        if (lane < segs) {
+                            if (e >= 0 && e < p.num_pages) {
+                                const int key = (tile_begin + t) * C::BN + lane * p.box_rows;
+                                row = (e * p.num_kv_heads + w.kvh) * p.page_size + key % p.page_size;
+                            } else if (e != kNoSegment && e != kPastSequence) {
+                                atomicOr(p.status, FA_STATUS_BAD_PAGE);
+                            }
+                        }
+                        if (lane < 16) rows_s[(t & 3) * 16 + lane] = row;  // read by V_t, at most 3 tiles later
                     } else {
                         row = lane < 16 ? rows_s[(t & 3) * 16 + lane] : p.oob_row;
                     }
@@ -361,8 +438,9 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
         // ------------------------------------------------------------ MMA warps
         // One warp issues tcgen05.mma only every ~60 cycles, so the products go
         // to two warps: warp 1 issues every S_i = K_i Q^T, warp 2 every
-        // O_t = V_t^T P_t^T, each with one commit per tile. The softmax warps
-        // release the ring slots and observe the P buffers' reuse themselves.
+        // O_t = V_t^T P_t^T. Each commits a tile's products twice: to the
+        // softmax warps' barrier, and to the ring slot's empty barrier, which
+        // frees the slot for the load warp as soon as the product completes.
         //
         // Ring-order rule: a slot's full barrier is waited on for item j only
         // after item j - NSLOT, which held the slot before, has been consumed
@@ -398,14 +476,16 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                 rank_tiles(w.L, tile_begin, tile_count);
                 if (is_s) {
                     ok = mbar_wait(q_full + 8 * (lu & 1), (lu >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+                    if (lu == 0) stamp(60);
                     const uint64_t qd = q_desc0 + (uint64_t)(((lu & 1) * C::Q_BYTES) >> 4);
                     for (int i = 0; ok && i < tile_count; ++i) {
-                        const int gi = gt + i, j = J0 + k_item(i), slot = j % NSLOT;
+                        const int gi = gt + i, j = J0 + k_item<C::VLAG>(i), slot = j % NSLOT;
                         ok = ring_turn(j) &&
                              mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns) &&
                              (gi < 2 || mbar_wait(s_empty + 8 * (gi & 1), ((gi >> 1) - 1) & 1, abort_flag, p.status,
                                                   p.wait_limit_ns));
                         if (!ok) break;
+                        if (gi == 0) stamp(61);
                         tc_fence_after_sync();
                         const uint64_t a0 = k_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
                         const uint32_t d = tmem + C::TMEM_S0 + C::BUF_COLS * (gi & 1);
@@ -416,20 +496,22 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                                         qd + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_s,
                                         ks >= C::NACC);
                         umma_commit(s_full + 8 * (gi & 1));
-                        st_release_u32(s_next, (uint32_t)(i + 1 < tile_count ? J0 + k_item(i + 1)
+                        umma_commit(slot_empty + 8 * slot);  // K_i's slot is free once S_i has completed
+                        st_release_u32(s_next, (uint32_t)(i + 1 < tile_count ? J0 + k_item<C::VLAG>(i + 1)
                                                                              : J0 + 2 * tile_count));
                     }
                     // Q buffer lu & 1 is read by no further product of this warp.
                     mbar_arrive(q_empty + 8 * (lu & 1));
                 } else {
                     for (int t = 0; ok && t < tile_count; ++t) {
-                        const int gi = gt + t, j = J0 + v_item(t, tile_count), slot = j % NSLOT;
+                        const int gi = gt + t, j = J0 + v_item<C::VLAG>(t, tile_count), slot = j % NSLOT;
                         ok = ring_turn(j) &&
                              mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns) &&
                              mbar_wait(p_full + 8 * (gi & 1), (gi >> 1) & 1, abort_flag, p.status, p.wait_limit_ns) &&
                              (gi < 2 || mbar_wait(o_empty + 8 * (gi & 1), ((gi >> 1) - 1) & 1, abort_flag, p.status,
                                                   p.wait_limit_ns));
                         if (!ok) break;
+                        if (gi == 0) stamp(62);
                         tc_fence_after_sync();
                         const uint64_t a0 = v_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
                         const uint64_t b0 = p_desc0 + (uint64_t)(((gi & 1) * C::P_BYTES) >> 4);
@@ -440,7 +522,8 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                                         b0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_pv,
                                         ks >= C::NACC);
                         umma_commit(o_full + 8 * (gi & 1));
-                        st_release_u32(o_next, (uint32_t)(t + 1 < tile_count ? J0 + v_item(t + 1, tile_count)
+                        umma_commit(slot_empty + 8 * slot);  // V_t's slot is free once O_t has completed
+                        st_release_u32(o_next, (uint32_t)(t + 1 < tile_count ? J0 + v_item<C::VLAG>(t + 1, tile_count)
                                                                              : J0 + 2 * tile_count));
                     }
                 }
@@ -455,13 +538,21 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
             mbar_wait(mma_done, 0, &keep_waiting, p.status, p.wait_limit_ns);
         }
         __syncwarp();
-    } else if (warp < C::WG0 + 4) {
+    } else if (warp < C::EPI) {
         // ------------------------------------------------- softmax / correction warps
-        const int wt = tid - 32 * C::WG0;             // 0..127
+        // NWG warpgroups; warpgroup g takes the unit's tiles whose index is g
+        // modulo NWG and keeps its own running max, sum and O; at the end of a
+        // unit the second folds its partial into the first, which pushes the
+        // result. Buffers of S, P and O are indexed by the global tile index,
+        // so any warpgroup may consume any buffer; the barrier phases order it.
+        const int wg = (warp - C::WG0) >> 2;          // softmax warpgroup
+        const int wt = tid - 32 * C::WG0 - 128 * wg;  // 0..127 within it
+        const uint32_t wg_bar = 1 + wg;               // its named barrier
         const int quad = warp & 3;                    // TMEM lane quadrant of this warp
         const int my_lane = 32 * quad + lane;         // key (S) or value column (O) of this thread
         const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
         const float c2 = p.scale_log2e;
+        const bool lead = wg == 0;                    // stores Q, stamps the trace, merges, pushes
 
         // Q rows of a unit -> K-major 128-byte-swizzled B operand; rows >= p.rows are zero.
         auto load_q = [&](const Unit& x, uint4 (&v)[2]) {
@@ -488,13 +579,14 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
 
         Unit w{cluster_id, 0, 0, 0};
         bool have = next_unit(p, n_clusters, n_units, w, false);
-        if (have) {
+        if (have && lead) {
             uint4 qv[2];
             load_q(w, qv);
             store_q(0, qv);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(q_full);
+            if (wt == 0) stamp(63);
         }
         mbar_wait(tmem_ready, 0, abort_flag, p.status, p.wait_limit_ns);
         tc_fence_after_sync();
@@ -509,19 +601,20 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
             const int L = w.L;
             int tile_begin, tile_count;
             rank_tiles(L, tile_begin, tile_count);
-            if (wt == 0 && lu < kTraceUnits) {
+            if (lead && wt == 0 && lu < kTraceUnits) {
                 stamp(unit_slot(lu, 0));
                 if (trace) trace[unit_slot(lu, 6)] = (unsigned long long)tile_count;
             }
             // The next unit of this cluster: its Q rows are fetched now and
             // stored once the S warp has left the buffer's previous unit (after
-            // this unit's first tile), so the S warp runs straight on into it.
+            // this warpgroup's first tile of the unit), so the S warp runs
+            // straight on into it.
             Unit nx = w;
             nx.u += n_clusters;
             const bool more = C::MULTI && next_unit(p, n_clusters, n_units, nx, false);
             uint4 qn[2];
-            bool q_pending = more;
-            if (more) load_q(nx, qn);
+            bool q_pending = more && lead;
+            if (q_pending) load_q(nx, qn);
             auto put_next_q = [&]() {  // before a fence.proxy.async and the warp's q_full arrive
                 if (lu >= 1)
                     mbar_wait(q_empty + 8 * ((lu + 1) & 1), ((lu - 1) >> 1) & 1, abort_flag, p.status,
@@ -534,24 +627,23 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                 l_part[r] = 0.f;
                 o_acc[r] = 0.f;
             }
-            int row_tok[NRV];  // visible-key bound of every row (0 for padding rows)
-#pragma unroll
-            for (int r = 0; r < NRV; ++r) row_tok[r] = r < p.rows ? L - p.num_q + r / p.heads_per_cta + 1 : 0;
+            // Row r = t * heads + hh (query token t) sees keys < L - T + t + 1, so
+            // the rows that see key k are a suffix: r >= (k - (L - T + 1) + 1) * heads.
+            const int vis0 = L - p.num_q + 1;
 
             float alpha_prev[NRV];
             bool rescaled_prev = false;
-            // O of tile t (global index gi) has completed: fold it into o_acc.
-            auto correct = [&](int t, int gi, const float (&a)[NRV], bool rescaled) {
+            // O of this warpgroup's tile with global index gi has completed:
+            // fold it into o_acc.
+            auto correct = [&](int gi, const float (&a)[NRV], bool rescaled) {
                 mbar_wait(o_full + 8 * (gi & 1), (gi >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
                 tc_fence_after_sync();
                 float ot[NRV];
                 tmem_ld4_sum(tmem + lane_addr + C::TMEM_O0 + C::BUF_COLS * (gi & 1), C::ACC_COLS, ot);
                 tc_fence_before_sync();
                 __syncwarp();
+                // O has completed, so (for tile gi + 2) the P buffer it read is free.
                 if (lane == 0) mbar_arrive(o_empty + 8 * (gi & 1));
-                // O_t has completed: V_t's ring slot is free, and so (for tile t + 2)
-                // is the P buffer it read.
-                if (wt == 0) mbar_arrive(slot_empty + 8 * ((J0 + v_item(t, tile_count)) % NSLOT));
                 if (rescaled) {
 #pragma unroll
                     for (int r = 0; r < NRV; ++r) o_acc[r] = fmaf(o_acc[r], a[r], ot[r]);
@@ -561,10 +653,18 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                 }
             };
 
-            for (int i = 0; i < tile_count; ++i) {
+            // This warpgroup's tiles: local index i congruent to wg modulo NWG
+            // (by local index, so a unit's arithmetic does not depend on the
+            // units its cluster took before). Their global indices share a
+            // parity, so within a unit a warpgroup uses one buffer of S, P, O
+            // and red_s: (gt + wg) & 1 with two warpgroups.
+            const int i0 = C::NWG == 2 ? wg : 0;
+            const int gt0 = gt;
+            int prev_gi = -1;  // this warpgroup's previous tile, still to be folded in
+            for (int i = i0; i < tile_count; i += C::NWG) {
                 const int gi = gt + i;
                 mbar_wait(s_full + 8 * (gi & 1), (gi >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
-                if (wt == 0 && i == 0) {
+                if (lead && wt == 0 && i == i0) {
                     if (gi == 0) stamp(2);
                     if (lu < kTraceUnits) stamp(unit_slot(lu, 1));
                 }
@@ -574,13 +674,12 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(s_empty + 8 * (gi & 1));
-                // S_i has completed, so no MMA reads K_i any more: free its ring slot.
-                if (wt == 0) mbar_arrive(slot_empty + 8 * ((J0 + k_item(i)) % NSLOT));
 
                 const int key0 = (tile_begin + i) * C::BN;
                 const int key = key0 + my_lane;
+                const int r_min = key < vis0 ? 0 : (key >= L ? NRV : (key - vis0 + 1) * p.heads_per_cta);
 #pragma unroll
-                for (int r = 0; r < NRV; ++r) s[r] = key < row_tok[r] ? s[r] : -INFINITY;
+                for (int r = 0; r < NRV; ++r) s[r] = (r >= r_min && r < p.rows) ? s[r] : -INFINITY;
 
                 // Lazy rescale: a row's running max moves only when some score
                 // exceeds it by more than the threshold. In the common case a single
@@ -594,7 +693,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                 seen_abort |= (*abort_flag != 0);
                 bool rescale = false;
                 float alpha[NRV];
-                if (named_barrier_or(1, 128, need || seen_abort)) {
+                if (named_barrier_or(wg_bar, 128, need || seen_abort)) {
                     {
                         int row;
                         const float wmax = warp_reduce_scatter<NRV, true>(s, lane, row);
@@ -602,7 +701,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                     }
                     seen_abort |= (*abort_flag != 0);
                     // The abort decision is reduced over the warpgroup, so it is uniform.
-                    if (named_barrier_or(1, 128, seen_abort)) {
+                    if (named_barrier_or(wg_bar, 128, seen_abort)) {
                         seen_abort = true;
                         break;
                     }
@@ -642,7 +741,11 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                 // P (bf16) -> K-major swizzled B operand of O^T = V^T P^T (rows >= NRV
                 // only feed output columns that are never read). Buffer gi & 1 was
                 // last read by O of global tile gi - 2, whose completion the
-                // correction of that tile observed.
+                // correction of that tile has observed: one warpgroup folded it in
+                // during its previous tile; two fold it in here, before the store.
+                if constexpr (C::NWG == 2) {
+                    if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
+                }
                 {
                     uint8_t* pb = smem + C::OFF_P + (gi & 1) * C::P_BYTES + (my_lane >> 6) * 2048;
                     const int kk = my_lane & 63;
@@ -654,7 +757,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                 // Last tile of the sequence: zero the V rows past L so that unused
                 // cache rows (whatever they hold) meet P = 0 as exact zeros.
                 if (key0 + C::BN > L) {
-                    const int j = J0 + v_item(i, tile_count), slot = j % NSLOT;
+                    const int j = J0 + v_item<C::VLAG>(i, tile_count), slot = j % NSLOT;
                     mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns);
                     if (key >= L) {
                         uint4* vrow0 =
@@ -668,7 +771,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                         }
                     }
                 }
-                const bool q_now = q_pending;  // uniform: the first tile of the unit
+                const bool q_now = q_pending;  // uniform: this warpgroup's first tile of the unit
                 if (q_now) put_next_q();
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -678,15 +781,18 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                 }
                 q_pending = false;
 
-                if (i >= 1) correct(i - 1, gi - 1, alpha_prev, rescaled_prev);
+                if constexpr (C::NWG == 1) {
+                    if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
+                }
 #pragma unroll
                 for (int r = 0; r < NRV; ++r) alpha_prev[r] = rescale ? alpha[r] : 1.f;
                 rescaled_prev = rescale;
+                prev_gi = gi;
             }
             // Bounded even after an abort. After an abort the O of the tile
             // that broke the loop was never issued; the wait gives up at once.
-            if (tile_count > 0) correct(tile_count - 1, gt + tile_count - 1, alpha_prev, rescaled_prev);
-            if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 2));
+            if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
+            if (lead && wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 2));
             gt += tile_count;
             J0 += 2 * tile_count;
             if (q_pending) {  // no tile stored it (no tiles, or an abort in the first)
@@ -697,97 +803,141 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
             }
 
             // ---------------------------------------------------- unit epilogue
-            // Row sums: per-thread partial sums -> warp reduce-scatter -> four warps.
+            // Row sums: per-thread partial sums -> warp reduce-scatter -> four
+            // warps, in this warpgroup's half of red_s.
+            float* red_w = red_s + (C::NWG == 2 ? ((gt0 + wg) & 1) : 0) * 4 * NRV;
             {
                 int row;
                 const float wsum = warp_reduce_scatter<NRV, false>(l_part, lane, row);
-                named_barrier_sync(1, 128);  // red_s may still be read by the last tile's max step
-                if (row_writer) red_s[quad * NRV + row] = wsum;
-                named_barrier_sync(1, 128);
+                named_barrier_sync(wg_bar, 128);  // red_s may still be read by the last tile's max step
+                if (row_writer) red_w[quad * NRV + row] = wsum;
+                named_barrier_sync(wg_bar, 128);
             }
-            const int BW = p.band_cols;
-            const int dv = my_lane;
-            if constexpr (C::MULTI) {
-                // Push this rank's normalised partial into the band owners'
-                // receive buffers (see splitk_merge_pushed) and go on with the
-                // next unit; the epilogue warps merge.
-                const int rb = lu % C::RECV_BUFS, rk = lu / C::RECV_BUFS;
-                // Every receiver has finished with this buffer's previous unit.
-                if (rk >= 1)
-                    mbar_wait<true>(recv_free + 8 * rb, (rk - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
-                if (P > 1 && !cluster_waited) {
-                    cluster_wait();  // every rank's barriers are initialised
-                    cluster_waited = true;
-                }
-                float v[NRV], lrow[NRV];
+            float lrow[NRV];
 #pragma unroll
-                for (int r = 0; r < NRV; ++r) {
-                    lrow[r] = red_s[r] + red_s[NRV + r] + red_s[2 * NRV + r] + red_s[3 * NRV + r];
-                    v[r] = lrow[r] > 0.f ? o_acc[r] * __frcp_rn(lrow[r]) : 0.f;  // lrow is uniform
-                }
-                const uint32_t recv0 = sbase + C::OFF_RECV + rb * C::RECV_BYTES;
-                const int q = dv / BW, col = dv % BW;
-                const uint32_t o_dst = recv0 + 4u * (uint32_t)((rank * BW + col) * NRV);
-                if (P > 1) {
-                    const uint32_t bar_q = map_shared_rank(recv_full + 8 * rb, q);
-                    const uint32_t dst_q = map_shared_rank(o_dst, q);
+            for (int r = 0; r < NRV; ++r) lrow[r] = red_w[r] + red_w[NRV + r] + red_w[2 * NRV + r] + red_w[3 * NRV + r];
+            if constexpr (C::NWG == 2) {
+                // Fold the second warpgroup's partial into the first's:
+                // m = max(m_a, m_b), both sides scaled by exp2((m_x - m) * c).
+                float* xo = reinterpret_cast<float*>(smem + C::OFF_XCHG);          // [128 dv][NRV]
+                float2* xms = reinterpret_cast<float2*>(smem + C::OFF_XCHG + C::XCHG_O_BYTES);  // [NRV]
+                if (!lead) {
+                    // The first warpgroup has read the previous unit's exchange.
+                    if (lu >= 1) named_barrier_sync(4, 256);
 #pragma unroll
                     for (int r4 = 0; r4 < NRV / 4; ++r4)
-                        st_async_f4(dst_q + 16 * r4, v[4 * r4], v[4 * r4 + 1], v[4 * r4 + 2], v[4 * r4 + 3], bar_q);
-                    for (int idx = wt; idx < P * NRV; idx += 128) {
-                        const int qq = idx / NRV, rr = idx % NRV;
-                        float mm = 0.f, ll = 0.f;
+                        reinterpret_cast<float4*>(xo + my_lane * NRV)[r4] =
+                            make_float4(o_acc[4 * r4], o_acc[4 * r4 + 1], o_acc[4 * r4 + 2], o_acc[4 * r4 + 3]);
+                    if (wt == 0)
 #pragma unroll
-                        for (int r = 0; r < NRV; ++r)
-                            if (r == rr) {
-                                mm = m_run[r];
-                                ll = lrow[r];
-                            }
-                        const uint32_t ms_dst = recv0 + C::RECV_O_BYTES + 8u * (uint32_t)(rank * NRV + rr);
-                        st_async_f2(map_shared_rank(ms_dst, qq), mm, ll, map_shared_rank(recv_full + 8 * rb, qq));
+                        for (int r = 0; r < NRV; ++r) xms[r] = make_float2(m_run[r], lrow[r]);
+                }
+                named_barrier_sync(3, 256);
+                if (lead) {
+                    float ob[NRV];
+#pragma unroll
+                    for (int r4 = 0; r4 < NRV / 4; ++r4) {
+                        const float4 v4 = reinterpret_cast<const float4*>(xo + my_lane * NRV)[r4];
+                        ob[4 * r4] = v4.x;
+                        ob[4 * r4 + 1] = v4.y;
+                        ob[4 * r4 + 2] = v4.z;
+                        ob[4 * r4 + 3] = v4.w;
                     }
+#pragma unroll
+                    for (int r = 0; r < NRV; ++r) {
+                        const float2 mb = xms[r];
+                        const float m = fmaxf(m_run[r], mb.x);
+                        const float aa = m_run[r] == -INFINITY ? 0.f : ex2_approx((m_run[r] - m) * c2);
+                        const float ab = mb.x == -INFINITY ? 0.f : ex2_approx((mb.x - m) * c2);
+                        o_acc[r] = o_acc[r] * aa + ob[r] * ab;
+                        lrow[r] = lrow[r] * aa + mb.y * ab;
+                        m_run[r] = m;
+                    }
+                    if (more) named_barrier_arrive(4, 256);  // exchange read: the second may reuse it
+                }
+            }
+            if (lead) {
+                const int BW = p.band_cols;
+                const int dv = my_lane;
+                if constexpr (C::MULTI) {
+                    // Push this rank's normalised partial into the band owners'
+                    // receive buffers (see splitk_merge_pushed) and go on with the
+                    // next unit; the epilogue warp merges.
+                    const int rb = lu % C::RECV_BUFS, rk = lu / C::RECV_BUFS;
+                    // Every receiver has finished with this buffer's previous unit.
+                    if (rk >= 1)
+                        mbar_wait<true>(recv_free + 8 * rb, (rk - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+                    if (P > 1 && !cluster_waited) {
+                        cluster_wait();  // every rank's barriers are initialised
+                        cluster_waited = true;
+                    }
+                    float v[NRV];
+#pragma unroll
+                    for (int r = 0; r < NRV; ++r) v[r] = lrow[r] > 0.f ? o_acc[r] * __frcp_rn(lrow[r]) : 0.f;
+                    const uint32_t recv0 = sbase + C::OFF_RECV + rb * C::RECV_BYTES;
+                    const int q = dv / BW, col = dv % BW;
+                    const uint32_t o_dst = recv0 + 4u * (uint32_t)((rank * BW + col) * NRV);
+                    if (P > 1) {
+                        const uint32_t bar_q = map_shared_rank(recv_full + 8 * rb, q);
+                        const uint32_t dst_q = map_shared_rank(o_dst, q);
+#pragma unroll
+                        for (int r4 = 0; r4 < NRV / 4; ++r4)
+                            st_async_f4(dst_q + 16 * r4, v[4 * r4], v[4 * r4 + 1], v[4 * r4 + 2], v[4 * r4 + 3],
+                                        bar_q);
+                        for (int idx = wt; idx < P * NRV; idx += 128) {
+                            const int qq = idx / NRV, rr = idx % NRV;
+                            float mm = 0.f, ll = 0.f;
+#pragma unroll
+                            for (int r = 0; r < NRV; ++r)
+                                if (r == rr) {
+                                    mm = m_run[r];
+                                    ll = lrow[r];
+                                }
+                            const uint32_t ms_dst = recv0 + C::RECV_O_BYTES + 8u * (uint32_t)(rank * NRV + rr);
+                            st_async_f2(map_shared_rank(ms_dst, qq), mm, ll, map_shared_rank(recv_full + 8 * rb, qq));
+                        }
+                    } else {
+                        float* o_loc = reinterpret_cast<float*>(smem + (o_dst - sbase));
+#pragma unroll
+                        for (int r4 = 0; r4 < NRV / 4; ++r4)
+                            reinterpret_cast<float4*>(o_loc)[r4] =
+                                make_float4(v[4 * r4], v[4 * r4 + 1], v[4 * r4 + 2], v[4 * r4 + 3]);
+                        if (wt == 0) {
+                            float2* ms_loc = reinterpret_cast<float2*>(smem + (recv0 - sbase) + C::RECV_O_BYTES);
+#pragma unroll
+                            for (int r = 0; r < NRV; ++r) ms_loc[r] = make_float2(m_run[r], lrow[r]);
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(recv_full + 8 * rb);
+                    }
+                    if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
                 } else {
-                    float* o_loc = reinterpret_cast<float*>(smem + (o_dst - sbase));
+                    float* stage_s = reinterpret_cast<float*>(smem + C::OFF_STAGE);
+                    const int q = dv / BW, jc = dv % BW;
 #pragma unroll
-                    for (int r4 = 0; r4 < NRV / 4; ++r4)
-                        reinterpret_cast<float4*>(o_loc)[r4] =
-                            make_float4(v[4 * r4], v[4 * r4 + 1], v[4 * r4 + 2], v[4 * r4 + 3]);
-                    if (wt == 0) {
-                        float2* ms_loc = reinterpret_cast<float2*>(smem + (recv0 - sbase) + C::RECV_O_BYTES);
-#pragma unroll
-                        for (int r = 0; r < NRV; ++r) ms_loc[r] = make_float2(m_run[r], lrow[r]);
+                    for (int r = 0; r < NRV; ++r) {
+                        if (wt == 0) maxsum_s[r] = make_float2(m_run[r], lrow[r]);
+                        float inv = 0.f;
+                        if (lrow[r] > 0.f) inv = __frcp_rn(lrow[r]);  // uniform: no divergence
+                        stage_s[(q * NRV + r) * BW + jc] = o_acc[r] * inv;
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(recv_full + 8 * rb);
+                    if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
+                    named_barrier_sync(wg_bar, 128);
+                    if (P > 1) {
+                        cluster_wait();  // every rank's publish barrier is initialised
+                        cluster_waited = true;
+                    }
+                    if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 4));
+                    splitk_merge_and_store<NRV>(p, P, rank, w.b, w.kvh, 0, stage_s, maxsum_s,
+                                                reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), publish_bar, 0u,
+                                                0u, abort_flag, wt, 128, wg_bar);
+                    if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 5));
                 }
-                if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
-            } else {
-                float* stage_s = reinterpret_cast<float*>(smem + C::OFF_STAGE);
-                const int q = dv / BW, jc = dv % BW;
-#pragma unroll
-                for (int r = 0; r < NRV; ++r) {
-                    const float l = red_s[r] + red_s[NRV + r] + red_s[2 * NRV + r] + red_s[3 * NRV + r];
-                    if (wt == 0) maxsum_s[r] = make_float2(m_run[r], l);
-                    float inv = 0.f;
-                    if (l > 0.f) inv = __frcp_rn(l);  // l is the same in every thread: no divergence
-                    stage_s[(q * NRV + r) * BW + jc] = o_acc[r] * inv;
-                }
-                if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
-                named_barrier_sync(1, 128);
-                if (P > 1) {
-                    cluster_wait();  // every rank's publish barrier is initialised
-                    cluster_waited = true;
-                }
-                if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 4));
-                splitk_merge_and_store<NRV>(p, P, rank, w.b, w.kvh, 0, stage_s, maxsum_s,
-                                            reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), publish_bar, 0u, 0u,
-                                            abort_flag, wt, 128, 1);
-                if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 5));
             }
             ++lu;
-            // Uniform over the warpgroup: stop after an abort.
+            // Uniform over the softmax warpgroups: stop after an abort.
             seen_abort |= (*abort_flag != 0);
-            if (named_barrier_or(1, 128, seen_abort) || !more) break;
+            if (named_barrier_or(C::NWG == 2 ? 3 : wg_bar, 128 * C::NWG, seen_abort) || !more) break;
             w = nx;
         }
         if (P > 1 && !cluster_waited) cluster_wait();  // pairs with the early arrive
