@@ -129,7 +129,8 @@ struct fa_decode {
     fad::KernelGeometry geo_latent;  // SIMT kernel, V = prefix of the K row
     fad::KernelGeometry geo_tc;      // tcgen05 kernel, 3-slot ring (two CTAs per SM)
     fad::KernelGeometry geo_tc_big;  // tcgen05 kernel, 6-slot ring (one CTA per SM, several units per cluster)
-    bool has_simt, has_latent, has_tc;
+    fad::KernelGeometry geo_mla;     // tcgen05 kernel of the MLA latent layout (64 heads per CTA)
+    bool has_simt, has_latent, has_tc, has_mla;
     int sm_count;
     int tc_big_clusters;             // clusters of geo_tc_big (fixed split) resident at once
     unsigned int* d_status;
@@ -278,7 +279,9 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
                  fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsShared, &tmp.geo_tc) &&
                  fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsAlone, &tmp.geo_tc_big) &&
                  page_fits(tmp.geo_tc.keys_per_tile);
-    if (!tmp.has_simt && !tmp.has_tc)
+    tmp.has_mla = fad::mla_tc_geometry(qk_depth, ov_depth, tmp.nope, tmp.group, num_q, &tmp.geo_mla) &&
+                  page_fits(tmp.geo_mla.keys_per_tile);
+    if (!tmp.has_simt && !tmp.has_tc && !tmp.has_mla)
         return fail(FA_ERR_UNSUPPORTED, "no kernel for (qk %d, ov %d), %d rows per CTA and page_size %d "
                                         "(built: 64/64, 128/128, 576/512; page size and key tile must divide "
                                         "one another)", qk_depth, ov_depth, tmp.rows, page_size);
@@ -307,6 +310,7 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
     if (tmp.has_latent && (rc = prepare_kernel(&tmp, tmp.geo_latent))) return rc;
     if (tmp.has_tc && (rc = prepare_kernel(&tmp, tmp.geo_tc))) return rc;
     if (tmp.has_tc && (rc = prepare_kernel(&tmp, tmp.geo_tc_big))) return rc;
+    if (tmp.has_mla && (rc = prepare_kernel(&tmp, tmp.geo_mla))) return rc;
     cudaDeviceGetAttribute(&tmp.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (tmp.has_tc && splitk > 0 && (rc = resident_clusters(&tmp, tmp.geo_tc_big, splitk, &tmp.tc_big_clusters)))
         return rc;
@@ -421,13 +425,19 @@ int fa_decode_check(fa_decode_t h, void* stream, uint32_t* status_out)
 int fa_decode_describe(fa_decode_t h, char* buf, int size)
 {
     if (!h || !buf || size < 1) return fail(FA_ERR_INVALID_ARG, "handle or buffer is NULL");
-    const fad::KernelGeometry& g = h->has_tc ? h->geo_tc : h->geo;
+    // The kernel a run takes by default: the MLA tcgen05 kernel for the latent
+    // layout where it applies, the deep-ring tcgen05 kernel for a fixed split,
+    // the shallow-ring one for the per-sequence split, else the SIMT kernel.
+    const bool tc = h->has_mla || h->has_tc;
+    const fad::KernelGeometry& g =
+        h->has_mla ? h->geo_mla : (h->has_tc ? (h->splitk > 0 ? h->geo_tc_big : h->geo_tc) : h->geo);
+    const int rows = h->has_mla ? 64 : h->rows, row_blocks = h->has_mla ? h->group / 64 : h->row_blocks;
     snprintf(buf, (size_t)size,
              "path=%s kernel=%s simt_kernel=%s latent_kernel=%s splitk=%d%s threads=%d keys_per_tile=%d "
              "stages=%d rows=%d rows_capacity=%d row_blocks=%d smem=%d",
-             h->has_tc ? "tcgen05" : "simt", g.name, h->has_simt ? h->geo.name : "none",
+             tc ? "tcgen05" : "simt", g.name, h->has_simt ? h->geo.name : "none",
              h->has_latent ? h->geo_latent.name : "none", h->splitk, h->splitk == 0 ? "(per sequence: 1/2/4)" : "",
-             g.threads, g.keys_per_tile, g.stages, h->rows, h->rows_capacity, h->row_blocks, g.smem_bytes);
+             g.threads, g.keys_per_tile, g.stages, rows, h->has_mla ? 64 : h->rows_capacity, row_blocks, g.smem_bytes);
     return FA_OK;
 }
 
@@ -457,11 +467,14 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     const bool latent = (v_pages == nullptr || v_pages == k_pages);
     if (latent && h->dv > h->dk)
         return fail(FA_ERR_INVALID_ARG, "latent layout (v_pages NULL or == k_pages) needs ov_depth <= qk_depth");
-    // Kernel choice: the latent-layout SIMT kernel for the MLA latent cache,
-    // else the tcgen05 kernel where it applies, else the SIMT kernel.
-    const bool use_latent = latent && h->has_latent;
-    const bool use_tc = !use_latent && h->has_tc && !(h->debug_flags & FA_DEBUG_FORCE_SIMT && h->has_simt);
-    if (!use_latent && !use_tc && !h->has_simt)
+    // Kernel choice: for the MLA latent cache the MLA tcgen05 kernel (64 heads
+    // per CTA) where it applies, else the latent-layout SIMT kernel; otherwise
+    // the tcgen05 kernel where it applies, else the SIMT kernel.
+    const bool force_simt = (h->debug_flags & FA_DEBUG_FORCE_SIMT) != 0;
+    const bool use_mla = latent && h->has_mla && !(force_simt && h->has_latent);
+    const bool use_latent = latent && !use_mla && h->has_latent;
+    const bool use_tc = !use_mla && !use_latent && h->has_tc && !(force_simt && h->has_simt);
+    if (!use_mla && !use_latent && !use_tc && !h->has_simt)
         return fail(FA_ERR_UNSUPPORTED, "no kernel for this call (latent layout %d)", (int)latent);
     // A fixed split takes the deep ring (one CTA per SM); when there are more
     // (sequence, kv head) units than clusters fit on the device at once, the
@@ -479,14 +492,18 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
             clusters = (units + rounds - 1) / rounds;
         }
     }
-    const fad::KernelGeometry& g =
-        use_latent ? h->geo_latent : (use_tc ? (tc_big ? h->geo_tc_big : h->geo_tc) : h->geo);
+    const fad::KernelGeometry& g = use_mla ? h->geo_mla
+                                   : use_latent ? h->geo_latent
+                                                : (use_tc ? (tc_big ? h->geo_tc_big : h->geo_tc) : h->geo);
+    // Heads per CTA: 64 for the MLA kernel, else the plan's rows.
+    const int row_blocks = use_mla ? h->group / 64 : h->row_blocks;
+    const int heads_per_cta = use_mla ? 64 : h->heads_per_cta;
     const int bn = g.keys_per_tile;
     const int box_rows = h->page_size < bn ? h->page_size : bn;
 
     int rc = encode_cache_map(h->k_map, k_pages, h->dk, cache_rows, box_rows);
     if (rc) return rc;
-    if (latent && !use_latent) {
+    if (latent && !use_latent && !use_mla) {
         // V = K row prefix through a separate-V kernel (e.g. qk == ov): same rows, V width.
         rc = encode_cache_map(h->v_map, k_pages, h->dk, cache_rows, box_rows);
     } else if (!latent) {
@@ -497,7 +514,7 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     fad::DecodeParams p;
     std::memset(&p, 0, sizeof p);
     p.tm_k = h->k_map.map;
-    if (!use_latent) p.tm_v = h->v_map.map;
+    if (!use_latent && !use_mla) p.tm_v = h->v_map.map;
     p.q = static_cast<const uint16_t*>(q);
     p.page_table = page_table;
     p.seq_lens = seq_lens;
@@ -513,9 +530,9 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     p.page_size = h->page_size;
     p.max_pages = max_pages_per_seq;
     p.num_pages = num_pages;
-    p.rows = h->rows;
-    p.row_blocks = h->row_blocks;
-    p.heads_per_cta = h->heads_per_cta;
+    p.rows = use_mla ? heads_per_cta : h->rows;
+    p.row_blocks = row_blocks;
+    p.heads_per_cta = heads_per_cta;
     p.tokens_per_cta = h->tokens_per_cta;
     p.box_rows = box_rows;
     p.oob_row = (int32_t)cache_rows;
@@ -536,7 +553,7 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
         p.band_cols = h->dv / P;
         p.out_chunk_cols = p.band_cols < 256 ? p.band_cols : 256;
         rc = encode_out_map(h->out_map[i], out, h->dv, h->hq, (int64_t)batch * h->num_q, p.out_chunk_cols,
-                            h->heads_per_cta, h->tokens_per_cta);
+                            heads_per_cta, h->tokens_per_cta);
         if (rc) return rc;
         p.tm_out = h->out_map[i].map;
 
@@ -544,7 +561,7 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
         cudaLaunchAttribute attr[1];
         // Cluster c (= blockIdx.y + gridDim.y * blockIdx.z) takes units
         // c, c + G, ... of u = b * Hkv + kvh; with G = units that is one unit each.
-        cfg.gridDim = clusters == units ? dim3(P, h->hkv * h->row_blocks, batch) : dim3(P, (unsigned)clusters, 1);
+        cfg.gridDim = clusters == units ? dim3(P, h->hkv * row_blocks, batch) : dim3(P, (unsigned)clusters, 1);
         cfg.blockDim = dim3(g.threads, 1, 1);
         cfg.dynamicSmemBytes = g.smem_bytes;
         cfg.stream = s;

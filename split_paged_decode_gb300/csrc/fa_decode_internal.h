@@ -69,6 +69,10 @@ bool simt_geometry(int qk_depth, int ov_depth, bool latent, int rows_capacity, K
 // Kernel variants of the tcgen05 path (head dim 128, <= 16 rows per CTA) with
 // a ring of `nslot` 32 KB K/V tile slots.
 bool tc_geometry(int qk_depth, int ov_depth, int rows, int nslot, KernelGeometry* g);
+// The tcgen05 kernel of the MLA latent layout (qk 576 = nope 512 + rope 64,
+// ov 512, V = the latent rows' first 512 columns) for num_q == 1 and a
+// multiple of 64 heads per kv head: 64 heads per CTA.
+bool mla_tc_geometry(int qk_depth, int ov_depth, int nope_depth, int heads_per_kv, int num_q, KernelGeometry* g);
 constexpr int kTcSlotsShared = 3;  // two CTAs per SM (grids of more than one wave)
 constexpr int kTcSlotsAlone = 6;   // one CTA per SM, 192 KB of loads in flight
 

@@ -1,0 +1,590 @@
+// kernel_mla_tc.cu -- the tcgen05 decode kernel for the MLA latent layout
+// (sm_103a): qk = 576 (nope 512 + rope 64), ov = 512, V = the first 512
+// columns of the same latent rows, many query heads per kv head.
+//
+// With 64 or more heads the fused tile is a dense contraction, so both
+// products run on the tensor core with 64 heads per CTA on N and keys / value
+// columns on M = 128:
+//   S^T [128 keys x 64 heads]  = K_tile [128 x 576] . Q^T         (A, B K-major)
+//   O^T [512 dv  x 64 heads]  += V_tile^T [512 x 128] . P^T        (A MN-major)
+// O^T (256 TMEM columns: four 128-dv blocks x 64 heads) accumulates in tensor
+// memory over the whole key range and is corrected in place only when the
+// lazy-rescale vote moves a head's running max; S^T is double-buffered (two
+// buffers of two accumulators). The 576-wide K tile streams through the ring
+// as four 128-column items plus the 64-column rope item, and V as four
+// 128-column items that re-read the same rows (they are still in L2).
+//
+// Warp roles (one CTA = one cluster rank of one (sequence, 64-head block)):
+//   warp 0      load: page-table walk (warp-wide blocks of entries, a block
+//               ahead) and TMA loads of the items into a ring of 3 x 32 KB
+//               slots, tile by tile in the order K(0) K(1) V(0) K(2) V(1) ...
+//   warp 1      MMA S: allocates the 512 TMEM columns, issues every S^T;
+//   warp 2      MMA O: issues every O^T += V^T P^T; each MMA warp frees a
+//               ring slot with a commit once the products that read it are done;
+//   warps 3-10  softmax: two warpgroups, each owning 32 of the 64 heads
+//               (thread = TMEM lane = key for S^T, = value column for O^T);
+//               online softmax in exp2 form, P^T to shared memory as bf16,
+//               in-place correction of O^T; then the split-K epilogue
+//               (splitk_combine.cuh) over all 256 softmax threads.
+//
+// Geometry follows the FA4Config page (Modular MAX docs): MLA depth split
+// into nope and rope (q_nope / q_rope), one O accumulator for the wide V
+// (single_o), V as the nope prefix of the shared latent row (use_shared_kv),
+// split-K clusters (splitk_partitions).
+#include "fa_decode_internal.h"
+#include "splitk_combine.cuh"
+#include "tcgen05.cuh"
+
+namespace fad {
+
+struct MlaCfg {
+    static constexpr int ROWS = 64;                 // heads per CTA (N of both MMAs)
+    static constexpr int BN = 128;                  // keys per tile (M of S^T)
+    static constexpr int DK = 576, DV = 512;
+    static constexpr int NSLOT = 3;
+    static constexpr int ATOM_BYTES = BN * 128;     // 16 KB: 64 columns of a tile
+    static constexpr int SLOT_BYTES = 2 * ATOM_BYTES;
+    static constexpr int KITEMS = 5;                // K: 4 x 128 columns + the 64-column rope
+    static constexpr int VITEMS = 4;                // V: 4 x 128 columns
+    static constexpr int Q_ATOM = ROWS * 128;       // 8 KB: 64 depth columns of the 64 heads
+    static constexpr int Q_BYTES = 9 * Q_ATOM;      // 72 KB
+    static constexpr int P_ATOM = ROWS * 128;       // 8 KB: 64 keys of P^T
+    static constexpr int P_BYTES = 2 * P_ATOM;      // 16 KB
+    // TMEM: S^T [2 buffers][2 accumulators][64 columns] at 0, O^T [4 dv blocks][64 columns] at 256.
+    static constexpr int S_ACC = 64, S_BUF = 2 * S_ACC, TMEM_S0 = 0, TMEM_O0 = 2 * S_BUF;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int WG0 = 3;                   // softmax warps 3-6 (heads 0-31), 7-10 (heads 32-63)
+    static constexpr int THREADS = 32 * (WG0 + 8);  // 352
+
+    static constexpr int OFF_RING = 0;                               // 3 x 32 KB
+    static constexpr int OFF_Q = NSLOT * SLOT_BYTES;                 // 9 atoms [64 heads][128 B]
+    static constexpr int OFF_P = OFF_Q + Q_BYTES;                    // [2 buffers][2 atoms][64 heads][128 B]
+    static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;              // float [2 warpgroups][4 quadrants][32]
+    static constexpr int OFF_MAXSUM = OFF_RED + 2 * 4 * 32 * 4;      // float2 [64]
+    // barriers: slot_full[3], slot_empty[3], s_full[2], s_empty[2], p_full[2],
+    // o_full[2], q_full, publish, mma_done, tmem_ready, v_zeroed[4]
+    static constexpr int OFF_BAR = OFF_MAXSUM + ROWS * 8;
+    static constexpr int NBAR = 2 * NSLOT + 16;
+    static constexpr int OFF_ROWS = OFF_BAR + NBAR * 8;              // int [4 tiles][16 segments]
+    static constexpr int OFF_MISC = OFF_ROWS + 4 * 16 * 4;           // tmem base, abort, S next item, O next item
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    // Epilogue, once every product has completed: the f32 stage
+    // [P][64][Dv / P] (128 KB) over the drained ring and Q, the bf16 band
+    // [Dv / P / OC][64][OC] (at most 64 KB) after it.
+    static constexpr int OFF_STAGE = 0;
+    static constexpr int OFF_OUT = ROWS * DV * 4;
+    static_assert(OFF_OUT + ROWS * DV * 2 <= OFF_RED, "epilogue buffers fit below the softmax scratch");
+    static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms on 1024 bytes");
+    static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
+};
+
+// Item positions: a tile's K items form one group and its V items another;
+// the groups come in the order K(0) K(1) V(0) K(2) V(1) ... K(n-1) V(n-2)
+// V(n-1). Group position of tile i's K and tile t's V, and the index of the
+// first item of the group at position g.
+__device__ __forceinline__ int mla_k_group(int i) { return i == 0 ? 0 : 2 * i - 1; }
+__device__ __forceinline__ int mla_v_group(int t, int n) { return t == n - 1 ? 2 * n - 1 : 2 * t + 2; }
+__device__ __forceinline__ int mla_group_item(int g, int n)
+{
+    const int nk = g == 0 ? 0 : min(n, (g + 2) / 2);  // K groups before position g
+    return MlaCfg::KITEMS * nk + MlaCfg::VITEMS * (g - nk);
+}
+
+__global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const __grid_constant__ DecodeParams p)
+{
+    using C = MlaCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int P = p.splitk;
+    const int rank = (int)blockIdx.x;
+    const int kvh = (int)blockIdx.y / p.row_blocks;
+    const int row_block = (int)blockIdx.y % p.row_blocks;
+    const int b = (int)blockIdx.z;
+
+    int L = p.seq_lens[b];
+    if (L < 0) {
+        if (tid == 0 && rank == 0) atomicOr(p.status, FA_STATUS_BAD_PAGE);
+        L = 0;
+    }
+    if (p.auto_split && auto_split_for_len(L) != P) return;  // uniform across the cluster
+
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    const uint32_t slot_full = bar0, slot_empty = bar0 + 8 * C::NSLOT;
+    const uint32_t s_full = bar0 + 16 * C::NSLOT, s_empty = s_full + 16, p_full = s_full + 32, o_full = s_full + 48;
+    const uint32_t q_full = s_full + 64, publish_bar = s_full + 72, mma_done = s_full + 80, tmem_ready = s_full + 88;
+    const uint32_t v_zeroed = s_full + 96;  // [4]: the last tile's V items with their rows past L zeroed
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    const uint32_t s_next = sbase + C::OFF_MISC + 8, o_next = sbase + C::OFF_MISC + 12;
+    float* red_s = reinterpret_cast<float*>(smem + C::OFF_RED);
+    float2* maxsum_s = reinterpret_cast<float2*>(smem + C::OFF_MAXSUM);
+
+    if (tid == 0) {
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(slot_full + 8 * s, 1);
+            mbar_init(slot_empty + 8 * s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full + 8 * i, 1);
+            mbar_init(s_empty + 8 * i, 8);  // one arrival per softmax warp
+            mbar_init(p_full + 8 * i, 8);
+            mbar_init(o_full + 8 * i, 1);
+        }
+        mbar_init(q_full, 8);
+        mbar_init(publish_bar, P);
+        mbar_init(mma_done, 2);
+        mbar_init(tmem_ready, 1);
+        for (int e = 0; e < C::VITEMS; ++e) mbar_init(v_zeroed + 8 * e, 8);
+        *abort_flag = 0;
+        // Next item of each kind to be consumed: K starts at item 0, V at the
+        // first item of V(0) (no earlier item is a V item, and with 5-item K
+        // groups on a 3-slot ring the S warp must not wait for one).
+        const int nt = (L + C::BN - 1) / C::BN;
+        const int tc0 = nt / P + (rank < nt % P ? 1 : 0);
+        *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 8) = 0;
+        *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 12) =
+            tc0 > 0 ? (uint32_t)mla_group_item(mla_v_group(0, tc0), tc0) : 0xffffffffu;
+        fence_mbarrier_init_cluster();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_map(&p.tm_k);
+    __syncthreads();
+    if (P > 1) cluster_arrive_relaxed();
+    uint32_t tmem = 0;
+    if (warp == 1) {
+        tmem_alloc(sbase + C::OFF_MISC, C::TMEM_COLS);
+        tmem_relinquish();
+        tc_fence_before_sync();
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem = *tmem_slot;
+        if (lane == 0) mbar_arrive(tmem_ready);
+    }
+
+    const int n_tiles = (L + C::BN - 1) / C::BN;
+    const int base_t = n_tiles / P, rem = n_tiles % P;
+    const int tile_begin = rank * base_t + min(rank, rem);
+    const int tile_count = base_t + (rank < rem ? 1 : 0);
+    // The rank holding the sequence's last, partial tile zeroes its V rows past L.
+    const bool v_tail = tile_count > 0 && (tile_begin + tile_count) * C::BN > L;
+
+    int issued = 0;
+    // Softmax state of this thread's 32 heads.
+    float m_run[32], l_part[32];
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ load warp
+        if (!(p.debug_flags & FA_DEBUG_SKIP_LOADS)) {
+            const uint64_t policy = l2_policy_evict_normal();  // V re-reads these rows from L2
+            const int segs = C::BN / p.box_rows;               // page segments per tile: 1, 2, ..., 16
+            const int tpb = 32 / segs;                         // tiles per block of page entries
+            int32_t* rows_s = reinterpret_cast<int32_t*>(smem + C::OFF_ROWS);
+            constexpr int kNoSegment = INT32_MIN, kPastSequence = INT32_MIN + 1;
+            auto block_entry = [&](int tb) -> int {
+                const int t = tb + lane / segs;
+                if (t >= tile_count) return kNoSegment;
+                const int key = (tile_begin + t) * C::BN + (lane % segs) * p.box_rows;
+                if (key >= L) return kPastSequence;
+                const int pslot = key / p.page_size;
+                if (pslot >= p.max_pages) return -1;
+                return p.page_table[(int64_t)b * p.max_pages + pslot];
+            };
+            int blk_cur = block_entry(0), blk_next = block_entry(tpb);
+            int jj = 0;
+            bool ok = true;
+            for (int g = 0; ok && g < 2 * tile_count; ++g) {
+                // group g: K of tile t or V of tile t
+                const bool is_v = (g == 2 * tile_count - 1) || (g > 0 && (g & 1) == 0);
+                const int t = is_v ? (g == 2 * tile_count - 1 ? tile_count - 1 : (g - 2) >> 1) : (g + 1) >> 1;
+                int32_t row;
+                if (!is_v) {
+                    if (t > 0 && (t & (tpb - 1)) == 0) {
+                        blk_cur = blk_next;
+                        blk_next = block_entry(t + tpb);
+                    }
+                    const int e = __shfl_sync(0xffffffffu, blk_cur, (t & (tpb - 1)) * segs + (lane & (segs - 1)));
+                    row = p.oob_row;  // zero fill past the sequence or on a bad page
+                    if (lane < segs) {
+                        if (e >= 0 && e < p.num_pages) {
+                            const int key = (tile_begin + t) * C::BN + lane * p.box_rows;
+                            row = (e * p.num_kv_heads + kvh) * p.page_size + key % p.page_size;
+                        } else if (e != kNoSegment && e != kPastSequence) {
+                            atomicOr(p.status, FA_STATUS_BAD_PAGE);
+                        }
+                    }
+                    if (lane < 16) rows_s[(t & 3) * 16 + lane] = row;
+                } else {
+                    row = lane < 16 ? rows_s[(t & 3) * 16 + lane] : p.oob_row;
+                }
+                const int n_in = is_v ? C::VITEMS : C::KITEMS;
+                for (int e = 0; e < n_in; ++e, ++jj) {
+                    const int slot = jj % C::NSLOT;
+                    if (jj >= C::NSLOT) {
+                        const bool got = mbar_wait(slot_empty + 8 * slot, ((jj / C::NSLOT) & 1) ^ 1, abort_flag,
+                                                   p.status, p.wait_limit_ns);
+                        if (!__all_sync(0xffffffffu, got)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    const bool rope = !is_v && e == C::KITEMS - 1;
+                    const int col = rope ? C::DV : 128 * e;
+                    if (lane == 0) mbar_arrive_expect_tx(slot_full + 8 * slot, rope ? C::ATOM_BYTES : C::SLOT_BYTES);
+                    __syncwarp();
+                    issued = jj + 1;
+                    if (lane < segs) {
+                        const uint32_t dst = sbase + C::OFF_RING + slot * C::SLOT_BYTES + lane * p.box_rows * 128;
+                        tma_load_2d(dst, &p.tm_k, col, row, slot_full + 8 * slot, policy);
+                        if (!rope) tma_load_2d(dst + C::ATOM_BYTES, &p.tm_k, col + 64, row, slot_full + 8 * slot, policy);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------ MMA warps
+        // Ring-order rule as in the GQA kernel: a slot's full barrier is
+        // waited on for item j only once every item before j - NSLOT + 1 of
+        // the other kind has been consumed (published next-item indices).
+        if (lane == 0) {
+            const bool is_s = (warp == 1);
+            const uint32_t other_next = is_s ? o_next : s_next;
+            auto ring_turn = [&](int j) -> bool {
+                return j < C::NSLOT ||
+                       counter_wait(other_next, (uint32_t)(j - C::NSLOT), abort_flag, p.status, p.wait_limit_ns);
+            };
+            bool ok = true;
+            if (is_s) {
+                const uint32_t id_s = umma_idesc_bf16_f32(128, C::ROWS, false, false);
+                const uint64_t q_desc0 = umma_smem_desc(sbase + C::OFF_Q, 16, 1024, kLayoutSwizzle128);
+                const uint64_t k_desc0 = umma_smem_desc(sbase + C::OFF_RING, 16, 1024, kLayoutSwizzle128);
+                ok = mbar_wait(q_full, 0, abort_flag, p.status, p.wait_limit_ns);
+                for (int i = 0; ok && i < tile_count; ++i) {
+                    const int j0 = mla_group_item(mla_k_group(i), tile_count);
+                    const uint32_t d0 = tmem + C::TMEM_S0 + C::S_BUF * (i & 1);
+                    for (int e = 0; ok && e < C::KITEMS; ++e) {
+                        const int j = j0 + e, slot = j % C::NSLOT;
+                        ok = ring_turn(j) &&
+                             mbar_wait(slot_full + 8 * slot, (j / C::NSLOT) & 1, abort_flag, p.status,
+                                       p.wait_limit_ns) &&
+                             (e > 0 || i < 2 ||
+                              mbar_wait(s_empty + 8 * (i & 1), ((i >> 1) - 1) & 1, abort_flag, p.status,
+                                        p.wait_limit_ns));
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        const uint64_t a0 = k_desc0 + (uint64_t)((slot * C::SLOT_BYTES) >> 4);
+                        const int steps = e == C::KITEMS - 1 ? 4 : 8;
+                        for (int ks = 0; ks < steps; ++ks) {
+                            const int gk = 8 * e + ks;  // K-step over the 576 depth columns
+                            umma_f16_ss(d0 + C::S_ACC * (gk & 1),
+                                        a0 + (uint64_t)(((ks >> 2) * C::ATOM_BYTES + (ks & 3) * 32) >> 4),
+                                        q_desc0 + (uint64_t)(((gk >> 2) * C::Q_ATOM + (gk & 3) * 32) >> 4), id_s,
+                                        gk >= 2);
+                        }
+                        umma_commit(slot_empty + 8 * slot);  // the item's slot is free once these complete
+                        st_release_u32(s_next, (uint32_t)(e + 1 < C::KITEMS
+                                                              ? j + 1
+                                                              : (i + 1 < tile_count
+                                                                     ? mla_group_item(mla_k_group(i + 1), tile_count)
+                                                                     : 0xffffffffu)));
+                    }
+                    if (ok) umma_commit(s_full + 8 * (i & 1));
+                }
+            } else {
+                const uint32_t id_pv = umma_idesc_bf16_f32(128, C::ROWS, true, false);
+                // A = V^T, MN-major: two 64-column atoms one atom apart (LBO), 8-key groups 1024 B apart (SBO)
+                const uint64_t v_desc0 = umma_smem_desc(sbase + C::OFF_RING, C::ATOM_BYTES, 1024, kLayoutSwizzle128);
+                // B = P^T, K-major: 64-key atoms of 64 heads x 128 B
+                const uint64_t p_desc0 = umma_smem_desc(sbase + C::OFF_P, 16, 1024, kLayoutSwizzle128);
+                mbar_wait(tmem_ready, 0, abort_flag, p.status, p.wait_limit_ns);
+                tc_fence_after_sync();
+                tmem = *tmem_slot;
+                for (int t = 0; ok && t < tile_count; ++t) {
+                    const int j0 = mla_group_item(mla_v_group(t, tile_count), tile_count);
+                    ok = mbar_wait(p_full + 8 * (t & 1), (t >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+                    for (int e = 0; ok && e < C::VITEMS; ++e) {
+                        const int j = j0 + e, slot = j % C::NSLOT;
+                        ok = ring_turn(j) &&
+                             mbar_wait(slot_full + 8 * slot, (j / C::NSLOT) & 1, abort_flag, p.status,
+                                       p.wait_limit_ns) &&
+                             (!v_tail || t + 1 < tile_count ||
+                              mbar_wait(v_zeroed + 8 * e, 0, abort_flag, p.status, p.wait_limit_ns));
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        const uint64_t a0 = v_desc0 + (uint64_t)((slot * C::SLOT_BYTES) >> 4);
+                        const uint64_t b0 = p_desc0 + (uint64_t)(((t & 1) * C::P_BYTES) >> 4);
+                        const uint32_t d = tmem + C::TMEM_O0 + 64 * e;  // dv block e
+#pragma unroll
+                        for (int ks = 0; ks < C::BN / 16; ++ks)
+                            umma_f16_ss(d, a0 + (uint64_t)((ks * 2048) >> 4),
+                                        b0 + (uint64_t)(((ks >> 2) * C::P_ATOM + (ks & 3) * 32) >> 4), id_pv,
+                                        t > 0 || ks > 0);
+                        umma_commit(slot_empty + 8 * slot);
+                        st_release_u32(o_next,
+                                       (uint32_t)(e + 1 < C::VITEMS
+                                                      ? j + 1
+                                                      : (t + 1 < tile_count
+                                                             ? mla_group_item(mla_v_group(t + 1, tile_count), tile_count)
+                                                             : 0xffffffffu)));
+                    }
+                    if (ok) umma_commit(o_full + 8 * (t & 1));
+                }
+            }
+            st_release_u32(is_s ? s_next : o_next, 0xffffffffu);
+            umma_commit(mma_done);
+            volatile int keep_waiting = 0;
+            mbar_wait(mma_done, 0, &keep_waiting, p.status, p.wait_limit_ns);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------- softmax warpgroups
+        const int wg = (warp - C::WG0) >> 2;          // heads 32 wg .. 32 wg + 31
+        const int wt = tid - 32 * C::WG0 - 128 * wg;  // 0..127
+        const uint32_t wg_bar = 1 + wg;
+        const int quad = warp & 3;
+        const int my_lane = 32 * quad + lane;         // key (S^T) or value column within a dv block (O^T)
+        const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
+        const float c2 = p.scale_log2e;
+        const int h0 = kvh * p.group + row_block * C::ROWS;  // first head of this CTA
+
+        // Q rows -> nine K-major 128-byte-swizzled atoms; each warpgroup stores half.
+        for (int idx = wt + 128 * wg; idx < C::ROWS * 72; idx += 256) {
+            const int r = idx / 72, u = idx % 72;  // 16-byte chunk u of head r
+            const uint4 v = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.num_q_heads + h0 + r) * C::DK)[u];
+            *reinterpret_cast<uint4*>(smem + C::OFF_Q + (u >> 3) * C::Q_ATOM + r * 128 + (((u & 7) ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_full);
+        mbar_wait(tmem_ready, 0, abort_flag, p.status, p.wait_limit_ns);
+        tc_fence_after_sync();
+        tmem = *tmem_slot;
+
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            m_run[r] = -INFINITY;
+            l_part[r] = 0.f;
+        }
+        const uint32_t col_wg = 32 * wg;  // this warpgroup's columns in every S^T / O^T accumulator
+        float* red_w = red_s + wg * 4 * 32;
+        bool seen_abort = false;
+        for (int i = 0; i < tile_count; ++i) {
+            mbar_wait(s_full + 8 * (i & 1), (i >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+            tc_fence_after_sync();
+            float s[32];
+            tmem_ld2_sum_x32(tmem + lane_addr + C::TMEM_S0 + C::S_BUF * (i & 1) + col_wg, C::S_ACC, s);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_empty + 8 * (i & 1));
+
+            const int key = (tile_begin + i) * C::BN + my_lane;
+            if (key >= L) {
+#pragma unroll
+                for (int r = 0; r < 32; ++r) s[r] = -INFINITY;
+            }
+            bool need = false;
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+                need |= (s[r] != -INFINITY) && (m_run[r] == -INFINITY || (s[r] - m_run[r]) * c2 > 8.0f);
+            seen_abort |= (*abort_flag != 0);
+            if (named_barrier_or(wg_bar, 128, need || seen_abort)) {
+                {
+                    int row;
+                    float v[32];
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) v[r] = s[r];
+                    // reduce-scatter: lane holds the max of head `row` over this warp's keys
+                    row = 0;
+#pragma unroll
+                    for (int w = 16, n = 32; w >= 1; w >>= 1, n >>= 1) {
+                        const bool up = (lane & w) != 0;
+#pragma unroll
+                        for (int k = 0; k < n / 2; ++k) {
+                            const float send = up ? v[k] : v[k + n / 2];
+                            const float keep = up ? v[k + n / 2] : v[k];
+                            v[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
+                        }
+                        row += up ? n / 2 : 0;
+                    }
+                    red_w[quad * 32 + row] = v[0];
+                }
+                seen_abort |= (*abort_flag != 0);
+                if (named_barrier_or(wg_bar, 128, seen_abort)) break;
+                bool moved = false;
+                float alpha[32];
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    const float tmax = fmaxf(fmaxf(red_w[r], red_w[32 + r]), fmaxf(red_w[64 + r], red_w[96 + r]));
+                    const bool move = (m_run[r] == -INFINITY) ? (tmax != -INFINITY)
+                                                              : ((tmax - m_run[r]) * c2 > 8.0f);
+                    alpha[r] = 1.f;
+                    if (move) {
+                        alpha[r] = (m_run[r] == -INFINITY) ? 0.f : ex2_approx((m_run[r] - tmax) * c2);
+                        m_run[r] = tmax;
+                        l_part[r] *= alpha[r];
+                        moved = true;  // uniform: every thread sees the same maxima
+                    }
+                }
+                if (moved && i > 0) {
+                    // Correct O^T in place: its last product (tile i - 1) must
+                    // have completed, and no later one is issued before this
+                    // tile's P is published.
+                    mbar_wait(o_full + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag, p.status,
+                              p.wait_limit_ns);
+                    tc_fence_after_sync();
+#pragma unroll 1
+                    for (int blk = 0; blk < 4; ++blk) {
+                        float o[32];
+                        const uint32_t ta = tmem + lane_addr + C::TMEM_O0 + 64 * blk + col_wg;
+                        tmem_ld_32x32b_x32(ta, o);
+#pragma unroll
+                        for (int r = 0; r < 32; ++r) o[r] *= alpha[r];
+                        tmem_st_32x32b_x32(ta, o);
+                    }
+                    tc_fence_before_sync();
+                }
+                named_barrier_sync(wg_bar, 128);  // red_w is read before the next tile's writes
+            }
+#pragma unroll
+            for (int r = 0; r < 32; ++r) {
+                const float pr = (s[r] == -INFINITY) ? 0.f : ex2_approx((s[r] - m_run[r]) * c2);
+                l_part[r] += pr;
+                s[r] = pr;
+            }
+            // P buffer i & 1 was last read by the O product of tile i - 2.
+            if (i >= 2)
+                mbar_wait(o_full + 8 * (i & 1), ((i - 2) >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+            {
+                uint8_t* pb = smem + C::OFF_P + (i & 1) * C::P_BYTES + (my_lane >> 6) * C::P_ATOM;
+                const int kk = my_lane & 63;
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    const int hr = col_wg + r;  // head row of P^T
+                    *reinterpret_cast<__nv_bfloat16*>(pb + hr * 128 + (((kk >> 3) ^ (hr & 7)) << 4) + (kk & 7) * 2) =
+                        __float2bfloat16_rn(s[r]);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full + 8 * (i & 1));
+        }
+        // The sequence's last tile: zero the V rows past L in each of its V
+        // items as it lands (P is already published: the O warp waits for
+        // each item's v_zeroed barrier), so unused cache rows, whatever they
+        // hold, meet P = 0 as exact zeros. Each warpgroup zeroes one of the
+        // item's two 64-column atoms. Ring order: the item that held the slot
+        // before has been consumed (both MMA warps' published progress).
+        if (v_tail && !seen_abort) {
+            const int t = tile_count - 1;
+            const int j0 = mla_group_item(mla_v_group(t, tile_count), tile_count);
+            const bool past = (tile_begin + t) * C::BN + my_lane >= L;
+            for (int e = 0; e < C::VITEMS; ++e) {
+                const int j = j0 + e, slot = j % C::NSLOT;
+                if (j >= C::NSLOT) {
+                    counter_wait(s_next, (uint32_t)(j - C::NSLOT), abort_flag, p.status, p.wait_limit_ns);
+                    counter_wait(o_next, (uint32_t)(j - C::NSLOT), abort_flag, p.status, p.wait_limit_ns);
+                }
+                mbar_wait(slot_full + 8 * slot, (j / C::NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns);
+                if (past) {
+                    uint4* row = reinterpret_cast<uint4*>(smem + C::OFF_RING + slot * C::SLOT_BYTES +
+                                                          wg * C::ATOM_BYTES + my_lane * 128);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) row[u] = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(v_zeroed + 8 * e);
+            }
+        }
+        // All products complete.
+        if (tile_count > 0)
+            mbar_wait(o_full + 8 * ((tile_count - 1) & 1), ((tile_count - 1) >> 1) & 1, abort_flag, p.status,
+                      p.wait_limit_ns);
+        tc_fence_after_sync();
+        // Row sums of this warpgroup's 32 heads: reduce-scatter over the warp, then four warps.
+        {
+            float v[32];
+#pragma unroll
+            for (int r = 0; r < 32; ++r) v[r] = l_part[r];
+            int row = 0;
+#pragma unroll
+            for (int w = 16, n = 32; w >= 1; w >>= 1, n >>= 1) {
+                const bool up = (lane & w) != 0;
+#pragma unroll
+                for (int k = 0; k < n / 2; ++k) {
+                    const float send = up ? v[k] : v[k + n / 2];
+                    const float keep = up ? v[k + n / 2] : v[k];
+                    v[k] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+                }
+                row += up ? n / 2 : 0;
+            }
+            named_barrier_sync(wg_bar, 128);
+            red_w[quad * 32 + row] = v[0];
+            named_barrier_sync(wg_bar, 128);
+        }
+        float inv[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const float l = red_w[r] + red_w[32 + r] + red_w[64 + r] + red_w[96 + r];
+            if (wt == 0) maxsum_s[col_wg + r] = make_float2(m_run[r], l);
+            inv[r] = l > 0.f ? __frcp_rn(l) : 0.f;
+        }
+        // Both warpgroups' products are complete before the stage overwrites
+        // the ring and Q.
+        named_barrier_sync(3, 256);
+        float* stage_s = reinterpret_cast<float*>(smem + C::OFF_STAGE);
+        const int BW = p.band_cols;
+#pragma unroll 1
+        for (int blk = 0; blk < 4; ++blk) {
+            float o[32];
+            tmem_ld_32x32b_x32(tmem + lane_addr + C::TMEM_O0 + 64 * blk + col_wg, o);
+            if (tile_count == 0) {  // no product was issued: the accumulator holds nothing of ours
+#pragma unroll
+                for (int r = 0; r < 32; ++r) o[r] = 0.f;
+            }
+            const int dv = 128 * blk + my_lane;
+            const int q = dv / BW, jc = dv % BW;
+#pragma unroll
+            for (int r = 0; r < 32; ++r) stage_s[(q * C::ROWS + col_wg + r) * BW + jc] = o[r] * inv[r];
+        }
+        tc_fence_before_sync();
+        named_barrier_sync(3, 256);
+        if (P > 1) cluster_wait();  // every rank's publish barrier is initialised
+        splitk_merge_and_store<C::ROWS>(p, P, rank, b, kvh, row_block, stage_s, maxsum_s,
+                                        reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), publish_bar, 0u, 0u,
+                                        abort_flag, tid - 32 * C::WG0, 256, 3);
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        volatile int keep_waiting = 0;
+        for (int j = issued > C::NSLOT ? issued - C::NSLOT : 0; j < issued; ++j)
+            mbar_wait(slot_full + 8 * (j % C::NSLOT), (j / C::NSLOT) & 1, &keep_waiting, p.status, p.wait_limit_ns);
+    }
+    if (P > 1 && warp < C::WG0) cluster_wait();  // pairs with the early arrive
+    __syncwarp();
+    if (P > 1) cluster_sync_all();  // peers may still read this CTA's staged bands until here
+}
+
+bool mla_tc_geometry(int qk, int ov, int nope, int heads_per_kv, int num_q, KernelGeometry* g)
+{
+    if (qk != MlaCfg::DK || ov != MlaCfg::DV || nope != MlaCfg::DV || num_q != 1 || heads_per_kv % MlaCfg::ROWS)
+        return false;
+    g->func = reinterpret_cast<const void*>(&mla_tc_decode_kernel);
+    g->threads = MlaCfg::THREADS;
+    g->keys_per_tile = MlaCfg::BN;
+    g->stages = MlaCfg::NSLOT;
+    g->rows_capacity = MlaCfg::ROWS;
+    g->smem_bytes = MlaCfg::SMEM_BYTES;
+    g->name = "mla_tc_d576_v512_bn128_n64_slots3";
+    return true;
+}
+
+}  // namespace fad

@@ -86,6 +86,50 @@ def test_latent_small(P):
     run_and_check(w, what=f"latent P{P}")
 
 
+def mla_wl(**kw):
+    base = dict(num_q_heads=128, num_kv_heads=1, qk_depth=576, nope_depth=512, ov_depth=512, latent=True,
+                splitk=2, batch=3, page_size=64, seq_len_lo=1, seq_len_hi=700, scale=1.0 / np.sqrt(192.0), seed=150)
+    base.update(kw)
+    return wl(**base)
+
+
+def test_mla_tensor_core_path_is_selected():
+    with DeviceCall(generate(mla_wl())) as call:
+        d = call.describe()
+        assert d.startswith("path=tcgen05") and "mla_tc" in d, d
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("P", [1, 2, 4, 8])
+def test_mla_splits(P, path):
+    """MLA latent layout, 128 heads (two 64-head blocks), ragged lengths across tiles."""
+    run_and_check(mla_wl(splitk=P, seed=150 + P), seq_lens=[700, 129, 2000], what=f"mla P{P} {path}", path=path)
+
+
+@pytest.mark.parametrize("Hq,ps", [(64, 64), (256, 128), (128, 32), (128, 256)])
+def test_mla_heads_and_pages(Hq, ps):
+    run_and_check(mla_wl(num_q_heads=Hq, page_size=ps, seed=160 + Hq + ps), seq_lens=[1, 300, 1000],
+                  what=f"mla Hq{Hq} ps{ps}")
+
+
+def test_mla_short_and_empty():
+    """Lengths 0 and 1, shorter than a tile and at tile edges; ranks without tiles."""
+    run_and_check(mla_wl(batch=6, splitk=4, seed=170), seq_lens=[0, 1, 127, 128, 129, 255], what="mla short")
+
+
+def test_mla_nonfinite_rows_past_the_sequence_do_not_leak():
+    w = mla_wl(batch=3, splitk=2, seed=171)
+    lens = [70, 200, 129]
+    inp = generate(w, seq_lens=lens)
+    for b, L in enumerate(lens):
+        last = int(inp.page_table[b, (L - 1) // 64])
+        inp.k_pages[last, :, L % 64:, :] = float("nan")
+    with DeviceCall(inp) as call:
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what="mla non-finite tails")
+
+
 def test_latent_explicit_v_cache():
     """(576, 512) with a separate V cache uses the separate-V kernel."""
     w = wl(num_q_heads=16, num_kv_heads=1, qk_depth=576, nope_depth=512, ov_depth=512, latent=False,
