@@ -153,7 +153,10 @@ int fa_decode_set_debug(fa_decode_t h, uint32_t flags, int64_t wait_limit_ns);
  *   [62] first V tile landed  [63] first unit's Q stored by the softmax warps
  * CTAs past n_words / FA_TRACE_WORDS_PER_CTA record nothing. The caller owns
  * the buffer (device memory, 8-byte aligned) and clears it; buf NULL turns
- * tracing off. The FMA kernel records nothing.
+ * tracing off. The MLA tcgen05 kernel (one unit per CTA) records [0]-[3],
+ * and for its unit [4] the softmax warps' tile loop done, [5] first S,
+ * [6] last O complete, [8] / [9] merge start / end, [10] tiles.
+ * The FMA kernel records nothing.
  */
 #define FA_TRACE_WORDS_PER_CTA 64
 int fa_decode_set_trace(fa_decode_t h, uint64_t* buf, int64_t n_words);

@@ -16,7 +16,7 @@
 //
 // Warp roles (one CTA = one cluster rank of one (sequence, 64-head block)):
 //   warp 0      load: page-table walk (warp-wide blocks of entries, a block
-//               ahead) and TMA loads of the items into a ring of 3 x 32 KB
+//               ahead) and TMA loads of the items into a ring of 4 x 32 KB
 //               slots, tile by tile in the order K(0) K(1) V(0) K(2) V(1) ...
 //   warp 1      MMA S: allocates the 512 TMEM columns, issues every S^T;
 //   warp 2      MMA O: issues every O^T += V^T P^T; each MMA warp frees a
@@ -41,7 +41,9 @@ struct MlaCfg {
     static constexpr int ROWS = 64;                 // heads per CTA (N of both MMAs)
     static constexpr int BN = 128;                  // keys per tile (M of S^T)
     static constexpr int DK = 576, DV = 512;
-    static constexpr int NSLOT = 3;
+    // Four 32 KB slots (in-flight bytes bound this kernel) leave room for one P buffer.
+    static constexpr int NSLOT = 4;
+    static constexpr int P_BUFS = 1;
     static constexpr int ATOM_BYTES = BN * 128;     // 16 KB: 64 columns of a tile
     static constexpr int SLOT_BYTES = 2 * ATOM_BYTES;
     static constexpr int KITEMS = 5;                // K: 4 x 128 columns + the 64-column rope
@@ -56,12 +58,12 @@ struct MlaCfg {
     static constexpr int WG0 = 3;                   // softmax warps 3-6 (heads 0-31), 7-10 (heads 32-63)
     static constexpr int THREADS = 32 * (WG0 + 8);  // 352
 
-    static constexpr int OFF_RING = 0;                               // 3 x 32 KB
+    static constexpr int OFF_RING = 0;                               // NSLOT x 32 KB
     static constexpr int OFF_Q = NSLOT * SLOT_BYTES;                 // 9 atoms [64 heads][128 B]
-    static constexpr int OFF_P = OFF_Q + Q_BYTES;                    // [2 buffers][2 atoms][64 heads][128 B]
-    static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;              // float [2 warpgroups][4 quadrants][32]
+    static constexpr int OFF_P = OFF_Q + Q_BYTES;                    // [P_BUFS][2 atoms][64 heads][128 B]
+    static constexpr int OFF_RED = OFF_P + P_BUFS * P_BYTES;         // float [2 warpgroups][4 quadrants][32]
     static constexpr int OFF_MAXSUM = OFF_RED + 2 * 4 * 32 * 4;      // float2 [64]
-    // barriers: slot_full[3], slot_empty[3], s_full[2], s_empty[2], p_full[2],
+    // barriers: slot_full[NSLOT], slot_empty[NSLOT], s_full[2], s_empty[2], p_full[2],
     // o_full[2], q_full, publish, mma_done, tmem_ready, v_zeroed[4]
     static constexpr int OFF_BAR = OFF_MAXSUM + ROWS * 8;
     static constexpr int NBAR = 2 * NSLOT + 16;
@@ -73,7 +75,8 @@ struct MlaCfg {
     // [Dv / P / OC][64][OC] (at most 64 KB) after it.
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_OUT = ROWS * DV * 4;
-    static_assert(OFF_OUT + ROWS * DV * 2 <= OFF_RED, "epilogue buffers fit below the softmax scratch");
+    static constexpr int OFF_WTAB = OFF_OUT + ROWS * DV * 2;         // float [P][64] combine weights
+    static_assert(OFF_WTAB + kMaxSplit * ROWS * 4 <= OFF_RED, "epilogue buffers fit below the softmax scratch");
     static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms on 1024 bytes");
     static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
 };
@@ -105,6 +108,15 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
     const int kvh = (int)blockIdx.y / p.row_blocks;
     const int row_block = (int)blockIdx.y % p.row_blocks;
     const int b = (int)blockIdx.z;
+
+    // Optional timeline trace (a profiling aid): one thread writes each event.
+    const int64_t cta_lin = (int64_t)blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+    unsigned long long* const trace =
+        (p.trace != nullptr && cta_lin < p.trace_ctas) ? p.trace + cta_lin * FA_TRACE_WORDS_PER_CTA : nullptr;
+    auto stamp = [&](int slot) {
+        if (trace) trace[slot] = global_timer_ns();
+    };
+    if (tid == 0) stamp(0);
 
     int L = p.seq_lens[b];
     if (L < 0) {
@@ -236,6 +248,7 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                     if (lane == 0) mbar_arrive_expect_tx(slot_full + 8 * slot, rope ? C::ATOM_BYTES : C::SLOT_BYTES);
                     __syncwarp();
                     issued = jj + 1;
+                    if (jj == 0 && lane == 0) stamp(1);
                     if (lane < segs) {
                         const uint32_t dst = sbase + C::OFF_RING + slot * C::SLOT_BYTES + lane * p.box_rows * 128;
                         tma_load_2d(dst, &p.tm_k, col, row, slot_full + 8 * slot, policy);
@@ -315,7 +328,7 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                         if (!ok) break;
                         tc_fence_after_sync();
                         const uint64_t a0 = v_desc0 + (uint64_t)((slot * C::SLOT_BYTES) >> 4);
-                        const uint64_t b0 = p_desc0 + (uint64_t)(((t & 1) * C::P_BYTES) >> 4);
+                        const uint64_t b0 = p_desc0 + (uint64_t)(((t % C::P_BUFS) * C::P_BYTES) >> 4);
                         const uint32_t d = tmem + C::TMEM_O0 + 64 * e;  // dv block e
 #pragma unroll
                         for (int ks = 0; ks < C::BN / 16; ++ks)
@@ -350,11 +363,22 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
         const float c2 = p.scale_log2e;
         const int h0 = kvh * p.group + row_block * C::ROWS;  // first head of this CTA
 
-        // Q rows -> nine K-major 128-byte-swizzled atoms; each warpgroup stores half.
-        for (int idx = wt + 128 * wg; idx < C::ROWS * 72; idx += 256) {
-            const int r = idx / 72, u = idx % 72;  // 16-byte chunk u of head r
-            const uint4 v = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.num_q_heads + h0 + r) * C::DK)[u];
-            *reinterpret_cast<uint4*>(smem + C::OFF_Q + (u >> 3) * C::Q_ATOM + r * 128 + (((u & 7) ^ (r & 7)) << 4)) = v;
+        // Q rows -> nine K-major 128-byte-swizzled atoms. Every load is issued
+        // before the first store, so the 18 chunks of a thread arrive together.
+        {
+            constexpr int kChunks = C::ROWS * (C::DK / 8) / 256;  // 16-byte chunks per thread
+            static_assert(kChunks * 256 == C::ROWS * (C::DK / 8), "Q chunks split evenly");
+            uint4 qv[kChunks];
+            const uint4* qg = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.num_q_heads + h0) * C::DK);
+#pragma unroll
+            for (int k = 0; k < kChunks; ++k) qv[k] = __ldg(qg + (wt + 128 * wg + 256 * k));
+#pragma unroll
+            for (int k = 0; k < kChunks; ++k) {
+                const int idx = wt + 128 * wg + 256 * k;
+                const int r = idx / 72, u = idx % 72;  // 16-byte chunk u of head r (heads are contiguous)
+                *reinterpret_cast<uint4*>(smem + C::OFF_Q + (u >> 3) * C::Q_ATOM + r * 128 +
+                                          (((u & 7) ^ (r & 7)) << 4)) = qv[k];
+            }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -373,6 +397,10 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
         bool seen_abort = false;
         for (int i = 0; i < tile_count; ++i) {
             mbar_wait(s_full + 8 * (i & 1), (i >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+            if (i == 0 && wt == 0 && wg == 0) {
+                stamp(2);
+                stamp(5);  // unit 0: first S observed
+            }
             tc_fence_after_sync();
             float s[32];
             tmem_ld2_sum_x32(tmem + lane_addr + C::TMEM_S0 + C::S_BUF * (i & 1) + col_wg, C::S_ACC, s);
@@ -454,11 +482,13 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                 l_part[r] += pr;
                 s[r] = pr;
             }
-            // P buffer i & 1 was last read by the O product of tile i - 2.
-            if (i >= 2)
-                mbar_wait(o_full + 8 * (i & 1), ((i - 2) >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+            // P buffer i % P_BUFS was last read by the O product of tile i - P_BUFS.
+            if (i >= C::P_BUFS) {
+                const int tp = i - C::P_BUFS;
+                mbar_wait(o_full + 8 * (tp & 1), (tp >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+            }
             {
-                uint8_t* pb = smem + C::OFF_P + (i & 1) * C::P_BYTES + (my_lane >> 6) * C::P_ATOM;
+                uint8_t* pb = smem + C::OFF_P + (i % C::P_BUFS) * C::P_BYTES + (my_lane >> 6) * C::P_ATOM;
                 const int kk = my_lane & 63;
 #pragma unroll
                 for (int r = 0; r < 32; ++r) {
@@ -499,11 +529,16 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                 if (lane == 0) mbar_arrive(v_zeroed + 8 * e);
             }
         }
+        if (wt == 0 && wg == 0) {
+            stamp(4);  // unit 0: the tile loop is done
+            if (trace) trace[10] = (unsigned long long)tile_count;
+        }
         // All products complete.
         if (tile_count > 0)
             mbar_wait(o_full + 8 * ((tile_count - 1) & 1), ((tile_count - 1) >> 1) & 1, abort_flag, p.status,
                       p.wait_limit_ns);
         tc_fence_after_sync();
+        if (wt == 0 && wg == 0) stamp(6);  // unit 0: last O product complete
         // Row sums of this warpgroup's 32 heads: reduce-scatter over the warp, then four warps.
         {
             float v[32];
@@ -553,9 +588,12 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
         tc_fence_before_sync();
         named_barrier_sync(3, 256);
         if (P > 1) cluster_wait();  // every rank's publish barrier is initialised
-        splitk_merge_and_store<C::ROWS>(p, P, rank, b, kvh, row_block, stage_s, maxsum_s,
-                                        reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), publish_bar, 0u, 0u,
-                                        abort_flag, tid - 32 * C::WG0, 256, 3);
+        if (wt == 0 && wg == 0) stamp(8);  // unit 0: merge started
+        splitk_merge_rows<C::ROWS>(p, P, rank, b, kvh, row_block, stage_s, maxsum_s,
+                                   reinterpret_cast<uint16_t*>(smem + C::OFF_OUT),
+                                   reinterpret_cast<float*>(smem + C::OFF_WTAB), publish_bar, abort_flag,
+                                   tid - 32 * C::WG0, 256, 3);
+        if (wt == 0 && wg == 0) stamp(9);  // unit 0: merge done
     }
 
     __syncthreads();
@@ -571,6 +609,7 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
     if (P > 1 && warp < C::WG0) cluster_wait();  // pairs with the early arrive
     __syncwarp();
     if (P > 1) cluster_sync_all();  // peers may still read this CTA's staged bands until here
+    if (tid == 0) stamp(3);
 }
 
 bool mla_tc_geometry(int qk, int ov, int nope, int heads_per_kv, int num_q, KernelGeometry* g)
