@@ -36,6 +36,8 @@
 // visibility rule of the fa4_lse_combine_write page (wait for the MMA's
 // barrier, then tcgen05.fence::after_thread_sync, before reading TMEM) is
 // applied to every TMEM read.
+#include <type_traits>
+
 #include "fa_decode_internal.h"
 #include "splitk_combine.cuh"
 #include "tcgen05.cuh"
@@ -217,6 +219,10 @@ __device__ __forceinline__ void item_at(int j, int n, bool& is_v, int& t)
 // correction; P then stays below 2^8, safe in bf16 and fp32.
 constexpr float kRescaleThreshold = 8.0f;
 
+// Units with at least this many tiles per rank are issued two items per pass
+// by the load warp (its issue rate bounds them); shorter ones one at a time.
+constexpr int kPairTiles = 16;
+
 template <int NSLOT, int NRV>
 __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>::MULTI ? 1 : 2)
     tc_decode_kernel(const __grid_constant__ DecodeParams p)
@@ -383,53 +389,73 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                 const bool guessed =
                     lu == 0 && w.u == cluster_id && tile_begin == spec_begin && tile_count <= spec_count;
                 int blk_cur = block_entry(0, guessed ? spec_raw : -2), blk_next = block_entry(tpb);
-                for (int j = 0; j < n_items; ++j) {
-                    const int jj = J0 + j, slot = jj % NSLOT;
-                    bool is_v;
-                    int t;
-                    item_at<C::VLAG>(j, tile_count, is_v, t);
-                    if (jj >= NSLOT) {
-                        const bool got = mbar_wait(slot_empty + 8 * slot, ((jj / NSLOT) & 1) ^ 1, abort_flag,
-                                                   p.status, p.wait_limit_ns);
-                        if (!__all_sync(0xffffffffu, got)) {
-                            ok = false;
-                            break;
-                        }
+                // One pass issues one item (lanes 0-15) or, for a long unit, two
+                // consecutive items (lanes 0-15 and 16-31; lane 16 h + s owns page
+                // segment s), so the waits, barrier arms and copies of a pair share
+                // their instructions: a long unit is bound by this warp's issue
+                // rate, a short one by the ring.
+                auto pass = [&](int j, auto two_tag) -> bool {
+                    constexpr bool TWO = decltype(two_tag)::value;
+                    // one item: every lane computes it, lane s owns segment s
+                    const int half = TWO ? (lane >> 4) : 0, sl = TWO ? (lane & 15) : lane;
+                    const int jh = j + half;  // this half's item in the unit
+                    const bool valid = TWO ? (jh < n_items) : true;
+                    const int jj = J0 + jh, slot = jj % NSLOT;
+                    bool is_v = true;
+                    int t = 0;
+                    if (valid) item_at<C::VLAG>(jh, tile_count, is_v, t);
+                    bool got = true;
+                    if (valid && jj >= NSLOT)
+                        got = mbar_wait(slot_empty + 8 * slot, ((jj / NSLOT) & 1) ^ 1, abort_flag, p.status,
+                                        p.wait_limit_ns);
+                    if (!__all_sync(0xffffffffu, got)) return false;
+                    const bool k_here = valid && !is_v;
+                    // A K tile of the pass that starts a new block of page entries.
+                    int kt = k_here ? t : -1;
+                    if (TWO) kt = max(kt, __shfl_xor_sync(0xffffffffu, kt, 16));  // one item: uniform already
+                    if (kt > 0 && (kt & (tpb - 1)) == 0) {
+                        // Waits only if the block fetched a block of tiles ago has not arrived.
+                        blk_cur = blk_next;
+                        blk_next = block_entry(kt + tpb);
                     }
-                    int32_t row;
-                    if (!is_v) {
-                        if (t > 0 && (t & (tpb - 1)) == 0) {
-                            // Waits only if the block fetched a block of tiles ago has not arrived.
-                            blk_cur = blk_next;
-                            blk_next = block_entry(t + tpb);
-                        }
-                        const int e = __shfl_sync(0xffffffffu, blk_cur, (t & (tpb - 1)) * segs + (lane & (segs - 1)));
-                        row = p.oob_row;  // zero fill past the sequence or on a bad page
-                        if (lane < segs) {
+                    const int e =
+                        __shfl_sync(0xffffffffu, blk_cur, ((k_here ? t : 0) & (tpb - 1)) * segs + (sl & (segs - 1)));
+                    int32_t row = p.oob_row;  // zero fill past the sequence or on a bad page
+                    if (k_here) {
+                        if (sl < segs) {
                             if (e >= 0 && e < p.num_pages) {
-                                const int key = (tile_begin + t) * C::BN + lane * p.box_rows;
-                                row = (e * p.num_kv_heads + w.kvh) * p.page_size + key % p.page_size;
+                                // the segment starts on a page boundary unless pages are longer than a tile
+                                const int off = p.page_size > C::BN ? ((tile_begin + t) * C::BN) % p.page_size : 0;
+                                row = (e * p.num_kv_heads + w.kvh) * p.page_size + off;
                             } else if (e != kNoSegment && e != kPastSequence) {
                                 atomicOr(p.status, FA_STATUS_BAD_PAGE);
                             }
                         }
-                        if (lane < 16) rows_s[(t & 3) * 16 + lane] = row;  // read by V_t, at most 3 tiles later
-                    } else {
-                        row = lane < 16 ? rows_s[(t & 3) * 16 + lane] : p.oob_row;
+                        if (sl < 16) rows_s[(t & 3) * 16 + sl] = row;  // read by V_t, at most 3 tiles later
                     }
-                    if (lane == 0) mbar_arrive_expect_tx(slot_full + 8 * slot, C::TILE_BYTES);
+                    // A one-tile unit has K0 and V0 side by side, possibly in one pass:
+                    // the K half's rows are written before the V half reads them.
+                    if (TWO) __syncwarp();
+                    if (valid && is_v) row = sl < 16 ? rows_s[(t & 3) * 16 + sl] : p.oob_row;
+                    if (valid && sl == 0) mbar_arrive_expect_tx(slot_full + 8 * slot, C::TILE_BYTES);
                     __syncwarp();
-                    issued = jj + 1;
-                    if (lane < segs) {
+                    issued = J0 + (TWO ? min(j + 2, n_items) : j + 1);
+                    if (valid && sl < segs) {
                         const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
-                        const uint32_t dst = sbase + C::OFF_RING + slot * C::TILE_BYTES + lane * p.box_rows * 128;
+                        const uint32_t dst = sbase + C::OFF_RING + slot * C::TILE_BYTES + sl * p.box_rows * 128;
                         tma_load_2d(dst, map, 0, row, slot_full + 8 * slot, policy);
                         tma_load_2d(dst + C::BOX_BYTES, map, 64, row, slot_full + 8 * slot, policy);
                     }
-                    if (lane == 0 && j == 0) {
-                        if (jj == 0) stamp(1);
-                        if (lu < kTraceUnits) stamp(unit_slot(lu, 7));
-                    }
+                    return true;
+                };
+                if (n_items > 0 && lane == 0) {
+                    if (J0 == 0) stamp(1);
+                    if (lu < kTraceUnits) stamp(unit_slot(lu, 7));
+                }
+                if (tile_count >= kPairTiles) {
+                    for (int j = 0; ok && j < n_items; j += 2) ok = pass(j, std::true_type{});
+                } else {
+                    for (int j = 0; ok && j < n_items; ++j) ok = pass(j, std::false_type{});
                 }
                 J0 += n_items;
             }
