@@ -139,6 +139,12 @@ struct fa_decode {
     uint64_t* trace;
     int64_t trace_words;
     MapCache k_map, v_map, out_map[3];
+    // Per-sequence split: the launches of the 2- and 4-CTA clusters run on two
+    // side streams forked from the caller's stream (their sequences are
+    // disjoint), so no launch waits for another's last wave. Owned by the
+    // handle; absent (null) for plans made without a handle.
+    cudaStream_t side[2];
+    cudaEvent_t fork, join[2];
 };
 
 namespace {
@@ -218,6 +224,18 @@ int resident_clusters(const fa_decode* h, const fad::KernelGeometry& g, int P, i
 }
 
 }  // namespace
+
+static void release_side_streams(fa_decode& h)
+{
+    for (int i = 0; i < 2; ++i) {
+        if (h.side[i]) cudaStreamDestroy(h.side[i]);
+        if (h.join[i]) cudaEventDestroy(h.join[i]);
+        h.side[i] = nullptr;
+        h.join[i] = nullptr;
+    }
+    if (h.fork) cudaEventDestroy(h.fork);
+    h.fork = nullptr;
+}
 
 // Validation, kernel choice and per-kernel attributes of a plan (the
 // FA4Config constructor and supported() checks). Allocates nothing; the
@@ -366,8 +384,21 @@ int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk
         cudaFree(tmp.d_status);
         return cuda_fail(e, "cudaMemset(status word)");
     }
+    if (splitk == 0) {
+        bool made = cudaStreamCreateWithFlags(&tmp.side[0], cudaStreamNonBlocking) == cudaSuccess &&
+                    cudaStreamCreateWithFlags(&tmp.side[1], cudaStreamNonBlocking) == cudaSuccess &&
+                    cudaEventCreateWithFlags(&tmp.fork, cudaEventDisableTiming) == cudaSuccess &&
+                    cudaEventCreateWithFlags(&tmp.join[0], cudaEventDisableTiming) == cudaSuccess &&
+                    cudaEventCreateWithFlags(&tmp.join[1], cudaEventDisableTiming) == cudaSuccess;
+        if (!made) {
+            release_side_streams(tmp);
+            cudaFree(tmp.d_status);
+            return fail(FA_ERR_CUDA, "creating the side streams of the per-sequence split");
+        }
+    }
     fa_decode* h = new (std::nothrow) fa_decode(tmp);
     if (!h) {
+        release_side_streams(tmp);
         cudaFree(tmp.d_status);
         return fail(FA_ERR_CUDA, "out of host memory");
     }
@@ -378,6 +409,7 @@ int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk
 int fa_decode_destroy(fa_decode_t h)
 {
     if (!h) return FA_OK;
+    release_side_streams(*h);
     cudaError_t e = cudaFree(h->d_status);
     delete h;
     if (e != cudaSuccess) return cuda_fail(e, "cudaFree(status word)");
@@ -547,6 +579,14 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     int splits[3];
     const int ns = split_list(h, splits);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Fork: launches after the first go to the side streams, which first wait
+    // for everything queued on the caller's stream.
+    const bool forked = ns > 1 && h->side[0] && h->side[1];
+    if (forked) {
+        cudaError_t e = cudaEventRecord(h->fork, s);
+        for (int i = 0; e == cudaSuccess && i < 2; ++i) e = cudaStreamWaitEvent(h->side[i], h->fork, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "forking the per-sequence split launches");
+    }
     for (int i = 0; i < ns; ++i) {
         const int P = splits[i];
         p.splitk = P;
@@ -564,7 +604,7 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
         cfg.gridDim = clusters == units ? dim3(P, h->hkv * row_blocks, batch) : dim3(P, (unsigned)clusters, 1);
         cfg.blockDim = dim3(g.threads, 1, 1);
         cfg.dynamicSmemBytes = g.smem_bytes;
-        cfg.stream = s;
+        cfg.stream = forked && i > 0 ? h->side[i - 1] : s;
         if (P > 1) {
             attr[0].id = cudaLaunchAttributeClusterDimension;
             attr[0].val.clusterDim.x = P;
@@ -576,6 +616,15 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
         void* args[1] = {&p};
         cudaError_t e = cudaLaunchKernelExC(&cfg, g.func, args);
         if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    }
+    if (forked) {
+        // Join: the caller's stream continues once both side launches are done.
+        cudaError_t e = cudaSuccess;
+        for (int i = 0; e == cudaSuccess && i < 2; ++i) {
+            e = cudaEventRecord(h->join[i], h->side[i]);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->join[i], 0);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "joining the per-sequence split launches");
     }
     return FA_OK;
 }
