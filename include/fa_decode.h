@@ -78,7 +78,9 @@ typedef struct fa_decode* fa_decode_t;
  * Built shapes: (Dk, Dv) in {(64,64), (128,128), (576,512)}; T * g <= 16
  * rows per CTA, or T == 1 with g a multiple of 16. Other shapes return
  * FA_ERR_UNSUPPORTED. Needs a current CUDA device of compute capability 10.3
- * (GB300). Allocates one small device status word.
+ * (GB300). Allocates one small device status word and, for a fixed split
+ * on the tensor-core path, a stream-K scratch (2 x resident clusters x rows x
+ * ov_depth fp32: at most about 3 MB).
  */
 int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk_depth,
                      int nope_depth, int ov_depth, int page_size, int num_q, int splitk);
@@ -106,6 +108,16 @@ int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk
  * the page-table stride and the extent of the cache views cannot be derived
  * from the others. Invalid page ids and over-long sequences are detected on the
  * device, read as zeros and reported by fa_decode_check; they never fault.
+ *
+ * With a fixed split and fewer (sequence, kv head) units than clusters fit on
+ * the device, the units' key ranges (each counted as a full page-table row)
+ * are laid end to end and cut into one equal range per resident cluster
+ * (stream-K; every rank keeps at least 4 tiles of 128 keys and no unit is
+ * shared by more than 16 clusters). Each cluster merges its ranks over
+ * distributed shared memory, and the last cluster of a shared unit merges
+ * the clusters' results through the handle's scratch. Runs of one handle must therefore not overlap (one stream at a
+ * time, or ordered by events); after fa_decode_check reports a status the
+ * handle's scratch is reset.
  */
 int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void* v_pages,
                   const int32_t* page_table, const int32_t* seq_lens, float scale,
@@ -126,13 +138,16 @@ int fa_decode_check(fa_decode_t h, void* stream, uint32_t* status_out);
  * two on one input); FA_DEBUG_TWO_CLUSTERS launches the tensor-core kernel of
  * a fixed split with at most two clusters, each working through its share of
  * the (sequence, kv head) units in turn, so that small inputs exercise the
- * multi-unit schedule that large batches get; wait_limit_ns bounds every
+ * multi-unit schedule that large batches get; FA_DEBUG_ONE_CHUNK turns the
+ * stream-K partition off (every (sequence, kv head) key range on one
+ * cluster); wait_limit_ns bounds every
  * device wait (0 restores the default of one second). Normal runs never need
  * this call.
  */
 #define FA_DEBUG_SKIP_LOADS 1u
 #define FA_DEBUG_FORCE_SIMT 2u   /* run the warp-level FMA kernel even where the tcgen05 one applies */
 #define FA_DEBUG_TWO_CLUSTERS 4u /* at most two clusters on the tensor-core path with a fixed split */
+#define FA_DEBUG_ONE_CHUNK 8u     /* no stream-K partition: one cluster per (sequence, kv head) */
 int fa_decode_set_debug(fa_decode_t h, uint32_t flags, int64_t wait_limit_ns);
 
 /*

@@ -129,11 +129,20 @@ struct fa_decode {
     fad::KernelGeometry geo_latent;  // SIMT kernel, V = prefix of the K row
     fad::KernelGeometry geo_tc;      // tcgen05 kernel, 3-slot ring (two CTAs per SM)
     fad::KernelGeometry geo_tc_big;  // tcgen05 kernel, 6-slot ring (one CTA per SM, several units per cluster)
+    fad::KernelGeometry geo_tc_sk;   // the same under the stream-K partition
     fad::KernelGeometry geo_mla;     // tcgen05 kernel of the MLA latent layout (64 heads per CTA)
     bool has_simt, has_latent, has_tc, has_mla;
     int sm_count;
     int tc_big_clusters;             // clusters of geo_tc_big (fixed split) resident at once
     unsigned int* d_status;
+    // Stream-K chunk scratch of geo_tc_big (fixed split): two slots per
+    // resident cluster; null for plans made without a handle.
+    void* d_chunk;
+    size_t chunk_count_bytes;
+    float* chunk_o;
+    float2* chunk_ms;
+    unsigned int* chunk_count;
+    int64_t chunk_items;             // slots the scratch holds
     uint32_t debug_flags;
     uint64_t wait_limit_ns;
     uint64_t* trace;
@@ -294,8 +303,9 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
     tmp.has_latent = tmp.has_simt && fad::simt_geometry(qk_depth, ov_depth, true, tmp.rows_capacity,
                                                         &tmp.geo_latent);
     tmp.has_tc = tmp.row_blocks == 1 &&
-                 fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsShared, &tmp.geo_tc) &&
-                 fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsAlone, &tmp.geo_tc_big) &&
+                 fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsShared, false, &tmp.geo_tc) &&
+                 fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsAlone, false, &tmp.geo_tc_big) &&
+                 fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsAlone, true, &tmp.geo_tc_sk) &&
                  page_fits(tmp.geo_tc.keys_per_tile);
     tmp.has_mla = fad::mla_tc_geometry(qk_depth, ov_depth, tmp.nope, tmp.group, num_q, &tmp.geo_mla) &&
                   page_fits(tmp.geo_mla.keys_per_tile);
@@ -328,6 +338,7 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
     if (tmp.has_latent && (rc = prepare_kernel(&tmp, tmp.geo_latent))) return rc;
     if (tmp.has_tc && (rc = prepare_kernel(&tmp, tmp.geo_tc))) return rc;
     if (tmp.has_tc && (rc = prepare_kernel(&tmp, tmp.geo_tc_big))) return rc;
+    if (tmp.has_tc && splitk > 0 && (rc = prepare_kernel(&tmp, tmp.geo_tc_sk))) return rc;
     if (tmp.has_mla && (rc = prepare_kernel(&tmp, tmp.geo_mla))) return rc;
     cudaDeviceGetAttribute(&tmp.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (tmp.has_tc && splitk > 0 && (rc = resident_clusters(&tmp, tmp.geo_tc_big, splitk, &tmp.tc_big_clusters)))
@@ -396,9 +407,33 @@ int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk
             return fail(FA_ERR_CUDA, "creating the side streams of the per-sequence split");
         }
     }
+    if (tmp.has_tc && splitk > 0 && tmp.tc_big_clusters > 0) {
+        // Stream-K scratch: per slot and rank, the band's fp32 rows and
+        // per-row (max, sum); one count per (unit, rank), zero between
+        // launches (the partition is used with fewer units than clusters).
+        const size_t items = (size_t)tmp.tc_big_clusters * 2;
+        const size_t rb = (size_t)tmp.geo_tc_big.rows_capacity;
+        tmp.chunk_items = (int64_t)items;
+        tmp.chunk_count_bytes = (items * splitk * sizeof(unsigned int) + 255) / 256 * 256;
+        const size_t ms_bytes = (items * splitk * rb * sizeof(float2) + 255) / 256 * 256;
+        const size_t o_bytes = items * rb * (size_t)ov_depth * sizeof(float);
+        e = cudaMalloc(&tmp.d_chunk, tmp.chunk_count_bytes + ms_bytes + o_bytes);
+        if (e == cudaSuccess) e = cudaMemset(tmp.d_chunk, 0, tmp.chunk_count_bytes);
+        if (e != cudaSuccess) {
+            if (tmp.d_chunk) cudaFree(tmp.d_chunk);
+            release_side_streams(tmp);
+            cudaFree(tmp.d_status);
+            return cuda_fail(e, "allocating the key-range chunk scratch");
+        }
+        uint8_t* base = static_cast<uint8_t*>(tmp.d_chunk);
+        tmp.chunk_count = reinterpret_cast<unsigned int*>(base);
+        tmp.chunk_ms = reinterpret_cast<float2*>(base + tmp.chunk_count_bytes);
+        tmp.chunk_o = reinterpret_cast<float*>(base + tmp.chunk_count_bytes + ms_bytes);
+    }
     fa_decode* h = new (std::nothrow) fa_decode(tmp);
     if (!h) {
         release_side_streams(tmp);
+        if (tmp.d_chunk) cudaFree(tmp.d_chunk);
         cudaFree(tmp.d_status);
         return fail(FA_ERR_CUDA, "out of host memory");
     }
@@ -410,6 +445,7 @@ int fa_decode_destroy(fa_decode_t h)
 {
     if (!h) return FA_OK;
     release_side_streams(*h);
+    if (h->d_chunk) cudaFree(h->d_chunk);
     cudaError_t e = cudaFree(h->d_status);
     delete h;
     if (e != cudaSuccess) return cuda_fail(e, "cudaFree(status word)");
@@ -446,6 +482,11 @@ int fa_decode_check(fa_decode_t h, void* stream, uint32_t* status_out)
     if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
     e = cudaMemset(h->d_status, 0, sizeof st);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    if (st && h->chunk_count) {
+        // A launch that gave up may have left chunk counts behind.
+        e = cudaMemset(h->chunk_count, 0, h->chunk_count_bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the chunk counts");
+    }
     if (status_out) *status_out = st;
     if (st) {
         return fail(FA_ERR_DEVICE, "device status 0x%x:%s%s", st, (st & FA_STATUS_TIMEOUT) ? " wait timed out" : "",
@@ -466,10 +507,11 @@ int fa_decode_describe(fa_decode_t h, char* buf, int size)
     const int rows = h->has_mla ? 64 : h->rows, row_blocks = h->has_mla ? h->group / 64 : h->row_blocks;
     snprintf(buf, (size_t)size,
              "path=%s kernel=%s simt_kernel=%s latent_kernel=%s splitk=%d%s threads=%d keys_per_tile=%d "
-             "stages=%d rows=%d rows_capacity=%d row_blocks=%d smem=%d",
+             "stages=%d rows=%d rows_capacity=%d row_blocks=%d smem=%d resident_clusters=%d",
              tc ? "tcgen05" : "simt", g.name, h->has_simt ? h->geo.name : "none",
              h->has_latent ? h->geo_latent.name : "none", h->splitk, h->splitk == 0 ? "(per sequence: 1/2/4)" : "",
-             g.threads, g.keys_per_tile, g.stages, rows, h->has_mla ? 64 : h->rows_capacity, row_blocks, g.smem_bytes);
+             g.threads, g.keys_per_tile, g.stages, rows, h->has_mla ? 64 : h->rows_capacity, row_blocks, g.smem_bytes,
+             h->tc_big_clusters);
     return FA_OK;
 }
 
@@ -515,8 +557,38 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     const bool tc_big = use_tc && h->splitk > 0;
     const int64_t units = (int64_t)h->hkv * batch;
     int64_t clusters = units;
+    // Stream-K partition (see DecodeParams::sk_tiles): 0 = off.
+    int sk_tiles = 0, sk_clusters = 0;
+    int64_t sk_total = 0;
     if (tc_big) {
         const int64_t most = (h->debug_flags & FA_DEBUG_TWO_CLUSTERS) ? 2 : h->tc_big_clusters;
+        if (units < most && h->chunk_count && !(h->debug_flags & FA_DEBUG_ONE_CHUNK) && units > 0) {
+            // Fewer units than resident clusters: give every resident cluster
+            // an equal share of all units' tiles (a full page-table row each),
+            // while every rank keeps kChunkMinTilesPerRank tiles and no unit is
+            // shared by more than kMaxSplit clusters.
+            const int64_t nv = ((int64_t)max_pages_per_seq * h->page_size + 127) / 128;
+            const int64_t total = units * nv;
+            int64_t G = total / ((int64_t)fad::kChunkMinTilesPerRank * h->splitk);
+            if (G > most) G = most;
+            if (nv <= INT32_MAX) {
+                for (; G > units; --G) {
+                    int widest = 0;
+                    for (int64_t u = 0; u < units; ++u) {
+                        const int n = fad::sk_cluster_of(total, (int)G, (u + 1) * nv - 1) -
+                                      fad::sk_cluster_of(total, (int)G, u * nv) + 1;
+                        if (n > widest) widest = n;
+                    }
+                    if (widest <= fad::kMaxSplit) break;
+                }
+                if (G > units && 2 * G <= h->chunk_items) {
+                    sk_tiles = (int)nv;
+                    sk_clusters = (int)G;
+                    sk_total = total;
+                    clusters = G;
+                }
+            }
+        }
         if (clusters > most) {
             // As many rounds as the resident clusters need, spread evenly: the
             // fewest clusters that still finish in that many rounds.
@@ -526,7 +598,9 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     }
     const fad::KernelGeometry& g = use_mla ? h->geo_mla
                                    : use_latent ? h->geo_latent
-                                                : (use_tc ? (tc_big ? h->geo_tc_big : h->geo_tc) : h->geo);
+                                                : (use_tc ? (tc_big ? (sk_tiles > 0 ? h->geo_tc_sk : h->geo_tc_big)
+                                                                    : h->geo_tc)
+                                                          : h->geo);
     // Heads per CTA: 64 for the MLA kernel, else the plan's rows.
     const int row_blocks = use_mla ? h->group / 64 : h->row_blocks;
     const int heads_per_cta = use_mla ? 64 : h->heads_per_cta;
@@ -575,6 +649,12 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     p.auto_split = h->splitk == 0 ? 1 : 0;
     p.trace = reinterpret_cast<unsigned long long*>(h->trace);
     p.trace_ctas = h->trace_words / FA_TRACE_WORDS_PER_CTA;
+    p.sk_tiles = sk_tiles;
+    p.sk_clusters = sk_clusters;
+    p.sk_total = sk_total;
+    p.chunk_o = h->chunk_o;
+    p.chunk_ms = h->chunk_ms;
+    p.chunk_count = h->chunk_count;
 
     int splits[3];
     const int ns = split_list(h, splits);
@@ -600,7 +680,8 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         // Cluster c (= blockIdx.y + gridDim.y * blockIdx.z) takes units
-        // c, c + G, ... of u = b * Hkv + kvh; with G = units that is one unit each.
+        // c, c + G, ... of u = b * Hkv + kvh (with G = units that is one unit
+        // each), or the units its stream-K range touches.
         cfg.gridDim = clusters == units ? dim3(P, h->hkv * row_blocks, batch) : dim3(P, (unsigned)clusters, 1);
         cfg.blockDim = dim3(g.threads, 1, 1);
         cfg.dynamicSmemBytes = g.smem_bytes;

@@ -20,6 +20,18 @@ __host__ __device__ inline int auto_split_for_len(int len)
     return len <= 1024 ? 1 : (len <= 4096 ? 2 : 4);
 }
 
+// Stream-K partition of `total` tiles over `clusters` ranges: the first tile
+// of cluster c's range, and the cluster whose range holds tile x (the largest
+// c with sk_begin(c) <= x).
+__host__ __device__ inline int64_t sk_begin(int64_t total, int clusters, int64_t c)
+{
+    return c * total / clusters;
+}
+__host__ __device__ inline int sk_cluster_of(int64_t total, int clusters, int64_t x)
+{
+    return (int)(((x + 1) * clusters + total - 1) / total - 1);
+}
+
 // Everything a decode kernel needs, passed by value as a __grid_constant__
 // parameter block (the tensor maps must live in parameter, constant or global
 // memory for TMA to read them).
@@ -49,6 +61,22 @@ struct DecodeParams {
     uint64_t wait_limit_ns;
     unsigned long long* trace;  // per-CTA timeline (FA_TRACE_WORDS_PER_CTA words each) or NULL
     int64_t trace_ctas;         // CTAs the trace buffer holds
+    // Stream-K partition (sk_tiles > 0; the deep-ring kernel only, when the
+    // units alone would leave resident clusters idle): each unit's key range
+    // counts as sk_tiles tiles of 128 keys (a full page-table row), the units'
+    // ranges are laid end to end (sk_total = units * sk_tiles) and cluster c
+    // of sk_clusters takes tiles [c * sk_total / G, (c + 1) * sk_total / G):
+    // the end of one unit and the start of the next at most. A unit whose
+    // range several clusters share is merged over DSMEM per cluster as usual;
+    // each cluster's normalised band and (max, sum) go to chunk_o / chunk_ms
+    // (slot 2c or 2c + 1: the cluster's first or second unit) and the last
+    // cluster to count in (chunk_count, which it resets) merges the chunks.
+    int sk_tiles;
+    int sk_clusters;
+    int64_t sk_total;
+    float* chunk_o;             // [slot][P][band_cols][rows_capacity]
+    float2* chunk_ms;           // [slot][P][rows_capacity]: (max, sum) in raw score units
+    unsigned int* chunk_count;  // [unit][P], zero between launches
 };
 
 // Geometry of one compiled kernel variant, for planning and validation.
@@ -67,12 +95,16 @@ struct KernelGeometry {
 bool simt_geometry(int qk_depth, int ov_depth, bool latent, int rows_capacity, KernelGeometry* g);
 
 // Kernel variants of the tcgen05 path (head dim 128, <= 16 rows per CTA) with
-// a ring of `nslot` 32 KB K/V tile slots.
-bool tc_geometry(int qk_depth, int ov_depth, int rows, int nslot, KernelGeometry* g);
+// a ring of `nslot` 32 KB K/V tile slots; stream_k selects the variant of the
+// deep ring that takes the stream-K partition.
+bool tc_geometry(int qk_depth, int ov_depth, int rows, int nslot, bool stream_k, KernelGeometry* g);
 // The tcgen05 kernel of the MLA latent layout (qk 576 = nope 512 + rope 64,
 // ov 512, V = the latent rows' first 512 columns) for num_q == 1 and a
 // multiple of 64 heads per kv head: 64 heads per CTA.
 bool mla_tc_geometry(int qk_depth, int ov_depth, int nope_depth, int heads_per_kv, int num_q, KernelGeometry* g);
+// The stream-K partition is used only while every cluster rank keeps at
+// least this many 128-key tiles of its range.
+constexpr int kChunkMinTilesPerRank = 4;
 constexpr int kTcSlotsShared = 3;  // two CTAs per SM (grids of more than one wave)
 constexpr int kTcSlotsAlone = 6;   // one CTA per SM, 192 KB of loads in flight
 

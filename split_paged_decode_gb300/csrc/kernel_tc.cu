@@ -223,10 +223,12 @@ constexpr float kRescaleThreshold = 8.0f;
 // by the load warp (its issue rate bounds them); shorter ones one at a time.
 constexpr int kPairTiles = 16;
 
-template <int NSLOT, int NRV>
+// SK: the stream-K partition (DecodeParams::sk_tiles; deep ring only).
+template <int NSLOT, int NRV, bool SK>
 __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>::MULTI ? 1 : 2)
     tc_decode_kernel(const __grid_constant__ DecodeParams p)
 {
+    static_assert(!SK || TcCfg<NSLOT, NRV>::MULTI, "stream-K needs the multi-unit variant");
     using C = TcCfg<NSLOT, NRV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -240,6 +242,17 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
     const int n_units = p.batch * p.num_kv_heads;
     const int cluster_id = (int)(blockIdx.y + gridDim.y * blockIdx.z);
     const int n_clusters = (int)(gridDim.y * gridDim.z);
+    // This cluster's units: c, c + G, ... or, under the stream-K partition,
+    // the one or two its tile range touches.
+    int u_first = cluster_id, u_step = n_clusters, u_end = n_units;
+    int64_t sk_g0 = 0, sk_g1 = 0;  // the cluster's stream-K tile range
+    if constexpr (SK) {
+        sk_g0 = sk_begin(p.sk_total, p.sk_clusters, cluster_id);
+        sk_g1 = sk_begin(p.sk_total, p.sk_clusters, cluster_id + 1);
+        u_first = (int)(sk_g0 / p.sk_tiles);
+        u_end = sk_g1 > sk_g0 ? (int)((sk_g1 - 1) / p.sk_tiles) + 1 : u_first;
+        u_step = 1;
+    }
 
     // Optional timeline trace (a profiling aid): one thread writes each event.
     const int64_t cta_lin = (int64_t)blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
@@ -256,11 +269,18 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
         tma_prefetch_map(&p.tm_v);
     }
 
-    // Tiles [tile_begin, tile_begin + tile_count) of a unit belong to this rank.
-    auto rank_tiles = [&](int L, int& tile_begin, int& tile_count) {
-        const int n_tiles = (L + C::BN - 1) / C::BN;
+    // Tiles [tile_begin, tile_begin + tile_count) of unit u (length L) belong
+    // to this rank: its share of all the unit's tiles or, under the stream-K
+    // partition, of those in the cluster's range (clipped to L).
+    auto rank_tiles = [&](int u, int L, int& tile_begin, int& tile_count) {
+        int n_tiles = (L + C::BN - 1) / C::BN, t0 = 0;
+        if constexpr (SK) {
+            const int64_t base = (int64_t)u * p.sk_tiles;
+            t0 = (int)min((int64_t)n_tiles, max(sk_g0, base) - base);
+            n_tiles = max((int)min((int64_t)n_tiles, min(sk_g1, base + p.sk_tiles) - base) - t0, 0);
+        }
         const int base = n_tiles / P, rem = n_tiles % P;
-        tile_begin = rank * base + min(rank, rem);
+        tile_begin = t0 + rank * base + min(rank, rem);
         tile_count = base + (rank < rem ? 1 : 0);
     };
     // Page-table entries reach the load warp in warp-wide blocks: lane l
@@ -273,23 +293,23 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
     const int segs = C::BN / p.box_rows;  // page segments per tile: 1, 2, 4, 8 or 16
     const int tpb = 32 / segs;            // tiles per block of page entries
     int spec_begin = -1, spec_count = 0, spec_raw = -1;
-    if (warp == 0 && cluster_id < n_units && p.max_pages <= INT32_MAX / C::BN / p.page_size) {
+    if (warp == 0 && u_first < u_end && p.max_pages <= INT32_MAX / C::BN / p.page_size) {
         int gb, gc;
-        rank_tiles(p.max_pages * p.page_size, gb, gc);
+        rank_tiles(u_first, p.max_pages * p.page_size, gb, gc);
         spec_begin = gb;
         spec_count = gc;
-        const int b0 = cluster_id / p.num_kv_heads;
+        const int b0 = u_first / p.num_kv_heads;
         const int t = lane / segs;
         const int pslot = ((gb + t) * C::BN + (lane % segs) * p.box_rows) / p.page_size;
         if (t < gc && pslot < p.max_pages) spec_raw = p.page_table[(int64_t)b0 * p.max_pages + pslot];
     }
-    if (cluster_id >= n_units) return;  // (grids never have more clusters than units)
+    if (u_first >= u_end) return;  // (grids never have more clusters than units or ranges)
     if (p.auto_split) {
         // A cluster with no unit in this launch (the per-sequence split gives
         // its sequences to another launch) leaves at once; the decision is the
         // same in every CTA of the cluster.
-        Unit first{cluster_id, 0, 0, 0};
-        if (!next_unit(p, n_clusters, n_units, first, tid == 0 && rank == 0)) return;
+        Unit first{u_first, 0, 0, 0};
+        if (!next_unit(p, u_step, u_end, first, tid == 0 && rank == 0)) return;
     }
 
     const uint32_t bar0 = sbase + C::OFF_BAR;
@@ -367,10 +387,10 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
             constexpr int kNoSegment = INT32_MIN, kPastSequence = INT32_MIN + 1;
             int J0 = 0, lu = 0;
             bool ok = true;
-            Unit w{cluster_id, 0, 0, 0};
-            for (; ok && next_unit(p, n_clusters, n_units, w, tid == 0 && rank == 0); w.u += n_clusters, ++lu) {
+            Unit w{u_first, 0, 0, 0};
+            for (; ok && next_unit(p, u_step, u_end, w, tid == 0 && rank == 0); w.u += u_step, ++lu) {
                 int tile_begin, tile_count;
-                rank_tiles(w.L, tile_begin, tile_count);
+                rank_tiles(w.u, w.L, tile_begin, tile_count);
                 const int n_items = 2 * tile_count;
                 // This lane's entry of the block starting at tile tb: the physical
                 // page, or kNoSegment / kPastSequence (zero fill, no error); -1
@@ -387,7 +407,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
                 // The guess holds when the unit's first tiles are the guessed ones
                 // (then every entry block_entry needs below was read).
                 const bool guessed =
-                    lu == 0 && w.u == cluster_id && tile_begin == spec_begin && tile_count <= spec_count;
+                    lu == 0 && w.u == u_first && tile_begin == spec_begin && tile_count <= spec_count;
                 int blk_cur = block_entry(0, guessed ? spec_raw : -2), blk_next = block_entry(tpb);
                 // One pass issues one item (lanes 0-15) or, for a long unit, two
                 // consecutive items (lanes 0-15 and 16-31; lane 16 h + s owns page
@@ -496,10 +516,10 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
             };
             int J0 = 0, gt = 0, lu = 0;
             bool ok = true;
-            Unit w{cluster_id, 0, 0, 0};
-            for (; ok && next_unit(p, n_clusters, n_units, w, false); w.u += n_clusters, ++lu) {
+            Unit w{u_first, 0, 0, 0};
+            for (; ok && next_unit(p, u_step, u_end, w, false); w.u += u_step, ++lu) {
                 int tile_begin, tile_count;
-                rank_tiles(w.L, tile_begin, tile_count);
+                rank_tiles(w.u, w.L, tile_begin, tile_count);
                 if (is_s) {
                     ok = mbar_wait(q_full + 8 * (lu & 1), (lu >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
                     if (lu == 0) stamp(60);
@@ -603,8 +623,8 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
             }
         };
 
-        Unit w{cluster_id, 0, 0, 0};
-        bool have = next_unit(p, n_clusters, n_units, w, false);
+        Unit w{u_first, 0, 0, 0};
+        bool have = next_unit(p, u_step, u_end, w, false);
         if (have && lead) {
             uint4 qv[2];
             load_q(w, qv);
@@ -626,7 +646,7 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
         while (have) {
             const int L = w.L;
             int tile_begin, tile_count;
-            rank_tiles(L, tile_begin, tile_count);
+            rank_tiles(w.u, L, tile_begin, tile_count);
             if (lead && wt == 0 && lu < kTraceUnits) {
                 stamp(unit_slot(lu, 0));
                 if (trace) trace[unit_slot(lu, 6)] = (unsigned long long)tile_count;
@@ -636,8 +656,8 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
             // this warpgroup's first tile of the unit), so the S warp runs
             // straight on into it.
             Unit nx = w;
-            nx.u += n_clusters;
-            const bool more = C::MULTI && next_unit(p, n_clusters, n_units, nx, false);
+            nx.u += u_step;
+            const bool more = C::MULTI && next_unit(p, u_step, u_end, nx, false);
             uint4 qn[2];
             bool q_pending = more && lead;
             if (q_pending) load_q(nx, qn);
@@ -974,9 +994,9 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
         // the softmax warps work on the next unit.
         bool cluster_waited = false;
         int lu = 0;
-        Unit w{cluster_id, 0, 0, 0};
+        Unit w{u_first, 0, 0, 0};
         const uint32_t expect = (uint32_t)pushed_bytes(P, p.band_cols, NRV);
-        for (; next_unit(p, n_clusters, n_units, w, false); w.u += n_clusters, ++lu) {
+        for (; next_unit(p, u_step, u_end, w, false); w.u += u_step, ++lu) {
             const int rb = lu % C::RECV_BUFS, rk = lu / C::RECV_BUFS;
             if (P > 1 && !cluster_waited) {
                 cluster_wait();  // every rank's barriers are initialised
@@ -995,10 +1015,17 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
             if (!__all_sync(0xffffffffu, got)) break;
             if (lane == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 4));
             const uint8_t* recv = smem + C::OFF_RECV + rb * C::RECV_BYTES;
-            splitk_merge_pushed<NRV>(p, P, rank, w.b, w.kvh, reinterpret_cast<const float*>(recv),
-                                     reinterpret_cast<const float2*>(recv + C::RECV_O_BYTES),
-                                     reinterpret_cast<float*>(smem + C::OFF_WTAB),
-                                     reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), lane);
+            if constexpr (SK)
+                splitk_merge_pushed_sk<NRV>(p, P, rank, w.b, w.kvh, w.u, cluster_id,
+                                            reinterpret_cast<const float*>(recv),
+                                            reinterpret_cast<const float2*>(recv + C::RECV_O_BYTES),
+                                            reinterpret_cast<float*>(smem + C::OFF_WTAB),
+                                            reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), lane);
+            else
+                splitk_merge_pushed<NRV>(p, P, rank, w.b, w.kvh, reinterpret_cast<const float*>(recv),
+                                         reinterpret_cast<const float2*>(recv + C::RECV_O_BYTES),
+                                         reinterpret_cast<float*>(smem + C::OFF_WTAB),
+                                         reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), lane);
             // Release the buffer to every sender: all lanes' reads of it are
             // complete (their results are in the band); one fence orders them
             // ahead of the senders' next pushes, then relaxed arrives.
@@ -1037,19 +1064,22 @@ __global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>:
     if (tid == 0) stamp(3);
 }
 
-bool tc_geometry(int qk, int ov, int rows, int nslot, KernelGeometry* g)
+bool tc_geometry(int qk, int ov, int rows, int nslot, bool stream_k, KernelGeometry* g)
 {
+    if (stream_k && nslot <= kTcSlotsShared) return false;
     if (qk != 128 || ov != 128 || rows < 1 || rows > 16) return false;
     const int nrv = rows <= 4 ? 4 : (rows <= 8 ? 8 : 16);
 #define FAD_TC(NS, NRV)                                                                   \
     if (nslot == NS && nrv == NRV) {                                                      \
-        g->func = reinterpret_cast<const void*>(&tc_decode_kernel<NS, NRV>);              \
+        g->func = stream_k ? reinterpret_cast<const void*>(&tc_decode_kernel<NS, NRV, NS != 3>) \
+                           : reinterpret_cast<const void*>(&tc_decode_kernel<NS, NRV, false>); \
         g->threads = TcCfg<NS, NRV>::THREADS;                                             \
         g->keys_per_tile = TcCfg<NS, NRV>::BN;                                            \
         g->stages = NS;                                                                   \
         g->rows_capacity = NRV;                                                           \
         g->smem_bytes = TcCfg<NS, NRV>::SMEM_BYTES;                                       \
-        g->name = "tc_d128_bn128_n16_r" #NRV "_slots" #NS;                                \
+        g->name = stream_k ? "tc_d128_bn128_n16_r" #NRV "_slots" #NS "_streamk"          \
+                           : "tc_d128_bn128_n16_r" #NRV "_slots" #NS;                     \
         return true;                                                                      \
     }
     FAD_TC(3, 4)

@@ -332,4 +332,153 @@ __device__ __forceinline__ void splitk_merge_pushed(const DecodeParams& p, int P
     }
 }
 
+// The same merge for unit `u` under the stream-K partition, in the cluster
+// `cluster`: when several clusters' ranges share the unit, the cluster's
+// merged band is one chunk of it. The chunk (fp32, normalised, with the
+// per-row Gmax and Gsum) goes to the scratch slot of (cluster, unit), and the
+// last of the unit's clusters to count in for this band merges the chunks by
+// the same rule one level up (in cluster order, so the result does not depend
+// on which cluster comes last), stores the band and lse (rank 0) and resets
+// the count. `wtab` is float [max(P, 16)][RB]; a unit has at most 16 chunks.
+template <int RB>
+__device__ __noinline__ void splitk_merge_pushed_sk(const DecodeParams& p, int P, int rank, int b, int kvh, int u,
+                                                    int cluster, const float* recv_o, const float2* recv_ms,
+                                                    float* wtab, uint16_t* out_s, int lane)
+{
+    const int64_t Nv = p.sk_tiles, TOT = p.sk_total;
+    const int G = p.sk_clusters;
+    const int c_first = sk_cluster_of(TOT, G, (int64_t)u * Nv);
+    const int S = sk_cluster_of(TOT, G, (int64_t)(u + 1) * Nv - 1) - c_first + 1;
+    if (S == 1) {  // the unit lies in this cluster's range alone
+        splitk_merge_pushed<RB>(p, P, rank, b, kvh, recv_o, recv_ms, wtab, out_s, lane);
+        return;
+    }
+    // Scratch slot of (cluster c, unit u): 2c, or 2c + 1 for the second unit
+    // of c's range. Only the unit's first cluster can have started in an
+    // earlier unit (every later one starts inside this unit).
+    const int first_second = sk_begin(TOT, G, c_first) < (int64_t)u * Nv ? 1 : 0;
+    auto slot = [&](int c) -> int64_t { return 2 * (int64_t)c + (c == c_first ? first_second : 0); };
+    const int BW = p.band_cols;
+    const float c = p.scale_log2e;
+    const int64_t mine = slot(cluster);
+    float* const my_o = p.chunk_o + (mine * P + rank) * BW * RB;
+    // This chunk: weights over the cluster's ranks, then the band.
+    for (int r = lane; r < RB; r += 32) {
+        float gmax = -INFINITY;
+        for (int q = 0; q < P; ++q) {
+            const float2 ms = recv_ms[q * RB + r];
+            if (ms.y > 0.f) gmax = fmaxf(gmax, ms.x);
+        }
+        float gsum = 0.f;
+        for (int q = 0; q < P; ++q) {
+            const float2 ms = recv_ms[q * RB + r];
+            const float w = ms.y > 0.f ? ms.y * ex2_approx((ms.x - gmax) * c) : 0.f;
+            wtab[q * RB + r] = w;
+            gsum += w;
+        }
+        const float inv = gsum > 0.f ? 1.f / gsum : 0.f;
+        for (int q = 0; q < P; ++q) wtab[q * RB + r] *= inv;
+        p.chunk_ms[(mine * P + rank) * RB + r] = make_float2(gmax, gsum);
+    }
+    __syncwarp();
+    for (int col = lane; col < BW; col += 32) {
+        float o[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) o[r] = 0.f;
+        for (int q = 0; q < P; ++q) {
+            const float4* src = reinterpret_cast<const float4*>(recv_o + (q * BW + col) * RB);
+#pragma unroll
+            for (int r4 = 0; r4 < RB / 4; ++r4) {
+                const float4 v = src[r4];
+                o[4 * r4 + 0] = fmaf(wtab[q * RB + 4 * r4 + 0], v.x, o[4 * r4 + 0]);
+                o[4 * r4 + 1] = fmaf(wtab[q * RB + 4 * r4 + 1], v.y, o[4 * r4 + 1]);
+                o[4 * r4 + 2] = fmaf(wtab[q * RB + 4 * r4 + 2], v.z, o[4 * r4 + 2]);
+                o[4 * r4 + 3] = fmaf(wtab[q * RB + 4 * r4 + 3], v.w, o[4 * r4 + 3]);
+            }
+        }
+        float4* dst = reinterpret_cast<float4*>(my_o + col * RB);
+#pragma unroll
+        for (int r4 = 0; r4 < RB / 4; ++r4) dst[r4] = make_float4(o[4 * r4], o[4 * r4 + 1], o[4 * r4 + 2], o[4 * r4 + 3]);
+    }
+    // Publish this chunk's band (every lane's writes, then one count); the
+    // cluster that completes the count reads every chunk's band.
+    __threadfence();
+    __syncwarp();
+    unsigned int* count = p.chunk_count + (int64_t)u * P + rank;
+    unsigned int last = 0;
+    if (lane == 0) last = atomicAdd(count, 1u) == (unsigned int)(S - 1) ? 1u : 0u;
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __threadfence();
+    // Chunk weights per row (lane r < RB <= 16), every chunk's (max, sum) in
+    // flight at once: these reads queue behind the streaming loads.
+    if (lane < RB) {
+        const int r = lane;
+        float2 ms[kMaxSplit];
+#pragma unroll
+        for (int k = 0; k < kMaxSplit; ++k)
+            ms[k] = k < S ? __ldcg(p.chunk_ms + (slot(c_first + k) * P + rank) * RB + r) : make_float2(-INFINITY, 0.f);
+        float gmax = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kMaxSplit; ++k)
+            if (ms[k].y > 0.f) gmax = fmaxf(gmax, ms[k].x);
+        float wk[kMaxSplit];
+        float gsum = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxSplit; ++k) {
+            wk[k] = ms[k].y > 0.f ? ms[k].y * ex2_approx((ms[k].x - gmax) * c) : 0.f;
+            gsum += wk[k];
+        }
+        const float inv = gsum > 0.f ? 1.f / gsum : 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxSplit; ++k)
+            if (k < S) wtab[k * RB + r] = wk[k] * inv;
+        if (rank == 0 && r < p.rows && p.lse != nullptr) {
+            const int t = r / p.heads_per_cta;
+            const int h = kvh * p.group + r % p.heads_per_cta;
+            p.lse[((int64_t)b * p.num_q + t) * p.num_q_heads + h] =
+                gsum > 0.f ? p.scale * gmax + lg2_approx(gsum) * 0.6931471805599453f : -INFINITY;
+        }
+    }
+    __syncwarp();
+    if (lane == 0) {
+        *count = 0u;            // every chunk of this launch has counted
+        tma_store_wait_read();  // the previous unit's store has read out_s
+    }
+    __syncwarp();
+    // The band: lane takes (column, 4-row group) pairs, every chunk's values
+    // of a pair in flight at once.
+    const int OC = p.out_chunk_cols;
+    for (int idx = lane; idx < BW * (RB / 4); idx += 32) {
+        const int col = idx / (RB / 4), r4 = idx % (RB / 4);
+        float4 v[kMaxSplit];
+#pragma unroll
+        for (int k = 0; k < kMaxSplit; ++k)
+            if (k < S)
+                v[k] = __ldcg(reinterpret_cast<const float4*>(p.chunk_o + ((slot(c_first + k) * P + rank) * BW + col) * RB) +
+                              r4);
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < kMaxSplit; ++k) {
+            if (k < S) {
+                const float* wr = wtab + k * RB + 4 * r4;
+                o[0] = fmaf(wr[0], v[k].x, o[0]);
+                o[1] = fmaf(wr[1], v[k].y, o[1]);
+                o[2] = fmaf(wr[2], v[k].z, o[2]);
+                o[3] = fmaf(wr[3], v[k].w, o[3]);
+            }
+        }
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(out_s) + (col / OC) * RB * OC + col % OC;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[(4 * r4 + i) * OC] = __float2bfloat16_rn(o[i]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        for (int c0 = 0; c0 < BW; c0 += OC)
+            tma_store_3d(&p.tm_out, smem_addr(out_s + (c0 / OC) * RB * OC), rank * BW + c0, kvh * p.group,
+                         b * p.num_q);
+        tma_store_commit();
+    }
+}
+
 }  // namespace fad

@@ -204,7 +204,7 @@ def test_multi_unit_rows(g, T):
 def test_multi_unit_matches_one_unit_per_cluster_bitwise():
     """A unit's arithmetic does not depend on which cluster takes it."""
     inp = generate(wl(batch=6, splitk=4, seed=97))
-    with DeviceCall(inp) as one, DeviceCall(inp, path="two_clusters") as many:
+    with DeviceCall(inp, path="one_chunk") as one, DeviceCall(inp, path="two_clusters") as many:
         one.run()
         many.run()
         assert one.status() == 0 and many.status() == 0
@@ -217,6 +217,83 @@ def test_many_units_default_grid():
     w = wl(batch=40, num_kv_heads=8, num_q_heads=32, splitk=4, page_size=128, seq_len_lo=1, seq_len_hi=3000,
            seed=98)
     run_and_check(w, rows=_sample_rows(w, 400, 9), what="many units")
+
+
+# --- stream-K partition: fewer units than resident clusters ----------------------------
+# With a fixed split and fewer (sequence, kv head) units than clusters fit on
+# the device, the units' key ranges (a full page-table row each) are laid end
+# to end and cut into one equal range per resident cluster; a unit shared by
+# several clusters is merged by the last of them through the handle's scratch.
+
+@pytest.mark.parametrize("P", [1, 2, 4, 8])
+def test_stream_k_long(P):
+    w = wl(batch=1, splitk=P, seq_len=P * 4 * 128 * 6 + 77, seed=110 + P)  # 2 units over ~12 clusters
+    run_and_check(w, what=f"stream-K P{P}")
+
+
+def test_stream_k_empty_and_short():
+    """Sequences of length 0 and 1 next to a long one: most of their clusters see no key."""
+    w = wl(batch=3, num_kv_heads=1, num_q_heads=4, splitk=2, seq_len_lo=1, seq_len_hi=5000, seed=115)
+    run_and_check(w, seq_lens=[0, 1, 5000], what="stream-K short")
+
+
+def test_stream_k_sixteen():
+    """One unit over 65541 keys: shared by the most clusters (16), a ragged last tile."""
+    w = wl(batch=1, num_kv_heads=1, num_q_heads=4, splitk=4, page_size=128, seq_len=65541, seed=116)
+    run_and_check(w, what="stream-K 16")
+
+
+@pytest.mark.parametrize("g,T", [(4, 4), (16, 1), (8, 1)])
+def test_stream_k_rows(g, T):
+    w = wl(batch=2, num_kv_heads=1, num_q_heads=g, num_q=T, splitk=2, seq_len_lo=2000, seq_len_hi=6000,
+           seed=117 + g)
+    run_and_check(w, what=f"stream-K g{g} T{T}")
+
+
+def test_stream_k_two_clusters():
+    """Two clusters, one unit: each takes half of its range."""
+    w = wl(batch=1, num_kv_heads=1, num_q_heads=4, splitk=4, seq_len=9000, seed=118)
+    run_and_check(w, what="stream-K two clusters", path="two_clusters")
+
+
+def test_stream_k_ranges_across_units():
+    """Three units of unequal length over ~26 clusters: ranges that end in one
+    unit and start in the next, and ranges past a short sequence's end."""
+    w = wl(batch=3, num_kv_heads=1, num_q_heads=4, splitk=2, seq_len_lo=3000, seq_len_hi=9000, seed=121)
+    run_and_check(w, seq_lens=[9000, 3000, 6001], what="stream-K across units")
+
+
+def test_stream_k_repeat_bitwise():
+    """The counts reset themselves and the chunk merge order is fixed: repeated
+    runs give the same bits; one cluster per unit agrees within tolerance."""
+    inp = generate(wl(batch=2, splitk=4, seq_len=20000, seed=119))
+    with DeviceCall(inp) as call, DeviceCall(inp, path="one_chunk") as one:
+        call.run()
+        assert call.status() == 0
+        out0, lse0 = call.out.clone(), call.lse.clone()
+        for _ in range(3):
+            call.out.fill_(float("nan"))
+            call.run()
+            assert call.status() == 0
+            assert torch.equal(call.out, out0) and torch.equal(call.lse, lse0)
+        check_against_oracle(call, what="stream-K repeat")
+        one.run()
+        assert one.status() == 0
+        assert torch.allclose(one.out.float(), out0.float(), atol=1e-2, rtol=1e-2)
+        assert torch.allclose(one.lse, lse0, atol=1e-4)
+
+
+def test_stream_k_after_timeout():
+    """A stream-K launch that gives up leaves no count behind once checked."""
+    inp = generate(wl(batch=1, splitk=2, seq_len=12000, seed=120))
+    with DeviceCall(inp) as call:
+        spd.fa_decode_set_debug(call.h, spd.FA_DEBUG_SKIP_LOADS, 20_000_000)  # 20 ms
+        call.run()
+        assert spd.fa_decode_check(call.h) & spd.FA_STATUS_TIMEOUT
+        spd.fa_decode_set_debug(call.h, 0, 0)
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what="stream-K after timeout")
 
 
 # --- the five workloads at full size -----------------------------------------------------
