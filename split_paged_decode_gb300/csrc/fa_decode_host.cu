@@ -562,31 +562,16 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     int64_t sk_total = 0;
     if (tc_big) {
         const int64_t most = (h->debug_flags & FA_DEBUG_TWO_CLUSTERS) ? 2 : h->tc_big_clusters;
-        if (units < most && h->chunk_count && !(h->debug_flags & FA_DEBUG_ONE_CHUNK) && units > 0) {
-            // Fewer units than resident clusters: give every resident cluster
-            // an equal share of all units' tiles (a full page-table row each),
-            // while every rank keeps kChunkMinTilesPerRank tiles and no unit is
-            // shared by more than kMaxSplit clusters.
+        if (h->chunk_count && !(h->debug_flags & FA_DEBUG_ONE_CHUNK)) {
+            // Fewer units than resident clusters: every resident cluster takes an
+            // equal share of all units' tiles (a full page-table row each).
             const int64_t nv = ((int64_t)max_pages_per_seq * h->page_size + 127) / 128;
-            const int64_t total = units * nv;
-            int64_t G = total / ((int64_t)fad::kChunkMinTilesPerRank * h->splitk);
-            if (G > most) G = most;
-            if (nv <= INT32_MAX) {
-                for (; G > units; --G) {
-                    int widest = 0;
-                    for (int64_t u = 0; u < units; ++u) {
-                        const int n = fad::sk_cluster_of(total, (int)G, (u + 1) * nv - 1) -
-                                      fad::sk_cluster_of(total, (int)G, u * nv) + 1;
-                        if (n > widest) widest = n;
-                    }
-                    if (widest <= fad::kMaxSplit) break;
-                }
-                if (G > units && 2 * G <= h->chunk_items) {
-                    sk_tiles = (int)nv;
-                    sk_clusters = (int)G;
-                    sk_total = total;
-                    clusters = G;
-                }
+            const int G = fad::sk_choose_clusters(units, nv, h->splitk, most, h->chunk_items);
+            if (G > 0) {
+                sk_tiles = (int)nv;
+                sk_clusters = G;
+                sk_total = units * nv;
+                clusters = G;
             }
         }
         if (clusters > most) {
