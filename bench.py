@@ -54,11 +54,11 @@ def hbm_peak():
 
 
 def kernel_source_hash() -> str:
-    """Hash of the device-code sources (the host planner is excluded)."""
+    """Hash of the device-code sources (the host planner's files are excluded)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "split_paged_decode_gb300", "csrc")
     for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")) and f != "fa_decode_host.cu":
+        if f.endswith((".cu", ".cuh", ".h")) and f not in ("fa_decode_host.cu", "stream_k_plan.h"):
             h.update(f.encode())
             h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]

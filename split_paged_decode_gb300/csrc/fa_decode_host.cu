@@ -13,6 +13,7 @@
 #include <string>
 
 #include "fa_decode_internal.h"
+#include "stream_k_plan.h"
 
 namespace {
 

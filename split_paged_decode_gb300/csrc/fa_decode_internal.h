@@ -12,9 +12,6 @@ namespace fad {
 
 constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // one second
 constexpr int kMaxSplit = 16;
-// The stream-K partition is used only while every cluster rank keeps at
-// least this many 128-key tiles of its range.
-constexpr int kChunkMinTilesPerRank = 4;
 
 // Per-sequence split rule for splitk == 0: short sequences keep one CTA per
 // (sequence, kv head), longer ones spread over 2 or 4.
@@ -33,29 +30,6 @@ __host__ __device__ inline int64_t sk_begin(int64_t total, int clusters, int64_t
 __host__ __device__ inline int sk_cluster_of(int64_t total, int clusters, int64_t x)
 {
     return (int)(((x + 1) * clusters + total - 1) / total - 1);
-}
-
-// Clusters of the stream-K partition for `units` units of `nv` tiles each
-// (cluster size P, at most `most` clusters resident, `slots` scratch slots of
-// two per cluster), or 0 when it does not apply: the resident clusters, fewer
-// while a rank would keep fewer than kChunkMinTilesPerRank tiles or a unit
-// would be shared by more than kMaxSplit clusters; only with more clusters
-// than units.
-inline int sk_choose_clusters(int64_t units, int64_t nv, int P, int64_t most, int64_t slots)
-{
-    if (units < 1 || nv < 1 || nv > INT32_MAX || units >= most) return 0;
-    const int64_t total = units * nv;
-    int64_t G = total / ((int64_t)kChunkMinTilesPerRank * P);
-    if (G > most) G = most;
-    for (; G > units; --G) {
-        int widest = 0;
-        for (int64_t u = 0; u < units; ++u) {
-            const int n = sk_cluster_of(total, (int)G, (u + 1) * nv - 1) - sk_cluster_of(total, (int)G, u * nv) + 1;
-            if (n > widest) widest = n;
-        }
-        if (widest <= kMaxSplit) break;
-    }
-    return (G > units && 2 * G <= slots) ? (int)G : 0;
 }
 
 // Everything a decode kernel needs, passed by value as a __grid_constant__
@@ -128,6 +102,9 @@ bool tc_geometry(int qk_depth, int ov_depth, int rows, int nslot, bool stream_k,
 // ov 512, V = the latent rows' first 512 columns) for num_q == 1 and a
 // multiple of 64 heads per kv head: 64 heads per CTA.
 bool mla_tc_geometry(int qk_depth, int ov_depth, int nope_depth, int heads_per_kv, int num_q, KernelGeometry* g);
+// The stream-K partition is used only while every cluster rank keeps at
+// least this many 128-key tiles of its range.
+constexpr int kChunkMinTilesPerRank = 4;
 constexpr int kTcSlotsShared = 3;  // two CTAs per SM (grids of more than one wave)
 constexpr int kTcSlotsAlone = 6;   // one CTA per SM, 192 KB of loads in flight
 

@@ -1,13 +1,14 @@
 // Host check of the stream-K partition that the tensor-core decode kernel
 // takes when a fixed split has fewer (sequence, kv head) units than resident
-// clusters (sk_begin, sk_cluster_of and sk_choose_clusters of
-// fa_decode_internal.h, the functions the kernel and the planner call).
+// clusters (sk_begin and sk_cluster_of of fa_decode_internal.h, which the
+// kernel and the planner call, and the planner's sk_choose_clusters of
+// stream_k_plan.h).
 // Built and run by tests/test_stream_k_partition.py; prints "ok <cases>" or
 // the first violated property, and exits non-zero on a violation.
 #include <cstdio>
 #include <cstdlib>
 
-#include "fa_decode_internal.h"
+#include "stream_k_plan.h"
 
 using namespace fad;
 

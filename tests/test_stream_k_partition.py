@@ -1,6 +1,7 @@
-"""The stream-K partition's arithmetic (fa_decode_internal.h), checked on the
-host: a small C++ program built against the same header the kernels and the
-planner include (see tests/stream_k_partition.cpp for the properties)."""
+"""The stream-K partition's arithmetic (fa_decode_internal.h, stream_k_plan.h),
+checked on the host: a small C++ program built against the same headers the
+kernels and the planner include (see tests/stream_k_partition.cpp for the
+properties)."""
 import os
 import shutil
 import subprocess
