@@ -138,7 +138,7 @@ int fa_decode_check(fa_decode_t h, void* stream, uint32_t* status_out);
  * two on one input); FA_DEBUG_TWO_CLUSTERS launches the tensor-core kernel of
  * a fixed split with at most two clusters, each working through its share of
  * the (sequence, kv head) units in turn, so that small inputs exercise the
- * multi-unit schedule that large batches get; FA_DEBUG_ONE_CHUNK turns the
+ * multi-unit schedule that large batches get; FA_DEBUG_NO_STREAM_K turns the
  * stream-K partition off (every (sequence, kv head) key range on one
  * cluster); wait_limit_ns bounds every
  * device wait (0 restores the default of one second). Normal runs never need
@@ -147,7 +147,7 @@ int fa_decode_check(fa_decode_t h, void* stream, uint32_t* status_out);
 #define FA_DEBUG_SKIP_LOADS 1u
 #define FA_DEBUG_FORCE_SIMT 2u   /* run the warp-level FMA kernel even where the tcgen05 one applies */
 #define FA_DEBUG_TWO_CLUSTERS 4u /* at most two clusters on the tensor-core path with a fixed split */
-#define FA_DEBUG_ONE_CHUNK 8u     /* no stream-K partition: one cluster per (sequence, kv head) */
+#define FA_DEBUG_NO_STREAM_K 8u     /* no stream-K partition: one cluster per (sequence, kv head) */
 int fa_decode_set_debug(fa_decode_t h, uint32_t flags, int64_t wait_limit_ns);
 
 /*

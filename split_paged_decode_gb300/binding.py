@@ -23,7 +23,7 @@ FA_STATUS_BAD_PAGE = 2
 FA_DEBUG_SKIP_LOADS = 1
 FA_DEBUG_FORCE_SIMT = 2
 FA_DEBUG_TWO_CLUSTERS = 4
-FA_DEBUG_ONE_CHUNK = 8
+FA_DEBUG_NO_STREAM_K = 8
 FA_TRACE_WORDS_PER_CTA = 64
 FA_NOALLOC_STATUS_SLOTS = 64
 

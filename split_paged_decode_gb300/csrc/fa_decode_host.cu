@@ -563,7 +563,7 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     int64_t sk_total = 0;
     if (tc_big) {
         const int64_t most = (h->debug_flags & FA_DEBUG_TWO_CLUSTERS) ? 2 : h->tc_big_clusters;
-        if (h->chunk_count && !(h->debug_flags & FA_DEBUG_ONE_CHUNK)) {
+        if (h->chunk_count && !(h->debug_flags & FA_DEBUG_NO_STREAM_K)) {
             // Fewer units than resident clusters: every resident cluster takes an
             // equal share of all units' tiles (a full page-table row each).
             const int64_t nv = ((int64_t)max_pages_per_seq * h->page_size + 127) / 128;

@@ -51,8 +51,8 @@ class DeviceCall:
             spd.fa_decode_set_debug(self.h, spd.FA_DEBUG_FORCE_SIMT, 0)
         elif path == "two_clusters":  # each cluster works through many units in turn
             spd.fa_decode_set_debug(self.h, spd.FA_DEBUG_TWO_CLUSTERS, 0)
-        elif path == "one_chunk":  # every unit's key range on one cluster
-            spd.fa_decode_set_debug(self.h, spd.FA_DEBUG_ONE_CHUNK, 0)
+        elif path == "no_stream_k":  # every unit's key range on one cluster
+            spd.fa_decode_set_debug(self.h, spd.FA_DEBUG_NO_STREAM_K, 0)
 
     def describe(self) -> str:
         return spd.fa_decode_describe(self.h)

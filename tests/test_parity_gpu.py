@@ -204,7 +204,7 @@ def test_multi_unit_rows(g, T):
 def test_multi_unit_matches_one_unit_per_cluster_bitwise():
     """A unit's arithmetic does not depend on which cluster takes it."""
     inp = generate(wl(batch=6, splitk=4, seed=97))
-    with DeviceCall(inp, path="one_chunk") as one, DeviceCall(inp, path="two_clusters") as many:
+    with DeviceCall(inp, path="no_stream_k") as one, DeviceCall(inp, path="two_clusters") as many:
         one.run()
         many.run()
         assert one.status() == 0 and many.status() == 0
@@ -267,7 +267,7 @@ def test_stream_k_repeat_bitwise():
     """The counts reset themselves and the chunk merge order is fixed: repeated
     runs give the same bits; one cluster per unit agrees within tolerance."""
     inp = generate(wl(batch=2, splitk=4, seq_len=20000, seed=119))
-    with DeviceCall(inp) as call, DeviceCall(inp, path="one_chunk") as one:
+    with DeviceCall(inp) as call, DeviceCall(inp, path="no_stream_k") as one:
         call.run()
         assert call.status() == 0
         out0, lse0 = call.out.clone(), call.lse.clone()
