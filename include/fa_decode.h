@@ -147,7 +147,7 @@ int fa_decode_check(fa_decode_t h, void* stream, uint32_t* status_out);
 #define FA_DEBUG_SKIP_LOADS 1u
 #define FA_DEBUG_FORCE_SIMT 2u   /* run the warp-level FMA kernel even where the tcgen05 one applies */
 #define FA_DEBUG_TWO_CLUSTERS 4u /* at most two clusters on the tensor-core path with a fixed split */
-#define FA_DEBUG_NO_STREAM_K 8u     /* no stream-K partition: one cluster per (sequence, kv head) */
+#define FA_DEBUG_NO_STREAM_K 8u  /* no stream-K partition: one cluster per (sequence, kv head) */
 int fa_decode_set_debug(fa_decode_t h, uint32_t flags, int64_t wait_limit_ns);
 
 /*

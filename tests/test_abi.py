@@ -41,6 +41,26 @@ def test_binding_names_match_header():
     assert set(declared_functions()) == set(spd.EXPORTED)
 
 
+def declared_constants():
+    consts = {}
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            for name, val in re.findall(r"^#define\s+(FA_\w+)\s+\(?(-?\d+)u?\)?", open(os.path.join(inc, f)).read(),
+                                        flags=re.M):
+                consts[name] = int(val)
+    return consts
+
+
+def test_binding_constants_match_header():
+    """Every status, error, debug and size constant the header defines has the
+    same value in the binding (the tests and callers use the binding's)."""
+    consts = declared_constants()
+    assert {"FA_OK", "FA_STATUS_TIMEOUT", "FA_DEBUG_NO_STREAM_K", "FA_TRACE_WORDS_PER_CTA"} <= set(consts)
+    for name, val in consts.items():
+        assert getattr(spd, name, None) == val, f"{name}: header {val}, binding {getattr(spd, name, None)}"
+
+
 def _create(lib, *args):
     h = ctypes.c_void_p()
     rc = lib.fa_decode_create(ctypes.byref(h), *args)
