@@ -117,7 +117,11 @@ def fa_decode_create(num_q_heads: int, num_kv_heads: int, qk_depth: int, nope_de
 def fa_decode_run(h: int, q, k_pages, v_pages, page_table, seq_lens, scale: float, out, lse, stream=None,
                   batch: int | None = None, max_pages_per_seq: int | None = None,
                   num_pages: int | None = None) -> None:
-    """Enqueue one decode forward. Sizes default to the torch tensors' shapes."""
+    """Enqueue one decode forward. Sizes default to the torch tensors' shapes.
+
+    Runs of one handle must not overlap on the GPU (one stream at a time, or
+    ordered by events): the handle's stream-K scratch is shared by its runs.
+    """
     if batch is None:
         batch = int(q.shape[0])
     if max_pages_per_seq is None:
