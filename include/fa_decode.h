@@ -210,6 +210,14 @@ int fa_decode_describe(fa_decode_t h, char* buf, int size);
  * The first call on each device looks up the array's device address there
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * The call itself makes no device allocation and frees nothing.
+ *
+ * Schedule: this call has no handle, hence no stream-K scratch and no side
+ * streams. A fixed split therefore never takes the stream-K partition (each
+ * (sequence, kv head) key range stays on one cluster: on a single long
+ * sequence, e.g. 131072 keys over 8 kv heads with split 8, that is 64 CTAs
+ * instead of about 120, roughly 25-30 % slower than fa_decode_run), and the
+ * per-sequence split (splitk 0) runs its three launches one after another on
+ * `stream`. Results agree with fa_decode_run within the rounding tolerance.
  */
 #define FA_NOALLOC_STATUS_SLOTS 64
 int fa_decode_run_noalloc(int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth, int ov_depth,

@@ -34,9 +34,13 @@ EXPORTED = ("fa_decode_create", "fa_decode_run", "fa_decode_check", "fa_decode_s
 
 
 class FaDecodeError(RuntimeError):
-    def __init__(self, code: int, message: str):
+    """A failed call: `code` is the FA_ERR_* return value; `status` holds the
+    device's FA_STATUS_* bits when the call reported them (else None)."""
+
+    def __init__(self, code: int, message: str, status: int | None = None):
         super().__init__(f"{message} (code {code})")
         self.code = code
+        self.status = status
 
 
 _lib = None
@@ -170,7 +174,8 @@ def fa_decode_run_noalloc(num_q_heads: int, num_kv_heads: int, qk_depth: int, no
 
     For callers that cannot allocate device memory. With wait=True the call
     synchronises the stream and returns the status bits (raising FaDecodeError
-    if any is set); with wait=False it only enqueues and returns None.
+    with code FA_ERR_DEVICE and those bits in `.status` if any is set); with
+    wait=False it only enqueues and returns None.
     """
     if batch is None:
         batch = int(q.shape[0])
@@ -179,10 +184,13 @@ def fa_decode_run_noalloc(num_q_heads: int, num_kv_heads: int, qk_depth: int, no
     if num_pages is None:
         num_pages = int(k_pages.shape[0])
     st = ctypes.c_uint32(0)
-    _check(load_library().fa_decode_run_noalloc(
+    rc = load_library().fa_decode_run_noalloc(
         num_q_heads, num_kv_heads, qk_depth, nope_depth, ov_depth, page_size, num_q, splitk, _addr(q),
         _addr(k_pages), _addr(v_pages), _addr(page_table), _addr(seq_lens), float(scale), _addr(out), _addr(lse),
-        _stream(stream), batch, max_pages_per_seq, num_pages, status_slot, ctypes.byref(st) if wait else None))
+        _stream(stream), batch, max_pages_per_seq, num_pages, status_slot, ctypes.byref(st) if wait else None)
+    if rc == FA_ERR_DEVICE:
+        raise FaDecodeError(rc, fa_decode_last_error(), status=int(st.value))
+    _check(rc)
     return int(st.value) if wait else None
 
 

@@ -11,6 +11,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "fa_decode_internal.h"
 #include "stream_k_plan.h"
@@ -171,49 +172,41 @@ int split_list(const fa_decode* h, int* list)
     return 3;
 }
 
-int prepare_kernel(const fa_decode* h, const fad::KernelGeometry& g)
+// Results of the per-kernel attribute calls and occupancy queries. They depend
+// only on (device, kernel, cluster size), so each is made once per process and
+// kept here: planning a call (fa_decode_run_noalloc plans every call) then
+// costs no driver round trip. cluster_size 0 marks "attributes set".
+struct PrepEntry {
+    int dev;
+    const void* func;
+    int cluster_size;
+    int clusters;
+};
+std::mutex g_prep_mutex;
+std::vector<PrepEntry> g_prep;
+
+bool prep_lookup(int dev, const void* func, int P, int* clusters)
 {
-    cudaError_t e = cudaFuncSetAttribute(g.func, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
-    int splits[3];
-    int n = split_list(h, splits);
-    for (int i = 0; i < n; ++i) {
-        const int P = splits[i];
-        if (P <= 1) continue;
-        if (P > 8) {
-            e = cudaFuncSetAttribute(g.func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster size)");
+    for (const PrepEntry& e : g_prep)
+        if (e.dev == dev && e.func == func && e.cluster_size == P) {
+            if (clusters) *clusters = e.clusters;
+            return true;
         }
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        cfg.gridDim = dim3(P, 1, 1);
-        cfg.blockDim = dim3(g.threads, 1, 1);
-        cfg.dynamicSmemBytes = g.smem_bytes;
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = P;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, g.func, &cfg);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
-        if (clusters < 1)
-            return fail(FA_ERR_UNSUPPORTED, "a cluster of %d CTAs with %d bytes of shared memory each cannot be "
-                                            "scheduled on this device", P, g.smem_bytes);
-    }
-    return FA_OK;
+    return false;
 }
 
-// Clusters of P CTAs of kernel g that the device holds at once.
-int resident_clusters(const fa_decode* h, const fad::KernelGeometry& g, int P, int* out)
+// Clusters of P CTAs of kernel g (P == 1: single CTAs) that the device holds
+// at once. Caller holds g_prep_mutex.
+int query_clusters(int dev, int sm_count, const fad::KernelGeometry& g, int P, int* out)
 {
+    if (prep_lookup(dev, g.func, P, out)) return FA_OK;
     cudaError_t e;
+    int n = 0;
     if (P <= 1) {
         int per_sm = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, g.func, g.threads, g.smem_bytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-        *out = per_sm * h->sm_count;
+        n = per_sm * sm_count;
     } else {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -226,11 +219,44 @@ int resident_clusters(const fa_decode* h, const fad::KernelGeometry& g, int P, i
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaOccupancyMaxActiveClusters(out, g.func, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, g.func, &cfg);
         if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
     }
-    if (*out < 1) return fail(FA_ERR_UNSUPPORTED, "kernel %s fits no cluster of %d CTAs", g.name, P);
+    if (n < 1)
+        return fail(FA_ERR_UNSUPPORTED, "kernel %s: a cluster of %d CTAs with %d bytes of shared memory each "
+                                        "cannot be scheduled on this device", g.name, P, g.smem_bytes);
+    g_prep.push_back(PrepEntry{dev, g.func, P, n});
+    *out = n;
     return FA_OK;
+}
+
+int prepare_kernel(const fa_decode* h, const fad::KernelGeometry& g)
+{
+    std::lock_guard<std::mutex> lock(g_prep_mutex);
+    if (!prep_lookup(h->device, g.func, 0, nullptr)) {
+        cudaError_t e = cudaFuncSetAttribute(g.func, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+        // Clusters of 16 are beyond the portable size of 8.
+        e = cudaFuncSetAttribute(g.func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster size)");
+        g_prep.push_back(PrepEntry{h->device, g.func, 0, 0});
+    }
+    int splits[3];
+    int n = split_list(h, splits);
+    for (int i = 0; i < n; ++i) {
+        if (splits[i] <= 1) continue;
+        int clusters = 0;
+        int rc = query_clusters(h->device, h->sm_count, g, splits[i], &clusters);
+        if (rc) return rc;
+    }
+    return FA_OK;
+}
+
+// Clusters of P CTAs of kernel g that the device holds at once.
+int resident_clusters(const fa_decode* h, const fad::KernelGeometry& g, int P, int* out)
+{
+    std::lock_guard<std::mutex> lock(g_prep_mutex);
+    return query_clusters(h->device, h->sm_count, g, P, out);
 }
 
 }  // namespace
@@ -266,7 +292,7 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
     if (!(splitk == 0 || splitk == 1 || splitk == 2 || splitk == 4 || splitk == 8 || splitk == 16))
         return fail(FA_ERR_INVALID_ARG, "splitk must be 0 (per sequence), 1, 2, 4, 8 or 16 (got %d)", splitk);
 
-    std::memset(&tmp, 0, sizeof tmp);
+    tmp = fa_decode{};
     tmp.hq = num_q_heads;
     tmp.hkv = num_kv_heads;
     tmp.group = num_q_heads / num_kv_heads;
@@ -334,6 +360,7 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
         return fail(FA_ERR_UNSUPPORTED, "device %d has compute capability %d.%d; this library is built for "
                                         "sm_103a (GB300)", dev, major, minor);
     tmp.device = dev;
+    cudaDeviceGetAttribute(&tmp.sm_count, cudaDevAttrMultiProcessorCount, dev);
     int rc = FA_OK;
     if (tmp.has_simt && (rc = prepare_kernel(&tmp, tmp.geo))) return rc;
     if (tmp.has_latent && (rc = prepare_kernel(&tmp, tmp.geo_latent))) return rc;
@@ -341,7 +368,6 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
     if (tmp.has_tc && (rc = prepare_kernel(&tmp, tmp.geo_tc_big))) return rc;
     if (tmp.has_tc && splitk > 0 && (rc = prepare_kernel(&tmp, tmp.geo_tc_sk))) return rc;
     if (tmp.has_mla && (rc = prepare_kernel(&tmp, tmp.geo_mla))) return rc;
-    cudaDeviceGetAttribute(&tmp.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (tmp.has_tc && splitk > 0 && (rc = resident_clusters(&tmp, tmp.geo_tc_big, splitk, &tmp.tc_big_clusters)))
         return rc;
     return FA_OK;
@@ -706,8 +732,11 @@ int fa_decode_run_noalloc(int num_q_heads, int num_kv_heads, int qk_depth, int n
     if (status_slot < 0 || status_slot >= FA_NOALLOC_STATUS_SLOTS)
         return fail(FA_ERR_INVALID_ARG, "status_slot %d is outside the %d status words of the static array",
                     status_slot, FA_NOALLOC_STATUS_SLOTS);
-    // The plan lives on this stack frame; its tensor maps are encoded on the host.
-    fa_decode plan;
+    // The plan lives on this stack frame; its tensor maps are encoded on the
+    // host. Without the handle's scratch and side streams the plan takes no
+    // stream-K partition and runs the per-sequence split's launches one after
+    // another on `stream`.
+    fa_decode plan{};
     int rc = plan_decode(plan, num_q_heads, num_kv_heads, qk_depth, nope_depth, ov_depth, page_size, num_q, splitk);
     if (rc) return rc;
     unsigned int* base = nullptr;

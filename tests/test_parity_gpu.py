@@ -1,8 +1,9 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 oracle.
 
 Bound: |out - ref| <= 1e-2 + 1e-2 |ref| element-wise on the bf16 output and
-|lse - ref| <= 1e-3 on the fp32 log-sum-exp; page gathering, the single-key
-case and page permutations are checked bit for bit.
+|lse - ref| <= 1e-3 on the fp32 log-sum-exp; the single-key case and page
+permutations are checked bit for bit here, page gathering on every path in
+test_gather_bit_exact.py.
 """
 import numpy as np
 import pytest
@@ -216,7 +217,7 @@ def test_many_units_default_grid():
     """More units than resident clusters without any debug flag (the batched shape)."""
     w = wl(batch=40, num_kv_heads=8, num_q_heads=32, splitk=4, page_size=128, seq_len_lo=1, seq_len_hi=3000,
            seed=98)
-    run_and_check(w, rows=_sample_rows(w, 400, 9), what="many units")
+    run_and_check(w, what="many units")
 
 
 # --- stream-K partition: fewer units than resident clusters ----------------------------
@@ -298,27 +299,16 @@ def test_stream_k_after_timeout():
 
 # --- the five workloads at full size -----------------------------------------------------
 
-def _sample_rows(w, n, seed):
-    rng = np.random.default_rng(seed)
-    return np.stack([rng.integers(0, w.batch, n), rng.integers(0, w.num_q, n),
-                     rng.integers(0, w.num_q_heads, n)], 1)
-
-
 @pytest.mark.parametrize("name", ["tiny", "batched_gqa", "long_context", "ragged_speculative", "mla"])
 def test_workload_full_size(name):
-    """Each workload at full size in the launch configuration the benchmark times."""
-    w = WORKLOADS[name]
-    rows = None
-    if name in ("ragged_speculative", "mla"):
-        rows = _sample_rows(w, 512, 7)
-    run_and_check(w, rows=rows, what=name)
+    """Each workload at full size in the launch configuration the benchmark
+    times, every output row compared with the oracle."""
+    run_and_check(WORKLOADS[name], what=name)
 
 
 @pytest.mark.parametrize("name", ["batched_gqa", "long_context", "ragged_speculative"])
 def test_workload_full_size_simt(name):
-    w = WORKLOADS[name]
-    rows = None if name != "ragged_speculative" else _sample_rows(w, 512, 8)
-    run_and_check(w, rows=rows, what=f"{name} simt", path="simt")
+    run_and_check(WORKLOADS[name], what=f"{name} simt", path="simt")
 
 
 # --- bit-exact properties ----------------------------------------------------------------
