@@ -74,6 +74,11 @@ def _load():
             lib.oracle_partitioned.argtypes = [ctypes.POINTER(_Shape), ctypes.c_double, p, p, p,
                                                p, p, p, ctypes.c_int, p, p, p, p, ctypes.c_int]
             lib.oracle_partitioned.restype = ctypes.c_int
+            lib.oracle_decode_fp8.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int, ctypes.c_double, p, p, p, p,
+                                              p, p, p, p, ctypes.c_int64, p, p, ctypes.c_int]
+            lib.oracle_decode_fp8.restype = ctypes.c_int
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_int]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
             lib.oracle_hardware_threads.argtypes = []
             lib.oracle_hardware_threads.restype = ctypes.c_int
             _lib = lib
@@ -180,4 +185,68 @@ def partitioned(q, k_pages, v_pages, page_table, seq_lens, scale: float, bounds,
         raise ValueError("oracle_partitioned rejected its arguments")
     if return_parts:
         return out, lse, pmax, psum
+    return out, lse
+
+
+def e4m3_value(code: int) -> float:
+    """The value the fp8 oracle reads for one OCP FP8 E4M3 code (0..255)."""
+    return float(_load().oracle_e4m3_value(int(code)))
+
+
+def decode_fp8(q, k8, v8, page_table, seq_lens, scale: float, *, k_rope=None, k_scale=None,
+               ov_depth: int | None = None, rows=None, threads: int = 1):
+    """Plain-definition attention in fp64 over an fp8 (E4M3) cache.
+
+    q [B,T,Hq,Dk] (uint16 bf16 bits), k8 [NP,Hkv,PS,Dk-R] (uint8 E4M3 codes),
+    v8 [NP,Hkv,PS,Dv] (uint8) or None for the latent layout (V = the first
+    ``ov_depth`` dequantized values of the fp8 part of the key row),
+    k_rope [NP,Hkv,PS,R] (uint16 bf16 bits) or None (R = 0), k_scale
+    [NP,Hkv,PS] float32 per-token K scale or None (ones). Returns (out, lse)
+    as ``decode`` does.
+    """
+    lib = _load()
+    q = _u16(q)
+    k8 = np.ascontiguousarray(k8)
+    if k8.dtype != np.uint8:
+        raise TypeError(f"expected uint8 E4M3 codes, got {k8.dtype}")
+    page_table = _i32(page_table)
+    seq_lens = _i32(seq_lens)
+    B, T, Hq, Dk = q.shape
+    NP, Hkv, PS, D8 = k8.shape
+    R = 0
+    if k_rope is not None:
+        k_rope = _u16(k_rope)
+        R = k_rope.shape[3]
+        if k_rope.shape[:3] != k8.shape[:3]:
+            raise ValueError("k_rope and k8 disagree on pages / heads / page_size")
+    if D8 + R != Dk:
+        raise ValueError(f"q depth {Dk} != fp8 part {D8} + rope part {R}")
+    if k_scale is not None:
+        k_scale = np.ascontiguousarray(k_scale, dtype=np.float32)
+        if k_scale.shape != k8.shape[:3]:
+            raise ValueError("k_scale must be [num_pages, num_kv_heads, page_size]")
+    if v8 is None:
+        if ov_depth is None:
+            raise ValueError("ov_depth is required for the latent layout")
+        Dv, v_in_k = int(ov_depth), 1
+    else:
+        v8 = np.ascontiguousarray(v8)
+        if v8.dtype != np.uint8:
+            raise TypeError(f"expected uint8 E4M3 codes, got {v8.dtype}")
+        Dv, v_in_k = v8.shape[3], 0
+    shape = _Shape(B, T, Hq, Hkv, Dk, Dv, PS, page_table.shape[1], NP, v_in_k)
+    if rows is None:
+        out = np.zeros((B, T, Hq, Dv), np.float64)
+        lse = np.zeros((B, T, Hq), np.float64)
+        rows_arr, n = None, 0
+    else:
+        rows_arr = _i32(rows).reshape(-1, 3)
+        n = rows_arr.shape[0]
+        out = np.zeros((n, Dv), np.float64)
+        lse = np.zeros((n,), np.float64)
+    rc = lib.oracle_decode_fp8(ctypes.byref(shape), R, float(scale), _ptr(q), _ptr(k8), _ptr(v8), _ptr(k_rope),
+                               _ptr(k_scale), _ptr(page_table), _ptr(seq_lens), _ptr(rows_arr), n, _ptr(out),
+                               _ptr(lse), int(threads))
+    if rc != 0:
+        raise ValueError("oracle_decode_fp8 rejected its arguments (bad page id, length or shape)")
     return out, lse

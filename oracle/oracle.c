@@ -99,6 +99,11 @@ typedef struct row_job {
     double *out, *lse, *pmax, *psum;
     int tid, nthreads;
     int failed;
+    /* fp8 cache (oracle_decode_fp8 only) */
+    const uint8_t *k8, *v8;
+    const uint16_t* krope;
+    const float* kscale;
+    int rope_depth;
 } row_job;
 
 /* q.k for one (row, key), unscaled, exact products of widened bf16. */
@@ -366,6 +371,176 @@ int oracle_partitioned(const oracle_shape* s, double scale, const uint16_t* q,
     proto.psum = part_sum;
     return run_jobs(&proto, split_worker, num_threads);
 }
+
+/* ------------------------------------------------------------------------
+ * fp8 KV cache: the cache dtype, the separate rope dtype and the per-token K
+ * scale of the FA4Config page (struct parameters qkv_dtype, rope_dtype_ and
+ * scale_dtype_; methods num_k_scale_bufs, q_rope_bytes and rope_depth).
+ *
+ * The cache holds OCP FP8 E4M3 codes (1 sign bit, 4 exponent bits with bias
+ * 7, 3 mantissa bits; exponent field 0 is subnormal, m/8 * 2^-6; the code
+ * S.1111.111 is NaN; there is no infinity; the largest finite value is 448).
+ * Key row j of kv head k, at cache row r = (page * Hkv + k) * PS + j % PS:
+ *   K_j[0 : qk - R)  = k_scale[r] * e4m3(k8[r][0 : qk - R])   (k_scale 1 if absent)
+ *   K_j[qk - R : qk] = bf16(k_rope[r][0 : R])                  (R = rope_depth, unscaled)
+ * Value row: V_j = e4m3(v8[r][0 : ov]) (no scale: the pages scale K only),
+ * or, in the latent layout, the first ov values of the dequantized fp8 part
+ * of the key row, k_scale[r] * e4m3(k8[r][0 : ov]) -- the stored row is one
+ * latent vector, so its K and V readings dequantize alike.
+ * Everything else is the plain definition of plain_row, in fp64.
+ * ------------------------------------------------------------------------ */
+static double decode_e4m3(uint8_t x)
+{
+    int sign = x >> 7;
+    int e = (x >> 3) & 15;
+    int m = x & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Cache row of key j of sequence b, kv head k, or -1 on a bad page id. */
+static int64_t cache_row(const oracle_shape* s, const int32_t* page_table, int b, int k, int64_t j)
+{
+    int64_t slot = j / s->page_size;
+    if (slot >= s->max_pages_per_seq) return -1;
+    int32_t phys = page_table[(int64_t)b * s->max_pages_per_seq + slot];
+    if (phys < 0 || phys >= s->num_pages) return -1;
+    return ((int64_t)phys * s->num_kv_heads + k) * s->page_size + j % s->page_size;
+}
+
+static int fp8_key(const row_job* J, int64_t r, double* dst)
+{
+    const oracle_shape* s = J->s;
+    const int d8 = s->qk_depth - J->rope_depth;
+    const double ks = J->kscale ? (double)J->kscale[r] : 1.0;
+    const uint8_t* src = J->k8 + r * d8;
+    for (int d = 0; d < d8; ++d) dst[d] = ks * decode_e4m3(src[d]);
+    for (int d = 0; d < J->rope_depth; ++d) dst[d8 + d] = widen_bf16(J->krope[r * J->rope_depth + d]);
+    return 0;
+}
+
+static int fp8_value(const row_job* J, int64_t r, double* dst)
+{
+    const oracle_shape* s = J->s;
+    if (s->v_in_k) {
+        const int d8 = s->qk_depth - J->rope_depth;
+        const double ks = J->kscale ? (double)J->kscale[r] : 1.0;
+        for (int d = 0; d < s->ov_depth; ++d) dst[d] = ks * decode_e4m3(J->k8[r * d8 + d]);
+    } else {
+        for (int d = 0; d < s->ov_depth; ++d) dst[d] = decode_e4m3(J->v8[r * s->ov_depth + d]);
+    }
+    return 0;
+}
+
+/* plain_row over the fp8 cache; kbuf holds qk_depth doubles, vbuf ov_depth. */
+static int plain_row_fp8(row_job* J, int b, int t, int h, double* o, double* lse_out, double* sbuf,
+                         double* kbuf, double* vbuf)
+{
+    const oracle_shape* s = J->s;
+    int group = s->num_q_heads / s->num_kv_heads;
+    int k = h / group;
+    int64_t L = J->lens[b];
+    int64_t n_vis = L - s->num_q + t + 1;
+    for (int d = 0; d < s->ov_depth; ++d) o[d] = 0.0;
+    if (n_vis <= 0) {
+        if (lse_out) *lse_out = -INFINITY;
+        return 0;
+    }
+    const uint16_t* qrow = J->q + (((int64_t)b * s->num_q + t) * s->num_q_heads + h) * s->qk_depth;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n_vis; ++j) {
+        int64_t r = cache_row(s, J->pt, b, k, j);
+        if (r < 0) return -1;
+        fp8_key(J, r, kbuf);
+        double acc = 0.0;
+        for (int d = 0; d < s->qk_depth; ++d) acc += widen_bf16(qrow[d]) * kbuf[d];
+        sbuf[j] = J->scale * acc;
+        if (sbuf[j] > m) m = sbuf[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n_vis; ++j) {
+        double e = exp(sbuf[j] - m);
+        l += e;
+        int64_t r = cache_row(s, J->pt, b, k, j);
+        fp8_value(J, r, vbuf);
+        for (int d = 0; d < s->ov_depth; ++d) o[d] += e * vbuf[d];
+    }
+    for (int d = 0; d < s->ov_depth; ++d) o[d] /= l;
+    if (lse_out) *lse_out = m + log(l);
+    return 0;
+}
+
+static void* fp8_worker(void* arg)
+{
+    row_job* J = (row_job*)arg;
+    const oracle_shape* s = J->s;
+    int64_t max_len = 0;
+    for (int b = 0; b < s->batch; ++b)
+        if (J->lens[b] > max_len) max_len = J->lens[b];
+    double* sbuf = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+    double* kbuf = (double*)malloc(sizeof(double) * (size_t)s->qk_depth);
+    double* vbuf = (double*)malloc(sizeof(double) * (size_t)s->ov_depth);
+    if (!sbuf || !kbuf || !vbuf) { J->failed = 1; free(sbuf); free(kbuf); free(vbuf); return NULL; }
+    int64_t total = J->rows ? J->n_rows : (int64_t)s->batch * s->num_q * s->num_q_heads;
+    for (int64_t i = J->tid; i < total; i += J->nthreads) {
+        int b, t, h;
+        if (J->rows) {
+            b = J->rows[3 * i];
+            t = J->rows[3 * i + 1];
+            h = J->rows[3 * i + 2];
+            if (b < 0 || b >= s->batch || t < 0 || t >= s->num_q || h < 0 || h >= s->num_q_heads) {
+                J->failed = 1;
+                break;
+            }
+        } else {
+            h = (int)(i % s->num_q_heads);
+            t = (int)((i / s->num_q_heads) % s->num_q);
+            b = (int)(i / ((int64_t)s->num_q_heads * s->num_q));
+        }
+        if (plain_row_fp8(J, b, t, h, J->out + i * s->ov_depth, J->lse ? J->lse + i : NULL, sbuf, kbuf, vbuf)) {
+            J->failed = 1;
+            break;
+        }
+    }
+    free(sbuf);
+    free(kbuf);
+    free(vbuf);
+    return NULL;
+}
+
+int oracle_decode_fp8(const oracle_shape* s, int rope_depth, double scale, const uint16_t* q,
+                      const uint8_t* k8, const uint8_t* v8, const uint16_t* k_rope, const float* k_scale,
+                      const int32_t* page_table, const int32_t* seq_lens,
+                      const int32_t* rows, int64_t n_rows,
+                      double* out, double* lse, int num_threads)
+{
+    if (!shape_ok(s) || !q || !k8 || (!v8 && !s->v_in_k) || !page_table || !seq_lens || !out) return -1;
+    if (rope_depth < 0 || rope_depth >= s->qk_depth || (rope_depth > 0 && !k_rope)) return -1;
+    if (s->v_in_k && s->ov_depth > s->qk_depth - rope_depth) return -1;
+    if (rows && n_rows < 0) return -1;
+    if (!lens_ok(s, seq_lens)) return -1;
+    row_job proto;
+    memset(&proto, 0, sizeof proto);
+    proto.s = s;
+    proto.scale = scale;
+    proto.q = q;
+    proto.k8 = k8;
+    proto.v8 = v8;
+    proto.krope = k_rope;
+    proto.kscale = k_scale;
+    proto.rope_depth = rope_depth;
+    proto.pt = page_table;
+    proto.lens = seq_lens;
+    proto.rows = rows;
+    proto.n_rows = n_rows;
+    proto.out = out;
+    proto.lse = lse;
+    return run_jobs(&proto, fp8_worker, num_threads);
+}
+
+/* One E4M3 code widened (for the pins). */
+double oracle_e4m3_value(int code) { return decode_e4m3((uint8_t)code); }
 
 int oracle_hardware_threads(void)
 {

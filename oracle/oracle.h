@@ -63,6 +63,25 @@ int oracle_partitioned(const oracle_shape* s, double scale, const uint16_t* q,
                        double* out, double* lse,
                        double* part_max, double* part_sum, int num_threads);
 
+/* Plain attention over an fp8 (OCP E4M3) cache, fp64 throughout. The shape's
+ * qk_depth is the full key width: an E4M3 part of qk_depth - rope_depth
+ * columns, dequantized with the per-token K scale, then rope_depth bf16
+ * columns (unscaled). Layouts, with r = (page * Hkv + kv head) * PS + j % PS:
+ *   k8       uint8 [num_pages][Hkv][PS][qk_depth - rope_depth]
+ *   v8       uint8 [num_pages][Hkv][PS][ov_depth], NULL for the latent layout
+ *            (V = the first ov_depth dequantized values of the E4M3 part)
+ *   k_rope   bf16 bits [num_pages][Hkv][PS][rope_depth], NULL if rope_depth 0
+ *   k_scale  float [num_pages][Hkv][PS], NULL for all ones
+ * rows / out / lse as for oracle_decode. Returns 0 or -1 on a bad argument. */
+int oracle_decode_fp8(const oracle_shape* s, int rope_depth, double scale, const uint16_t* q,
+                      const uint8_t* k8, const uint8_t* v8, const uint16_t* k_rope, const float* k_scale,
+                      const int32_t* page_table, const int32_t* seq_lens,
+                      const int32_t* rows, int64_t n_rows,
+                      double* out, double* lse, int num_threads);
+
+/* The value of one E4M3 code (0..255) as the fp8 oracle reads it. */
+double oracle_e4m3_value(int code);
+
 /* Threads the host offers (sysconf), for reporting the baseline's core count. */
 int oracle_hardware_threads(void);
 

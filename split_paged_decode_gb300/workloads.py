@@ -15,6 +15,19 @@ Draw recipe (all on a CPU ``torch.Generator`` seeded with the workload seed):
 The pool holds exactly the pages the sequences need plus ``ceil(1 %)`` (at
 least one) spare pages that no page table entry names. Unused page-table
 entries are -1.
+
+fp8 caches (``kv_dtype == "e4m3"``), same generator, in this order:
+  1. lengths as above;
+  2. Q as above (bf16); K as fp32 N(0, 1) over the fp8 part of the row
+     (qk_depth - rope_depth columns); the rope part (``rope_depth`` columns)
+     as bf16 N(0, 1) in its own cache; V as fp32 N(0, 1) (separate-V layout);
+  3. the page permutation;
+  4. quantisation to OCP FP8 E4M3 codes by torch's float8_e4m3fn cast
+     (round to nearest even): with ``k_scale`` every key row gets the fp32
+     scale max|K_row| / 448 and stores K_row / scale (clamped to +-448),
+     otherwise K and V are cast as drawn;
+  5. garbage past L_b and in spare pages: codes of +-448, scale 1e4, rope
+     +-1e4.
 """
 from __future__ import annotations
 
@@ -44,6 +57,9 @@ class DecodeWorkload:
     page_order: str = "random"  # "random" or "identity"
     scale: float = 0.0          # 0.0 means 1 / sqrt(qk_depth)
     seed: int = 0
+    kv_dtype: str = "bf16"      # "bf16" or "e4m3" (OCP FP8 E4M3 codes)
+    k_scale: bool = False       # e4m3: a per-token fp32 K scale
+    rope_depth: int = 0         # e4m3: trailing key columns kept in bf16 in their own cache
 
     @property
     def group(self) -> int:
@@ -88,6 +104,10 @@ class DecodeInputs:
     page_table: torch.Tensor   # [B, max_pages_per_seq] int32, -1 where unused
     seq_lens: torch.Tensor     # [B] int32
     scale: float
+    # e4m3 caches: k_pages / v_pages hold uint8 codes [NP, Hkv, PS, D]; the
+    # rope part of the key row and the per-token K scale live apart.
+    k_rope: torch.Tensor | None = None   # [NP, Hkv, PS, rope_depth] bf16
+    k_scale: torch.Tensor | None = None  # [NP, Hkv, PS] fp32
 
     @property
     def num_pages(self) -> int:
@@ -114,6 +134,10 @@ def generate(w: DecodeWorkload, seq_lens=None) -> DecodeInputs:
 
     ``seq_lens`` overrides step 1 with explicit lengths (a list or tensor).
     """
+    if w.kv_dtype == "e4m3":
+        return _generate_e4m3(w, seq_lens)
+    if w.kv_dtype != "bf16":
+        raise ValueError(f"kv_dtype {w.kv_dtype!r}: bf16 or e4m3")
     gen = torch.Generator().manual_seed(w.seed)
     if seq_lens is None:
         lens = draw_lengths(w, gen)
@@ -159,6 +183,69 @@ def generate(w: DecodeWorkload, seq_lens=None) -> DecodeInputs:
             c[pid] = garbage(tuple(c.shape[1:]))
 
     return DecodeInputs(w, q, k_pages, v_pages, page_table, lens, float(w.softmax_scale))
+
+
+def _pool(w: DecodeWorkload, lens: torch.Tensor):
+    ps = w.page_size
+    pages_per_seq = [(int(L) + ps - 1) // ps for L in lens.tolist()]
+    used = sum(pages_per_seq)
+    return pages_per_seq, used, used + max(1, math.ceil(used / 100)), max(1, max(pages_per_seq) if pages_per_seq else 1)
+
+
+def _generate_e4m3(w: DecodeWorkload, seq_lens=None) -> DecodeInputs:
+    gen = torch.Generator().manual_seed(w.seed)
+    lens = draw_lengths(w, gen) if seq_lens is None else torch.as_tensor(seq_lens, dtype=torch.int32).reshape(w.batch)
+    ps = w.page_size
+    pages_per_seq, used, num_pages, max_pages = _pool(w, lens)
+    d8 = w.qk_depth - w.rope_depth
+    q = _randn_bf16((w.batch, w.num_q, w.num_q_heads, w.qk_depth), gen)
+    k = torch.randn((num_pages, w.num_kv_heads, ps, d8), generator=gen, dtype=torch.float32)
+    k_rope = _randn_bf16((num_pages, w.num_kv_heads, ps, w.rope_depth), gen) if w.rope_depth else None
+    v = None if w.latent else torch.randn((num_pages, w.num_kv_heads, ps, w.ov_depth), generator=gen,
+                                          dtype=torch.float32)
+    perm = torch.arange(num_pages, dtype=torch.int64) if w.page_order == "identity" else \
+        torch.randperm(num_pages, generator=gen)
+    page_table = torch.full((w.batch, max_pages), -1, dtype=torch.int32)
+    cursor = 0
+    for b, n in enumerate(pages_per_seq):
+        page_table[b, :n] = perm[cursor:cursor + n].to(torch.int32)
+        cursor += n
+
+    def e4m3(x):
+        return x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
+    k_scale = None
+    if w.k_scale:
+        k_scale = k.abs().amax(dim=3) / 448.0
+        k8 = e4m3(k / k_scale.unsqueeze(3))
+    else:
+        k8 = e4m3(k)
+    v8 = None if v is None else e4m3(v)
+
+    def garbage_codes(shape):
+        sign = torch.randint(0, 2, shape, generator=gen, dtype=torch.uint8)
+        return (sign << 7) | 0x7E  # +-448
+
+    def garbage_bf16(shape):
+        sign = torch.randint(0, 2, shape, generator=gen, dtype=torch.int8).to(torch.float32)
+        return ((sign * 2.0 - 1.0) * 1.0e4).to(torch.bfloat16)
+
+    def spoil(sel_page, rows):
+        for c in [k8] + ([v8] if v8 is not None else []):
+            c[sel_page, :, rows, :] = garbage_codes((c.shape[1], rows.stop - rows.start, c.shape[3]))
+        if k_rope is not None:
+            k_rope[sel_page, :, rows, :] = garbage_bf16((k_rope.shape[1], rows.stop - rows.start, k_rope.shape[3]))
+        if k_scale is not None:
+            k_scale[sel_page, :, rows] = 1.0e4
+
+    for b, L in enumerate(lens.tolist()):
+        n = pages_per_seq[b]
+        tail = n * ps - int(L)
+        if n and tail:
+            spoil(int(page_table[b, n - 1]), slice(ps - tail, ps))
+    for pid in perm[used:].tolist():
+        spoil(pid, slice(0, ps))
+    return DecodeInputs(w, q, k8, v8, page_table, lens, float(w.softmax_scale), k_rope=k_rope, k_scale=k_scale)
 
 
 def bf16_bits(t: torch.Tensor):

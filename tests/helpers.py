@@ -23,6 +23,13 @@ def oracle_threads() -> int:
 
 def run_oracle(inp: DecodeInputs, rows=None):
     w = inp.workload
+    if w.kv_dtype == "e4m3":
+        return oracle.decode_fp8(bf16_bits(inp.q), inp.k_pages.numpy(),
+                                 None if inp.v_pages is None else inp.v_pages.numpy(), inp.page_table.numpy(),
+                                 inp.seq_lens.numpy(), inp.scale,
+                                 k_rope=None if inp.k_rope is None else bf16_bits(inp.k_rope),
+                                 k_scale=None if inp.k_scale is None else inp.k_scale.numpy(),
+                                 ov_depth=w.ov_depth, rows=rows, threads=oracle_threads())
     v = None if inp.v_pages is None else bf16_bits(inp.v_pages)
     return oracle.decode(bf16_bits(inp.q), bf16_bits(inp.k_pages), v, inp.page_table.numpy(),
                          inp.seq_lens.numpy(), inp.scale, ov_depth=w.ov_depth, rows=rows,

@@ -3,8 +3,9 @@
 Each case copies oracle.c, plants one plausible slip (a wrong index, a dropped
 term, a wrong sign, a transposed axis), builds the copy into a temporary
 library and runs the pin suite (test_oracle.py) against it in a child
-process. The suite has to fail for every mutant; the untouched copy has to
-pass, which shows that the harness itself works.
+process (test_oracle.py and test_oracle_fp8.py). The suite has to fail for
+every mutant; the untouched copy has to pass, which shows that the harness
+itself works.
 """
 import os
 import shutil
@@ -38,6 +39,21 @@ MUTANTS = {
                               "const double c = J->scale;"),
     "combine_lse_unscaled_max": ("*lse_out = J->scale * gmax + log(gsum);",
                                  "*lse_out = gmax + log(gsum);"),
+    # the fp8 cache (oracle_decode_fp8)
+    "e4m3_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "e4m3_subnormal_exponent": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    "e4m3_sign_dropped": ("return sign ? -v : v;", "return v;"),
+    "fp8_k_scale_dropped": ("for (int d = 0; d < d8; ++d) dst[d] = ks * decode_e4m3(src[d]);",
+                            "for (int d = 0; d < d8; ++d) dst[d] = decode_e4m3(src[d]);"),
+    "fp8_rope_column_rotated": ("dst[d8 + d] = widen_bf16(J->krope[r * J->rope_depth + d]);",
+                                "dst[d8 + d] = widen_bf16(J->krope[r * J->rope_depth + (d + 1) % J->rope_depth]);"),
+    "fp8_rope_scaled": ("dst[d8 + d] = widen_bf16(J->krope[r * J->rope_depth + d]);",
+                        "dst[d8 + d] = ks * widen_bf16(J->krope[r * J->rope_depth + d]);"),
+    "fp8_separate_v_scaled": ("for (int d = 0; d < s->ov_depth; ++d) dst[d] = decode_e4m3(J->v8[r * s->ov_depth + d]);",
+                              "for (int d = 0; d < s->ov_depth; ++d) dst[d] = (J->kscale ? (double)J->kscale[r] : 1.0) * decode_e4m3(J->v8[r * s->ov_depth + d]);"),
+    "fp8_latent_v_unscaled": ("for (int d = 0; d < s->ov_depth; ++d) dst[d] = ks * decode_e4m3(J->k8[r * d8 + d]);",
+                              "for (int d = 0; d < s->ov_depth; ++d) dst[d] = decode_e4m3(J->k8[r * d8 + d]);"),
+    "fp8_row_stride": ("const uint8_t* src = J->k8 + r * d8;", "const uint8_t* src = J->k8 + r * s->qk_depth;"),
 }
 
 
@@ -57,7 +73,8 @@ def _build_and_run(name, tmpdir):
                     "-lpthread"], check=True)
     env = dict(os.environ, SPD_ORACLE_LIB=so)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle.py")],
+                        os.path.join(ROOT, "tests", "test_oracle.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_fp8.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     return r.returncode
 
