@@ -39,13 +39,30 @@ sys.path.insert(0, ROOT)
 METRIC = "decode attention KV HBM GB/s"
 FALLBACK_HBM_GBS = 6800.0
 WORKLOAD_NAMES = ["tiny", "batched_gqa", "long_context", "ragged_speculative", "mla"]
+# The head-dim-128 workloads again over an fp8 (E4M3) cache with per-token K scales.
+FP8_WORKLOADS = {"batched_gqa_e4m3": "batched_gqa", "long_context_e4m3": "long_context",
+                 "ragged_speculative_e4m3": "ragged_speculative"}
+
+
+def workload(name: str):
+    from split_paged_decode_gb300.workloads import WORKLOADS
+
+    if name in FP8_WORKLOADS:
+        return WORKLOADS[FP8_WORKLOADS[name]].with_(name=name, kv_dtype="e4m3", k_scale=True)
+    return WORKLOADS[name]
 
 
 def min_bytes(w, seq_lens) -> int:
-    """K + V + Q + O bytes, each element once; the latent row once."""
+    """K + V + Q + O bytes, each element once; the latent row once. An E4M3
+    cache counts one byte per K / V element plus its 4-byte per-token K scale
+    and the bf16 rope part."""
     total_keys = int(sum(int(x) for x in seq_lens))
     row = w.qk_depth if w.latent else w.qk_depth + w.ov_depth
-    kv = total_keys * w.num_kv_heads * row * 2
+    if w.kv_dtype == "e4m3":
+        per_key = (row - w.rope_depth) + 2 * w.rope_depth + (4 if w.k_scale else 0)
+        kv = total_keys * w.num_kv_heads * per_key
+    else:
+        kv = total_keys * w.num_kv_heads * row * 2
     q = w.batch * w.num_q * w.num_q_heads * w.qk_depth * 2
     o = w.batch * w.num_q * w.num_q_heads * w.ov_depth * 2
     return kv + q + o
@@ -93,6 +110,7 @@ def workload_config(w, nbytes: int) -> dict:
             "page_size": w.page_size, "splitk": w.splitk,
             "seq_lens": "fixed %d" % w.seq_len if w.seq_len else
             f"uniform [{w.seq_len_lo}, {w.seq_len_hi}] seed {w.seed}",
+            "kv_dtype": w.kv_dtype if w.kv_dtype == "bf16" else f"{w.kv_dtype}, per-token K scale {w.k_scale}",
             "min_bytes_per_step": nbytes, "l2": "flushed before every timed step (512 MiB write)"}
 
 
@@ -264,12 +282,26 @@ def time_oracle(inp, min_seconds: float, max_reps: int = 1000, threads: int | No
 
     if threads is None:
         threads = oracle.hardware_threads()
-    q, k = bf16_bits(inp.q), bf16_bits(inp.k_pages)
-    v = None if inp.v_pages is None else bf16_bits(inp.v_pages)
     pt, lens = inp.page_table.numpy(), inp.seq_lens.numpy()
+    q = bf16_bits(inp.q)
+    if inp.workload.kv_dtype == "e4m3":
+        k8 = inp.k_pages.numpy()
+        v8 = None if inp.v_pages is None else inp.v_pages.numpy()
+        rope = None if inp.k_rope is None else bf16_bits(inp.k_rope)
+        ks = None if inp.k_scale is None else inp.k_scale.numpy()
+
+        def run():
+            oracle.decode_fp8(q, k8, v8, pt, lens, inp.scale, k_rope=rope, k_scale=ks,
+                              ov_depth=inp.workload.ov_depth, threads=threads)
+    else:
+        k = bf16_bits(inp.k_pages)
+        v = None if inp.v_pages is None else bf16_bits(inp.v_pages)
+
+        def run():
+            oracle.decode(q, k, v, pt, lens, inp.scale, ov_depth=inp.workload.ov_depth, threads=threads)
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.decode(q, k, v, pt, lens, inp.scale, ov_depth=inp.workload.ov_depth, threads=threads)
+        run()
         reps += 1
         el = time.perf_counter() - t0
         if el >= min_seconds or reps >= max_reps:
@@ -305,11 +337,11 @@ def cpu_baseline(w, seconds: float, single_core_seconds: float) -> dict:
 
 
 def run_reference(args, world, rank):
-    from split_paged_decode_gb300.workloads import WORKLOADS, generate
+    from split_paged_decode_gb300.workloads import generate
 
     if rank != 0:
         return
-    w = WORKLOADS[args.workload]
+    w = workload(args.workload)
     sample, inp, desc = oracle_sample(w)
     nbytes = min_bytes(sample, inp.seq_lens.tolist())
     for _ in range(args.warmup):
@@ -356,13 +388,22 @@ def measure(spd, torch, w, dev, stream, steps, warmup, flush, clocks, keep=False
     pt, lens = inp.page_table.to(dev), inp.seq_lens.to(dev)
     out = torch.empty((w.batch, w.num_q, w.num_q_heads, w.ov_depth), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.batch, w.num_q, w.num_q_heads), dtype=torch.float32, device=dev)
-    h = spd.fa_decode_create(w.num_q_heads, w.num_kv_heads, w.qk_depth, w.nope_depth, w.ov_depth,
-                             w.page_size, w.num_q, w.splitk)
+    e4m3 = w.kv_dtype == "e4m3"
+    if e4m3:
+        ks = None if inp.k_scale is None else inp.k_scale.to(dev)
+        h = spd.fa_decode_create_kv(w.num_q_heads, w.num_kv_heads, w.qk_depth, w.nope_depth, w.ov_depth,
+                                    w.page_size, w.num_q, w.splitk, spd.FA_KV_E4M3, w.rope_depth)
+    else:
+        h = spd.fa_decode_create(w.num_q_heads, w.num_kv_heads, w.qk_depth, w.nope_depth, w.ov_depth,
+                                 w.page_size, w.num_q, w.splitk)
     m.kernel = spd.fa_decode_describe(h).split()[1].split("=", 1)[1]
     m.launches_per_step = 3 if w.splitk == 0 else 1
 
     def step():
-        spd.fa_decode_run(h, q, k, v, pt, lens, inp.scale, out, lse, stream=stream)
+        if e4m3:
+            spd.fa_decode_run_kv(h, q, k, v, None, ks, pt, lens, inp.scale, out, lse, stream=stream)
+        else:
+            spd.fa_decode_run(h, q, k, v, pt, lens, inp.scale, out, lse, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -429,16 +470,16 @@ def run_gpu(args, world, rank, local):
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     peak, peak_kind = hbm_peak()
-    w = WORKLOADS[args.workload]
+    w = workload(args.workload)
     clocks = ClockSampler(local).start()
     try:
         barrier(world)
         head = measure(spd, torch, w, dev, stream, args.steps, args.warmup, flush, clocks, keep=True)
         others = {}
         if not args.headline_only:
-            for name in WORKLOAD_NAMES:
+            for name in WORKLOAD_NAMES + list(FP8_WORKLOADS):
                 if name != w.name:
-                    others[name] = measure(spd, torch, WORKLOADS[name], dev, stream, args.steps, args.warmup,
+                    others[name] = measure(spd, torch, workload(name), dev, stream, args.steps, args.warmup,
                                            flush, clocks)
         barrier(world)
     finally:
@@ -500,7 +541,8 @@ def run_gpu(args, world, rank, local):
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3 KV, bf16 Q/out",
+        "data": "synthetic",
         "config": dict(workload_config(w, nbytes), parallelism=f"replicas x{world}"),
         "query_tokens_per_s": world * w.batch * w.num_q / (ms_max * 1e-3),
         "roofline_pct": 100.0 * gbs / world / peak,
@@ -520,7 +562,7 @@ def run_gpu(args, world, rank, local):
         if others:
             for name in ("tiny", "long_context"):
                 if name in line["workloads"]:
-                    cb = cpu_baseline(WORKLOADS[name], 1.0, 1.0)
+                    cb = cpu_baseline(workload(name), 1.0, 1.0)
                     line["workloads"][name]["cpu_baseline_gbs"] = cb["value"]
                     line["workloads"][name]["cpu_baseline_cores"] = cb["cores"]
                     line["workloads"][name]["cpu_single_core_gbs"] = cb["single_core"]["value"]
@@ -532,7 +574,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="batched_gqa", choices=WORKLOAD_NAMES)
+    ap.add_argument("--workload", default="batched_gqa", choices=WORKLOAD_NAMES + list(FP8_WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle timing budget of cpu_baseline")
     ap.add_argument("--cpu-single-core-seconds", type=float, default=3.0,

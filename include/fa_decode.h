@@ -125,6 +125,52 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
                   int batch, int max_pages_per_seq, int num_pages);
 
 /*
+ * The cache's element format (FA4Config page, struct parameters qkv_dtype,
+ * rope_dtype_ and scale_dtype_; methods num_k_scale_bufs, q_rope_bytes,
+ * rope_depth). FA_KV_BF16 is the cache fa_decode_create takes. FA_KV_E4M3 is
+ * an fp8 cache of OCP FP8 E4M3 codes (1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; no infinity; largest finite value 448), read as
+ *   K_j = k_scale_j * e4m3(k_pages row j)   (k_scale_j = 1 without scales)
+ *   V_j = e4m3(v_pages row j)                (V carries no scale)
+ * with Q, out and lse as for a bf16 cache. It halves the cache bytes that
+ * every decode step reads.
+ */
+#define FA_KV_BF16 0
+#define FA_KV_E4M3 1
+
+/*
+ * Create a plan for a cache of format kv_format. The first nine arguments are
+ * those of fa_decode_create (which is this call with FA_KV_BF16, 0).
+ *   kv_format   FA_KV_BF16 or FA_KV_E4M3
+ *   rope_depth  trailing key columns stored apart in bf16 (the pages' separate
+ *               rope dtype, for a latent cache); 0 for FA_KV_BF16
+ * Built for E4M3: qk_depth == ov_depth == 128 with a separate V cache,
+ * rope_depth 0, T * g <= 16 rows per CTA (the tcgen05 GQA kernel, every
+ * split). Other E4M3 shapes return FA_ERR_UNSUPPORTED. Allocates as
+ * fa_decode_create does.
+ */
+int fa_decode_create_kv(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth,
+                        int ov_depth, int page_size, int num_q, int splitk, int kv_format, int rope_depth);
+
+/*
+ * Enqueue one decode forward over the handle's cache format. Arguments as for
+ * fa_decode_run, plus:
+ *   k_pages / v_pages  for FA_KV_E4M3: uint8 E4M3 codes [num_pages][num_kv_heads]
+ *                      [page_size][depth], 16-byte aligned; v_pages must be a
+ *                      separate cache
+ *   k_rope_pages       bf16 [num_pages][num_kv_heads][page_size][rope_depth], or
+ *                      NULL; must be NULL while rope_depth is 0
+ *   k_scale            fp32 [num_pages][num_kv_heads][page_size] per-token K
+ *                      scales, 16-byte aligned, or NULL for unit scales; NULL
+ *                      for a bf16 cache
+ * fa_decode_run on an E4M3 handle returns FA_ERR_INVALID_ARG. Rows past L_b
+ * and unused pages may hold any codes and scales; they are never used.
+ */
+int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const void* v_pages, const void* k_rope_pages,
+                     const float* k_scale, const int32_t* page_table, const int32_t* seq_lens, float scale,
+                     void* out, float* lse, void* stream, int batch, int max_pages_per_seq, int num_pages);
+
+/*
  * Wait for `stream`, then read and clear the handle's device status word.
  * *status_out (may be NULL) receives the FA_STATUS_* bits raised by runs since
  * the last check. Returns FA_ERR_DEVICE when any bit was set, else FA_OK.

@@ -409,13 +409,21 @@ static int64_t cache_row(const oracle_shape* s, const int32_t* page_table, int b
     return ((int64_t)phys * s->num_kv_heads + k) * s->page_size + j % s->page_size;
 }
 
+/* decode_e4m3 of every code, filled once. */
+static double e4m3_table[256];
+static pthread_once_t e4m3_once = PTHREAD_ONCE_INIT;
+static void fill_e4m3_table(void)
+{
+    for (int c = 0; c < 256; ++c) e4m3_table[c] = decode_e4m3((uint8_t)c);
+}
+
 static int fp8_key(const row_job* J, int64_t r, double* dst)
 {
     const oracle_shape* s = J->s;
     const int d8 = s->qk_depth - J->rope_depth;
     const double ks = J->kscale ? (double)J->kscale[r] : 1.0;
     const uint8_t* src = J->k8 + r * d8;
-    for (int d = 0; d < d8; ++d) dst[d] = ks * decode_e4m3(src[d]);
+    for (int d = 0; d < d8; ++d) dst[d] = ks * e4m3_table[src[d]];
     for (int d = 0; d < J->rope_depth; ++d) dst[d8 + d] = widen_bf16(J->krope[r * J->rope_depth + d]);
     return 0;
 }
@@ -426,9 +434,9 @@ static int fp8_value(const row_job* J, int64_t r, double* dst)
     if (s->v_in_k) {
         const int d8 = s->qk_depth - J->rope_depth;
         const double ks = J->kscale ? (double)J->kscale[r] : 1.0;
-        for (int d = 0; d < s->ov_depth; ++d) dst[d] = ks * decode_e4m3(J->k8[r * d8 + d]);
+        for (int d = 0; d < s->ov_depth; ++d) dst[d] = ks * e4m3_table[J->k8[r * d8 + d]];
     } else {
-        for (int d = 0; d < s->ov_depth; ++d) dst[d] = decode_e4m3(J->v8[r * s->ov_depth + d]);
+        for (int d = 0; d < s->ov_depth; ++d) dst[d] = e4m3_table[J->v8[r * s->ov_depth + d]];
     }
     return 0;
 }
@@ -520,6 +528,7 @@ int oracle_decode_fp8(const oracle_shape* s, int rope_depth, double scale, const
     if (s->v_in_k && s->ov_depth > s->qk_depth - rope_depth) return -1;
     if (rows && n_rows < 0) return -1;
     if (!lens_ok(s, seq_lens)) return -1;
+    pthread_once(&e4m3_once, fill_e4m3_table);
     row_job proto;
     memset(&proto, 0, sizeof proto);
     proto.s = s;

@@ -26,9 +26,12 @@ FA_DEBUG_TWO_CLUSTERS = 4
 FA_DEBUG_NO_STREAM_K = 8
 FA_TRACE_WORDS_PER_CTA = 64
 FA_NOALLOC_STATUS_SLOTS = 64
+FA_KV_BF16 = 0
+FA_KV_E4M3 = 1
 
 # Every symbol include/fa_decode.h declares.
-EXPORTED = ("fa_decode_create", "fa_decode_run", "fa_decode_check", "fa_decode_set_debug",
+EXPORTED = ("fa_decode_create", "fa_decode_run", "fa_decode_create_kv", "fa_decode_run_kv", "fa_decode_check",
+            "fa_decode_set_debug",
             "fa_decode_set_trace", "fa_decode_describe", "fa_decode_run_noalloc", "fa_decode_destroy",
             "fa_decode_last_error")
 
@@ -62,6 +65,10 @@ def load_library(path: str | None = None):
     lib.fa_decode_create.restype = i32
     lib.fa_decode_run.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, i32, i32, i32]
     lib.fa_decode_run.restype = i32
+    lib.fa_decode_create_kv.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i32, i32, i32, i32, i32]
+    lib.fa_decode_create_kv.restype = i32
+    lib.fa_decode_run_kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, i32, i32, i32]
+    lib.fa_decode_run_kv.restype = i32
     lib.fa_decode_check.argtypes = [vp, vp, ctypes.POINTER(u32)]
     lib.fa_decode_check.restype = i32
     lib.fa_decode_set_debug.argtypes = [vp, u32, i64]
@@ -135,6 +142,32 @@ def fa_decode_run(h: int, q, k_pages, v_pages, page_table, seq_lens, scale: floa
     _check(load_library().fa_decode_run(h, _addr(q), _addr(k_pages), _addr(v_pages), _addr(page_table),
                                         _addr(seq_lens), float(scale), _addr(out), _addr(lse), _stream(stream),
                                         batch, max_pages_per_seq, num_pages))
+
+
+def fa_decode_create_kv(num_q_heads: int, num_kv_heads: int, qk_depth: int, nope_depth: int, ov_depth: int,
+                        page_size: int, num_q: int, splitk: int, kv_format: int, rope_depth: int = 0) -> int:
+    """Create a plan for a cache of format kv_format (FA_KV_BF16 / FA_KV_E4M3)."""
+    h = ctypes.c_void_p()
+    _check(load_library().fa_decode_create_kv(ctypes.byref(h), num_q_heads, num_kv_heads, qk_depth, nope_depth,
+                                              ov_depth, page_size, num_q, splitk, kv_format, rope_depth))
+    return int(h.value)
+
+
+def fa_decode_run_kv(h: int, q, k_pages, v_pages, k_rope_pages, k_scale, page_table, seq_lens, scale: float, out,
+                     lse, stream=None, batch: int | None = None, max_pages_per_seq: int | None = None,
+                     num_pages: int | None = None) -> None:
+    """Enqueue one decode forward over the handle's cache format (E4M3 codes
+    as uint8 tensors, per-token K scales as an fp32 tensor or None)."""
+    if batch is None:
+        batch = int(q.shape[0])
+    if max_pages_per_seq is None:
+        max_pages_per_seq = int(page_table.shape[1])
+    if num_pages is None:
+        num_pages = int(k_pages.shape[0])
+    _check(load_library().fa_decode_run_kv(h, _addr(q), _addr(k_pages), _addr(v_pages), _addr(k_rope_pages),
+                                           _addr(k_scale), _addr(page_table), _addr(seq_lens), float(scale),
+                                           _addr(out), _addr(lse), _stream(stream), batch, max_pages_per_seq,
+                                           num_pages))
 
 
 def fa_decode_check(h: int, stream=None) -> int:

@@ -66,19 +66,21 @@ struct MapCache {
 };
 
 // Tensor map over the K (or V) rows of the paged cache: [num_pages*Hkv*PS][depth]
-// bf16, boxes of 64 columns x box_rows rows, 128-byte swizzle, zero fill.
-int encode_cache_map(MapCache& c, const void* base, int depth, int64_t rows, int box_rows)
+// elements of `elem` bytes (2: bf16, 1: E4M3 codes), boxes of 128 bytes x
+// box_rows rows, 128-byte swizzle, zero fill.
+int encode_cache_map(MapCache& c, const void* base, int depth, int64_t rows, int box_rows, int elem = 2)
 {
-    if (c.valid && c.ptr == base && c.key0 == (uint64_t)depth && c.key1 == (uint64_t)rows &&
-        c.key2 == (uint64_t)box_rows)
+    const uint64_t k2 = ((uint64_t)elem << 32) | (uint64_t)box_rows;
+    if (c.valid && c.ptr == base && c.key0 == (uint64_t)depth && c.key1 == (uint64_t)rows && c.key2 == k2)
         return FA_OK;
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[2] = {(cuuint64_t)depth, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)depth * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)depth * elem};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&c.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = enc(&c.map, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                     const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -90,7 +92,7 @@ int encode_cache_map(MapCache& c, const void* base, int depth, int64_t rows, int
     c.ptr = base;
     c.key0 = depth;
     c.key1 = rows;
-    c.key2 = box_rows;
+    c.key2 = k2;
     return FA_OK;
 }
 
@@ -125,6 +127,8 @@ int encode_out_map(MapCache& c, void* out, int dv, int hq, int64_t bt, int chunk
 
 struct fa_decode {
     int hq, hkv, group, dk, nope, dv, page_size, num_q, splitk;
+    int kv_format;                   // FA_KV_BF16 or FA_KV_E4M3
+    int rope_depth;                  // E4M3: trailing key columns kept in bf16 apart (0)
     int rows, row_blocks, heads_per_cta, tokens_per_cta, rows_capacity;
     int device;
     fad::KernelGeometry geo;         // SIMT kernel, separate V cache (or V = K rows)
@@ -277,8 +281,13 @@ static void release_side_streams(fa_decode& h)
 // FA4Config constructor and supported() checks). Allocates nothing; the
 // caller provides the status word.
 static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth, int ov_depth,
-                       int page_size, int num_q, int splitk)
+                       int page_size, int num_q, int splitk, int kv_format = FA_KV_BF16, int rope_depth = 0)
 {
+    if (kv_format != FA_KV_BF16 && kv_format != FA_KV_E4M3)
+        return fail(FA_ERR_INVALID_ARG, "kv_format must be FA_KV_BF16 or FA_KV_E4M3 (got %d)", kv_format);
+    if (rope_depth < 0 || rope_depth >= qk_depth || (kv_format == FA_KV_BF16 && rope_depth != 0))
+        return fail(FA_ERR_INVALID_ARG, "rope_depth must be 0 for a bf16 cache and in [0, qk_depth) for E4M3 "
+                                        "(got %d)", rope_depth);
     if (num_q_heads < 1 || num_kv_heads < 1)
         return fail(FA_ERR_INVALID_ARG, "head counts must be >= 1 (got %d q, %d kv)", num_q_heads, num_kv_heads);
     if (num_q_heads % num_kv_heads)
@@ -302,6 +311,8 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
     tmp.page_size = page_size;
     tmp.num_q = num_q;
     tmp.splitk = splitk;
+    tmp.kv_format = kv_format;
+    tmp.rope_depth = rope_depth;
     tmp.wait_limit_ns = fad::kDefaultWaitLimitNs;
 
     // Rows of one CTA: the T*g fused GQA rows, or 16-head blocks for wide groups.
@@ -325,21 +336,35 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
     if (page_size % 8)
         return fail(FA_ERR_UNSUPPORTED, "page_size %d is not a multiple of 8", page_size);
     auto page_fits = [&](int bn) { return page_size % bn == 0 || bn % page_size == 0; };
-    tmp.has_simt = fad::simt_geometry(qk_depth, ov_depth, false, tmp.rows_capacity, &tmp.geo) &&
-                   page_fits(tmp.geo.keys_per_tile);
-    tmp.has_latent = tmp.has_simt && fad::simt_geometry(qk_depth, ov_depth, true, tmp.rows_capacity,
-                                                        &tmp.geo_latent);
-    tmp.has_tc = tmp.row_blocks == 1 &&
-                 fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsShared, false, &tmp.geo_tc) &&
-                 fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsAlone, false, &tmp.geo_tc_big) &&
-                 fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsAlone, true, &tmp.geo_tc_sk) &&
-                 page_fits(tmp.geo_tc.keys_per_tile);
-    tmp.has_mla = fad::mla_tc_geometry(qk_depth, ov_depth, tmp.nope, tmp.group, num_q, &tmp.geo_mla) &&
-                  page_fits(tmp.geo_mla.keys_per_tile);
-    if (!tmp.has_simt && !tmp.has_tc && !tmp.has_mla)
-        return fail(FA_ERR_UNSUPPORTED, "no kernel for (qk %d, ov %d), %d rows per CTA and page_size %d "
-                                        "(built: 64/64, 128/128, 576/512; page size and key tile must divide "
-                                        "one another)", qk_depth, ov_depth, tmp.rows, page_size);
+    if (kv_format == FA_KV_E4M3) {
+        // The E4M3 cache: the tcgen05 GQA kernel (head dim 128, <= 16 rows per CTA).
+        const auto geo = fad::tc_fp8_geometry;
+        tmp.has_tc = tmp.row_blocks == 1 && rope_depth == 0 &&
+                     geo(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsShared, false, &tmp.geo_tc) &&
+                     geo(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsAlone, false, &tmp.geo_tc_big) &&
+                     geo(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsAlone, true, &tmp.geo_tc_sk) &&
+                     page_fits(tmp.geo_tc.keys_per_tile);
+        if (!tmp.has_tc)
+            return fail(FA_ERR_UNSUPPORTED, "no E4M3-cache kernel for (qk %d, ov %d, rope %d), %d rows per CTA and "
+                                            "page_size %d (built: qk = ov = 128, rope 0, <= 16 rows per CTA)",
+                        qk_depth, ov_depth, rope_depth, tmp.rows, page_size);
+    } else {
+        tmp.has_simt = fad::simt_geometry(qk_depth, ov_depth, false, tmp.rows_capacity, &tmp.geo) &&
+                       page_fits(tmp.geo.keys_per_tile);
+        tmp.has_latent = tmp.has_simt && fad::simt_geometry(qk_depth, ov_depth, true, tmp.rows_capacity,
+                                                            &tmp.geo_latent);
+        tmp.has_tc = tmp.row_blocks == 1 &&
+                     fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsShared, false, &tmp.geo_tc) &&
+                     fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsAlone, false, &tmp.geo_tc_big) &&
+                     fad::tc_geometry(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsAlone, true, &tmp.geo_tc_sk) &&
+                     page_fits(tmp.geo_tc.keys_per_tile);
+        tmp.has_mla = fad::mla_tc_geometry(qk_depth, ov_depth, tmp.nope, tmp.group, num_q, &tmp.geo_mla) &&
+                      page_fits(tmp.geo_mla.keys_per_tile);
+        if (!tmp.has_simt && !tmp.has_tc && !tmp.has_mla)
+            return fail(FA_ERR_UNSUPPORTED, "no kernel for (qk %d, ov %d), %d rows per CTA and page_size %d "
+                                            "(built: 64/64, 128/128, 576/512; page size and key tile must divide "
+                                            "one another)", qk_depth, ov_depth, tmp.rows, page_size);
+    }
     int splits[3];
     const int ns = split_list(&tmp, splits);
     for (int i = 0; i < ns; ++i) {
@@ -408,11 +433,19 @@ const char* fa_decode_last_error(void) { return g_last_error.c_str(); }
 int fa_decode_create(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth,
                      int ov_depth, int page_size, int num_q, int splitk)
 {
+    return fa_decode_create_kv(out, num_q_heads, num_kv_heads, qk_depth, nope_depth, ov_depth, page_size, num_q,
+                               splitk, FA_KV_BF16, 0);
+}
+
+int fa_decode_create_kv(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth,
+                        int ov_depth, int page_size, int num_q, int splitk, int kv_format, int rope_depth)
+{
     g_last_error.clear();
     if (!out) return fail(FA_ERR_INVALID_ARG, "out handle pointer is NULL");
     *out = nullptr;
     fa_decode tmp;
-    int rc = plan_decode(tmp, num_q_heads, num_kv_heads, qk_depth, nope_depth, ov_depth, page_size, num_q, splitk);
+    int rc = plan_decode(tmp, num_q_heads, num_kv_heads, qk_depth, nope_depth, ov_depth, page_size, num_q, splitk,
+                         kv_format, rope_depth);
     if (rc) return rc;
 
     cudaError_t e = cudaMalloc(&tmp.d_status, 256);
@@ -546,7 +579,23 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
                   const int32_t* page_table, const int32_t* seq_lens, float scale, void* out, float* lse,
                   void* stream, int batch, int max_pages_per_seq, int num_pages)
 {
+    if (h && h->kv_format != FA_KV_BF16)
+        return fail(FA_ERR_INVALID_ARG, "this handle reads an E4M3 cache: call fa_decode_run_kv");
+    return fa_decode_run_kv(h, q, k_pages, v_pages, nullptr, nullptr, page_table, seq_lens, scale, out, lse, stream,
+                            batch, max_pages_per_seq, num_pages);
+}
+
+int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const void* v_pages, const void* k_rope_pages,
+                     const float* k_scale, const int32_t* page_table, const int32_t* seq_lens, float scale,
+                     void* out, float* lse, void* stream, int batch, int max_pages_per_seq, int num_pages)
+{
     if (!h) return fail(FA_ERR_INVALID_ARG, "handle is NULL");
+    const bool e4m3 = h->kv_format == FA_KV_E4M3;
+    if (!e4m3 && (k_rope_pages || k_scale))
+        return fail(FA_ERR_INVALID_ARG, "k_rope_pages and k_scale apply to an E4M3 cache only");
+    if (e4m3 && k_rope_pages)
+        return fail(FA_ERR_UNSUPPORTED, "a separate bf16 rope cache is not built for this shape");
+    if (k_scale && !is_aligned(k_scale, 16)) return fail(FA_ERR_INVALID_ARG, "k_scale must be 16-byte aligned");
     if (batch < 0) return fail(FA_ERR_INVALID_ARG, "batch must be >= 0 (got %d)", batch);
     if (batch == 0) return FA_OK;
     if (!q || !k_pages || !page_table || !seq_lens || !out)
@@ -566,6 +615,8 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
                     (long long)cache_rows);
 
     const bool latent = (v_pages == nullptr || v_pages == k_pages);
+    if (e4m3 && latent)
+        return fail(FA_ERR_UNSUPPORTED, "the E4M3 cache is built with a separate V cache only");
     if (latent && h->dv > h->dk)
         return fail(FA_ERR_INVALID_ARG, "latent layout (v_pages NULL or == k_pages) needs ov_depth <= qk_depth");
     // Kernel choice: for the MLA latent cache the MLA tcgen05 kernel (64 heads
@@ -619,13 +670,14 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     const int bn = g.keys_per_tile;
     const int box_rows = h->page_size < bn ? h->page_size : bn;
 
-    int rc = encode_cache_map(h->k_map, k_pages, h->dk, cache_rows, box_rows);
+    const int elem = e4m3 ? 1 : 2;
+    int rc = encode_cache_map(h->k_map, k_pages, h->dk, cache_rows, box_rows, elem);
     if (rc) return rc;
     if (latent && !use_latent && !use_mla) {
         // V = K row prefix through a separate-V kernel (e.g. qk == ov): same rows, V width.
         rc = encode_cache_map(h->v_map, k_pages, h->dk, cache_rows, box_rows);
     } else if (!latent) {
-        rc = encode_cache_map(h->v_map, v_pages, h->dv, cache_rows, box_rows);
+        rc = encode_cache_map(h->v_map, v_pages, h->dv, cache_rows, box_rows, elem);
     }
     if (rc) return rc;
 
@@ -667,6 +719,7 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
     p.chunk_o = h->chunk_o;
     p.chunk_ms = h->chunk_ms;
     p.chunk_count = h->chunk_count;
+    p.k_scale = k_scale;
 
     int splits[3];
     const int ns = split_list(h, splits);

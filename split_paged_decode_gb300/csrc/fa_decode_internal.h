@@ -77,6 +77,9 @@ struct DecodeParams {
     float* chunk_o;             // [slot][P][band_cols][rows_capacity]
     float2* chunk_ms;           // [slot][P][rows_capacity]: (max, sum) in raw score units
     unsigned int* chunk_count;  // [unit][P], zero between launches
+    // fp8 cache: per-token K scales, float [num_pages * Hkv * PS] (the cache
+    // row index), or NULL for unit scales.
+    const float* k_scale;
 };
 
 // Geometry of one compiled kernel variant, for planning and validation.
@@ -98,6 +101,9 @@ bool simt_geometry(int qk_depth, int ov_depth, bool latent, int rows_capacity, K
 // a ring of `nslot` 32 KB K/V tile slots; stream_k selects the variant of the
 // deep ring that takes the stream-K partition.
 bool tc_geometry(int qk_depth, int ov_depth, int rows, int nslot, bool stream_k, KernelGeometry* g);
+// The same kernel over an fp8 (OCP E4M3) cache: nslot counts 32 KB of ring
+// (twice as many 16 KB E4M3 tile slots).
+bool tc_fp8_geometry(int qk_depth, int ov_depth, int rows, int nslot, bool stream_k, KernelGeometry* g);
 // The tcgen05 kernel of the MLA latent layout (qk 576 = nope 512 + rope 64,
 // ov 512, V = the latent rows' first 512 columns) for num_q == 1 and a
 // multiple of 64 heads per kv head: 64 heads per CTA.

@@ -1,1086 +1,20 @@
-// kernel_tc.cu -- the tcgen05 (5th-generation tensor core) decode kernel for
-// GQA rows of head dimension 128 (sm_103a).
-//
-// The T*g <= 16 query rows of one kv head are too few to fill an MMA M
-// dimension, so both products are issued transposed, with the keys (resp.
-// the value columns) on M = 128 and the query rows on N = 16:
-//   S^T [128 keys x 16 rows]  = K_tile [128 x 128] . Q^T          (A, B K-major)
-//   O^T [128 dv x 16 rows]    = V_tile^T [128 dv x 128 keys] . P^T (A MN-major)
-// with fp32 accumulators in tensor memory. This keeps the tile dense on the
-// tensor pipe while HBM stays the bound.
-//
-// Warp roles (one CTA = one cluster rank; a cluster works on one
-// (sequence, kv head) unit at a time, the deep-ring variant on several in turn):
-//   warp 0     load: page-table walk (warp-wide blocks of entries fetched a
-//              block ahead),
-//              TMA loads of 128-key K and V tiles (two 64-column
-//              128-byte-swizzled boxes per page segment, one lane per
-//              segment) into a ring of NSLOT 32 KB slots, in the order the
-//              MMA warps consume them (V lagging K by VLAG tiles, see k_item)
-//   warp 1     MMA S: allocates 256 TMEM columns (S and O, two buffers of four
-//              accumulators each) and issues every S_i = K_i Q^T;
-//   warp 2     MMA O: issues every O_t = V_t^T P_t^T; each MMA warp commits a
-//              tile's products to the softmax warps and to the ring slot it read;
-//   warps 3-6  softmax + correction (thread = TMEM lane = key for S, = value
-//              column for O): online softmax in exp2 form with the running
-//              max in raw score units, P^T to shared memory as bf16, and the
-//              correction O <- O * alpha + O_tile in registers; then the
-//              split-K epilogue (splitk_combine.cuh): in the shallow-ring
-//              variant they merge themselves, in the deep-ring variant they
-//              push their partial to the band owners and go on;
-//   warp 7     (deep ring) epilogue: merges the pushed partials, stores the band.
-//
-// Geometry and vocabulary follow the FA4Config page (Modular MAX docs):
-// TMEM_S / TMEM_O / TMEM_P column maps, num_kv_stages, GQA fusion (field
-// group), split-K clusters (splitk_partitions, with_splitk); the TMEM
-// visibility rule of the fa4_lse_combine_write page (wait for the MMA's
-// barrier, then tcgen05.fence::after_thread_sync, before reading TMEM) is
-// applied to every TMEM read.
-#include <type_traits>
-
-#include "fa_decode_internal.h"
-#include "splitk_combine.cuh"
-#include "tcgen05.cuh"
+// kernel_tc.cu -- the bf16-cache instantiations of the tcgen05 GQA decode
+// kernel (kernel_tc.cuh) and their geometry.
+#include "kernel_tc.cuh"
 
 namespace fad {
-
-template <int NSLOT, int NRV>
-struct TcCfg {
-    // The deep-ring variant (one CTA per SM) works through several
-    // (sequence, kv head) units per cluster; it keeps dedicated Q, stage and
-    // output buffers so that a unit's epilogue overlaps the next unit's
-    // loads. The shallow-ring variant (two CTAs per SM) takes one unit per
-    // cluster and stages its epilogue in the drained ring.
-    static constexpr bool MULTI = NSLOT > kTcSlotsShared;
-    // V tiles are issued VLAG tiles after their K (<= 3: rows_s ring). A lag
-    // of 2 was measured slower than 1 on the deep ring: K tiles then wait in
-    // the ring for an S buffer instead.
-    static constexpr int VLAG = 1;
-    static constexpr int D = 128;       // qk_depth == ov_depth
-    static constexpr int BN = 128;      // keys per tile (M of S^T)
-    static constexpr int NR = 16;       // padded query rows (N of both MMAs)
-    static_assert(NRV == 4 || NRV == 8 || NRV == 16, "real rows per CTA");
-    // Softmax warpgroups: two (taking alternate tiles) where the registers of
-    // one CTA per SM allow it, else one.
-    static constexpr int NWG = (MULTI && NRV <= 8) ? 2 : 1;
-    static constexpr int WG0 = 3;       // first softmax warp (warps 3-6, 7-10 each cover TMEM quadrants 3, 0, 1, 2)
-    static constexpr int EPI = WG0 + 4 * NWG;  // the multi-unit variant's epilogue warp
-    static constexpr int THREADS = MULTI ? 32 * (EPI + 1) : 224;
-    static constexpr int TILE_BYTES = BN * D * 2;        // 32 KB: one K or V tile
-    static constexpr int BOX_BYTES = BN * 128;           // one 64-column box of a tile
-    static constexpr int Q_BYTES = NR * D * 2;           // 4 KB
-    static constexpr int P_BYTES = NR * BN * 2;          // 4 KB
-    // Each product's 8 K-steps are spread over NACC independent accumulators
-    // (K-step ks accumulates into ks % NACC), so dependent MMAs form chains of
-    // depth 8 / NACC; readers sum the NACC partials. 16 columns per
-    // accumulator (N = 16): S[2 buffers][NACC] then O[2 buffers][NACC].
-    static constexpr int NACC = 4;
-    static constexpr int ACC_COLS = 16;
-    static constexpr int BUF_COLS = NACC * ACC_COLS;              // 64
-    static constexpr int TMEM_S0 = 0, TMEM_O0 = 2 * BUF_COLS;     // 0 / 128
-    static constexpr int TMEM_COLS = 4 * BUF_COLS;                // 256
-
-    static constexpr int Q_BUFS = MULTI ? 2 : 1;                  // by unit parity
-    static constexpr int OFF_RING = 0;                            // NSLOT x 32 KB
-    static constexpr int OFF_Q = NSLOT * TILE_BYTES;              // K-major SW128 [Q_BUFS][2 boxes][16][128 B]
-    static constexpr int OFF_P = OFF_Q + Q_BUFS * Q_BYTES;        // [2 buffers][2 atoms][16][128 B]
-    static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;           // float [2][4][NRV]
-    static constexpr int OFF_MAXSUM = OFF_RED + 2 * 4 * NR * 4;   // float2 [NRV]
-    static constexpr int OFF_BAR = OFF_MAXSUM + NR * 8;
-    // barriers: slot_full[NSLOT], slot_empty[NSLOT], s_full[2], s_empty[2],
-    // p_full[2], o_full[2], o_empty[2], q_full[2], q_empty[2], publish,
-    // mma_done, tmem_ready, recv_full[2], recv_free[2], (spare)
-    static constexpr int NBAR = 2 * NSLOT + 22;
-    static constexpr int OFF_ROWS = OFF_BAR + NBAR * 8;          // int [4 tiles][16 segments]
-    static constexpr int OFF_MISC = OFF_ROWS + 4 * 16 * 4;       // tmem base, abort, S next item, O next item
-    static constexpr int MISC_END = OFF_MISC + 16;
-    // Epilogue buffers. Single-unit variant: f32 stage [P][NRV][Dv / P] in the
-    // drained ring (slot 0) that peers pull from, bf16 output band in slot 1.
-    // Multi-unit variant: receive buffers that peers push into (one or two,
-    // by unit, as space allows: float [P][Dv / P][NRV] + float2 [P][NRV]),
-    // the combine weights float [P][NRV] and the output band.
-    static constexpr int OUT_BYTES = NRV * D * 2;
-    static constexpr int RECV_BUFS = NRV <= 8 ? 2 : 1;
-    static constexpr int RECV_O_BYTES = NRV * D * 4;
-    static constexpr int RECV_BYTES = RECV_O_BYTES + kMaxSplit * NRV * 8;
-    static constexpr int OFF_RECV = (MISC_END + 127) / 128 * 128;
-    static constexpr int OFF_WTAB = OFF_RECV + RECV_BUFS * RECV_BYTES;
-    static constexpr int OFF_STAGE = 0;
-    static constexpr int OFF_OUT = MULTI ? (OFF_WTAB + kMaxSplit * NRV * 4 + 127) / 128 * 128 : TILE_BYTES;
-    // Two softmax warpgroups: the second's partial O [128 dv][NRV] and (max, sum) [NRV].
-    static constexpr int XCHG_O_BYTES = NWG == 2 ? D * NRV * 4 : 0;
-    static constexpr int OFF_XCHG = OFF_OUT + OUT_BYTES;
-    static constexpr int END_MULTI = OFF_XCHG + (NWG == 2 ? XCHG_O_BYTES + NRV * 8 : 0);
-    static constexpr int SMEM_BYTES = (MULTI ? END_MULTI : MISC_END) + 1024;
-    static_assert(NSLOT >= 2, "ring of at least one K and one V tile");
-    static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms on 1024 bytes");
-    static_assert(OFF_OUT % 128 == 0, "TMA store source on 128 bytes");
-    // 227 KB of dynamic shared memory per CTA; two CTAs of the shallow ring
-    // share an SM's 228 KB, each with 1 KB reserved by the system.
-    static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
-    static_assert(MULTI || 2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs per SM");
-};
-
-// One unit of work: the query rows of kv head `kvh` of sequence `b`, units
-// numbered u = b * Hkv + kvh. Cluster c of G takes units c, c + G, c + 2G, ...
-struct Unit {
-    int u, b, kvh, L;
-};
-
-// Advances w.u to this cluster's next unit that this launch handles (with
-// the per-sequence split rule, sequences of another split are skipped) and
-// fills in the rest; false when none is left. Every role of the CTA walks
-// the same sequence of units.
-__device__ __forceinline__ bool next_unit(const DecodeParams& p, int stride, int n_units, Unit& w, bool report)
-{
-    for (; w.u < n_units; w.u += stride) {
-        const int b = w.u / p.num_kv_heads;
-        int L = p.seq_lens[b];
-        if (L < 0) {
-            if (report) atomicOr(p.status, FA_STATUS_BAD_PAGE);
-            L = 0;
-        }
-        if (p.auto_split && auto_split_for_len(L) != p.splitk) continue;
-        w.b = b;
-        w.kvh = w.u - b * p.num_kv_heads;
-        w.L = L;
-        return true;
-    }
-    return false;
-}
-
-// Warp reduce-scatter of N per-row values (max or sum over the warp's 32
-// lanes): recursive halving exchanges half of the remaining rows at each of
-// the first log2(N) steps, then a butterfly finishes. On return v[0] holds
-// the reduction of row `row`; lanes whose low (32 / N) bits are zero hold
-// distinct rows.
-template <bool kMax>
-__device__ __forceinline__ float rs_op(float a, float b) { return kMax ? fmaxf(a, b) : a + b; }
-
-template <int N, int W, bool kMax, int M>
-__device__ __forceinline__ void reduce_scatter_step(float (&v)[M], int lane, int& row)
-{
-    if constexpr (N > 1) {
-        const bool up = (lane & W) != 0;
-#pragma unroll
-        for (int k = 0; k < N / 2; ++k) {
-            const float send = up ? v[k] : v[k + N / 2];
-            const float keep = up ? v[k + N / 2] : v[k];
-            v[k] = rs_op<kMax>(keep, __shfl_xor_sync(0xffffffffu, send, W));
-        }
-        row += up ? N / 2 : 0;
-        reduce_scatter_step<N / 2, W / 2, kMax, M>(v, lane, row);
-    } else {
-#pragma unroll
-        for (int w = W; w >= 1; w >>= 1) v[0] = rs_op<kMax>(v[0], __shfl_xor_sync(0xffffffffu, v[0], w));
-    }
-}
-
-template <int N, bool kMax>
-__device__ __forceinline__ float warp_reduce_scatter(const float (&in)[N], int lane, int& row)
-{
-    float v[N];
-#pragma unroll
-    for (int k = 0; k < N; ++k) v[k] = in[k];
-    row = 0;
-    reduce_scatter_step<N, 16, kMax, N>(v, lane, row);
-    return v[0];
-}
-
-// Load order of a unit's n tiles with V lagging D tiles behind K: K0 .. K_D,
-// then V_t K_{t+D+1} for t = 0 .. n-D-2, then the remaining V in order; for
-// D = 1: K0 K1 V0 K2 V1 ... K_{n-1} V_{n-2} V_{n-1}. A later V spends less
-// time in the ring waiting for its P.
-template <int D>
-__device__ __forceinline__ int k_item(int i) { return i <= D ? i : 2 * i - D; }
-template <int D>
-__device__ __forceinline__ int v_item(int t, int n) { return t <= n - D - 2 ? D + 1 + 2 * t : n + t; }
-// Inverse: the tile and kind of position j.
-template <int D>
-__device__ __forceinline__ void item_at(int j, int n, bool& is_v, int& t)
-{
-    if (j < min(n, D + 1)) {
-        is_v = false;
-        t = j;
-        return;
-    }
-    const int m = j - (D + 1);
-    if (m < 2 * (n - D - 1)) {
-        is_v = (m & 1) == 0;
-        t = is_v ? (m >> 1) : ((m - 1) >> 1) + D + 1;
-    } else {
-        is_v = true;
-        t = j - n;
-    }
-}
-
-// Lazy rescaling: the running max of a row moves only when a tile's max
-// exceeds it by more than this many exp2 units, so most tiles skip the
-// correction; P then stays below 2^8, safe in bf16 and fp32.
-constexpr float kRescaleThreshold = 8.0f;
-
-// Units with at least this many tiles per rank are issued two items per pass
-// by the load warp (its issue rate bounds them); shorter ones one at a time.
-constexpr int kPairTiles = 16;
-
-// SK: the stream-K partition (DecodeParams::sk_tiles; deep ring only).
-template <int NSLOT, int NRV, bool SK>
-__global__ void __launch_bounds__(TcCfg<NSLOT, NRV>::THREADS, TcCfg<NSLOT, NRV>::MULTI ? 1 : 2)
-    tc_decode_kernel(const __grid_constant__ DecodeParams p)
-{
-    static_assert(!SK || TcCfg<NSLOT, NRV>::MULTI, "stream-K needs the multi-unit variant");
-    using C = TcCfg<NSLOT, NRV>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    const uint32_t sbase = smem_addr(smem);
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    const int P = p.splitk;
-    const int rank = (int)blockIdx.x;
-    const int n_units = p.batch * p.num_kv_heads;
-    const int cluster_id = (int)(blockIdx.y + gridDim.y * blockIdx.z);
-    const int n_clusters = (int)(gridDim.y * gridDim.z);
-    // This cluster's units: c, c + G, ... or, under the stream-K partition,
-    // the one or two its tile range touches.
-    int u_first = cluster_id, u_step = n_clusters, u_end = n_units;
-    int64_t sk_g0 = 0, sk_g1 = 0;  // the cluster's stream-K tile range
-    if constexpr (SK) {
-        sk_g0 = sk_begin(p.sk_total, p.sk_clusters, cluster_id);
-        sk_g1 = sk_begin(p.sk_total, p.sk_clusters, cluster_id + 1);
-        u_first = (int)(sk_g0 / p.sk_tiles);
-        u_end = sk_g1 > sk_g0 ? (int)((sk_g1 - 1) / p.sk_tiles) + 1 : u_first;
-        u_step = 1;
-    }
-
-    // Optional timeline trace (a profiling aid): one thread writes each event.
-    const int64_t cta_lin = (int64_t)blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
-    unsigned long long* const trace =
-        (p.trace != nullptr && cta_lin < p.trace_ctas) ? p.trace + cta_lin * FA_TRACE_WORDS_PER_CTA : nullptr;
-    auto stamp = [&](int slot) {
-        if (trace) trace[slot] = global_timer_ns();
-    };
-    constexpr int kTraceUnits = 7;
-    auto unit_slot = [](int k, int e) { return 4 + 8 * k + e; };
-    if (tid == 0) stamp(0);
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&p.tm_k);
-        tma_prefetch_map(&p.tm_v);
-    }
-
-    // Tiles [tile_begin, tile_begin + tile_count) of unit u (length L) belong
-    // to this rank: its share of all the unit's tiles or, under the stream-K
-    // partition, of those in the cluster's range (clipped to L).
-    auto rank_tiles = [&](int u, int L, int& tile_begin, int& tile_count) {
-        int n_tiles = (L + C::BN - 1) / C::BN, t0 = 0;
-        if constexpr (SK) {
-            const int64_t base = (int64_t)u * p.sk_tiles;
-            t0 = (int)min((int64_t)n_tiles, max(sk_g0, base) - base);
-            n_tiles = max((int)min((int64_t)n_tiles, min(sk_g1, base + p.sk_tiles) - base) - t0, 0);
-        }
-        const int base = n_tiles / P, rem = n_tiles % P;
-        tile_begin = t0 + rank * base + min(rank, rem);
-        tile_count = base + (rank < rem ? 1 : 0);
-    };
-    // Page-table entries reach the load warp in warp-wide blocks: lane l
-    // holds the entry of (tile tb + l / segs, page segment l % segs) of the
-    // block starting at tile tb, fetched one block ahead, and a tile's entries
-    // are shuffled out of it. The first block is fetched before the sequence
-    // length is known, guessing that the sequence fills its page-table row;
-    // the guess is checked once the length has arrived, so the two reads
-    // overlap instead of following one another.
-    const int segs = C::BN / p.box_rows;  // page segments per tile: 1, 2, 4, 8 or 16
-    const int tpb = 32 / segs;            // tiles per block of page entries
-    int spec_begin = -1, spec_count = 0, spec_raw = -1;
-    if (warp == 0 && u_first < u_end && p.max_pages <= INT32_MAX / C::BN / p.page_size) {
-        int gb, gc;
-        rank_tiles(u_first, p.max_pages * p.page_size, gb, gc);
-        spec_begin = gb;
-        spec_count = gc;
-        const int b0 = u_first / p.num_kv_heads;
-        const int t = lane / segs;
-        const int pslot = ((gb + t) * C::BN + (lane % segs) * p.box_rows) / p.page_size;
-        if (t < gc && pslot < p.max_pages) spec_raw = p.page_table[(int64_t)b0 * p.max_pages + pslot];
-    }
-    if (u_first >= u_end) return;  // (grids never have more clusters than units or ranges)
-    if (p.auto_split) {
-        // A cluster with no unit in this launch (the per-sequence split gives
-        // its sequences to another launch) leaves at once; the decision is the
-        // same in every CTA of the cluster.
-        Unit first{u_first, 0, 0, 0};
-        if (!next_unit(p, u_step, u_end, first, tid == 0 && rank == 0)) return;
-    }
-
-    const uint32_t bar0 = sbase + C::OFF_BAR;
-    const uint32_t slot_full = bar0, slot_empty = bar0 + 8 * NSLOT;
-    const uint32_t s_full = bar0 + 16 * NSLOT, s_empty = s_full + 16, p_full = s_full + 32;
-    const uint32_t o_full = s_full + 48, o_empty = s_full + 64, q_full = s_full + 80, q_empty = s_full + 96;
-    const uint32_t publish_bar = s_full + 112, mma_done = s_full + 120, tmem_ready = s_full + 128;
-    const uint32_t recv_full = s_full + 136, recv_free = s_full + 152;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-    // Ring-order progress of the two MMA warps: the global index of the next
-    // K (resp. V) item each will consume; every earlier item of its kind has
-    // been consumed.
-    const uint32_t s_next = sbase + C::OFF_MISC + 8, o_next = sbase + C::OFF_MISC + 12;
-    float* red_s = reinterpret_cast<float*>(smem + C::OFF_RED);  // [2][4][NRV]: by tile parity (= warpgroup)
-    float2* maxsum_s = reinterpret_cast<float2*>(smem + C::OFF_MAXSUM);
-
-    if (tid == 0) {
-        for (int s = 0; s < NSLOT; ++s) {
-            mbar_init(slot_full + 8 * s, 1);
-            mbar_init(slot_empty + 8 * s, 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(s_full + 8 * i, 1);
-            mbar_init(s_empty + 8 * i, 4);
-            mbar_init(p_full + 8 * i, 4);
-            mbar_init(o_full + 8 * i, 1);
-            mbar_init(o_empty + 8 * i, 4);
-            mbar_init(q_full + 8 * i, 4);  // one arrival per softmax warp
-            mbar_init(q_empty + 8 * i, 1);
-        }
-        mbar_init(publish_bar, P);
-        mbar_init(mma_done, 2);
-        mbar_init(tmem_ready, 1);
-        for (int i = 0; i < 2; ++i) {
-            // P > 1: the epilogue warp's expect_tx arrive plus the pushed bytes;
-            // P == 1: the epilogue warp and the four softmax warps arrive.
-            mbar_init(recv_full + 8 * i, P > 1 ? 1 : 5);
-            mbar_init(recv_free + 8 * i, P);  // one arrival per receiving rank
-        }
-        *abort_flag = 0;
-        *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 8) = 0;
-        *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 12) = 0;
-        fence_mbarrier_init_cluster();
-    }
-    __syncthreads();  // barriers initialised; the load warp may start at once
-    // Peers arrive on this CTA's publish barrier only after the matching
-    // cluster wait (before the first merge), so the prologue does not wait here.
-    if (P > 1) cluster_arrive_relaxed();
-    uint32_t tmem = 0;
-    if (warp == 1) {
-        tmem_alloc(sbase + C::OFF_MISC, C::TMEM_COLS);
-        tmem_relinquish();
-        tc_fence_before_sync();
-        __syncwarp();
-        tc_fence_after_sync();
-        tmem = *tmem_slot;
-        if (lane == 0) mbar_arrive(tmem_ready);
-    }
-
-    // Softmax / correction state (warps 3-6), real rows only.
-    float m_run[NRV], l_part[NRV], o_acc[NRV];
-
-    // Items (K or V tiles) and tiles are numbered globally over the units of
-    // this cluster, so ring slots, buffers and barrier phases run on across
-    // unit boundaries. Within a unit of n tiles the items come in the order
-    // K0 K1 V0 K2 V1 ... K_{n-1} V_{n-2} V_{n-1}.
-    int issued = 0;
-    if (warp == 0) {
-        // ------------------------------------------------------------------ load warp
-        // All 32 lanes run the loop; lane s owns page segment s of every tile.
-        if (!(p.debug_flags & FA_DEBUG_SKIP_LOADS)) {
-            const uint64_t policy = l2_policy_evict_first();
-            int32_t* rows_s = reinterpret_cast<int32_t*>(smem + C::OFF_ROWS);
-            constexpr int kNoSegment = INT32_MIN, kPastSequence = INT32_MIN + 1;
-            int J0 = 0, lu = 0;
-            bool ok = true;
-            Unit w{u_first, 0, 0, 0};
-            for (; ok && next_unit(p, u_step, u_end, w, tid == 0 && rank == 0); w.u += u_step, ++lu) {
-                int tile_begin, tile_count;
-                rank_tiles(w.u, w.L, tile_begin, tile_count);
-                const int n_items = 2 * tile_count;
-                // This lane's entry of the block starting at tile tb: the physical
-                // page, or kNoSegment / kPastSequence (zero fill, no error); -1
-                // past the page table. `raw` >= -1: that entry, already read.
-                auto block_entry = [&](int tb, int raw = -2) -> int {
-                    const int t = tb + lane / segs;
-                    if (t >= tile_count) return kNoSegment;
-                    const int key = (tile_begin + t) * C::BN + (lane % segs) * p.box_rows;
-                    if (key >= w.L) return kPastSequence;
-                    const int pslot = key / p.page_size;
-                    if (pslot >= p.max_pages) return -1;
-                    return raw >= -1 ? raw : p.page_table[(int64_t)w.b * p.max_pages + pslot];
-                };
-                // The guess holds when the unit's first tiles are the guessed ones
-                // (then every entry block_entry needs below was read).
-                const bool guessed =
-                    lu == 0 && w.u == u_first && tile_begin == spec_begin && tile_count <= spec_count;
-                int blk_cur = block_entry(0, guessed ? spec_raw : -2), blk_next = block_entry(tpb);
-                // One pass issues one item (lanes 0-15) or, for a long unit, two
-                // consecutive items (lanes 0-15 and 16-31; lane 16 h + s owns page
-                // segment s), so the waits, barrier arms and copies of a pair share
-                // their instructions: a long unit is bound by this warp's issue
-                // rate, a short one by the ring.
-                auto pass = [&](int j, auto two_tag) -> bool {
-                    constexpr bool TWO = decltype(two_tag)::value;
-                    // one item: every lane computes it, lane s owns segment s
-                    const int half = TWO ? (lane >> 4) : 0, sl = TWO ? (lane & 15) : lane;
-                    const int jh = j + half;  // this half's item in the unit
-                    const bool valid = TWO ? (jh < n_items) : true;
-                    const int jj = J0 + jh, slot = jj % NSLOT;
-                    bool is_v = true;
-                    int t = 0;
-                    if (valid) item_at<C::VLAG>(jh, tile_count, is_v, t);
-                    bool got = true;
-                    if (valid && jj >= NSLOT)
-                        got = mbar_wait(slot_empty + 8 * slot, ((jj / NSLOT) & 1) ^ 1, abort_flag, p.status,
-                                        p.wait_limit_ns);
-                    if (!__all_sync(0xffffffffu, got)) return false;
-                    const bool k_here = valid && !is_v;
-                    // A K tile of the pass that starts a new block of page entries.
-                    int kt = k_here ? t : -1;
-                    if (TWO) kt = max(kt, __shfl_xor_sync(0xffffffffu, kt, 16));  // one item: uniform already
-                    if (kt > 0 && (kt & (tpb - 1)) == 0) {
-                        // Waits only if the block fetched a block of tiles ago has not arrived.
-                        blk_cur = blk_next;
-                        blk_next = block_entry(kt + tpb);
-                    }
-                    const int e =
-                        __shfl_sync(0xffffffffu, blk_cur, ((k_here ? t : 0) & (tpb - 1)) * segs + (sl & (segs - 1)));
-                    int32_t row = p.oob_row;  // zero fill past the sequence or on a bad page
-                    if (k_here) {
-                        if (sl < segs) {
-                            if (e >= 0 && e < p.num_pages) {
-                                // the segment starts on a page boundary unless pages are longer than a tile
-                                const int off = p.page_size > C::BN ? ((tile_begin + t) * C::BN) % p.page_size : 0;
-                                row = (e * p.num_kv_heads + w.kvh) * p.page_size + off;
-                            } else if (e != kNoSegment && e != kPastSequence) {
-                                atomicOr(p.status, FA_STATUS_BAD_PAGE);
-                            }
-                        }
-                        if (sl < 16) rows_s[(t & 3) * 16 + sl] = row;  // read by V_t, at most 3 tiles later
-                    }
-                    // A one-tile unit has K0 and V0 side by side, possibly in one pass:
-                    // the K half's rows are written before the V half reads them.
-                    if (TWO) __syncwarp();
-                    if (valid && is_v) row = sl < 16 ? rows_s[(t & 3) * 16 + sl] : p.oob_row;
-                    if (valid && sl == 0) mbar_arrive_expect_tx(slot_full + 8 * slot, C::TILE_BYTES);
-                    __syncwarp();
-                    issued = J0 + (TWO ? min(j + 2, n_items) : j + 1);
-                    if (valid && sl < segs) {
-                        const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
-                        const uint32_t dst = sbase + C::OFF_RING + slot * C::TILE_BYTES + sl * p.box_rows * 128;
-                        tma_load_2d(dst, map, 0, row, slot_full + 8 * slot, policy);
-                        tma_load_2d(dst + C::BOX_BYTES, map, 64, row, slot_full + 8 * slot, policy);
-                    }
-                    return true;
-                };
-                if (n_items > 0 && lane == 0) {
-                    if (J0 == 0) stamp(1);
-                    if (lu < kTraceUnits) stamp(unit_slot(lu, 7));
-                }
-                if (tile_count >= kPairTiles) {
-                    for (int j = 0; ok && j < n_items; j += 2) ok = pass(j, std::true_type{});
-                } else {
-                    for (int j = 0; ok && j < n_items; ++j) ok = pass(j, std::false_type{});
-                }
-                J0 += n_items;
-            }
-        }
-    } else if (warp == 1 || warp == 2) {
-        // ------------------------------------------------------------ MMA warps
-        // One warp issues tcgen05.mma only every ~60 cycles, so the products go
-        // to two warps: warp 1 issues every S_i = K_i Q^T, warp 2 every
-        // O_t = V_t^T P_t^T. Each commits a tile's products twice: to the
-        // softmax warps' barrier, and to the ring slot's empty barrier, which
-        // frees the slot for the load warp as soon as the product completes.
-        //
-        // Ring-order rule: a slot's full barrier is waited on for item j only
-        // after item j - NSLOT, which held the slot before, has been consumed
-        // (a parity wait on a barrier whose previous phase has not completed
-        // would alias with that phase). Each warp consumes its own kind in
-        // order, so it waits for the other warp's published next-item index
-        // to pass j - NSLOT.
-        if (lane == 0) {
-            const bool is_s = (warp == 1);
-            const uint32_t other_next = is_s ? o_next : s_next;
-            const uint32_t id_s = umma_idesc_bf16_f32(128, C::NR, false, false);
-            const uint64_t q_desc0 = umma_smem_desc(sbase + C::OFF_Q, 16, 1024, kLayoutSwizzle128);
-            const uint64_t k_desc0 = umma_smem_desc(sbase + C::OFF_RING, 16, 1024, kLayoutSwizzle128);
-            const uint32_t id_pv = umma_idesc_bf16_f32(128, C::NR, true, false);
-            // A = V^T, MN-major: 64-column atoms one box apart (LBO), 8-key groups 1024 B apart (SBO)
-            const uint64_t v_desc0 = umma_smem_desc(sbase + C::OFF_RING, C::BOX_BYTES, 1024, kLayoutSwizzle128);
-            // B = P, K-major: 64-key atoms of 16 rows x 128 B
-            const uint64_t p_desc0 = umma_smem_desc(sbase + C::OFF_P, 16, 1024, kLayoutSwizzle128);
-            if (!is_s) {
-                mbar_wait(tmem_ready, 0, abort_flag, p.status, p.wait_limit_ns);
-                tc_fence_after_sync();
-                tmem = *tmem_slot;
-            }
-            auto ring_turn = [&](int j) -> bool {  // item j may wait on its slot
-                return j < NSLOT ||
-                       counter_wait(other_next, (uint32_t)(j - NSLOT), abort_flag, p.status, p.wait_limit_ns);
-            };
-            int J0 = 0, gt = 0, lu = 0;
-            bool ok = true;
-            Unit w{u_first, 0, 0, 0};
-            for (; ok && next_unit(p, u_step, u_end, w, false); w.u += u_step, ++lu) {
-                int tile_begin, tile_count;
-                rank_tiles(w.u, w.L, tile_begin, tile_count);
-                if (is_s) {
-                    ok = mbar_wait(q_full + 8 * (lu & 1), (lu >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
-                    if (lu == 0) stamp(60);
-                    const uint64_t qd = q_desc0 + (uint64_t)(((lu & 1) * C::Q_BYTES) >> 4);
-                    for (int i = 0; ok && i < tile_count; ++i) {
-                        const int gi = gt + i, j = J0 + k_item<C::VLAG>(i), slot = j % NSLOT;
-                        ok = ring_turn(j) &&
-                             mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns) &&
-                             (gi < 2 || mbar_wait(s_empty + 8 * (gi & 1), ((gi >> 1) - 1) & 1, abort_flag, p.status,
-                                                  p.wait_limit_ns));
-                        if (!ok) break;
-                        if (gi == 0) stamp(61);
-                        tc_fence_after_sync();
-                        const uint64_t a0 = k_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
-                        const uint32_t d = tmem + C::TMEM_S0 + C::BUF_COLS * (gi & 1);
-#pragma unroll
-                        for (int ks = 0; ks < C::D / 16; ++ks)
-                            umma_f16_ss(d + C::ACC_COLS * (ks % C::NACC),
-                                        a0 + (uint64_t)(((ks >> 2) * C::BOX_BYTES + (ks & 3) * 32) >> 4),
-                                        qd + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_s,
-                                        ks >= C::NACC);
-                        umma_commit(s_full + 8 * (gi & 1));
-                        umma_commit(slot_empty + 8 * slot);  // K_i's slot is free once S_i has completed
-                        st_release_u32(s_next, (uint32_t)(i + 1 < tile_count ? J0 + k_item<C::VLAG>(i + 1)
-                                                                             : J0 + 2 * tile_count));
-                    }
-                    // Q buffer lu & 1 is read by no further product of this warp.
-                    mbar_arrive(q_empty + 8 * (lu & 1));
-                } else {
-                    for (int t = 0; ok && t < tile_count; ++t) {
-                        const int gi = gt + t, j = J0 + v_item<C::VLAG>(t, tile_count), slot = j % NSLOT;
-                        ok = ring_turn(j) &&
-                             mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns) &&
-                             mbar_wait(p_full + 8 * (gi & 1), (gi >> 1) & 1, abort_flag, p.status, p.wait_limit_ns) &&
-                             (gi < 2 || mbar_wait(o_empty + 8 * (gi & 1), ((gi >> 1) - 1) & 1, abort_flag, p.status,
-                                                  p.wait_limit_ns));
-                        if (!ok) break;
-                        if (gi == 0) stamp(62);
-                        tc_fence_after_sync();
-                        const uint64_t a0 = v_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
-                        const uint64_t b0 = p_desc0 + (uint64_t)(((gi & 1) * C::P_BYTES) >> 4);
-                        const uint32_t d = tmem + C::TMEM_O0 + C::BUF_COLS * (gi & 1);
-#pragma unroll
-                        for (int ks = 0; ks < C::BN / 16; ++ks)
-                            umma_f16_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)((ks * 2048) >> 4),
-                                        b0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_pv,
-                                        ks >= C::NACC);
-                        umma_commit(o_full + 8 * (gi & 1));
-                        umma_commit(slot_empty + 8 * slot);  // V_t's slot is free once O_t has completed
-                        st_release_u32(o_next, (uint32_t)(t + 1 < tile_count ? J0 + v_item<C::VLAG>(t + 1, tile_count)
-                                                                             : J0 + 2 * tile_count));
-                    }
-                }
-                gt += tile_count;
-                J0 += 2 * tile_count;
-            }
-            st_release_u32(is_s ? s_next : o_next, 0xffffffffu);  // nothing more to wait for
-            // mma_done expects one commit from each MMA warp: it fires once every
-            // MMA of both warps has completed.
-            umma_commit(mma_done);
-            volatile int keep_waiting = 0;
-            mbar_wait(mma_done, 0, &keep_waiting, p.status, p.wait_limit_ns);
-        }
-        __syncwarp();
-    } else if (warp < C::EPI) {
-        // ------------------------------------------------- softmax / correction warps
-        // NWG warpgroups; warpgroup g takes the unit's tiles whose index is g
-        // modulo NWG and keeps its own running max, sum and O; at the end of a
-        // unit the second folds its partial into the first, which pushes the
-        // result. Buffers of S, P and O are indexed by the global tile index,
-        // so any warpgroup may consume any buffer; the barrier phases order it.
-        const int wg = (warp - C::WG0) >> 2;          // softmax warpgroup
-        const int wt = tid - 32 * C::WG0 - 128 * wg;  // 0..127 within it
-        const uint32_t wg_bar = 1 + wg;               // its named barrier
-        const int quad = warp & 3;                    // TMEM lane quadrant of this warp
-        const int my_lane = 32 * quad + lane;         // key (S) or value column (O) of this thread
-        const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
-        const float c2 = p.scale_log2e;
-        const bool lead = wg == 0;                    // stores Q, stamps the trace, merges, pushes
-
-        // Q rows of a unit -> K-major 128-byte-swizzled B operand; rows >= p.rows are zero.
-        auto load_q = [&](const Unit& x, uint4 (&v)[2]) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int idx = wt + 128 * k, r = idx >> 4, u = idx & 15;  // 16-byte chunk u of row r
-                v[k] = make_uint4(0, 0, 0, 0);
-                if (r < p.rows) {
-                    const int t = r / p.heads_per_cta;
-                    const int h = x.kvh * p.group + r % p.heads_per_cta;
-                    v[k] = reinterpret_cast<const uint4*>(
-                        p.q + (((int64_t)x.b * p.num_q + t) * p.num_q_heads + h) * C::D)[u];
-                }
-            }
-        };
-        auto store_q = [&](int buf, const uint4 (&v)[2]) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int idx = wt + 128 * k, r = idx >> 4, u = idx & 15;
-                *reinterpret_cast<uint4*>(smem + C::OFF_Q + buf * C::Q_BYTES + (u >> 3) * 2048 + r * 128 +
-                                          (((u & 7) ^ (r & 7)) << 4)) = v[k];
-            }
-        };
-
-        Unit w{u_first, 0, 0, 0};
-        bool have = next_unit(p, u_step, u_end, w, false);
-        if (have && lead) {
-            uint4 qv[2];
-            load_q(w, qv);
-            store_q(0, qv);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(q_full);
-            if (wt == 0) stamp(63);
-        }
-        mbar_wait(tmem_ready, 0, abort_flag, p.status, p.wait_limit_ns);
-        tc_fence_after_sync();
-        tmem = *tmem_slot;
-
-        // lanes holding distinct rows after a reduce-scatter of NRV values
-        const bool row_writer = (lane & (32 / NRV - 1)) == 0;
-        bool seen_abort = false;  // sticky: this thread has seen the abort flag
-        bool cluster_waited = false;
-        int J0 = 0, gt = 0, lu = 0;
-        while (have) {
-            const int L = w.L;
-            int tile_begin, tile_count;
-            rank_tiles(w.u, L, tile_begin, tile_count);
-            if (lead && wt == 0 && lu < kTraceUnits) {
-                stamp(unit_slot(lu, 0));
-                if (trace) trace[unit_slot(lu, 6)] = (unsigned long long)tile_count;
-            }
-            // The next unit of this cluster: its Q rows are fetched now and
-            // stored once the S warp has left the buffer's previous unit (after
-            // this warpgroup's first tile of the unit), so the S warp runs
-            // straight on into it.
-            Unit nx = w;
-            nx.u += u_step;
-            const bool more = C::MULTI && next_unit(p, u_step, u_end, nx, false);
-            uint4 qn[2];
-            bool q_pending = more && lead;
-            if (q_pending) load_q(nx, qn);
-            auto put_next_q = [&]() {  // before a fence.proxy.async and the warp's q_full arrive
-                if (lu >= 1)
-                    mbar_wait(q_empty + 8 * ((lu + 1) & 1), ((lu - 1) >> 1) & 1, abort_flag, p.status,
-                              p.wait_limit_ns);
-                store_q((lu + 1) & 1, qn);
-            };
-#pragma unroll
-            for (int r = 0; r < NRV; ++r) {
-                m_run[r] = -INFINITY;
-                l_part[r] = 0.f;
-                o_acc[r] = 0.f;
-            }
-            // Row r = t * heads + hh (query token t) sees keys < L - T + t + 1, so
-            // the rows that see key k are a suffix: r >= (k - (L - T + 1) + 1) * heads.
-            const int vis0 = L - p.num_q + 1;
-
-            float alpha_prev[NRV];
-            bool rescaled_prev = false;
-            // O of this warpgroup's tile with global index gi has completed:
-            // fold it into o_acc.
-            auto correct = [&](int gi, const float (&a)[NRV], bool rescaled) {
-                mbar_wait(o_full + 8 * (gi & 1), (gi >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
-                tc_fence_after_sync();
-                float ot[NRV];
-                tmem_ld4_sum(tmem + lane_addr + C::TMEM_O0 + C::BUF_COLS * (gi & 1), C::ACC_COLS, ot);
-                tc_fence_before_sync();
-                __syncwarp();
-                // O has completed, so (for tile gi + 2) the P buffer it read is free.
-                if (lane == 0) mbar_arrive(o_empty + 8 * (gi & 1));
-                if (rescaled) {
-#pragma unroll
-                    for (int r = 0; r < NRV; ++r) o_acc[r] = fmaf(o_acc[r], a[r], ot[r]);
-                } else {
-#pragma unroll
-                    for (int r = 0; r < NRV; ++r) o_acc[r] += ot[r];
-                }
-            };
-
-            // This warpgroup's tiles: local index i congruent to wg modulo NWG
-            // (by local index, so a unit's arithmetic does not depend on the
-            // units its cluster took before). Their global indices share a
-            // parity, so within a unit a warpgroup uses one buffer of S, P, O
-            // and red_s: (gt + wg) & 1 with two warpgroups.
-            const int i0 = C::NWG == 2 ? wg : 0;
-            const int gt0 = gt;
-            int prev_gi = -1;  // this warpgroup's previous tile, still to be folded in
-            for (int i = i0; i < tile_count; i += C::NWG) {
-                const int gi = gt + i;
-                mbar_wait(s_full + 8 * (gi & 1), (gi >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
-                if (lead && wt == 0 && i == i0) {
-                    if (gi == 0) stamp(2);
-                    if (lu < kTraceUnits) stamp(unit_slot(lu, 1));
-                }
-                tc_fence_after_sync();
-                float s[NRV];
-                tmem_ld4_sum(tmem + lane_addr + C::TMEM_S0 + C::BUF_COLS * (gi & 1), C::ACC_COLS, s);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s_empty + 8 * (gi & 1));
-
-                const int key0 = (tile_begin + i) * C::BN;
-                const int key = key0 + my_lane;
-                const int r_min = key < vis0 ? 0 : (key >= L ? NRV : (key - vis0 + 1) * p.heads_per_cta);
-#pragma unroll
-                for (int r = 0; r < NRV; ++r) s[r] = (r >= r_min && r < p.rows) ? s[r] : -INFINITY;
-
-                // Lazy rescale: a row's running max moves only when some score
-                // exceeds it by more than the threshold. In the common case a single
-                // reducing barrier confirms that no thread needs it; otherwise the
-                // tile max is exchanged and the rows that exceed are moved.
-                bool need = false;
-#pragma unroll
-                for (int r = 0; r < NRV; ++r)
-                    need |= (s[r] != -INFINITY) &&
-                            (m_run[r] == -INFINITY || (s[r] - m_run[r]) * c2 > kRescaleThreshold);
-                seen_abort |= (*abort_flag != 0);
-                bool rescale = false;
-                float alpha[NRV];
-                if (named_barrier_or(wg_bar, 128, need || seen_abort)) {
-                    {
-                        int row;
-                        const float wmax = warp_reduce_scatter<NRV, true>(s, lane, row);
-                        if (row_writer) red_s[((gi & 1) * 4 + quad) * NRV + row] = wmax;
-                    }
-                    seen_abort |= (*abort_flag != 0);
-                    // The abort decision is reduced over the warpgroup, so it is uniform.
-                    if (named_barrier_or(wg_bar, 128, seen_abort)) {
-                        seen_abort = true;
-                        break;
-                    }
-                    float tmax[NRV];
-                    const float* rq = red_s + (gi & 1) * 4 * NRV;
-#pragma unroll
-                    for (int r4 = 0; r4 < NRV / 4; ++r4) {
-                        const float4 a0 = reinterpret_cast<const float4*>(rq)[r4];
-                        const float4 a1 = reinterpret_cast<const float4*>(rq + NRV)[r4];
-                        const float4 a2 = reinterpret_cast<const float4*>(rq + 2 * NRV)[r4];
-                        const float4 a3 = reinterpret_cast<const float4*>(rq + 3 * NRV)[r4];
-                        tmax[4 * r4 + 0] = fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x));
-                        tmax[4 * r4 + 1] = fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y));
-                        tmax[4 * r4 + 2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
-                        tmax[4 * r4 + 3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
-                    }
-                    rescale = true;
-#pragma unroll
-                    for (int r = 0; r < NRV; ++r) {
-                        const bool move = (m_run[r] == -INFINITY) ? (tmax[r] != -INFINITY)
-                                                                  : ((tmax[r] - m_run[r]) * c2 > kRescaleThreshold);
-                        alpha[r] = 1.f;
-                        if (move) {
-                            alpha[r] = (m_run[r] == -INFINITY) ? 0.f : ex2_approx((m_run[r] - tmax[r]) * c2);
-                            m_run[r] = tmax[r];
-                            l_part[r] *= alpha[r];
-                        }
-                    }
-                }
-#pragma unroll
-                for (int r = 0; r < NRV; ++r) {
-                    const float pr = (s[r] == -INFINITY) ? 0.f : ex2_approx((s[r] - m_run[r]) * c2);
-                    l_part[r] += pr;
-                    s[r] = pr;
-                }
-
-                // P (bf16) -> K-major swizzled B operand of O^T = V^T P^T (rows >= NRV
-                // only feed output columns that are never read). Buffer gi & 1 was
-                // last read by O of global tile gi - 2, whose completion the
-                // correction of that tile has observed: one warpgroup folded it in
-                // during its previous tile; two fold it in here, before the store.
-                if constexpr (C::NWG == 2) {
-                    if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
-                }
-                {
-                    uint8_t* pb = smem + C::OFF_P + (gi & 1) * C::P_BYTES + (my_lane >> 6) * 2048;
-                    const int kk = my_lane & 63;
-#pragma unroll
-                    for (int r = 0; r < NRV; ++r)
-                        *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((((kk >> 3) ^ (r & 7))) << 4) +
-                                                          (kk & 7) * 2) = __float2bfloat16_rn(s[r]);
-                }
-                // Last tile of the sequence: zero the V rows past L so that unused
-                // cache rows (whatever they hold) meet P = 0 as exact zeros.
-                if (key0 + C::BN > L) {
-                    const int j = J0 + v_item<C::VLAG>(i, tile_count), slot = j % NSLOT;
-                    mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns);
-                    if (key >= L) {
-                        uint4* vrow0 =
-                            reinterpret_cast<uint4*>(smem + C::OFF_RING + slot * C::TILE_BYTES + my_lane * 128);
-                        uint4* vrow1 = reinterpret_cast<uint4*>(smem + C::OFF_RING + slot * C::TILE_BYTES +
-                                                                C::BOX_BYTES + my_lane * 128);
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            vrow0[u] = make_uint4(0, 0, 0, 0);
-                            vrow1[u] = make_uint4(0, 0, 0, 0);
-                        }
-                    }
-                }
-                const bool q_now = q_pending;  // uniform: this warpgroup's first tile of the unit
-                if (q_now) put_next_q();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(p_full + 8 * (gi & 1));
-                    if (q_now) mbar_arrive(q_full + 8 * ((lu + 1) & 1));
-                }
-                q_pending = false;
-
-                if constexpr (C::NWG == 1) {
-                    if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
-                }
-#pragma unroll
-                for (int r = 0; r < NRV; ++r) alpha_prev[r] = rescale ? alpha[r] : 1.f;
-                rescaled_prev = rescale;
-                prev_gi = gi;
-            }
-            // Bounded even after an abort. After an abort the O of the tile
-            // that broke the loop was never issued; the wait gives up at once.
-            if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
-            if (lead && wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 2));
-            gt += tile_count;
-            J0 += 2 * tile_count;
-            if (q_pending) {  // no tile stored it (no tiles, or an abort in the first)
-                put_next_q();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(q_full + 8 * ((lu + 1) & 1));
-            }
-
-            // ---------------------------------------------------- unit epilogue
-            // Row sums: per-thread partial sums -> warp reduce-scatter -> four
-            // warps, in this warpgroup's half of red_s.
-            float* red_w = red_s + (C::NWG == 2 ? ((gt0 + wg) & 1) : 0) * 4 * NRV;
-            {
-                int row;
-                const float wsum = warp_reduce_scatter<NRV, false>(l_part, lane, row);
-                named_barrier_sync(wg_bar, 128);  // red_s may still be read by the last tile's max step
-                if (row_writer) red_w[quad * NRV + row] = wsum;
-                named_barrier_sync(wg_bar, 128);
-            }
-            float lrow[NRV];
-#pragma unroll
-            for (int r = 0; r < NRV; ++r) lrow[r] = red_w[r] + red_w[NRV + r] + red_w[2 * NRV + r] + red_w[3 * NRV + r];
-            if constexpr (C::NWG == 2) {
-                // Fold the second warpgroup's partial into the first's:
-                // m = max(m_a, m_b), both sides scaled by exp2((m_x - m) * c).
-                float* xo = reinterpret_cast<float*>(smem + C::OFF_XCHG);          // [128 dv][NRV]
-                float2* xms = reinterpret_cast<float2*>(smem + C::OFF_XCHG + C::XCHG_O_BYTES);  // [NRV]
-                if (!lead) {
-                    // The first warpgroup has read the previous unit's exchange.
-                    if (lu >= 1) named_barrier_sync(4, 256);
-#pragma unroll
-                    for (int r4 = 0; r4 < NRV / 4; ++r4)
-                        reinterpret_cast<float4*>(xo + my_lane * NRV)[r4] =
-                            make_float4(o_acc[4 * r4], o_acc[4 * r4 + 1], o_acc[4 * r4 + 2], o_acc[4 * r4 + 3]);
-                    if (wt == 0)
-#pragma unroll
-                        for (int r = 0; r < NRV; ++r) xms[r] = make_float2(m_run[r], lrow[r]);
-                }
-                named_barrier_sync(3, 256);
-                if (lead) {
-                    float ob[NRV];
-#pragma unroll
-                    for (int r4 = 0; r4 < NRV / 4; ++r4) {
-                        const float4 v4 = reinterpret_cast<const float4*>(xo + my_lane * NRV)[r4];
-                        ob[4 * r4] = v4.x;
-                        ob[4 * r4 + 1] = v4.y;
-                        ob[4 * r4 + 2] = v4.z;
-                        ob[4 * r4 + 3] = v4.w;
-                    }
-#pragma unroll
-                    for (int r = 0; r < NRV; ++r) {
-                        const float2 mb = xms[r];
-                        const float m = fmaxf(m_run[r], mb.x);
-                        const float aa = m_run[r] == -INFINITY ? 0.f : ex2_approx((m_run[r] - m) * c2);
-                        const float ab = mb.x == -INFINITY ? 0.f : ex2_approx((mb.x - m) * c2);
-                        o_acc[r] = o_acc[r] * aa + ob[r] * ab;
-                        lrow[r] = lrow[r] * aa + mb.y * ab;
-                        m_run[r] = m;
-                    }
-                    if (more) named_barrier_arrive(4, 256);  // exchange read: the second may reuse it
-                }
-            }
-            if (lead) {
-                const int BW = p.band_cols;
-                const int dv = my_lane;
-                if constexpr (C::MULTI) {
-                    // Push this rank's normalised partial into the band owners'
-                    // receive buffers (see splitk_merge_pushed) and go on with the
-                    // next unit; the epilogue warp merges.
-                    const int rb = lu % C::RECV_BUFS, rk = lu / C::RECV_BUFS;
-                    // Every receiver has finished with this buffer's previous unit.
-                    if (rk >= 1)
-                        mbar_wait<true>(recv_free + 8 * rb, (rk - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
-                    if (P > 1 && !cluster_waited) {
-                        cluster_wait();  // every rank's barriers are initialised
-                        cluster_waited = true;
-                    }
-                    float v[NRV];
-#pragma unroll
-                    for (int r = 0; r < NRV; ++r) v[r] = lrow[r] > 0.f ? o_acc[r] * __frcp_rn(lrow[r]) : 0.f;
-                    const uint32_t recv0 = sbase + C::OFF_RECV + rb * C::RECV_BYTES;
-                    const int q = dv / BW, col = dv % BW;
-                    const uint32_t o_dst = recv0 + 4u * (uint32_t)((rank * BW + col) * NRV);
-                    if (P > 1) {
-                        const uint32_t bar_q = map_shared_rank(recv_full + 8 * rb, q);
-                        const uint32_t dst_q = map_shared_rank(o_dst, q);
-#pragma unroll
-                        for (int r4 = 0; r4 < NRV / 4; ++r4)
-                            st_async_f4(dst_q + 16 * r4, v[4 * r4], v[4 * r4 + 1], v[4 * r4 + 2], v[4 * r4 + 3],
-                                        bar_q);
-                        for (int idx = wt; idx < P * NRV; idx += 128) {
-                            const int qq = idx / NRV, rr = idx % NRV;
-                            float mm = 0.f, ll = 0.f;
-#pragma unroll
-                            for (int r = 0; r < NRV; ++r)
-                                if (r == rr) {
-                                    mm = m_run[r];
-                                    ll = lrow[r];
-                                }
-                            const uint32_t ms_dst = recv0 + C::RECV_O_BYTES + 8u * (uint32_t)(rank * NRV + rr);
-                            st_async_f2(map_shared_rank(ms_dst, qq), mm, ll, map_shared_rank(recv_full + 8 * rb, qq));
-                        }
-                    } else {
-                        float* o_loc = reinterpret_cast<float*>(smem + (o_dst - sbase));
-#pragma unroll
-                        for (int r4 = 0; r4 < NRV / 4; ++r4)
-                            reinterpret_cast<float4*>(o_loc)[r4] =
-                                make_float4(v[4 * r4], v[4 * r4 + 1], v[4 * r4 + 2], v[4 * r4 + 3]);
-                        if (wt == 0) {
-                            float2* ms_loc = reinterpret_cast<float2*>(smem + (recv0 - sbase) + C::RECV_O_BYTES);
-#pragma unroll
-                            for (int r = 0; r < NRV; ++r) ms_loc[r] = make_float2(m_run[r], lrow[r]);
-                        }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(recv_full + 8 * rb);
-                    }
-                    if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
-                } else {
-                    float* stage_s = reinterpret_cast<float*>(smem + C::OFF_STAGE);
-                    const int q = dv / BW, jc = dv % BW;
-#pragma unroll
-                    for (int r = 0; r < NRV; ++r) {
-                        if (wt == 0) maxsum_s[r] = make_float2(m_run[r], lrow[r]);
-                        float inv = 0.f;
-                        if (lrow[r] > 0.f) inv = __frcp_rn(lrow[r]);  // uniform: no divergence
-                        stage_s[(q * NRV + r) * BW + jc] = o_acc[r] * inv;
-                    }
-                    if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
-                    named_barrier_sync(wg_bar, 128);
-                    if (P > 1) {
-                        cluster_wait();  // every rank's publish barrier is initialised
-                        cluster_waited = true;
-                    }
-                    if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 4));
-                    splitk_merge_and_store<NRV>(p, P, rank, w.b, w.kvh, 0, stage_s, maxsum_s,
-                                                reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), publish_bar, 0u,
-                                                0u, abort_flag, wt, 128, wg_bar);
-                    if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 5));
-                }
-            }
-            ++lu;
-            // Uniform over the softmax warpgroups: stop after an abort.
-            seen_abort |= (*abort_flag != 0);
-            if (named_barrier_or(C::NWG == 2 ? 3 : wg_bar, 128 * C::NWG, seen_abort) || !more) break;
-            w = nx;
-        }
-        if (P > 1 && !cluster_waited) cluster_wait();  // pairs with the early arrive
-        tc_fence_before_sync();
-    } else {
-        // ------------------------------------------- epilogue warp (multi-unit variant)
-        // Merges each unit's pushed partials and stores the output band while
-        // the softmax warps work on the next unit.
-        bool cluster_waited = false;
-        int lu = 0;
-        Unit w{u_first, 0, 0, 0};
-        const uint32_t expect = (uint32_t)pushed_bytes(P, p.band_cols, NRV);
-        for (; next_unit(p, u_step, u_end, w, false); w.u += u_step, ++lu) {
-            const int rb = lu % C::RECV_BUFS, rk = lu / C::RECV_BUFS;
-            if (P > 1 && !cluster_waited) {
-                cluster_wait();  // every rank's barriers are initialised
-                cluster_waited = true;
-            }
-            // This buffer's previous phase completed (this warp waited for it),
-            // so the arrival belongs to this unit's phase; pushed bytes that
-            // landed earlier are already counted against it.
-            if (lane == 0) {
-                if (P > 1)
-                    mbar_arrive_expect_tx(recv_full + 8 * rb, expect);
-                else
-                    mbar_arrive(recv_full + 8 * rb);
-            }
-            const bool got = mbar_wait<true>(recv_full + 8 * rb, rk & 1, abort_flag, p.status, p.wait_limit_ns);
-            if (!__all_sync(0xffffffffu, got)) break;
-            if (lane == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 4));
-            const uint8_t* recv = smem + C::OFF_RECV + rb * C::RECV_BYTES;
-            if constexpr (SK)
-                splitk_merge_pushed_sk<NRV>(p, P, rank, w.b, w.kvh, w.u, cluster_id,
-                                            reinterpret_cast<const float*>(recv),
-                                            reinterpret_cast<const float2*>(recv + C::RECV_O_BYTES),
-                                            reinterpret_cast<float*>(smem + C::OFF_WTAB),
-                                            reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), lane);
-            else
-                splitk_merge_pushed<NRV>(p, P, rank, w.b, w.kvh, reinterpret_cast<const float*>(recv),
-                                         reinterpret_cast<const float2*>(recv + C::RECV_O_BYTES),
-                                         reinterpret_cast<float*>(smem + C::OFF_WTAB),
-                                         reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), lane);
-            // Release the buffer to every sender: all lanes' reads of it are
-            // complete (their results are in the band); one fence orders them
-            // ahead of the senders' next pushes, then relaxed arrives.
-            __syncwarp();
-            if (lane == 0) {
-                if (P > 1) {
-                    fence_acq_rel_cluster();
-                    for (int q = 0; q < P; ++q) mbar_arrive_cluster_relaxed(map_shared_rank(recv_free + 8 * rb, q));
-                } else {
-                    mbar_arrive(recv_free + 8 * rb);
-                }
-            }
-            if (lane == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 5));
-        }
-        if (lane == 0) tma_store_wait_read();  // the last band has been read out of shared memory
-        __syncwarp();
-        if (P > 1 && !cluster_waited) cluster_wait();  // pairs with the early arrive
-    }
-
-    // All TMEM reads and MMAs are complete (the MMA lanes waited for mma_done).
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after_sync();
-        tmem_dealloc(tmem, C::TMEM_COLS);
-    }
-    if (warp == 0 && lane == 0 && *abort_flag) {
-        // Gave up early: wait (bounded) until the copies of the last NSLOT
-        // issued items have landed, so none is in flight when the CTA exits.
-        volatile int keep_waiting = 0;
-        for (int j = issued > NSLOT ? issued - NSLOT : 0; j < issued; ++j)
-            mbar_wait(slot_full + 8 * (j % NSLOT), (j / NSLOT) & 1, &keep_waiting, p.status, p.wait_limit_ns);
-    }
-    if (P > 1 && warp < C::WG0) cluster_wait();  // pairs with the early arrive (the other warps waited above)
-    __syncwarp();
-    if (P > 1) cluster_sync_all();  // peers may still read this CTA's staged bands until here
-    if (tid == 0) stamp(3);
-}
 
 bool tc_geometry(int qk, int ov, int rows, int nslot, bool stream_k, KernelGeometry* g)
 {
     if (stream_k && nslot <= kTcSlotsShared) return false;
     if (qk != 128 || ov != 128 || rows < 1 || rows > 16) return false;
     const int nrv = rows <= 4 ? 4 : (rows <= 8 ? 8 : 16);
-#define FAD_TC(NS, NRV)                                                                   \
-    if (nslot == NS && nrv == NRV) {                                                      \
-        g->func = stream_k ? reinterpret_cast<const void*>(&tc_decode_kernel<NS, NRV, NS != 3>) \
-                           : reinterpret_cast<const void*>(&tc_decode_kernel<NS, NRV, false>); \
-        g->threads = TcCfg<NS, NRV>::THREADS;                                             \
-        g->keys_per_tile = TcCfg<NS, NRV>::BN;                                            \
-        g->stages = NS;                                                                   \
-        g->rows_capacity = NRV;                                                           \
-        g->smem_bytes = TcCfg<NS, NRV>::SMEM_BYTES;                                       \
-        g->name = stream_k ? "tc_d128_bn128_n16_r" #NRV "_slots" #NS "_streamk"          \
-                           : "tc_d128_bn128_n16_r" #NRV "_slots" #NS;                     \
-        return true;                                                                      \
+#define FAD_TC(NS, NRV)                                                                              \
+    if (nslot == NS && nrv == NRV) {                                                                 \
+        tc_variant<NS, NRV, false>(stream_k,                                                         \
+                                   stream_k ? "tc_d128_bn128_n16_r" #NRV "_slots" #NS "_streamk"     \
+                                            : "tc_d128_bn128_n16_r" #NRV "_slots" #NS, g);           \
+        return true;                                                                                 \
     }
     FAD_TC(3, 4)
     FAD_TC(3, 8)

@@ -45,6 +45,29 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(int M, int N, bool a_
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format 0) and an
+// f32 accumulator; the other fields as for kind::f16.
+__host__ __device__ constexpr uint32_t umma_idesc_e4m3_f32(int M, int N, bool a_mn_major, bool b_mn_major)
+{
+    return (1u << 4)                                   // D: f32
+           | (0u << 7)                                 // A: E4M3
+           | (0u << 10)                                // B: E4M3
+           | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T with 8-bit operands (K = 32), one thread.
+__device__ __forceinline__ void umma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate)

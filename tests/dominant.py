@@ -76,7 +76,9 @@ def choose_positions(w, lens, splitk_of=None, salt: int = 0) -> dict:
 
 
 def plant(inp, positions: dict, alpha: float = 64.0):
-    """Modify `inp` in place (q and the K cache) so that each chosen key dominates."""
+    """Modify `inp` in place (q and the K cache) so that each chosen key dominates.
+    An E4M3 cache gets the code of 448 in the dominant columns and, with
+    per-token scales, the scale 0.25 (key value 112) for the chosen row."""
     w = inp.workload
     cols = dom_cols(w)
     q = inp.q.float()
@@ -85,14 +87,26 @@ def plant(inp, positions: dict, alpha: float = 64.0):
     ps = w.page_size
     for (b, k), j in positions.items():
         page = int(inp.page_table[b, j // ps])
-        inp.k_pages[page, k, j % ps, cols] = alpha
+        if w.kv_dtype == "e4m3":
+            inp.k_pages[page, k, j % ps, cols] = 0x7E
+            if inp.k_scale is not None:
+                inp.k_scale[page, k, j % ps] = 0.25
+        else:
+            inp.k_pages[page, k, j % ps, cols] = alpha
     return inp
 
 
+def _e4m3(codes: torch.Tensor, dtype) -> torch.Tensor:
+    return codes.contiguous().view(torch.float8_e4m3fn).to(dtype)
+
+
 def value_row(inp, b: int, k: int, j: int) -> torch.Tensor:
+    """V_j as bf16 (an E4M3 value row widened exactly)."""
     w = inp.workload
     ps = w.page_size
     page = int(inp.page_table[b, j // ps])
+    if w.kv_dtype == "e4m3":
+        return _e4m3(inp.v_pages[page, k, j % ps, :], torch.bfloat16)
     if inp.v_pages is None:
         return inp.k_pages[page, k, j % ps, :w.ov_depth]
     return inp.v_pages[page, k, j % ps, :]
@@ -103,6 +117,11 @@ def _gather_keys(inp, b: int, k: int, L: int) -> torch.Tensor:
     ps = w.page_size
     j = torch.arange(L)
     pages = inp.page_table[b, (j // ps)].long()
+    if w.kv_dtype == "e4m3":
+        kk = _e4m3(inp.k_pages[pages, k, j % ps, :], torch.float64)
+        if inp.k_scale is not None:
+            kk = kk * inp.k_scale[pages, k, j % ps].double().unsqueeze(1)
+        return kk
     return inp.k_pages[pages, k, j % ps, :].double()
 
 
@@ -133,8 +152,10 @@ def check_margin(inp, positions: dict):
 
 
 def check_bit_exact(out: torch.Tensor, inp, positions: dict, what: str = "") -> int:
-    """Every output row of a query that sees its chosen key equals V_j bitwise.
-    Returns the number of rows checked."""
+    """Every output row of a query that sees its chosen key equals V_j exactly:
+    the same value in every column (bf16 values compared exactly; +0 and -0
+    count as equal, since sum_j p_j V_j turns an E4M3 -0 into +0). Returns the
+    number of rows checked."""
     w = inp.workload
     g = w.num_q_heads // w.num_kv_heads
     out = out.cpu()
@@ -147,12 +168,12 @@ def check_bit_exact(out: torch.Tensor, inp, positions: dict, what: str = "") -> 
             if j >= L - w.num_q + t + 1:
                 continue
             got = out[b, t, k * g:(k + 1) * g, :]
-            same = (got.view(torch.int16) == v.view(torch.int16).unsqueeze(0)).all(dim=1)
+            same = (got.float() == v.float().unsqueeze(0)).all(dim=1)
             checked += g
             if not bool(same.all()):
                 h = int(torch.nonzero(~same)[0, 0]) + k * g
                 bad.append((b, t, h, j))
-    assert not bad, f"{what}: {len(bad)} rows differ from V_j bitwise, first (b, t, h, j) = {bad[0]}"
+    assert not bad, f"{what}: {len(bad)} rows differ from V_j, first (b, t, h, j) = {bad[0]}"
     return checked
 
 

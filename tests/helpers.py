@@ -52,8 +52,15 @@ class DeviceCall:
         self.lse = torch.full((w.batch, w.num_q, w.num_q_heads), float("nan"), dtype=torch.float32,
                               device=device)
         P = w.splitk if splitk is None else splitk
-        self.h = spd.fa_decode_create(w.num_q_heads, w.num_kv_heads, w.qk_depth, w.nope_depth,
-                                      w.ov_depth, w.page_size, w.num_q, P)
+        self.e4m3 = w.kv_dtype == "e4m3"
+        self.ks = None if inp.k_scale is None else inp.k_scale.to(device)
+        self.rope = None if inp.k_rope is None else inp.k_rope.to(device)
+        if self.e4m3:
+            self.h = spd.fa_decode_create_kv(w.num_q_heads, w.num_kv_heads, w.qk_depth, w.nope_depth,
+                                             w.ov_depth, w.page_size, w.num_q, P, spd.FA_KV_E4M3, w.rope_depth)
+        else:
+            self.h = spd.fa_decode_create(w.num_q_heads, w.num_kv_heads, w.qk_depth, w.nope_depth,
+                                          w.ov_depth, w.page_size, w.num_q, P)
         if path == "simt":
             spd.fa_decode_set_debug(self.h, spd.FA_DEBUG_FORCE_SIMT, 0)
         elif path == "two_clusters":  # each cluster works through many units in turn
@@ -65,8 +72,12 @@ class DeviceCall:
         return spd.fa_decode_describe(self.h)
 
     def run(self, stream=None):
-        spd.fa_decode_run(self.h, self.q, self.k, self.v, self.pt, self.lens, self.inp.scale, self.out,
-                          self.lse, stream=stream)
+        if self.e4m3:
+            spd.fa_decode_run_kv(self.h, self.q, self.k, self.v, self.rope, self.ks, self.pt, self.lens,
+                                 self.inp.scale, self.out, self.lse, stream=stream)
+        else:
+            spd.fa_decode_run(self.h, self.q, self.k, self.v, self.pt, self.lens, self.inp.scale, self.out,
+                              self.lse, stream=stream)
 
     def status(self) -> int:
         return spd.fa_decode_check(self.h)

@@ -1,0 +1,153 @@
+"""The fp8 (OCP E4M3) cache on the GPU, through the C ABI, against the fp64
+fp8 oracle (oracle_decode_fp8).
+
+The kernel reads E4M3 K and V tiles and an optional per-token K scale; its
+arithmetic error is bounded like the bf16 path's (Q and P are carried as two
+E4M3 operands each, ~8 bits), so the bound is the same:
+|out - ref| <= 1e-2 + 1e-2 |ref| and |lse - ref| <= 1e-3. Page gathering is
+checked bit for bit with dominant keys (see dominant.py).
+"""
+import pytest
+import torch
+
+import split_paged_decode_gb300 as spd
+from split_paged_decode_gb300.workloads import WORKLOADS, DecodeWorkload, generate
+
+import dominant
+from helpers import DeviceCall, check_against_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from split_paged_decode_gb300 import build
+
+    build.build_library()
+    spd.load_library()
+
+
+def wl(**kw):
+    base = dict(name="fp8", batch=3, num_q=1, num_q_heads=8, num_kv_heads=2, qk_depth=128, ov_depth=128,
+                page_size=64, splitk=2, seq_len_lo=1, seq_len_hi=700, seed=900, kv_dtype="e4m3", k_scale=True)
+    base.update(kw)
+    return DecodeWorkload(**base)
+
+
+def run_and_check(w, seq_lens=None, path="auto", what=""):
+    inp = generate(w, seq_lens=seq_lens)
+    with DeviceCall(inp, path=path) as call:
+        assert "e4m3" in call.describe(), call.describe()
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what=what or w.name)
+
+
+@pytest.mark.parametrize("scaled", [True, False])
+@pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
+def test_splits(P, scaled):
+    run_and_check(wl(splitk=P, k_scale=scaled, seed=900 + P), what=f"fp8 P{P} scale {scaled}")
+
+
+@pytest.mark.parametrize("ps", [8, 16, 32, 128, 256])
+def test_page_sizes(ps):
+    run_and_check(wl(page_size=ps, splitk=4, seed=910 + ps), what=f"fp8 ps{ps}")
+
+
+@pytest.mark.parametrize("g,T", [(1, 1), (4, 1), (8, 1), (16, 1), (4, 4), (2, 8)])
+def test_rows_per_cta(g, T):
+    run_and_check(wl(num_q_heads=2 * g, num_q=T, splitk=4, seed=920 + g * T), what=f"fp8 g{g} T{T}")
+
+
+def test_causal_short_and_empty():
+    w = wl(num_q=4, batch=10, splitk=4, seed=930)
+    run_and_check(w, seq_lens=[0, 1, 2, 3, 4, 63, 64, 65, 127, 129], what="fp8 short/empty")
+
+
+@pytest.mark.parametrize("P", [2, 4, 16])
+def test_multi_unit_schedule(P):
+    w = wl(batch=7, splitk=P, seed=940 + P)
+    run_and_check(w, seq_lens=[0, 1, 130, 700, 129, 2000, 64], path="two_clusters", what=f"fp8 multi-unit P{P}")
+
+
+@pytest.mark.parametrize("P", [1, 4, 8])
+def test_stream_k(P):
+    w = wl(batch=2, num_kv_heads=1, num_q_heads=4, splitk=P, seq_len_lo=9000, seq_len_hi=20000, seed=950 + P)
+    run_and_check(w, what=f"fp8 stream-K P{P}")
+
+
+def test_per_sequence_split():
+    w = wl(batch=12, num_q=4, splitk=0, seed=960)
+    run_and_check(w, seq_lens=[1, 5, 1024, 1025, 4096, 4097, 8192, 9000, 64, 65, 2000, 3000], what="fp8 auto split")
+
+
+def test_nonfinite_codes_and_scales_past_the_sequence_do_not_leak():
+    w = wl(batch=3, splitk=2, seed=970)
+    lens = [70, 200, 129]
+    inp = generate(w, seq_lens=lens)
+    for b, L in enumerate(lens):
+        last = int(inp.page_table[b, (L - 1) // 64])
+        inp.k_pages[last, :, L % 64:, :] = 0x7F   # NaN code
+        inp.v_pages[last, :, L % 64:, :] = 0xFF
+        inp.k_scale[last, :, L % 64:] = float("nan")
+    with DeviceCall(inp) as call:
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what="fp8 non-finite tails")
+
+
+def test_bad_page_id_is_reported_not_faulted():
+    inp = generate(wl(batch=3, splitk=2, seed=980))
+    bad = inp.page_table.clone()
+    bad[1, 0] = inp.num_pages + 1000
+    with DeviceCall(inp) as call:
+        call.pt = bad.cuda()
+        call.run()
+        assert spd.fa_decode_check(call.h) & spd.FA_STATUS_BAD_PAGE
+        rows = [(b, 0, h) for b in (0, 2) for h in range(8)]
+        check_against_oracle(call, rows=rows, what="fp8 bad page neighbours")
+
+
+def test_timeout_and_recovery():
+    inp = generate(wl(batch=2, splitk=2, seed=981))
+    with DeviceCall(inp) as call:
+        spd.fa_decode_set_debug(call.h, spd.FA_DEBUG_SKIP_LOADS, 20_000_000)
+        call.run()
+        assert spd.fa_decode_check(call.h) & spd.FA_STATUS_TIMEOUT
+        spd.fa_decode_set_debug(call.h, 0, 0)
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what="fp8 after timeout")
+
+
+def test_bf16_entry_point_refuses_an_e4m3_handle():
+    inp = generate(wl(seed=982))
+    with DeviceCall(inp) as call:
+        with pytest.raises(spd.FaDecodeError) as e:
+            spd.fa_decode_run(call.h, call.q, call.k, call.v, call.pt, call.lens, inp.scale, call.out, call.lse)
+        assert e.value.code == spd.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("scaled", [True, False])
+@pytest.mark.parametrize("P,ps,path", [(1, 64, "auto"), (4, 16, "auto"), (8, 128, "auto"), (16, 256, "auto"),
+                                       (4, 64, "two_clusters")])
+def test_gather_bit_exact(P, ps, path, scaled):
+    w = wl(batch=6, splitk=P, page_size=ps, seq_len_lo=1, seq_len_hi=3000, k_scale=scaled, seed=990 + P + ps)
+    inp = generate(w, seq_lens=[1, 130, 700, 2000, 129, 4097])
+    pos = dominant.choose_positions(w, inp.seq_lens.tolist(), salt=P + ps)
+    dominant.plant(inp, pos)
+    dominant.check_margin(inp, pos)
+    with DeviceCall(inp, path=path) as call:
+        call.run()
+        assert call.status() == 0
+        dominant.check_bit_exact(call.out, inp, pos, what=f"fp8 gather P{P} ps{ps} {path}")
+        check_against_oracle(call, what=f"fp8 gather P{P} ps{ps} oracle")
+
+
+@pytest.mark.parametrize("name", ["batched_gqa", "long_context", "ragged_speculative"])
+def test_workload_full_size(name):
+    """The head-dim-128 workloads with an E4M3 cache and per-token K scales."""
+    w = WORKLOADS[name].with_(kv_dtype="e4m3", k_scale=True)
+    run_and_check(w, what=f"{name} e4m3")

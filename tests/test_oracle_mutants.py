@@ -43,16 +43,16 @@ MUTANTS = {
     "e4m3_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
     "e4m3_subnormal_exponent": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
     "e4m3_sign_dropped": ("return sign ? -v : v;", "return v;"),
-    "fp8_k_scale_dropped": ("for (int d = 0; d < d8; ++d) dst[d] = ks * decode_e4m3(src[d]);",
-                            "for (int d = 0; d < d8; ++d) dst[d] = decode_e4m3(src[d]);"),
+    "fp8_k_scale_dropped": ("for (int d = 0; d < d8; ++d) dst[d] = ks * e4m3_table[src[d]];",
+                            "for (int d = 0; d < d8; ++d) dst[d] = e4m3_table[src[d]];"),
     "fp8_rope_column_rotated": ("dst[d8 + d] = widen_bf16(J->krope[r * J->rope_depth + d]);",
                                 "dst[d8 + d] = widen_bf16(J->krope[r * J->rope_depth + (d + 1) % J->rope_depth]);"),
     "fp8_rope_scaled": ("dst[d8 + d] = widen_bf16(J->krope[r * J->rope_depth + d]);",
                         "dst[d8 + d] = ks * widen_bf16(J->krope[r * J->rope_depth + d]);"),
-    "fp8_separate_v_scaled": ("for (int d = 0; d < s->ov_depth; ++d) dst[d] = decode_e4m3(J->v8[r * s->ov_depth + d]);",
-                              "for (int d = 0; d < s->ov_depth; ++d) dst[d] = (J->kscale ? (double)J->kscale[r] : 1.0) * decode_e4m3(J->v8[r * s->ov_depth + d]);"),
-    "fp8_latent_v_unscaled": ("for (int d = 0; d < s->ov_depth; ++d) dst[d] = ks * decode_e4m3(J->k8[r * d8 + d]);",
-                              "for (int d = 0; d < s->ov_depth; ++d) dst[d] = decode_e4m3(J->k8[r * d8 + d]);"),
+    "fp8_separate_v_scaled": ("for (int d = 0; d < s->ov_depth; ++d) dst[d] = e4m3_table[J->v8[r * s->ov_depth + d]];",
+                              "for (int d = 0; d < s->ov_depth; ++d) dst[d] = (J->kscale ? (double)J->kscale[r] : 1.0) * e4m3_table[J->v8[r * s->ov_depth + d]];"),
+    "fp8_latent_v_unscaled": ("for (int d = 0; d < s->ov_depth; ++d) dst[d] = ks * e4m3_table[J->k8[r * d8 + d]];",
+                              "for (int d = 0; d < s->ov_depth; ++d) dst[d] = e4m3_table[J->k8[r * d8 + d]];"),
     "fp8_row_stride": ("const uint8_t* src = J->k8 + r * d8;", "const uint8_t* src = J->k8 + r * s->qk_depth;"),
 }
 
