@@ -430,6 +430,7 @@ def measure(spd, torch, w, dev, stream, steps, warmup, flush, clocks, keep=False
     if keep:
         m.h, m.step = h, step
         m.dev_tensors = (q, k, v, pt, lens, out, lse)
+        m.dev_scale = ks if e4m3 else None
     else:
         spd.fa_decode_destroy(h)
     return m
@@ -442,12 +443,14 @@ def host_enqueue_us(spd, torch, m, stream, calls: int = 50) -> dict:
     w, inp = m.w, m.inp
     q, k, v, pt, lens, out, lse = m.dev_tensors
     res = {}
-    for name in ("fa_decode_run", "fa_decode_run_noalloc"):
+    # the allocation-free entry point takes a bf16 cache only
+    names = ("fa_decode_run_kv",) if w.kv_dtype == "e4m3" else ("fa_decode_run", "fa_decode_run_noalloc")
+    for name in names:
         ts = []
         for _ in range(calls):
             t0 = time.perf_counter()
-            if name == "fa_decode_run":
-                spd.fa_decode_run(m.h, q, k, v, pt, lens, inp.scale, out, lse, stream=stream)
+            if name != "fa_decode_run_noalloc":
+                m.step()
             else:
                 spd.fa_decode_run_noalloc(w.num_q_heads, w.num_kv_heads, w.qk_depth, w.nope_depth, w.ov_depth,
                                           w.page_size, w.num_q, w.splitk, q, k, v, pt, lens, inp.scale, out, lse,
@@ -492,9 +495,10 @@ def run_gpu(args, world, rank, local):
     pin = lambda t: None if t is None else t.pin_memory()  # noqa: E731
     hq, hk, hv, hpt, hlens = pin(inp.q), pin(inp.k_pages), pin(inp.v_pages), pin(inp.page_table), \
         pin(inp.seq_lens)
+    hks, ks = pin(inp.k_scale), head.dev_scale
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hpt, hlens) if t is not None)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hpt, hlens, hks) if t is not None)
     d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
     e2e_steps = max(3, min(args.steps, 20))
 
@@ -505,6 +509,8 @@ def run_gpu(args, world, rank, local):
             v.copy_(hv, non_blocking=True)
         pt.copy_(hpt, non_blocking=True)
         lens.copy_(hlens, non_blocking=True)
+        if ks is not None:
+            ks.copy_(hks, non_blocking=True)
         head.step()
         hout.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)

@@ -99,28 +99,48 @@ struct TcCfg {
     static constexpr float RESCALE = FP8 ? 4.0f : 8.0f;
     // fp8 per-token K scales: a ring of KS entries of BN floats, by K tile.
     static constexpr int KS = FP8 ? (MULTI ? 8 : 4) : 0;
-    // Each product's 8 K-steps are spread over NACC independent accumulators
-    // (K-step ks accumulates into ks % NACC), so dependent MMAs form chains of
-    // depth 8 / NACC; readers sum the NACC partials. 16 columns per
-    // accumulator (N = 16): S[2 buffers][NACC] then O[2 buffers][NACC].
-    static constexpr int NACC = 4;
-    static constexpr int ACC_COLS = 16;
+    // bf16: each product's 8 K-steps are spread over NACC = 4 independent
+    // accumulators of N = 16 columns (K-step ks accumulates into ks % NACC),
+    // so dependent MMAs form chains of depth 2. fp8: the high and low E4M3
+    // parts of Q (of P) are the rows 0-15 and 16-31 of one N = 32 operand, so
+    // a product is 4 K-steps of 32 over NACC = 2 accumulators of 32 columns,
+    // half the MMA instructions (their issue bounds the tile rate). Either
+    // way a buffer is 64 columns holding four 16-column partials, and readers
+    // sum the four at a 16-column stride.
+    static constexpr int NACC = FP8 ? 2 : 4;
+    static constexpr int MMA_N = FP8 ? 32 : 16;
+    static constexpr int ACC_COLS = MMA_N;                        // columns of one accumulator
+    static constexpr int PART_COLS = 16;                          // reader stride between partials
     static constexpr int BUF_COLS = NACC * ACC_COLS;              // 64
-    static constexpr int TMEM_S0 = 0, TMEM_O0 = 2 * BUF_COLS;     // 0 / 128
-    static constexpr int TMEM_COLS = 4 * BUF_COLS;                // 256
+    // P and O buffers (by global tile index). Two: a buffer is reused two
+    // tiles later, so with two softmax warpgroups a warpgroup folds in its
+    // previous tile's O before it writes the next P. Four (two warpgroups,
+    // fp8, whose smaller ring leaves room): a warpgroup publishes a tile's P
+    // first and folds in the previous O after.
+    static constexpr int NPB = (NWG == 2 && FP8) ? 4 : 2;
+    // Fold in the previous tile's O before writing P (else after publishing it).
+    static constexpr bool FOLD_FIRST = NWG == 2 && NPB == 2;
+    static constexpr int TMEM_S0 = 0, TMEM_O0 = 2 * BUF_COLS;     // S [2], then O [NPB]
+    static constexpr int TMEM_COLS = (2 + NPB) * BUF_COLS <= 256 ? 256 : 512;
+    // Units with at least this many tiles per rank are issued two items per
+    // pass by the load warp (its per-item cost bounds them), shorter ones one
+    // at a time; measured: pairs for every unit on the fp8 kernel and the
+    // shallow ring, from 16 tiles on the bf16 deep ring.
+    static constexpr int PAIR_TILES = (FP8 || !MULTI) ? 0 : 16;
 
     static constexpr int Q_BUFS = MULTI ? 2 : 1;                  // by unit parity
     static constexpr int OFF_RING = 0;                            // NSLOT x 32 KB
     static constexpr int OFF_Q = NSLOT * TILE_BYTES;              // K-major SW128 [Q_BUFS][2 boxes][16][128 B]
     static constexpr int OFF_P = OFF_Q + Q_BUFS * Q_BYTES;        // [2 buffers][2 atoms][16][128 B]
-    static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;           // float [2][4][NRV]
+    static constexpr int OFF_RED = OFF_P + NPB * P_BYTES;         // float [2][4][NRV]
     static constexpr int OFF_MAXSUM = OFF_RED + 2 * 4 * NR * 4;   // float2 [NRV]
     static constexpr int OFF_BAR = OFF_MAXSUM + NR * 8;
     // barriers: slot_full[NSLOT], slot_empty[NSLOT], s_full[2], s_empty[2],
     // p_full[2], o_full[2], o_empty[2], q_full[2], q_empty[2], publish,
     // mma_done, tmem_ready, recv_full[2], recv_free[2], (spare)
-    // then (fp8) ks_full[KS], ks_empty[KS]
-    static constexpr int NBAR = 2 * NSLOT + 22 + 2 * KS;
+    // then (fp8) ks_full[KS], ks_empty[KS], then p_full[NPB], o_full[NPB],
+    // o_empty[NPB] (the pairs above at p_full / o_full / o_empty are unused)
+    static constexpr int NBAR = 2 * NSLOT + 22 + 2 * KS + 3 * NPB;
     static constexpr int OFF_ROWS = OFF_BAR + NBAR * 8;          // int [4 tiles][16 segments]
     static constexpr int OFF_MISC = OFF_ROWS + 4 * 16 * 4;       // tmem base, abort, S next item, O next item
     static constexpr int OFF_KS = (OFF_MISC + 16 + 127) / 128 * 128;      // float [KS][BN]
@@ -251,9 +271,6 @@ __device__ __forceinline__ void item_at(int j, int n, bool& is_v, int& t)
 // correction; P then stays below 2^RESCALE (2^8 for bf16; 2^4 for the fp8
 // split of P).
 
-// Units with at least this many tiles per rank are issued two items per pass
-// by the load warp (its issue rate bounds them); shorter ones one at a time.
-constexpr int kPairTiles = 16;
 
 // SK: the stream-K partition (DecodeParams::sk_tiles; deep ring only).
 // FP8: the E4M3 cache (DecodeParams::k_scale: per-token K scales or NULL).
@@ -348,12 +365,14 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
 
     const uint32_t bar0 = sbase + C::OFF_BAR;
     const uint32_t slot_full = bar0, slot_empty = bar0 + 8 * NSLOT;
-    const uint32_t s_full = bar0 + 16 * NSLOT, s_empty = s_full + 16, p_full = s_full + 32;
-    const uint32_t o_full = s_full + 48, o_empty = s_full + 64, q_full = s_full + 80, q_empty = s_full + 96;
+    const uint32_t s_full = bar0 + 16 * NSLOT, s_empty = s_full + 16;
+    const uint32_t q_full = s_full + 80, q_empty = s_full + 96;
     const uint32_t publish_bar = s_full + 112, mma_done = s_full + 120, tmem_ready = s_full + 128;
     const uint32_t recv_full = s_full + 136, recv_free = s_full + 152;
     // fp8: the per-token K scale ring (entry = global K tile index % KS)
     const uint32_t ks_full = bar0 + 8 * (2 * NSLOT + 22), ks_empty = ks_full + 8 * C::KS;
+    // P / O buffers, by global tile index gi: buffer gi % NPB, phase (gi / NPB) & 1
+    const uint32_t p_full = ks_empty + 8 * C::KS, o_full = p_full + 8 * C::NPB, o_empty = o_full + 8 * C::NPB;
     float* ks_s = reinterpret_cast<float*>(smem + C::OFF_KS);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -372,9 +391,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         for (int i = 0; i < 2; ++i) {
             mbar_init(s_full + 8 * i, 1);
             mbar_init(s_empty + 8 * i, 4);
-            mbar_init(p_full + 8 * i, 4);
-            mbar_init(o_full + 8 * i, 1);
-            mbar_init(o_empty + 8 * i, 4);
+
             mbar_init(q_full + 8 * i, 4);  // one arrival per softmax warp
             mbar_init(q_empty + 8 * i, 1);
         }
@@ -390,6 +407,11 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         for (int i = 0; i < C::KS; ++i) {
             mbar_init(ks_full + 8 * i, 1);   // the load warp's expect_tx arrive plus the copied bytes
             mbar_init(ks_empty + 8 * i, 4);  // the four softmax warps that read the tile's scales
+        }
+        for (int i = 0; i < C::NPB; ++i) {
+            mbar_init(p_full + 8 * i, 4);    // the four softmax warps that wrote P
+            mbar_init(o_full + 8 * i, 1);    // the O warp's commit
+            mbar_init(o_empty + 8 * i, 4);   // the four softmax warps that read O
         }
         *abort_flag = 0;
         *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 8) = 0;
@@ -544,7 +566,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                     if (J0 == 0) stamp(1);
                     if (lu < kTraceUnits) stamp(unit_slot(lu, 7));
                 }
-                if (tile_count >= kPairTiles) {
+                if (tile_count >= C::PAIR_TILES) {
                     for (int j = 0; ok && j < n_items; j += 2) ok = pass(j, std::true_type{});
                 } else {
                     for (int j = 0; ok && j < n_items; ++j) ok = pass(j, std::false_type{});
@@ -570,12 +592,12 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         if (lane == 0) {
             const bool is_s = (warp == 1);
             const uint32_t other_next = is_s ? o_next : s_next;
-            const uint32_t id_s = FP8 ? umma_idesc_e4m3_f32(128, C::NR, false, false)
-                                      : umma_idesc_bf16_f32(128, C::NR, false, false);
+            const uint32_t id_s = FP8 ? umma_idesc_e4m3_f32(128, C::MMA_N, false, false)
+                                      : umma_idesc_bf16_f32(128, C::MMA_N, false, false);
             const uint64_t q_desc0 = umma_smem_desc(sbase + C::OFF_Q, 16, 1024, kLayoutSwizzle128);
             const uint64_t k_desc0 = umma_smem_desc(sbase + C::OFF_RING, 16, 1024, kLayoutSwizzle128);
-            const uint32_t id_pv = FP8 ? umma_idesc_e4m3_f32(128, C::NR, true, false)
-                                       : umma_idesc_bf16_f32(128, C::NR, true, false);
+            const uint32_t id_pv = FP8 ? umma_idesc_e4m3_f32(128, C::MMA_N, true, false)
+                                       : umma_idesc_bf16_f32(128, C::MMA_N, true, false);
             // A = V^T, MN-major: 64-column atoms one box apart (LBO), 8-key groups 1024 B apart (SBO)
             const uint64_t v_desc0 = umma_smem_desc(sbase + C::OFF_RING, C::BOX_BYTES, 1024, kLayoutSwizzle128);
             // B = P, K-major: 64-key atoms of 16 rows x 128 B
@@ -618,12 +640,11 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                                             qd + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_s,
                                             ks >= C::NACC);
                         } else {
-                            // (16 Q_hi, Q_lo) x four K-steps of 32 depth columns, one accumulator
+                            // rows (16 Q_hi, Q_lo) x four K-steps of 32 depth columns
 #pragma unroll
-                            for (int ks = 0; ks < 8; ++ks)
-                                umma_f8_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)(((ks & 3) * 32) >> 4),
-                                           qd + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_s,
-                                           ks >= C::NACC);
+                            for (int ks = 0; ks < 4; ++ks)
+                                umma_f8_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)((ks * 32) >> 4),
+                                           qd + (uint64_t)((ks * 32) >> 4), id_s, ks >= C::NACC);
                         }
                         umma_commit(s_full + 8 * (gi & 1));
                         umma_commit(slot_empty + 8 * slot);  // K_i's slot is free once S_i has completed
@@ -637,15 +658,16 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                         const int gi = gt + t, j = J0 + v_item<C::VLAG>(t, tile_count), slot = j % NSLOT;
                         ok = ring_turn(j) &&
                              mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns) &&
-                             mbar_wait(p_full + 8 * (gi & 1), (gi >> 1) & 1, abort_flag, p.status, p.wait_limit_ns) &&
-                             (gi < 2 || mbar_wait(o_empty + 8 * (gi & 1), ((gi >> 1) - 1) & 1, abort_flag, p.status,
-                                                  p.wait_limit_ns));
+                             mbar_wait(p_full + 8 * (gi % C::NPB), (gi / C::NPB) & 1, abort_flag, p.status,
+                                       p.wait_limit_ns) &&
+                             (gi < C::NPB || mbar_wait(o_empty + 8 * (gi % C::NPB), ((gi / C::NPB) - 1) & 1,
+                                                       abort_flag, p.status, p.wait_limit_ns));
                         if (!ok) break;
                         if (gi == 0) stamp(62);
                         tc_fence_after_sync();
                         const uint64_t a0 = v_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
-                        const uint64_t b0 = p_desc0 + (uint64_t)(((gi & 1) * C::P_BYTES) >> 4);
-                        const uint32_t d = tmem + C::TMEM_O0 + C::BUF_COLS * (gi & 1);
+                        const uint64_t b0 = p_desc0 + (uint64_t)(((gi % C::NPB) * C::P_BYTES) >> 4);
+                        const uint32_t d = tmem + C::TMEM_O0 + C::BUF_COLS * (gi % C::NPB);
                         if constexpr (!FP8) {
 #pragma unroll
                             for (int ks = 0; ks < C::BN / 16; ++ks)
@@ -653,14 +675,13 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                                             b0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_pv,
                                             ks >= C::NACC);
                         } else {
-                            // (16 P_hi, P_lo) x four K-steps of 32 keys (four 8-key groups of V^T)
+                            // rows (16 P_hi, P_lo) x four K-steps of 32 keys (four 8-key groups of V^T)
 #pragma unroll
-                            for (int ks = 0; ks < 8; ++ks)
-                                umma_f8_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)(((ks & 3) * 4096) >> 4),
-                                           b0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_pv,
-                                           ks >= C::NACC);
+                            for (int ks = 0; ks < 4; ++ks)
+                                umma_f8_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)((ks * 4096) >> 4),
+                                           b0 + (uint64_t)((ks * 32) >> 4), id_pv, ks >= C::NACC);
                         }
-                        umma_commit(o_full + 8 * (gi & 1));
+                        umma_commit(o_full + 8 * (gi % C::NPB));
                         umma_commit(slot_empty + 8 * slot);  // V_t's slot is free once O_t has completed
                         st_release_u32(o_next, (uint32_t)(t + 1 < tile_count ? J0 + v_item<C::VLAG>(t + 1, tile_count)
                                                                              : J0 + 2 * tile_count));
@@ -820,10 +841,10 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             // O of this warpgroup's tile with global index gi has completed:
             // fold it into o_acc.
             auto correct = [&](int gi, const float (&a)[NRV], bool rescaled) {
-                mbar_wait(o_full + 8 * (gi & 1), (gi >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+                mbar_wait(o_full + 8 * (gi % C::NPB), (gi / C::NPB) & 1, abort_flag, p.status, p.wait_limit_ns);
                 tc_fence_after_sync();
                 float ot[NRV];
-                tmem_ld4_sum(tmem + lane_addr + C::TMEM_O0 + C::BUF_COLS * (gi & 1), C::ACC_COLS, ot);
+                tmem_ld4_sum(tmem + lane_addr + C::TMEM_O0 + C::BUF_COLS * (gi % C::NPB), C::PART_COLS, ot);
                 if constexpr (FP8) {
 #pragma unroll
                     for (int r = 0; r < NRV; ++r) ot[r] *= 0.0625f;  // the P split carries a factor 16
@@ -831,7 +852,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 tc_fence_before_sync();
                 __syncwarp();
                 // O has completed, so (for tile gi + 2) the P buffer it read is free.
-                if (lane == 0) mbar_arrive(o_empty + 8 * (gi & 1));
+                if (lane == 0) mbar_arrive(o_empty + 8 * (gi % C::NPB));
                 if (rescaled) {
 #pragma unroll
                     for (int r = 0; r < NRV; ++r) o_acc[r] = fmaf(o_acc[r], a[r], ot[r]);
@@ -858,7 +879,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 }
                 tc_fence_after_sync();
                 float s[NRV];
-                tmem_ld4_sum(tmem + lane_addr + C::TMEM_S0 + C::BUF_COLS * (gi & 1), C::ACC_COLS, s);
+                tmem_ld4_sum(tmem + lane_addr + C::TMEM_S0 + C::BUF_COLS * (gi & 1), C::PART_COLS, s);
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(s_empty + 8 * (gi & 1));
@@ -940,15 +961,16 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 }
 
                 // P (bf16) -> K-major swizzled B operand of O^T = V^T P^T (rows >= NRV
-                // only feed output columns that are never read). Buffer gi & 1 was
-                // last read by O of global tile gi - 2, whose completion the
-                // correction of that tile has observed: one warpgroup folded it in
-                // during its previous tile; two fold it in here, before the store.
-                if constexpr (C::NWG == 2) {
+                // only feed output columns that are never read). Buffer gi % NPB was
+                // last read by O of global tile gi - NPB, whose completion a
+                // correction has observed: one warpgroup folded it in during its
+                // previous tile, as do two with four buffers; two warpgroups with
+                // two buffers fold it in here, before the store.
+                if constexpr (C::FOLD_FIRST) {
                     if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
                 }
                 if constexpr (!FP8) {
-                    uint8_t* pb = smem + C::OFF_P + (gi & 1) * C::P_BYTES + (my_lane >> 6) * 2048;
+                    uint8_t* pb = smem + C::OFF_P + (gi % C::NPB) * C::P_BYTES + (my_lane >> 6) * 2048;
                     const int kk = my_lane & 63;
 #pragma unroll
                     for (int r = 0; r < NRV; ++r)
@@ -956,7 +978,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                                                           (kk & 7) * 2) = __float2bfloat16_rn(s[r]);
                 } else {
                     // P <= 16: the operands 16 e4m3(P) and e4m3(16 (P - e4m3(P))), [16 rows][128 keys]
-                    uint8_t* pb = smem + C::OFF_P + (gi & 1) * C::P_BYTES + (my_lane & 15);
+                    uint8_t* pb = smem + C::OFF_P + (gi % C::NPB) * C::P_BYTES + (my_lane & 15);
                     const int kc = my_lane >> 4;
 #pragma unroll
                     for (int r = 0; r < NRV; ++r) {
@@ -988,12 +1010,13 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(p_full + 8 * (gi & 1));
+                    mbar_arrive(p_full + 8 * (gi % C::NPB));
                     if (q_now) mbar_arrive(q_full + 8 * ((lu + 1) & 1));
                 }
                 q_pending = false;
 
-                if constexpr (C::NWG == 1) {
+                // Fold in this warpgroup's previous tile once this one's P is out.
+                if constexpr (!C::FOLD_FIRST) {
                     if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
                 }
 #pragma unroll
