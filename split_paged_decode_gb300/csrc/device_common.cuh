@@ -208,6 +208,19 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch (no-ops for a launch without the attribute)
+// ---------------------------------------------------------------------------
+// Wait until the grids this one depends on have completed and their memory
+// is visible; every read of an input a previous kernel may have written
+// comes after this.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next kernel in the stream to be scheduled once every CTA of this
+// grid has started (it still waits in grid_dependency_wait for this grid to
+// complete before it reads anything).
+__device__ __forceinline__ void grid_dependency_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// ---------------------------------------------------------------------------
 // Cluster and distributed shared memory
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank()

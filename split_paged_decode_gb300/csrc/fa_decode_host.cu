@@ -20,6 +20,10 @@ namespace {
 
 thread_local std::string g_last_error;
 
+// The one-launch per-sequence split reads every length in every CTA; above
+// this batch the planner keeps one launch per cluster size.
+constexpr int kDynSplitMaxBatch = 4096;
+
 int fail(int code, const char* fmt, ...)
 {
     char buf[512];
@@ -565,11 +569,13 @@ int fa_decode_describe(fa_decode_t h, char* buf, int size)
     const fad::KernelGeometry& g =
         h->has_mla ? h->geo_mla : (h->has_tc ? (h->splitk > 0 ? h->geo_tc_big : h->geo_tc) : h->geo);
     const int rows = h->has_mla ? 64 : h->rows, row_blocks = h->has_mla ? h->group / 64 : h->row_blocks;
+    const char* per_seq = h->splitk != 0 ? "" : (h->has_tc && !h->has_mla ? "(per sequence: 1/2/4, one launch)"
+                                                                         : "(per sequence: 1/2/4)");
     snprintf(buf, (size_t)size,
              "path=%s kernel=%s simt_kernel=%s latent_kernel=%s splitk=%d%s threads=%d keys_per_tile=%d "
              "stages=%d rows=%d rows_capacity=%d row_blocks=%d smem=%d resident_clusters=%d",
              tc ? "tcgen05" : "simt", g.name, h->has_simt ? h->geo.name : "none",
-             h->has_latent ? h->geo_latent.name : "none", h->splitk, h->splitk == 0 ? "(per sequence: 1/2/4)" : "",
+             h->has_latent ? h->geo_latent.name : "none", h->splitk, per_seq,
              g.threads, g.keys_per_tile, g.stages, rows, h->has_mla ? 64 : h->rows_capacity, row_blocks, g.smem_bytes,
              h->tc_big_clusters);
     return FA_OK;
@@ -722,7 +728,18 @@ int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const vo
     p.k_scale = k_scale;
 
     int splits[3];
-    const int ns = split_list(h, splits);
+    int ns = split_list(h, splits);
+    // The per-sequence split on the tcgen05 shallow ring runs as one launch of
+    // 4-CTA clusters, each serving one unit of split 4, two of split 2 or four
+    // of split 1 (chosen on the device from the lengths; see dyn_group); the
+    // other kernels launch once per cluster size.
+    const bool dyn = h->splitk == 0 && use_tc && batch <= kDynSplitMaxBatch;
+    if (dyn) {
+        splits[0] = 4;
+        ns = 1;
+        p.auto_split = 0;
+        p.dyn_split = 1;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // Fork: launches after the first go to the side streams, which first wait
     // for everything queued on the caller's stream.
@@ -737,13 +754,14 @@ int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const vo
         p.splitk = P;
         p.band_cols = h->dv / P;
         p.out_chunk_cols = p.band_cols < 256 ? p.band_cols : 256;
+        if (dyn) p.out_chunk_cols = h->dv / 4;  // stores in boxes of the narrowest band (split 4)
         rc = encode_out_map(h->out_map[i], out, h->dv, h->hq, (int64_t)batch * h->num_q, p.out_chunk_cols,
                             heads_per_cta, h->tokens_per_cta);
         if (rc) return rc;
         p.tm_out = h->out_map[i].map;
 
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         // Cluster c (= blockIdx.y + gridDim.y * blockIdx.z) takes units
         // c, c + G, ... of u = b * Hkv + kvh (with G = units that is one unit
         // each), or the units its stream-K range touches.
@@ -751,13 +769,19 @@ int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const vo
         cfg.blockDim = dim3(g.threads, 1, 1);
         cfg.dynamicSmemBytes = g.smem_bytes;
         cfg.stream = forked && i > 0 ? h->side[i - 1] : s;
+        // Programmatic dependent launch: the kernel may be scheduled while the
+        // previous kernel in the stream finishes; it waits for that kernel's
+        // completion (griddepcontrol.wait) before reading any input.
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
         if (P > 1) {
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = P;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = P;
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.numAttrs = 2;
         }
         void* args[1] = {&p};
         cudaError_t e = cudaLaunchKernelExC(&cfg, g.func, args);

@@ -52,6 +52,7 @@ struct DecodeParams {
     int tokens_per_cta;  // tokens covered by one CTA (T, or 1 when row-blocked)
     int splitk;          // cluster size P of this launch
     int auto_split;      // 1: a cluster works on sequence b only if auto_split_for_len(L_b) == P
+    int dyn_split;       // 1: per-sequence split in one launch of 4-CTA clusters (tcgen05 shallow ring)
     int box_rows;        // key rows per K/V TMA box: min(page_size, keys per tile)
     int band_cols;       // output columns owned by one cluster rank: Dv / P
     int out_chunk_cols;  // columns per output TMA store box: min(band_cols, 256)

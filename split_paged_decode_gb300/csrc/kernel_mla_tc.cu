@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
         if (trace) trace[slot] = global_timer_ns();
     };
     if (tid == 0) stamp(0);
+    grid_dependency_wait();  // inputs may come from the previous kernel in the stream
+    grid_dependency_launch();
 
     int L = p.seq_lens[b];
     if (L < 0) {

@@ -91,6 +91,8 @@ __global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREA
     const int kvh = (int)blockIdx.y / p.row_blocks;
     const int row_block = (int)blockIdx.y % p.row_blocks;
     const int b = (int)blockIdx.z;
+    grid_dependency_wait();  // inputs may come from the previous kernel in the stream
+    grid_dependency_launch();
 
     int L = p.seq_lens[b];
     if (L < 0) {

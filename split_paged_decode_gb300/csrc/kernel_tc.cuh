@@ -201,6 +201,67 @@ __device__ __forceinline__ bool next_unit(const DecodeParams& p, int stride, int
     return false;
 }
 
+// The per-sequence split in one launch (FA4Config page, field
+// dynamic_cluster_dim: the cluster size a sequence uses is chosen at run
+// time). Every cluster has 4 CTAs. The (sequence, kv head) units are ordered
+// by the split their sequence takes (4, then 2, then 1; by unit index within
+// a split) and cut into groups: one unit of split 4, two of split 2 or four of
+// split 1; cluster c serves group c. Each CTA learns its unit, its split P,
+// its partition index within the unit and the cluster rank of the unit's
+// first partition; a CTA of a group that runs out of units is idle (it takes
+// part in the cluster barriers only). Called by every lane of a warp; every
+// warp of every CTA of the cluster reaches the same answer.
+struct DynSlot {
+    bool active;  // the cluster serves a group
+    bool idle;    // this CTA serves no unit of it
+    int P, rank, rbase, u;
+};
+
+__device__ __forceinline__ DynSlot dyn_group(const DecodeParams& p, int c, int x)
+{
+    const int lane = threadIdx.x & 31;
+    // Sequences per split class, 32 at a time.
+    int n4 = 0, n2 = 0, n1 = 0;
+    for (int b0 = 0; b0 < p.batch; b0 += 32) {
+        const int b = b0 + lane;
+        const int P = b < p.batch ? auto_split_for_len(max(p.seq_lens[b], 0)) : 0;
+        n4 += __popc(__ballot_sync(0xffffffffu, P == 4));
+        n2 += __popc(__ballot_sync(0xffffffffu, P == 2));
+        n1 += __popc(__ballot_sync(0xffffffffu, P == 1));
+    }
+    const int H = p.num_kv_heads;
+    const int g4 = n4 * H, g2 = (n2 * H + 1) / 2, g1 = (n1 * H + 3) / 4;
+    DynSlot d{false, true, 1, 0, 0, 0};
+    int cls, k;  // split class and the index of this CTA's unit within it
+    if (c < g4) {
+        cls = 4; k = c;
+    } else if (c < g4 + g2) {
+        cls = 2; k = 2 * (c - g4) + x / 2;
+    } else if (c < g4 + g2 + g1) {
+        cls = 1; k = 4 * (c - g4 - g2) + x;
+    } else {
+        return d;  // the same for every CTA of the cluster
+    }
+    d.active = true;
+    d.P = cls;
+    d.rank = x % cls;
+    d.rbase = x - d.rank;
+    if (k >= (cls == 4 ? n4 : cls == 2 ? n2 : n1) * H) return d;  // idle
+    // The (k / H)-th sequence of the class, kv head k % H.
+    int want = k / H, b_sel = -1;
+    for (int b0 = 0; b0 < p.batch && b_sel < 0; b0 += 32) {
+        const int b = b0 + lane;
+        const int P = b < p.batch ? auto_split_for_len(max(p.seq_lens[b], 0)) : 0;
+        const unsigned m = __ballot_sync(0xffffffffu, P == cls);
+        const int n = __popc(m);
+        if (want < n) b_sel = b0 + (int)__fns(m, 0, want + 1);
+        else want -= n;
+    }
+    d.idle = false;
+    d.u = b_sel * H + k % H;
+    return d;
+}
+
 // Warp reduce-scatter of N per-row values (max or sum over the warp's 32
 // lanes): recursive halving exchanges half of the remaining rows at each of
 // the first log2(N) steps, then a butterfly finishes. On return v[0] holds
@@ -288,8 +349,11 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int P = p.splitk;
-    const int rank = (int)blockIdx.x;
+    const int CL = p.splitk;  // CTAs per cluster
+    // This CTA's split partition: P partitions of a unit, this one `rank`, the
+    // unit's first partition at cluster rank rbase (0 unless the cluster
+    // serves several units of a smaller split, see dyn_group).
+    int P = CL, rank = (int)blockIdx.x, rbase = 0;
     const int n_units = p.batch * p.num_kv_heads;
     const int cluster_id = (int)(blockIdx.y + gridDim.y * blockIdx.z);
     const int n_clusters = (int)(gridDim.y * gridDim.z);
@@ -303,6 +367,22 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         u_first = (int)(sk_g0 / p.sk_tiles);
         u_end = sk_g1 > sk_g0 ? (int)((sk_g1 - 1) / p.sk_tiles) + 1 : u_first;
         u_step = 1;
+    }
+
+    bool idle = false;  // (dynamic groups) this CTA serves no unit
+    if constexpr (!C::MULTI) {
+        if (p.dyn_split) {
+            grid_dependency_wait();  // seq_lens may come from the previous kernel
+            const DynSlot d = dyn_group(p, cluster_id, (int)blockIdx.x);
+            if (!d.active) return;  // the same in every CTA of the cluster
+            P = d.P;
+            rank = d.rank;
+            rbase = d.rbase;
+            idle = d.idle;
+            u_first = idle ? 0 : d.u;
+            u_end = idle ? 0 : d.u + 1;
+            u_step = 1;
+        }
     }
 
     // Optional timeline trace (a profiling aid): one thread writes each event.
@@ -344,6 +424,8 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
     const int segs = C::BN / p.box_rows;  // page segments per tile: 1, 2, 4, 8 or 16
     const int tpb = 32 / segs;            // tiles per block of page entries
     int spec_begin = -1, spec_count = 0, spec_raw = -1;
+    grid_dependency_wait();  // inputs may come from the previous kernel in the stream
+    grid_dependency_launch();
     if (warp == 0 && u_first < u_end && p.max_pages <= INT32_MAX / C::BN / p.page_size) {
         int gb, gc;
         rank_tiles(u_first, p.max_pages * p.page_size, gb, gc);
@@ -354,7 +436,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         const int pslot = ((gb + t) * C::BN + (lane % segs) * p.box_rows) / p.page_size;
         if (t < gc && pslot < p.max_pages) spec_raw = p.page_table[(int64_t)b0 * p.max_pages + pslot];
     }
-    if (u_first >= u_end) return;  // (grids never have more clusters than units or ranges)
+    if (u_first >= u_end && !idle) return;  // (grids never have more clusters than units or ranges)
     if (p.auto_split) {
         // A cluster with no unit in this launch (the per-sequence split gives
         // its sequences to another launch) leaves at once; the decision is the
@@ -395,7 +477,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             mbar_init(q_full + 8 * i, 4);  // one arrival per softmax warp
             mbar_init(q_empty + 8 * i, 1);
         }
-        mbar_init(publish_bar, P);
+        mbar_init(publish_bar, P);  // the unit's partitions
         mbar_init(mma_done, 2);
         mbar_init(tmem_ready, 1);
         for (int i = 0; i < 2; ++i) {
@@ -421,7 +503,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
     __syncthreads();  // barriers initialised; the load warp may start at once
     // Peers arrive on this CTA's publish barrier only after the matching
     // cluster wait (before the first merge), so the prologue does not wait here.
-    if (P > 1) cluster_arrive_relaxed();
+    if (CL > 1) cluster_arrive_relaxed();
     uint32_t tmem = 0;
     if (warp == 1) {
         tmem_alloc(sbase + C::OFF_MISC, C::TMEM_COLS);
@@ -1092,7 +1174,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 }
             }
             if (lead) {
-                const int BW = p.band_cols;
+                const int BW = p.ov_depth / P;  // this partition's output band
                 const int dv = my_lane;
                 if constexpr (C::MULTI) {
                     // Push this rank's normalised partial into the band owners'
@@ -1158,14 +1240,14 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                     }
                     if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
                     named_barrier_sync(wg_bar, 128);
-                    if (P > 1) {
+                    if (CL > 1) {
                         cluster_wait();  // every rank's publish barrier is initialised
                         cluster_waited = true;
                     }
                     if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 4));
                     splitk_merge_and_store<NRV>(p, P, rank, w.b, w.kvh, 0, stage_s, maxsum_s,
                                                 reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), publish_bar, 0u,
-                                                0u, abort_flag, wt, 128, wg_bar);
+                                                0u, abort_flag, wt, 128, wg_bar, rbase, BW);
                     if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 5));
                 }
             }
@@ -1175,7 +1257,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             if (named_barrier_or(C::NWG == 2 ? 3 : wg_bar, 128 * C::NWG, seen_abort) || !more) break;
             w = nx;
         }
-        if (P > 1 && !cluster_waited) cluster_wait();  // pairs with the early arrive
+        if (CL > 1 && !cluster_waited) cluster_wait();  // pairs with the early arrive
         tc_fence_before_sync();
     } else {
         // ------------------------------------------- epilogue warp (multi-unit variant)
@@ -1249,9 +1331,9 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         for (int g = ks_issued > C::KS ? ks_issued - C::KS : 0; g < ks_issued; ++g)
             mbar_wait(ks_full + 8 * (g % C::KS), (g / C::KS) & 1, &keep_waiting, p.status, p.wait_limit_ns);
     }
-    if (P > 1 && warp < C::WG0) cluster_wait();  // pairs with the early arrive (the other warps waited above)
+    if (CL > 1 && warp < C::WG0) cluster_wait();  // pairs with the early arrive (the other warps waited above)
     __syncwarp();
-    if (P > 1) cluster_sync_all();  // peers may still read this CTA's staged bands until here
+    if (CL > 1) cluster_sync_all();  // peers may still read this CTA's staged bands until here
     if (tid == 0) stamp(3);
 }
 

@@ -45,15 +45,21 @@ namespace fad {
 // cannot reach a rank before that rank's unit-n phase has completed (it would
 // need that rank's reads of the peer's unit-n stage), so one publish barrier
 // alternates parity safely. stage_free_bar == 0: a single unit, no arrivals.
+//
+// The P partitions are the cluster ranks rbase .. rbase + P - 1 (rbase > 0
+// when a cluster serves several units of a smaller split; `rank` is this
+// CTA's index among them), each owning bw = Dv / P output columns (bw 0: the
+// launch's band width).
 template <int RB>
 __device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, int P, int rank, int b,
                                                        int kvh, int row_block, const float* stage_s,
                                                        const float2* maxsum_s, uint16_t* out_s,
                                                        uint32_t publish_bar, uint32_t publish_parity,
                                                        uint32_t stage_free_bar, volatile int* abort_flag,
-                                                       int tid, int nthreads, uint32_t bar_id)
+                                                       int tid, int nthreads, uint32_t bar_id, int rbase = 0,
+                                                       int bw = 0)
 {
-    const int BW = p.band_cols;
+    const int BW = bw > 0 ? bw : p.band_cols;
     const float c = p.scale_log2e;
     const uint32_t stage_base = smem_addr(stage_s);
     const uint32_t maxsum_base = smem_addr(maxsum_s);
@@ -63,7 +69,7 @@ __device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, in
             // Round 1: every rank tells every rank (itself included) that its
             // stage is complete. The preceding CTA barrier orders the other
             // threads' staging writes before this release.
-            for (int q = 0; q < P; ++q) mbar_arrive_cluster(map_shared_rank(publish_bar, q));
+            for (int q = 0; q < P; ++q) mbar_arrive_cluster(map_shared_rank(publish_bar, rbase + q));
         }
         mbar_wait<true>(publish_bar, publish_parity, abort_flag, p.status, p.wait_limit_ns);
     }
@@ -75,7 +81,7 @@ __device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, in
         float mq[kMaxSplit], wq[kMaxSplit];
         float gmax = -INFINITY;
         for (int q = 0; q < P; ++q) {
-            float2 ms = (P > 1) ? ld_dsmem_f2(map_shared_rank(maxsum_base + 8u * r, q)) : maxsum_s[r];
+            float2 ms = (P > 1) ? ld_dsmem_f2(map_shared_rank(maxsum_base + 8u * r, rbase + q)) : maxsum_s[r];
             mq[q] = ms.x;
             wq[q] = ms.y;
             if (ms.y > 0.f) gmax = fmaxf(gmax, ms.x);
@@ -92,7 +98,7 @@ __device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, in
         const uint32_t off = 4u * ((uint32_t)(rank * RB + r) * BW + j);
         for (int q = 0; q < P; ++q) {
             if (wq[q] <= 0.f) continue;
-            float4 v = (P > 1) ? ld_dsmem_f4(map_shared_rank(stage_base + off, q))
+            float4 v = (P > 1) ? ld_dsmem_f4(map_shared_rank(stage_base + off, rbase + q))
                                : *reinterpret_cast<const float4*>(stage_s + (rank * RB + r) * BW + j);
             const float w = wq[q] * inv;
             o.x = fmaf(w, v.x, o.x);
@@ -122,7 +128,7 @@ __device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, in
         // band); release the peers' stages for their next unit.
         if (stage_free_bar != 0) {
             if (P > 1)
-                for (int q = 0; q < P; ++q) mbar_arrive_cluster(map_shared_rank(stage_free_bar, q));
+                for (int q = 0; q < P; ++q) mbar_arrive_cluster(map_shared_rank(stage_free_bar, rbase + q));
             else
                 mbar_arrive(stage_free_bar);
         }

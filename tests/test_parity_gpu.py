@@ -408,3 +408,76 @@ def test_run_rejects_misaligned_pointer():
                               call.out, call.lse, batch=3, max_pages_per_seq=call.pt.shape[1],
                               num_pages=call.k.shape[0])
         assert e.value.code == spd.FA_ERR_INVALID_ARG
+
+
+# --- the per-sequence split in one launch, and programmatic dependent launch -------------
+
+def _split_of(L):
+    return 1 if L <= 1024 else (2 if L <= 4096 else 4)
+
+
+@pytest.mark.parametrize("hkv,lens", [
+    (1, [5000, 2000, 3000, 4000, 10, 20, 30, 40, 50]),        # 1 unit of split 4, 3 of 2, 5 of 1: idle CTAs
+    (3, [100, 2500, 9000, 1024, 1025, 4096, 4097, 1]),        # odd kv heads
+    (2, [1, 2, 3, 4, 5, 6, 7]),                               # split 1 only
+    (2, [8000, 6000, 5000]),                                  # split 4 only
+    (2, [0, 3000, 0, 700, 0]),                                # empty sequences between
+])
+def test_per_sequence_split_one_launch(hkv, lens):
+    """4-CTA clusters serving one unit of split 4, two of split 2 or four of
+    split 1, chosen on the device; groups that run out of units leave CTAs idle."""
+    w = wl(batch=len(lens), num_q=4, num_q_heads=4 * hkv, num_kv_heads=hkv, splitk=0, seq_len_lo=1,
+           seq_len_hi=9000, seed=190 + hkv)
+    inp = generate(w, seq_lens=lens)
+    with DeviceCall(inp) as call:
+        assert "one launch" in call.describe(), call.describe()
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what=f"one-launch split hkv{hkv}")
+
+
+def test_one_launch_split_is_one_kernel():
+    """The per-sequence split on the tensor-core path is one launch: the
+    per-CTA trace (which holds the last launch of a call) shows an entry for
+    exactly the 4 CTAs of every group of units, and no other."""
+    lens = [5000, 2000, 3000, 10, 20, 30, 4097, 1025, 700]
+    w = wl(batch=len(lens), num_q=4, num_q_heads=8, num_kv_heads=2, splitk=0, seq_len_lo=1, seq_len_hi=9000,
+           seed=195)
+    inp = generate(w, seq_lens=lens)
+    H = w.num_kv_heads
+    n = {P: sum(1 for L in lens if _split_of(L) == P) * H for P in (1, 2, 4)}
+    groups = n[4] + (n[2] + 1) // 2 + (n[1] + 3) // 4
+    with DeviceCall(inp) as call:
+        ctas = 4 * w.batch * H
+        buf = torch.zeros(ctas * spd.FA_TRACE_WORDS_PER_CTA, dtype=torch.int64, device="cuda")
+        spd.fa_decode_set_trace(call.h, buf)
+        call.run()
+        assert call.status() == 0
+        entered = int((buf.view(ctas, -1)[:, 0] > 0).sum())
+        assert entered == 4 * groups, (entered, groups)
+        spd.fa_decode_set_trace(call.h, None)
+        check_against_oracle(call, what="one-launch split, traced")
+
+
+@pytest.mark.parametrize("splitk", [4, 0])
+def test_chained_launches_read_the_previous_output(splitk):
+    """Programmatic dependent launch: a decode whose queries are the previous
+    decode's output, enqueued back to back on one stream, reads that output
+    only once it is complete."""
+    w = wl(batch=6, num_q=1, num_q_heads=8, num_kv_heads=2, splitk=splitk, seq_len_lo=500, seq_len_hi=9000,
+           seed=196 + splitk)
+    inp = generate(w)
+    with DeviceCall(inp) as a, DeviceCall(inp) as b:
+        b.q = a.out  # [B, T, Hq, 128]: the first decode's output is the second's queries
+        for _ in range(3):
+            a.out.fill_(float("nan"))
+            b.out.fill_(float("nan"))
+            a.run()
+            b.run()
+            torch.cuda.synchronize()
+            assert a.status() == 0 and b.status() == 0
+            check_against_oracle(a, what="chain first")
+            chained = generate(w)
+            chained.q = a.out.cpu()
+            b.inp = chained
+            check_against_oracle(b, what="chain second")
