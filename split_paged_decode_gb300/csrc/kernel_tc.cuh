@@ -120,8 +120,14 @@ struct TcCfg {
     static constexpr int NPB = (NWG == 2 && FP8) ? 4 : 2;
     // Fold in the previous tile's O before writing P (else after publishing it).
     static constexpr bool FOLD_FIRST = NWG == 2 && NPB == 2;
+    // Two warpgroups keep their O in tensor memory, one fragment each (the
+    // two TMEM_O fragments of the fa4_lse_combine_write page): the O MMA
+    // accumulates a warpgroup's tiles straight into its fragment, a moved max
+    // rescales the fragment in place, and at the end of a unit each
+    // warpgroup combines both fragments for half of the rows.
+    static constexpr bool TMEM_O = NWG == 2;
     static constexpr int TMEM_S0 = 0, TMEM_O0 = 2 * BUF_COLS;     // S [2], then O [NPB]
-    static constexpr int TMEM_COLS = (2 + NPB) * BUF_COLS <= 256 ? 256 : 512;
+    static constexpr int TMEM_COLS = (TMEM_O || (2 + NPB) * BUF_COLS <= 256) ? 256 : 512;
     // Units with at least this many tiles per rank are issued two items per
     // pass by the load warp (its per-item cost bounds them), shorter ones one
     // at a time; measured: pairs for every unit on the fp8 kernel and the
@@ -159,10 +165,10 @@ struct TcCfg {
     static constexpr int OFF_WTAB = OFF_RECV + RECV_BUFS * RECV_BYTES;
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_OUT = MULTI ? (OFF_WTAB + kMaxSplit * NRV * 4 + 127) / 128 * 128 : TILE_BYTES;
-    // Two softmax warpgroups: the second's partial O [128 dv][NRV] and (max, sum) [NRV].
-    static constexpr int XCHG_O_BYTES = NWG == 2 ? D * NRV * 4 : 0;
+    // Two softmax warpgroups: (max, sum) [2][NRV] of both (TMEM_O).
+    static constexpr int XCHG_O_BYTES = 0;
     static constexpr int OFF_XCHG = OFF_OUT + OUT_BYTES;
-    static constexpr int END_MULTI = OFF_XCHG + (NWG == 2 ? XCHG_O_BYTES + NRV * 8 : 0);
+    static constexpr int END_MULTI = OFF_XCHG + (NWG == 2 ? 2 * NRV * 8 : 0);
     static constexpr int SMEM_BYTES = (MULTI ? END_MULTI : MISC_END) + 1024;
     static_assert(NSLOT >= 2, "ring of at least one K and one V tile");
     static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms on 1024 bytes");
@@ -483,7 +489,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         for (int i = 0; i < 2; ++i) {
             // P > 1: the epilogue warp's expect_tx arrive plus the pushed bytes;
             // P == 1: the epilogue warp and the four softmax warps arrive.
-            mbar_init(recv_full + 8 * i, P > 1 ? 1 : 5);
+            mbar_init(recv_full + 8 * i, P > 1 ? 1 : 1 + 4 * C::NWG);
             mbar_init(recv_free + 8 * i, P);  // one arrival per receiving rank
         }
         for (int i = 0; i < C::KS; ++i) {
@@ -493,7 +499,8 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         for (int i = 0; i < C::NPB; ++i) {
             mbar_init(p_full + 8 * i, 4);    // the four softmax warps that wrote P
             mbar_init(o_full + 8 * i, 1);    // the O warp's commit
-            mbar_init(o_empty + 8 * i, 4);   // the four softmax warps that read O
+            // the four softmax warps that read O; TMEM_O: the eight that read both fragments
+            mbar_init(o_empty + 8 * i, C::TMEM_O ? 8 : 4);
         }
         *abort_flag = 0;
         *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 8) = 0;
@@ -738,32 +745,43 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 } else {
                     for (int t = 0; ok && t < tile_count; ++t) {
                         const int gi = gt + t, j = J0 + v_item<C::VLAG>(t, tile_count), slot = j % NSLOT;
+                        // TMEM_O: tile t goes to the fragment of warpgroup t % 2, whose
+                        // first tile of a unit overwrites it once both warpgroups have
+                        // read it for the previous unit (o_empty[f], one phase per unit).
+                        const int frag = t % 2;
+                        const bool frag_first = t < 2;
                         ok = ring_turn(j) &&
                              mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns) &&
                              mbar_wait(p_full + 8 * (gi % C::NPB), (gi / C::NPB) & 1, abort_flag, p.status,
                                        p.wait_limit_ns) &&
-                             (gi < C::NPB || mbar_wait(o_empty + 8 * (gi % C::NPB), ((gi / C::NPB) - 1) & 1,
-                                                       abort_flag, p.status, p.wait_limit_ns));
+                             (C::TMEM_O
+                                  ? (!frag_first || lu == 0 ||
+                                     mbar_wait(o_empty + 8 * frag, (lu - 1) & 1, abort_flag, p.status, p.wait_limit_ns))
+                                  : (gi < C::NPB || mbar_wait(o_empty + 8 * (gi % C::NPB), ((gi / C::NPB) - 1) & 1,
+                                                              abort_flag, p.status, p.wait_limit_ns)));
                         if (!ok) break;
                         if (gi == 0) stamp(62);
                         tc_fence_after_sync();
                         const uint64_t a0 = v_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
                         const uint64_t b0 = p_desc0 + (uint64_t)(((gi % C::NPB) * C::P_BYTES) >> 4);
-                        const uint32_t d = tmem + C::TMEM_O0 + C::BUF_COLS * (gi % C::NPB);
+                        const uint32_t d =
+                            tmem + C::TMEM_O0 + C::BUF_COLS * (C::TMEM_O ? frag : (gi % C::NPB));
+                        // TMEM_O: every tile but the fragment's first of the unit accumulates.
+                        const bool acc_all = C::TMEM_O && !frag_first;
                         if constexpr (!FP8) {
 #pragma unroll
                             for (int ks = 0; ks < C::BN / 16; ++ks)
                                 umma_f16_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)((ks * 2048) >> 4),
                                             b0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_pv,
-                                            ks >= C::NACC);
+                                            acc_all || ks >= C::NACC);
                         } else {
                             // rows (16 P_hi, P_lo) x four K-steps of 32 keys (four 8-key groups of V^T)
 #pragma unroll
                             for (int ks = 0; ks < 4; ++ks)
                                 umma_f8_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)((ks * 4096) >> 4),
-                                           b0 + (uint64_t)((ks * 32) >> 4), id_pv, ks >= C::NACC);
+                                           b0 + (uint64_t)((ks * 32) >> 4), id_pv, acc_all || ks >= C::NACC);
                         }
-                        umma_commit(o_full + 8 * (gi % C::NPB));
+                        umma_commit(o_full + 8 * (C::TMEM_O ? frag : (gi % C::NPB)));
                         umma_commit(slot_empty + 8 * slot);  // V_t's slot is free once O_t has completed
                         st_release_u32(o_next, (uint32_t)(t + 1 < tile_count ? J0 + v_item<C::VLAG>(t + 1, tile_count)
                                                                              : J0 + 2 * tile_count));
@@ -875,6 +893,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         bool seen_abort = false;  // sticky: this thread has seen the abort flag
         bool cluster_waited = false;
         int J0 = 0, gt = 0, lu = 0;
+        int wc = 0;  // TMEM_O: this warpgroup's tiles so far (phases of its o_full barrier)
         while (have) {
             const int L = w.L;
             int tile_begin, tile_count;
@@ -952,6 +971,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             const int i0 = C::NWG == 2 ? wg : 0;
             const int gt0 = gt;
             int prev_gi = -1;  // this warpgroup's previous tile, still to be folded in
+            int wc_unit = 0;   // TMEM_O: this warpgroup's tiles of the unit so far
             for (int i = i0; i < tile_count; i += C::NWG) {
                 const int gi = gt + i;
                 mbar_wait(s_full + 8 * (gi & 1), (gi >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
@@ -1048,7 +1068,18 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 // correction has observed: one warpgroup folded it in during its
                 // previous tile, as do two with four buffers; two warpgroups with
                 // two buffers fold it in here, before the store.
-                if constexpr (C::FOLD_FIRST) {
+                if constexpr (C::TMEM_O) {
+                    // The fragment's previous O product read the P buffer this tile
+                    // reuses, and must finish before a rescale touches the fragment.
+                    if (wc_unit > 0) {
+                        mbar_wait(o_full + 8 * wg, (wc - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+                        tc_fence_after_sync();
+                        if (rescale) {
+                            tmem_scale4<NRV>(tmem + lane_addr + C::TMEM_O0 + C::BUF_COLS * wg, C::PART_COLS, alpha);
+                            tc_fence_before_sync();
+                        }
+                    }
+                } else if constexpr (C::FOLD_FIRST) {
                     if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
                 }
                 if constexpr (!FP8) {
@@ -1098,7 +1129,10 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 q_pending = false;
 
                 // Fold in this warpgroup's previous tile once this one's P is out.
-                if constexpr (!C::FOLD_FIRST) {
+                if constexpr (C::TMEM_O) {
+                    ++wc;
+                    ++wc_unit;
+                } else if constexpr (!C::FOLD_FIRST) {
                     if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
                 }
 #pragma unroll
@@ -1108,7 +1142,14 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             }
             // Bounded even after an abort. After an abort the O of the tile
             // that broke the loop was never issued; the wait gives up at once.
-            if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
+            if constexpr (C::TMEM_O) {
+                if (wc_unit > 0) {  // the fragment's last product is complete
+                    mbar_wait(o_full + 8 * wg, (wc - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+                    tc_fence_after_sync();
+                }
+            } else {
+                if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
+            }
             if (lead && wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 2));
             gt += tile_count;
             J0 += 2 * tile_count;
@@ -1133,47 +1174,104 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             float lrow[NRV];
 #pragma unroll
             for (int r = 0; r < NRV; ++r) lrow[r] = red_w[r] + red_w[NRV + r] + red_w[2 * NRV + r] + red_w[3 * NRV + r];
-            if constexpr (C::NWG == 2) {
-                // Fold the second warpgroup's partial into the first's:
-                // m = max(m_a, m_b), both sides scaled by exp2((m_x - m) * c).
-                float* xo = reinterpret_cast<float*>(smem + C::OFF_XCHG);          // [128 dv][NRV]
-                float2* xms = reinterpret_cast<float2*>(smem + C::OFF_XCHG + C::XCHG_O_BYTES);  // [NRV]
-                if (!lead) {
-                    // The first warpgroup has read the previous unit's exchange.
-                    if (lu >= 1) named_barrier_sync(4, 256);
+            if constexpr (C::TMEM_O) {
+                // Combine the two warpgroups' O fragments (fa4_lse_combine_write
+                // page): per row m = max(m_0, m_1), l = sum_w l_w exp2((m_w - m) c)
+                // and the final scales f_w = exp2((m_w - m) c) / l (own and peer);
+                // warpgroup w combines and pushes rows [w NRV / 2, (w + 1) NRV / 2),
+                // disjoint column ranges of both fragments.
+                float2* xms = reinterpret_cast<float2*>(smem + C::OFF_XCHG);  // [2][NRV]
+                if (wt == 0)
 #pragma unroll
-                    for (int r4 = 0; r4 < NRV / 4; ++r4)
-                        reinterpret_cast<float4*>(xo + my_lane * NRV)[r4] =
-                            make_float4(o_acc[4 * r4], o_acc[4 * r4 + 1], o_acc[4 * r4 + 2], o_acc[4 * r4 + 3]);
-                    if (wt == 0)
-#pragma unroll
-                        for (int r = 0; r < NRV; ++r) xms[r] = make_float2(m_run[r], lrow[r]);
-                }
+                    for (int r = 0; r < NRV; ++r) xms[wg * NRV + r] = make_float2(m_run[r], lrow[r]);
                 named_barrier_sync(3, 256);
-                if (lead) {
-                    float ob[NRV];
+                constexpr int HR = NRV / 2;
+                const int r0 = wg * HR;
+                float fsc[2][NRV];
 #pragma unroll
-                    for (int r4 = 0; r4 < NRV / 4; ++r4) {
-                        const float4 v4 = reinterpret_cast<const float4*>(xo + my_lane * NRV)[r4];
-                        ob[4 * r4] = v4.x;
-                        ob[4 * r4 + 1] = v4.y;
-                        ob[4 * r4 + 2] = v4.z;
-                        ob[4 * r4 + 3] = v4.w;
-                    }
-#pragma unroll
-                    for (int r = 0; r < NRV; ++r) {
-                        const float2 mb = xms[r];
-                        const float m = fmaxf(m_run[r], mb.x);
-                        const float aa = m_run[r] == -INFINITY ? 0.f : ex2_approx((m_run[r] - m) * c2);
-                        const float ab = mb.x == -INFINITY ? 0.f : ex2_approx((mb.x - m) * c2);
-                        o_acc[r] = o_acc[r] * aa + ob[r] * ab;
-                        lrow[r] = lrow[r] * aa + mb.y * ab;
-                        m_run[r] = m;
-                    }
-                    if (more) named_barrier_arrive(4, 256);  // exchange read: the second may reuse it
+                for (int r = 0; r < NRV; ++r) {
+                    const float2 a = xms[r], b = xms[NRV + r];
+                    const float m = fmaxf(a.x, b.x);
+                    const float sa = a.x == -INFINITY ? 0.f : ex2_approx((a.x - m) * c2);
+                    const float sb = b.x == -INFINITY ? 0.f : ex2_approx((b.x - m) * c2);
+                    const float l = a.y * sa + b.y * sb;
+                    const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
+                    fsc[0][r] = sa * inv * (FP8 ? 0.0625f : 1.f);  // the fp8 P split carries a factor 16
+                    fsc[1][r] = sb * inv * (FP8 ? 0.0625f : 1.f);
+                    m_run[r] = m;
+                    lrow[r] = l;
                 }
+                float v[HR];
+#pragma unroll
+                for (int k = 0; k < HR; ++k) v[k] = 0.f;
+                // A warpgroup without tiles in this unit left its fragment untouched.
+#pragma unroll
+                for (int f = 0; f < 2; ++f) {
+                    if (tile_count > f) {
+                        float part[HR];
+                        tmem_ld4_sum(tmem + lane_addr + C::TMEM_O0 + C::BUF_COLS * f + r0, C::PART_COLS, part);
+#pragma unroll
+                        for (int k = 0; k < HR; ++k) v[k] = fmaf(part[k], fsc[f][r0 + k], v[k]);
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {  // both fragments read: the O warp may overwrite them
+                    mbar_arrive(o_empty);
+                    mbar_arrive(o_empty + 8);
+                }
+                const int BW = p.ov_depth / P;
+                const int dv = my_lane;
+                const int rb = lu % C::RECV_BUFS, rk = lu / C::RECV_BUFS;
+                if (rk >= 1)
+                    mbar_wait<true>(recv_free + 8 * rb, (rk - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+                if (P > 1 && !cluster_waited) {
+                    cluster_wait();  // every rank's barriers are initialised
+                    cluster_waited = true;
+                }
+                const uint32_t recv0 = sbase + C::OFF_RECV + rb * C::RECV_BYTES;
+                const int q = dv / BW, col = dv % BW;
+                const uint32_t o_dst = recv0 + 4u * (uint32_t)((rank * BW + col) * NRV + r0);
+                if (P > 1) {
+                    const uint32_t bar_q = map_shared_rank(recv_full + 8 * rb, q);
+                    const uint32_t dst_q = map_shared_rank(o_dst, q);
+                    if constexpr (HR == 4) {
+                        st_async_f4(dst_q, v[0], v[1], v[2], v[3], bar_q);
+                    } else {
+                        st_async_f2(dst_q, v[0], v[1], bar_q);
+                    }
+                    if (lead) {
+                        for (int idx = wt; idx < P * NRV; idx += 128) {
+                            const int qq = idx / NRV, rr = idx % NRV;
+                            float mm = 0.f, ll = 0.f;
+#pragma unroll
+                            for (int r = 0; r < NRV; ++r)
+                                if (r == rr) {
+                                    mm = m_run[r];
+                                    ll = lrow[r];
+                                }
+                            const uint32_t ms_dst = recv0 + C::RECV_O_BYTES + 8u * (uint32_t)(rank * NRV + rr);
+                            st_async_f2(map_shared_rank(ms_dst, qq), mm, ll, map_shared_rank(recv_full + 8 * rb, qq));
+                        }
+                    }
+                } else {
+                    float* o_loc = reinterpret_cast<float*>(smem + (o_dst - sbase));
+                    if constexpr (HR == 4) {
+                        *reinterpret_cast<float4*>(o_loc) = make_float4(v[0], v[1], v[2], v[3]);
+                    } else {
+                        *reinterpret_cast<float2*>(o_loc) = make_float2(v[0], v[1]);
+                    }
+                    if (lead && wt == 0) {
+                        float2* ms_loc = reinterpret_cast<float2*>(smem + (recv0 - sbase) + C::RECV_O_BYTES);
+#pragma unroll
+                        for (int r = 0; r < NRV; ++r) ms_loc[r] = make_float2(m_run[r], lrow[r]);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(recv_full + 8 * rb);
+                }
+                if (lead && wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
             }
-            if (lead) {
+            if (!C::TMEM_O && lead) {
                 const int BW = p.ov_depth / P;  // this partition's output band
                 const int dv = my_lane;
                 if constexpr (C::MULTI) {

@@ -164,6 +164,26 @@ __device__ __forceinline__ void tmem_ld_32x32b(uint32_t taddr, float (&v)[16])
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Four accumulators of 2 columns each, `acc_stride` columns apart, summed.
+__device__ __forceinline__ void tmem_ld4_sum(uint32_t taddr, uint32_t acc_stride, float (&v)[2])
+{
+    uint32_t r[8];
+    __syncwarp();
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%8];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%2, %3}, [%9];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%4, %5}, [%10];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%6, %7}, [%11];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr), "r"(taddr + acc_stride), "r"(taddr + 2 * acc_stride), "r"(taddr + 3 * acc_stride)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        v[i] = (__uint_as_float(r[i]) + __uint_as_float(r[2 + i])) +
+               (__uint_as_float(r[4 + i]) + __uint_as_float(r[6 + i]));
+}
+
 // Four accumulators of N columns each (N = 4, 8, 16), `acc_stride` columns
 // apart, loaded with one wait and summed: the partial products of an MMA
 // chain that was spread over four independent accumulators.
@@ -255,6 +275,34 @@ __device__ __forceinline__ void tmem_ld2_sum_x32(uint32_t taddr, uint32_t acc_st
         : "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) + __uint_as_float(r[32 + i]);
+}
+
+// Scale columns [0, N) of four accumulators `acc_stride` columns apart by
+// a[c] (column c), in place: load, multiply, store, wait for the stores.
+template <int N>
+__device__ __forceinline__ void tmem_scale4(uint32_t taddr, uint32_t acc_stride, const float (&a)[N])
+{
+    static_assert(N == 4 || N == 8, "columns per accumulator");
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float v[N];
+        tmem_ld_32x32b(taddr + k * acc_stride, v);
+        uint32_t w[N];
+#pragma unroll
+        for (int c = 0; c < N; ++c) w[c] = __float_as_uint(v[c] * a[c]);
+        __syncwarp();
+        if constexpr (N == 4) {
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr + k * acc_stride),
+                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                         : "memory");
+        } else {
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                             taddr + k * acc_stride),
+                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                         : "memory");
+        }
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Store 32 lanes x 32 columns (the inverse of tmem_ld_32x32b_x32) and wait
