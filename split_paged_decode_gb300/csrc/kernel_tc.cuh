@@ -112,22 +112,22 @@ struct TcCfg {
     static constexpr int ACC_COLS = MMA_N;                        // columns of one accumulator
     static constexpr int PART_COLS = 16;                          // reader stride between partials
     static constexpr int BUF_COLS = NACC * ACC_COLS;              // 64
-    // P and O buffers (by global tile index). Two: a buffer is reused two
-    // tiles later, so with two softmax warpgroups a warpgroup folds in its
-    // previous tile's O before it writes the next P. Four (two warpgroups,
-    // fp8, whose smaller ring leaves room): a warpgroup publishes a tile's P
-    // first and folds in the previous O after.
+    // P buffers (by global tile index): buffer gi % NPB, reused NPB tiles
+    // later once the O product that read it has completed. Four with two
+    // warpgroups on the fp8 kernel (whose smaller ring leaves room), else two.
     static constexpr int NPB = (NWG == 2 && FP8) ? 4 : 2;
-    // Fold in the previous tile's O before writing P (else after publishing it).
-    static constexpr bool FOLD_FIRST = NWG == 2 && NPB == 2;
-    // Two warpgroups keep their O in tensor memory, one fragment each (the
-    // two TMEM_O fragments of the fa4_lse_combine_write page): the O MMA
+    // O stays in tensor memory, one fragment per softmax warpgroup (the
+    // TMEM_O fragments of the fa4_lse_combine_write page): the O MMA
     // accumulates a warpgroup's tiles straight into its fragment, a moved max
-    // rescales the fragment in place, and at the end of a unit each
-    // warpgroup combines both fragments for half of the rows.
-    static constexpr bool TMEM_O = NWG == 2;
-    static constexpr int TMEM_S0 = 0, TMEM_O0 = 2 * BUF_COLS;     // S [2], then O [NPB]
-    static constexpr int TMEM_COLS = (TMEM_O || (2 + NPB) * BUF_COLS <= 256) ? 256 : 512;
+    // rescales the fragment in place, and the unit epilogue reads it once
+    // (two warpgroups: each combines both fragments for half of the rows).
+    // With one warpgroup the O barriers go by P buffer, so that writing P
+    // waits only for the product two tiles back, and a rescale for the
+    // previous one; with two they go by fragment.
+    static constexpr bool O_BAR_BY_FRAG = NWG == 2;
+    static constexpr int N_OBAR = O_BAR_BY_FRAG ? 2 : NPB;
+    static constexpr int TMEM_S0 = 0, TMEM_O0 = 2 * BUF_COLS;     // S [2], then O [NWG]
+    static constexpr int TMEM_COLS = 256;
     // Units with at least this many tiles per rank are issued two items per
     // pass by the load warp (its per-item cost bounds them), shorter ones one
     // at a time; measured: pairs for every unit on the fp8 kernel and the
@@ -165,7 +165,7 @@ struct TcCfg {
     static constexpr int OFF_WTAB = OFF_RECV + RECV_BUFS * RECV_BYTES;
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_OUT = MULTI ? (OFF_WTAB + kMaxSplit * NRV * 4 + 127) / 128 * 128 : TILE_BYTES;
-    // Two softmax warpgroups: (max, sum) [2][NRV] of both (TMEM_O).
+    // Two softmax warpgroups: (max, sum) [2][NRV] of both.
     static constexpr int XCHG_O_BYTES = 0;
     static constexpr int OFF_XCHG = OFF_OUT + OUT_BYTES;
     static constexpr int END_MULTI = OFF_XCHG + (NWG == 2 ? 2 * NRV * 8 : 0);
@@ -499,8 +499,8 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         for (int i = 0; i < C::NPB; ++i) {
             mbar_init(p_full + 8 * i, 4);    // the four softmax warps that wrote P
             mbar_init(o_full + 8 * i, 1);    // the O warp's commit
-            // the four softmax warps that read O; TMEM_O: the eight that read both fragments
-            mbar_init(o_empty + 8 * i, C::TMEM_O ? 8 : 4);
+            // o_empty[f]: every softmax warp, once it has read fragment f at the end of a unit
+            mbar_init(o_empty + 8 * i, 4 * C::NWG);
         }
         *abort_flag = 0;
         *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 8) = 0;
@@ -522,8 +522,8 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         if (lane == 0) mbar_arrive(tmem_ready);
     }
 
-    // Softmax / correction state (warps 3-6), real rows only.
-    float m_run[NRV], l_part[NRV], o_acc[NRV];
+    // Softmax state (warps 3-6, 7-10), real rows only.
+    float m_run[NRV], l_part[NRV];
 
     // Items (K or V tiles) and tiles are numbered globally over the units of
     // this cluster, so ring slots, buffers and barrier phases run on across
@@ -745,29 +745,25 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 } else {
                     for (int t = 0; ok && t < tile_count; ++t) {
                         const int gi = gt + t, j = J0 + v_item<C::VLAG>(t, tile_count), slot = j % NSLOT;
-                        // TMEM_O: tile t goes to the fragment of warpgroup t % 2, whose
-                        // first tile of a unit overwrites it once both warpgroups have
-                        // read it for the previous unit (o_empty[f], one phase per unit).
-                        const int frag = t % 2;
-                        const bool frag_first = t < 2;
+                        // Tile t goes to the fragment of warpgroup t % NWG, whose first
+                        // tile of a unit overwrites it once every warpgroup has read it
+                        // for the previous unit (o_empty[f], one phase per unit).
+                        const int frag = t % C::NWG;
+                        const bool frag_first = t < C::NWG;
                         ok = ring_turn(j) &&
                              mbar_wait(slot_full + 8 * slot, (j / NSLOT) & 1, abort_flag, p.status, p.wait_limit_ns) &&
                              mbar_wait(p_full + 8 * (gi % C::NPB), (gi / C::NPB) & 1, abort_flag, p.status,
                                        p.wait_limit_ns) &&
-                             (C::TMEM_O
-                                  ? (!frag_first || lu == 0 ||
-                                     mbar_wait(o_empty + 8 * frag, (lu - 1) & 1, abort_flag, p.status, p.wait_limit_ns))
-                                  : (gi < C::NPB || mbar_wait(o_empty + 8 * (gi % C::NPB), ((gi / C::NPB) - 1) & 1,
-                                                              abort_flag, p.status, p.wait_limit_ns)));
+                             (!frag_first || lu == 0 ||
+                              mbar_wait(o_empty + 8 * frag, (lu - 1) & 1, abort_flag, p.status, p.wait_limit_ns));
                         if (!ok) break;
                         if (gi == 0) stamp(62);
                         tc_fence_after_sync();
                         const uint64_t a0 = v_desc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
                         const uint64_t b0 = p_desc0 + (uint64_t)(((gi % C::NPB) * C::P_BYTES) >> 4);
-                        const uint32_t d =
-                            tmem + C::TMEM_O0 + C::BUF_COLS * (C::TMEM_O ? frag : (gi % C::NPB));
-                        // TMEM_O: every tile but the fragment's first of the unit accumulates.
-                        const bool acc_all = C::TMEM_O && !frag_first;
+                        const uint32_t d = tmem + C::TMEM_O0 + C::BUF_COLS * frag;
+                        // Every tile but the fragment's first of the unit accumulates.
+                        const bool acc_all = !frag_first;
                         if constexpr (!FP8) {
 #pragma unroll
                             for (int ks = 0; ks < C::BN / 16; ++ks)
@@ -781,7 +777,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                                 umma_f8_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)((ks * 4096) >> 4),
                                            b0 + (uint64_t)((ks * 32) >> 4), id_pv, acc_all || ks >= C::NACC);
                         }
-                        umma_commit(o_full + 8 * (C::TMEM_O ? frag : (gi % C::NPB)));
+                        umma_commit(o_full + 8 * (C::O_BAR_BY_FRAG ? frag : (gi % C::NPB)));
                         umma_commit(slot_empty + 8 * slot);  // V_t's slot is free once O_t has completed
                         st_release_u32(o_next, (uint32_t)(t + 1 < tile_count ? J0 + v_item<C::VLAG>(t + 1, tile_count)
                                                                              : J0 + 2 * tile_count));
@@ -893,7 +889,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         bool seen_abort = false;  // sticky: this thread has seen the abort flag
         bool cluster_waited = false;
         int J0 = 0, gt = 0, lu = 0;
-        int wc = 0;  // TMEM_O: this warpgroup's tiles so far (phases of its o_full barrier)
+        int wc = 0;  // two warpgroups: this warpgroup's tiles so far (phases of its o_full barrier)
         while (have) {
             const int L = w.L;
             int tile_begin, tile_count;
@@ -922,47 +918,16 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             for (int r = 0; r < NRV; ++r) {
                 m_run[r] = -INFINITY;
                 l_part[r] = 0.f;
-                o_acc[r] = 0.f;
             }
             // Row r = t * heads + hh (query token t) sees keys < L - T + t + 1, so
             // the rows that see key k are a suffix: r >= (k - (L - T + 1) + 1) * heads.
             const int vis0 = L - p.num_q + 1;
 
-            // fp8: this unit's S = acc / (16 sigma_r); its Q (and the multipliers)
-            // are published on the unit's q_full phase.
-            float qmul[NRV];
-            if constexpr (FP8) {
-                mbar_wait(q_full + 8 * (lu & 1), (lu >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
-                const float* qi = reinterpret_cast<const float*>(smem + C::OFF_QINV) + (lu & 1) * C::NR;
-#pragma unroll
-                for (int r = 0; r < NRV; ++r) qmul[r] = qi[r];
-            }
-            float alpha_prev[NRV];
-            bool rescaled_prev = false;
-            // O of this warpgroup's tile with global index gi has completed:
-            // fold it into o_acc.
-            auto correct = [&](int gi, const float (&a)[NRV], bool rescaled) {
-                mbar_wait(o_full + 8 * (gi % C::NPB), (gi / C::NPB) & 1, abort_flag, p.status, p.wait_limit_ns);
-                tc_fence_after_sync();
-                float ot[NRV];
-                tmem_ld4_sum(tmem + lane_addr + C::TMEM_O0 + C::BUF_COLS * (gi % C::NPB), C::PART_COLS, ot);
-                if constexpr (FP8) {
-#pragma unroll
-                    for (int r = 0; r < NRV; ++r) ot[r] *= 0.0625f;  // the P split carries a factor 16
-                }
-                tc_fence_before_sync();
-                __syncwarp();
-                // O has completed, so (for tile gi + 2) the P buffer it read is free.
-                if (lane == 0) mbar_arrive(o_empty + 8 * (gi % C::NPB));
-                if (rescaled) {
-#pragma unroll
-                    for (int r = 0; r < NRV; ++r) o_acc[r] = fmaf(o_acc[r], a[r], ot[r]);
-                } else {
-#pragma unroll
-                    for (int r = 0; r < NRV; ++r) o_acc[r] += ot[r];
-                }
-            };
-
+            // fp8: this unit's S = acc / (16 sigma_r); its Q (and the multipliers,
+            // read from shared memory at every tile) are published on the unit's
+            // q_full phase.
+            const float4* qinv = reinterpret_cast<const float4*>(smem + C::OFF_QINV) + (lu & 1) * (C::NR / 4);
+            if constexpr (FP8) mbar_wait(q_full + 8 * (lu & 1), (lu >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
             // This warpgroup's tiles: local index i congruent to wg modulo NWG
             // (by local index, so a unit's arithmetic does not depend on the
             // units its cluster took before). Their global indices share a
@@ -970,8 +935,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             // and red_s: (gt + wg) & 1 with two warpgroups.
             const int i0 = C::NWG == 2 ? wg : 0;
             const int gt0 = gt;
-            int prev_gi = -1;  // this warpgroup's previous tile, still to be folded in
-            int wc_unit = 0;   // TMEM_O: this warpgroup's tiles of the unit so far
+            int wc_unit = 0;   // this warpgroup's tiles of the unit so far
             for (int i = i0; i < tile_count; i += C::NWG) {
                 const int gi = gt + i;
                 mbar_wait(s_full + 8 * (gi & 1), (gi >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
@@ -996,24 +960,35 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                         if (lane == 0) mbar_arrive(ks_empty + 8 * kse);
                     }
 #pragma unroll
-                    for (int r = 0; r < NRV; ++r) s[r] *= qmul[r] * ksc;
+                    for (int r4 = 0; r4 < NRV / 4; ++r4) {
+                        const float4 qm = qinv[r4];
+                        s[4 * r4 + 0] *= qm.x * ksc;
+                        s[4 * r4 + 1] *= qm.y * ksc;
+                        s[4 * r4 + 2] *= qm.z * ksc;
+                        s[4 * r4 + 3] *= qm.w * ksc;
+                    }
                 }
 
                 const int key0 = (tile_begin + i) * C::BN;
                 const int key = key0 + my_lane;
                 const int r_min = key < vis0 ? 0 : (key >= L ? NRV : (key - vis0 + 1) * p.heads_per_cta);
 #pragma unroll
-                for (int r = 0; r < NRV; ++r) s[r] = (r >= r_min && r < p.rows) ? s[r] : -INFINITY;
+                for (int r = 0; r < NRV; ++r) s[r] = ((r >= r_min) & (r < p.rows)) ? s[r] : -INFINITY;
 
                 // Lazy rescale: a row's running max moves only when some score
                 // exceeds it by more than the threshold. In the common case a single
                 // reducing barrier confirms that no thread needs it; otherwise the
                 // tile max is exchanged and the rows that exceed are moved.
+                // Evaluated without short-circuit branches: a finite score over an
+                // empty row, or one more than the threshold above the row's max (a
+                // masked score gives -inf or NaN there, which compares false).
                 bool need = false;
 #pragma unroll
-                for (int r = 0; r < NRV; ++r)
-                    need |= (s[r] != -INFINITY) &&
-                            (m_run[r] == -INFINITY || (s[r] - m_run[r]) * c2 > C::RESCALE);
+                for (int r = 0; r < NRV; ++r) {
+                    const bool first = (m_run[r] == -INFINITY) & (s[r] != -INFINITY);
+                    const bool over = (s[r] - m_run[r]) * c2 > C::RESCALE;
+                    need = need | first | over;
+                }
                 seen_abort |= (*abort_flag != 0);
                 bool rescale = false;
                 float alpha[NRV];
@@ -1055,9 +1030,12 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                         }
                     }
                 }
+                // exp2(-inf) = +0 for masked scores (a row whose max is still -inf
+                // would give NaN from the difference, hence the select first).
 #pragma unroll
                 for (int r = 0; r < NRV; ++r) {
-                    const float pr = (s[r] == -INFINITY) ? 0.f : ex2_approx((s[r] - m_run[r]) * c2);
+                    const float x = (s[r] == -INFINITY) ? -INFINITY : (s[r] - m_run[r]) * c2;
+                    const float pr = ex2_approx(x);
                     l_part[r] += pr;
                     s[r] = pr;
                 }
@@ -1068,7 +1046,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 // correction has observed: one warpgroup folded it in during its
                 // previous tile, as do two with four buffers; two warpgroups with
                 // two buffers fold it in here, before the store.
-                if constexpr (C::TMEM_O) {
+                if constexpr (C::O_BAR_BY_FRAG) {
                     // The fragment's previous O product read the P buffer this tile
                     // reuses, and must finish before a rescale touches the fragment.
                     if (wc_unit > 0) {
@@ -1079,8 +1057,22 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                             tc_fence_before_sync();
                         }
                     }
-                } else if constexpr (C::FOLD_FIRST) {
-                    if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
+                } else {
+                    // One warpgroup: a rescale waits for the previous tile's O (and
+                    // with it every earlier one); otherwise only the product that
+                    // read this P buffer, NPB tiles back, has to be complete.
+                    if (rescale && i > 0) {
+                        const int gp = gi - 1;
+                        mbar_wait(o_full + 8 * (gp % C::NPB), (gp / C::NPB) & 1, abort_flag, p.status,
+                                  p.wait_limit_ns);
+                        tc_fence_after_sync();
+                        tmem_scale4<NRV>(tmem + lane_addr + C::TMEM_O0, C::PART_COLS, alpha);
+                        tc_fence_before_sync();
+                    } else if (gi >= C::NPB) {
+                        const int gp = gi - C::NPB;
+                        mbar_wait(o_full + 8 * (gp % C::NPB), (gp / C::NPB) & 1, abort_flag, p.status,
+                                  p.wait_limit_ns);
+                    }
                 }
                 if constexpr (!FP8) {
                     uint8_t* pb = smem + C::OFF_P + (gi % C::NPB) * C::P_BYTES + (my_lane >> 6) * 2048;
@@ -1128,27 +1120,16 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 }
                 q_pending = false;
 
-                // Fold in this warpgroup's previous tile once this one's P is out.
-                if constexpr (C::TMEM_O) {
-                    ++wc;
-                    ++wc_unit;
-                } else if constexpr (!C::FOLD_FIRST) {
-                    if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
-                }
-#pragma unroll
-                for (int r = 0; r < NRV; ++r) alpha_prev[r] = rescale ? alpha[r] : 1.f;
-                rescaled_prev = rescale;
-                prev_gi = gi;
+                ++wc;
+                ++wc_unit;
             }
             // Bounded even after an abort. After an abort the O of the tile
             // that broke the loop was never issued; the wait gives up at once.
-            if constexpr (C::TMEM_O) {
-                if (wc_unit > 0) {  // the fragment's last product is complete
-                    mbar_wait(o_full + 8 * wg, (wc - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
-                    tc_fence_after_sync();
-                }
-            } else {
-                if (prev_gi >= 0) correct(prev_gi, alpha_prev, rescaled_prev);
+            if (wc_unit > 0) {  // the fragment's last product is complete
+                const int gl = C::O_BAR_BY_FRAG ? wg : (gt + wc_unit - 1) % C::NPB;
+                const int ph = C::O_BAR_BY_FRAG ? (wc - 1) : (gt + wc_unit - 1) / C::NPB;
+                mbar_wait(o_full + 8 * gl, ph & 1, abort_flag, p.status, p.wait_limit_ns);
+                tc_fence_after_sync();
             }
             if (lead && wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 2));
             gt += tile_count;
@@ -1174,7 +1155,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             float lrow[NRV];
 #pragma unroll
             for (int r = 0; r < NRV; ++r) lrow[r] = red_w[r] + red_w[NRV + r] + red_w[2 * NRV + r] + red_w[3 * NRV + r];
-            if constexpr (C::TMEM_O) {
+            if constexpr (C::NWG == 2) {
                 // Combine the two warpgroups' O fragments (fa4_lse_combine_write
                 // page): per row m = max(m_0, m_1), l = sum_w l_w exp2((m_w - m) c)
                 // and the final scales f_w = exp2((m_w - m) c) / l (own and peer);
@@ -1271,7 +1252,23 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 }
                 if (lead && wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
             }
-            if (!C::TMEM_O && lead) {
+            if constexpr (C::NWG == 1) {
+                // This thread's value column of the O fragment (zero when the rank
+                // has no tiles of the unit: the fragment still holds an earlier
+                // unit's O); then the O warp may overwrite it.
+                float o_acc[NRV];
+#pragma unroll
+                for (int r = 0; r < NRV; ++r) o_acc[r] = 0.f;
+                if (wc_unit > 0) {
+                    tmem_ld4_sum(tmem + lane_addr + C::TMEM_O0, C::PART_COLS, o_acc);
+                    if constexpr (FP8) {
+#pragma unroll
+                        for (int r = 0; r < NRV; ++r) o_acc[r] *= 0.0625f;  // the P split carries a factor 16
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_empty);
                 const int BW = p.ov_depth / P;  // this partition's output band
                 const int dv = my_lane;
                 if constexpr (C::MULTI) {

@@ -282,7 +282,7 @@ __device__ __forceinline__ void tmem_ld2_sum_x32(uint32_t taddr, uint32_t acc_st
 template <int N>
 __device__ __forceinline__ void tmem_scale4(uint32_t taddr, uint32_t acc_stride, const float (&a)[N])
 {
-    static_assert(N == 4 || N == 8, "columns per accumulator");
+    static_assert(N == 4 || N == 8 || N == 16, "columns per accumulator");
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         float v[N];
@@ -295,10 +295,16 @@ __device__ __forceinline__ void tmem_scale4(uint32_t taddr, uint32_t acc_stride,
             asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr + k * acc_stride),
                          "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
                          : "memory");
-        } else {
+        } else if constexpr (N == 8) {
             asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
                              taddr + k * acc_stride),
                          "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                         : "memory");
+        } else {
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                         "%12, %13, %14, %15, %16};" ::"r"(taddr + k * acc_stride),
+                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+                         "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
                          : "memory");
         }
     }
