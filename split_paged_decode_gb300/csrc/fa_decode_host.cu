@@ -473,8 +473,8 @@ int fa_decode_create_kv(fa_decode_t* out, int num_q_heads, int num_kv_heads, int
     }
     if (tmp.has_tc && splitk > 0 && tmp.tc_big_clusters > 0) {
         // Stream-K scratch: per slot and rank, the band's fp32 rows and
-        // per-row (max, sum); one count per (unit, rank), zero between
-        // launches (the partition is used with fewer units than clusters).
+        // per-row (max, sum), and one count per (slot, rank) for the shared
+        // units, zero between launches.
         const size_t items = (size_t)tmp.tc_big_clusters * 2;
         const size_t rb = (size_t)tmp.geo_tc_big.rows_capacity;
         tmp.chunk_items = (int64_t)items;
@@ -647,8 +647,10 @@ int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const vo
     if (tc_big) {
         const int64_t most = (h->debug_flags & FA_DEBUG_TWO_CLUSTERS) ? 2 : h->tc_big_clusters;
         if (h->chunk_count && !(h->debug_flags & FA_DEBUG_NO_STREAM_K)) {
-            // Fewer units than resident clusters: every resident cluster takes an
-            // equal share of all units' tiles (a full page-table row each).
+            // Every cluster of the partition takes an equal share of all units'
+            // tiles (a full page-table row each): with fewer units than resident
+            // clusters, or with more when whole-unit rounds would leave some
+            // clusters idle at the end.
             const int64_t nv = ((int64_t)max_pages_per_seq * h->page_size + 127) / 128;
             const int G = fad::sk_choose_clusters(units, nv, h->splitk, most, h->chunk_items);
             if (G > 0) {

@@ -77,7 +77,7 @@ struct DecodeParams {
     int64_t sk_total;
     float* chunk_o;             // [slot][P][band_cols][rows_capacity]
     float2* chunk_ms;           // [slot][P][rows_capacity]: (max, sum) in raw score units
-    unsigned int* chunk_count;  // [unit][P], zero between launches
+    unsigned int* chunk_count;  // [slot][P]: per shared unit, at its first cluster's slot; zero between launches
     // fp8 cache: per-token K scales, float [num_pages * Hkv * PS] (the cache
     // row index), or NULL for unit scales.
     const float* k_scale;

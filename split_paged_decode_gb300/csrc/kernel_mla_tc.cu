@@ -415,10 +415,16 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
 #pragma unroll
                 for (int r = 0; r < 32; ++r) s[r] = -INFINITY;
             }
+            // Without short-circuit branches (one per head otherwise): a finite
+            // score over an empty row, or one more than the threshold above the
+            // row's max (a masked score compares false).
             bool need = false;
 #pragma unroll
-            for (int r = 0; r < 32; ++r)
-                need |= (s[r] != -INFINITY) && (m_run[r] == -INFINITY || (s[r] - m_run[r]) * c2 > 8.0f);
+            for (int r = 0; r < 32; ++r) {
+                const bool first = (m_run[r] == -INFINITY) & (s[r] != -INFINITY);
+                const bool over = (s[r] - m_run[r]) * c2 > 8.0f;
+                need = need | first | over;
+            }
             seen_abort |= (*abort_flag != 0);
             if (named_barrier_or(wg_bar, 128, need || seen_abort)) {
                 {
@@ -478,9 +484,12 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                 }
                 named_barrier_sync(wg_bar, 128);  // red_w is read before the next tile's writes
             }
+            // exp2(-inf) = +0 for masked scores (the select keeps an empty row's
+            // -inf - -inf from giving NaN).
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
-                const float pr = (s[r] == -INFINITY) ? 0.f : ex2_approx((s[r] - m_run[r]) * c2);
+                const float x = (s[r] == -INFINITY) ? -INFINITY : (s[r] - m_run[r]) * c2;
+                const float pr = ex2_approx(x);
                 l_part[r] += pr;
                 s[r] = pr;
             }

@@ -410,7 +410,9 @@ __device__ __noinline__ void splitk_merge_pushed_sk(const DecodeParams& p, int P
     // cluster that completes the count reads every chunk's band.
     __threadfence();
     __syncwarp();
-    unsigned int* count = p.chunk_count + (int64_t)u * P + rank;
+    // One count per shared unit, at its first cluster's slot for it (slots are
+    // distinct across the shared units of a launch).
+    unsigned int* count = p.chunk_count + slot(c_first) * P + rank;
     unsigned int last = 0;
     if (lane == 0) last = atomicAdd(count, 1u) == (unsigned int)(S - 1) ? 1u : 0u;
     if (!__shfl_sync(0xffffffffu, last, 0)) return;

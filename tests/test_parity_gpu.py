@@ -257,6 +257,15 @@ def test_stream_k_two_clusters():
     run_and_check(w, what="stream-K two clusters", path="two_clusters")
 
 
+def test_stream_k_more_units_than_clusters():
+    """Three units over two clusters (whole-unit rounds would be 2 against an
+    equal share of 1.5): each range holds one whole unit and half of the
+    middle one, which the two clusters merge through the scratch."""
+    w = wl(batch=3, num_kv_heads=1, num_q_heads=4, splitk=4, seq_len_lo=3000, seq_len_hi=9000, seed=123)
+    run_and_check(w, seq_lens=[9000, 8500, 9000], what="stream-K more units than clusters", path="two_clusters")
+    run_and_check(w, seq_lens=[9000, 1, 4000], what="stream-K more units, short middle unit", path="two_clusters")
+
+
 def test_stream_k_ranges_across_units():
     """Three units of unequal length over ~26 clusters: ranges that end in one
     unit and start in the next, and ranges past a short sequence's end."""
