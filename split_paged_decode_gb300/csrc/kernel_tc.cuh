@@ -155,20 +155,18 @@ struct TcCfg {
     // Epilogue buffers. Single-unit variant: f32 stage [P][NRV][Dv / P] in the
     // drained ring (slot 0) that peers pull from, bf16 output band in slot 1.
     // Multi-unit variant: receive buffers that peers push into (one or two,
-    // by unit, as space allows: float [P][Dv / P][NRV] + float2 [P][NRV]),
-    // the combine weights float [P][NRV] and the output band.
+    // by unit, as space allows), each with one partial per (rank, softmax
+    // warpgroup): float [NWG P][Dv / P][NRV] + float2 [NWG P][NRV]; the
+    // combine weights float [NWG P][NRV] and the output band.
     static constexpr int OUT_BYTES = NRV * D * 2;
-    static constexpr int RECV_BUFS = NRV <= 8 ? 2 : 1;
-    static constexpr int RECV_O_BYTES = NRV * D * 4;
-    static constexpr int RECV_BYTES = RECV_O_BYTES + kMaxSplit * NRV * 8;
+    static constexpr int RECV_BUFS = NWG * NRV <= 8 ? 2 : 1;
+    static constexpr int RECV_O_BYTES = NWG * NRV * D * 4;       // [NWG P][Dv / P][NRV]
+    static constexpr int RECV_BYTES = RECV_O_BYTES + NWG * kMaxSplit * NRV * 8;
     static constexpr int OFF_RECV = (MISC_END + 127) / 128 * 128;
     static constexpr int OFF_WTAB = OFF_RECV + RECV_BUFS * RECV_BYTES;
     static constexpr int OFF_STAGE = 0;
-    static constexpr int OFF_OUT = MULTI ? (OFF_WTAB + kMaxSplit * NRV * 4 + 127) / 128 * 128 : TILE_BYTES;
-    // Two softmax warpgroups: (max, sum) [2][NRV] of both.
-    static constexpr int XCHG_O_BYTES = 0;
-    static constexpr int OFF_XCHG = OFF_OUT + OUT_BYTES;
-    static constexpr int END_MULTI = OFF_XCHG + (NWG == 2 ? 2 * NRV * 8 : 0);
+    static constexpr int OFF_OUT = MULTI ? (OFF_WTAB + NWG * kMaxSplit * NRV * 4 + 127) / 128 * 128 : TILE_BYTES;
+    static constexpr int END_MULTI = OFF_OUT + OUT_BYTES;
     static constexpr int SMEM_BYTES = (MULTI ? END_MULTI : MISC_END) + 1024;
     static_assert(NSLOT >= 2, "ring of at least one K and one V tile");
     static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms on 1024 bytes");
@@ -499,8 +497,8 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         for (int i = 0; i < C::NPB; ++i) {
             mbar_init(p_full + 8 * i, 4);    // the four softmax warps that wrote P
             mbar_init(o_full + 8 * i, 1);    // the O warp's commit
-            // o_empty[f]: every softmax warp, once it has read fragment f at the end of a unit
-            mbar_init(o_empty + 8 * i, 4 * C::NWG);
+            // o_empty[f]: the four warps of warpgroup f, once they have read its fragment at the end of a unit
+            mbar_init(o_empty + 8 * i, 4);
         }
         *abort_flag = 0;
         *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 8) = 0;
@@ -1155,112 +1153,19 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             float lrow[NRV];
 #pragma unroll
             for (int r = 0; r < NRV; ++r) lrow[r] = red_w[r] + red_w[NRV + r] + red_w[2 * NRV + r] + red_w[3 * NRV + r];
-            if constexpr (C::NWG == 2) {
-                // Combine the two warpgroups' O fragments (fa4_lse_combine_write
-                // page): per row m = max(m_0, m_1), l = sum_w l_w exp2((m_w - m) c)
-                // and the final scales f_w = exp2((m_w - m) c) / l (own and peer);
-                // warpgroup w combines and pushes rows [w NRV / 2, (w + 1) NRV / 2),
-                // disjoint column ranges of both fragments.
-                float2* xms = reinterpret_cast<float2*>(smem + C::OFF_XCHG);  // [2][NRV]
-                if (wt == 0)
-#pragma unroll
-                    for (int r = 0; r < NRV; ++r) xms[wg * NRV + r] = make_float2(m_run[r], lrow[r]);
-                named_barrier_sync(3, 256);
-                constexpr int HR = NRV / 2;
-                const int r0 = wg * HR;
-                float fsc[2][NRV];
-#pragma unroll
-                for (int r = 0; r < NRV; ++r) {
-                    const float2 a = xms[r], b = xms[NRV + r];
-                    const float m = fmaxf(a.x, b.x);
-                    const float sa = a.x == -INFINITY ? 0.f : ex2_approx((a.x - m) * c2);
-                    const float sb = b.x == -INFINITY ? 0.f : ex2_approx((b.x - m) * c2);
-                    const float l = a.y * sa + b.y * sb;
-                    const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
-                    fsc[0][r] = sa * inv * (FP8 ? 0.0625f : 1.f);  // the fp8 P split carries a factor 16
-                    fsc[1][r] = sb * inv * (FP8 ? 0.0625f : 1.f);
-                    m_run[r] = m;
-                    lrow[r] = l;
-                }
-                float v[HR];
-#pragma unroll
-                for (int k = 0; k < HR; ++k) v[k] = 0.f;
-                // A warpgroup without tiles in this unit left its fragment untouched.
-#pragma unroll
-                for (int f = 0; f < 2; ++f) {
-                    if (tile_count > f) {
-                        float part[HR];
-                        tmem_ld4_sum(tmem + lane_addr + C::TMEM_O0 + C::BUF_COLS * f + r0, C::PART_COLS, part);
-#pragma unroll
-                        for (int k = 0; k < HR; ++k) v[k] = fmaf(part[k], fsc[f][r0 + k], v[k]);
-                    }
-                }
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) {  // both fragments read: the O warp may overwrite them
-                    mbar_arrive(o_empty);
-                    mbar_arrive(o_empty + 8);
-                }
-                const int BW = p.ov_depth / P;
-                const int dv = my_lane;
-                const int rb = lu % C::RECV_BUFS, rk = lu / C::RECV_BUFS;
-                if (rk >= 1)
-                    mbar_wait<true>(recv_free + 8 * rb, (rk - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
-                if (P > 1 && !cluster_waited) {
-                    cluster_wait();  // every rank's barriers are initialised
-                    cluster_waited = true;
-                }
-                const uint32_t recv0 = sbase + C::OFF_RECV + rb * C::RECV_BYTES;
-                const int q = dv / BW, col = dv % BW;
-                const uint32_t o_dst = recv0 + 4u * (uint32_t)((rank * BW + col) * NRV + r0);
-                if (P > 1) {
-                    const uint32_t bar_q = map_shared_rank(recv_full + 8 * rb, q);
-                    const uint32_t dst_q = map_shared_rank(o_dst, q);
-                    if constexpr (HR == 4) {
-                        st_async_f4(dst_q, v[0], v[1], v[2], v[3], bar_q);
-                    } else {
-                        st_async_f2(dst_q, v[0], v[1], bar_q);
-                    }
-                    if (lead) {
-                        for (int idx = wt; idx < P * NRV; idx += 128) {
-                            const int qq = idx / NRV, rr = idx % NRV;
-                            float mm = 0.f, ll = 0.f;
-#pragma unroll
-                            for (int r = 0; r < NRV; ++r)
-                                if (r == rr) {
-                                    mm = m_run[r];
-                                    ll = lrow[r];
-                                }
-                            const uint32_t ms_dst = recv0 + C::RECV_O_BYTES + 8u * (uint32_t)(rank * NRV + rr);
-                            st_async_f2(map_shared_rank(ms_dst, qq), mm, ll, map_shared_rank(recv_full + 8 * rb, qq));
-                        }
-                    }
-                } else {
-                    float* o_loc = reinterpret_cast<float*>(smem + (o_dst - sbase));
-                    if constexpr (HR == 4) {
-                        *reinterpret_cast<float4*>(o_loc) = make_float4(v[0], v[1], v[2], v[3]);
-                    } else {
-                        *reinterpret_cast<float2*>(o_loc) = make_float2(v[0], v[1]);
-                    }
-                    if (lead && wt == 0) {
-                        float2* ms_loc = reinterpret_cast<float2*>(smem + (recv0 - sbase) + C::RECV_O_BYTES);
-#pragma unroll
-                        for (int r = 0; r < NRV; ++r) ms_loc[r] = make_float2(m_run[r], lrow[r]);
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(recv_full + 8 * rb);
-                }
-                if (lead && wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
-            }
-            if constexpr (C::NWG == 1) {
-                // This thread's value column of the O fragment (zero when the rank
-                // has no tiles of the unit: the fragment still holds an earlier
-                // unit's O); then the O warp may overwrite it.
+            {
+                // This thread's value column of the warpgroup's O fragment (zero
+                // when the warpgroup has no tiles of the unit: the fragment still
+                // holds an earlier unit's O); then the O warp may overwrite it.
+                // With two warpgroups each pushes its fragment as a partial of its
+                // own, (O_w / l_w, m_w, l_w), and the epilogue warp's LSE combine
+                // takes the 2P partials of the unit, so neither warpgroup waits for
+                // the other at the end of a unit.
                 float o_acc[NRV];
 #pragma unroll
                 for (int r = 0; r < NRV; ++r) o_acc[r] = 0.f;
                 if (wc_unit > 0) {
-                    tmem_ld4_sum(tmem + lane_addr + C::TMEM_O0, C::PART_COLS, o_acc);
+                    tmem_ld4_sum(tmem + lane_addr + C::TMEM_O0 + C::BUF_COLS * wg, C::PART_COLS, o_acc);
                     if constexpr (FP8) {
 #pragma unroll
                         for (int r = 0; r < NRV; ++r) o_acc[r] *= 0.0625f;  // the P split carries a factor 16
@@ -1268,13 +1173,14 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(o_empty);
+                if (lane == 0) mbar_arrive(o_empty + 8 * wg);
                 const int BW = p.ov_depth / P;  // this partition's output band
                 const int dv = my_lane;
                 if constexpr (C::MULTI) {
-                    // Push this rank's normalised partial into the band owners'
-                    // receive buffers (see splitk_merge_pushed) and go on with the
-                    // next unit; the epilogue warp merges.
+                    // Push this warpgroup's normalised partial (chunk NWG rank + wg)
+                    // into the band owners' receive buffers (see
+                    // splitk_merge_pushed) and go on with the next unit; the
+                    // epilogue warp merges.
                     const int rb = lu % C::RECV_BUFS, rk = lu / C::RECV_BUFS;
                     // Every receiver has finished with this buffer's previous unit.
                     if (rk >= 1)
@@ -1288,7 +1194,8 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                     for (int r = 0; r < NRV; ++r) v[r] = lrow[r] > 0.f ? o_acc[r] * __frcp_rn(lrow[r]) : 0.f;
                     const uint32_t recv0 = sbase + C::OFF_RECV + rb * C::RECV_BYTES;
                     const int q = dv / BW, col = dv % BW;
-                    const uint32_t o_dst = recv0 + 4u * (uint32_t)((rank * BW + col) * NRV);
+                    const int chunk = C::NWG * rank + wg;
+                    const uint32_t o_dst = recv0 + 4u * (uint32_t)((chunk * BW + col) * NRV);
                     if (P > 1) {
                         const uint32_t bar_q = map_shared_rank(recv_full + 8 * rb, q);
                         const uint32_t dst_q = map_shared_rank(o_dst, q);
@@ -1305,7 +1212,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                                     mm = m_run[r];
                                     ll = lrow[r];
                                 }
-                            const uint32_t ms_dst = recv0 + C::RECV_O_BYTES + 8u * (uint32_t)(rank * NRV + rr);
+                            const uint32_t ms_dst = recv0 + C::RECV_O_BYTES + 8u * (uint32_t)(chunk * NRV + rr);
                             st_async_f2(map_shared_rank(ms_dst, qq), mm, ll, map_shared_rank(recv_full + 8 * rb, qq));
                         }
                     } else {
@@ -1317,12 +1224,12 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                         if (wt == 0) {
                             float2* ms_loc = reinterpret_cast<float2*>(smem + (recv0 - sbase) + C::RECV_O_BYTES);
 #pragma unroll
-                            for (int r = 0; r < NRV; ++r) ms_loc[r] = make_float2(m_run[r], lrow[r]);
+                            for (int r = 0; r < NRV; ++r) ms_loc[chunk * NRV + r] = make_float2(m_run[r], lrow[r]);
                         }
                         __syncwarp();
                         if (lane == 0) mbar_arrive(recv_full + 8 * rb);
                     }
-                    if (wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
+                    if (lead && wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 3));
                 } else {
                     float* stage_s = reinterpret_cast<float*>(smem + C::OFF_STAGE);
                     const int q = dv / BW, jc = dv % BW;
@@ -1361,7 +1268,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         bool cluster_waited = false;
         int lu = 0;
         Unit w{u_first, 0, 0, 0};
-        const uint32_t expect = (uint32_t)pushed_bytes(P, p.band_cols, NRV);
+        const uint32_t expect = (uint32_t)pushed_bytes(C::NWG * P, p.band_cols, NRV);
         for (; next_unit(p, u_step, u_end, w, false); w.u += u_step, ++lu) {
             const int rb = lu % C::RECV_BUFS, rk = lu / C::RECV_BUFS;
             if (P > 1 && !cluster_waited) {
@@ -1386,12 +1293,12 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                                             reinterpret_cast<const float*>(recv),
                                             reinterpret_cast<const float2*>(recv + C::RECV_O_BYTES),
                                             reinterpret_cast<float*>(smem + C::OFF_WTAB),
-                                            reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), lane);
+                                            reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), lane, C::NWG * P);
             else
                 splitk_merge_pushed<NRV>(p, P, rank, w.b, w.kvh, reinterpret_cast<const float*>(recv),
                                          reinterpret_cast<const float2*>(recv + C::RECV_O_BYTES),
                                          reinterpret_cast<float*>(smem + C::OFF_WTAB),
-                                         reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), lane);
+                                         reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), lane, C::NWG * P);
             // Release the buffer to every sender: all lanes' reads of it are
             // complete (their results are in the band); one fence orders them
             // ahead of the senders' next pushes, then relaxed arrives.

@@ -268,14 +268,15 @@ __device__ __forceinline__ void splitk_merge_rows(const DecodeParams& p, int P, 
 // ---------------------------------------------------------------------------
 __host__ __device__ constexpr int pushed_bytes(int P, int BW, int RB) { return P * BW * RB * 4 + P * RB * 8; }
 
-// Merge by one warp (`lane` 0..31) of the partials in this rank's receive
-// buffer, cast, TMA store of the band and lse (rank 0). The caller has waited
-// for the buffer's recv_full phase; it releases the buffer afterwards.
-// `wtab` is float [P][RB] of scratch for the combine weights.
+// Merge by one warp (`lane` 0..31) of the `nq` partials in this rank's
+// receive buffer (one per rank, or one per (rank, softmax warpgroup)), cast,
+// TMA store of the band and lse (rank 0). The caller has waited for the
+// buffer's recv_full phase; it releases the buffer afterwards. `wtab` is
+// float [nq][RB] of scratch for the combine weights.
 template <int RB>
 __device__ __forceinline__ void splitk_merge_pushed(const DecodeParams& p, int P, int rank, int b, int kvh,
                                                     const float* recv_o, const float2* recv_ms, float* wtab,
-                                                    uint16_t* out_s, int lane)
+                                                    uint16_t* out_s, int lane, int nq)
 {
     const int BW = p.band_cols;
     const float c = p.scale_log2e;
@@ -286,19 +287,19 @@ __device__ __forceinline__ void splitk_merge_pushed(const DecodeParams& p, int P
     // w_q = sum_q * exp2((max_q - Gmax) * c) / Gsum (0 for an empty partition).
     for (int r = lane; r < RB; r += 32) {
         float gmax = -INFINITY;
-        for (int q = 0; q < P; ++q) {
+        for (int q = 0; q < nq; ++q) {
             const float2 ms = recv_ms[q * RB + r];
             if (ms.y > 0.f) gmax = fmaxf(gmax, ms.x);
         }
         float gsum = 0.f;
-        for (int q = 0; q < P; ++q) {
+        for (int q = 0; q < nq; ++q) {
             const float2 ms = recv_ms[q * RB + r];
             const float w = ms.y > 0.f ? ms.y * ex2_approx((ms.x - gmax) * c) : 0.f;
             wtab[q * RB + r] = w;
             gsum += w;
         }
         const float inv = gsum > 0.f ? 1.f / gsum : 0.f;
-        for (int q = 0; q < P; ++q) wtab[q * RB + r] *= inv;
+        for (int q = 0; q < nq; ++q) wtab[q * RB + r] *= inv;
         if (rank == 0 && r < p.rows && p.lse != nullptr) {
             const int t = r / p.heads_per_cta;
             const int h = kvh * p.group + r % p.heads_per_cta;
@@ -313,7 +314,7 @@ __device__ __forceinline__ void splitk_merge_pushed(const DecodeParams& p, int P
         float o[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) o[r] = 0.f;
-        for (int q = 0; q < P; ++q) {
+        for (int q = 0; q < nq; ++q) {
             const float4* src = reinterpret_cast<const float4*>(recv_o + (q * BW + col) * RB);
 #pragma unroll
             for (int r4 = 0; r4 < RB / 4; ++r4) {
@@ -345,18 +346,18 @@ __device__ __forceinline__ void splitk_merge_pushed(const DecodeParams& p, int P
 // last of the unit's clusters to count in for this band merges the chunks by
 // the same rule one level up (in cluster order, so the result does not depend
 // on which cluster comes last), stores the band and lse (rank 0) and resets
-// the count. `wtab` is float [max(P, 16)][RB]; a unit has at most 16 chunks.
+// the count. `wtab` is float [max(nq, 16)][RB]; a unit has at most 16 chunks.
 template <int RB>
 __device__ __noinline__ void splitk_merge_pushed_sk(const DecodeParams& p, int P, int rank, int b, int kvh, int u,
                                                     int cluster, const float* recv_o, const float2* recv_ms,
-                                                    float* wtab, uint16_t* out_s, int lane)
+                                                    float* wtab, uint16_t* out_s, int lane, int nq)
 {
     const int64_t Nv = p.sk_tiles, TOT = p.sk_total;
     const int G = p.sk_clusters;
     const int c_first = sk_cluster_of(TOT, G, (int64_t)u * Nv);
     const int S = sk_cluster_of(TOT, G, (int64_t)(u + 1) * Nv - 1) - c_first + 1;
     if (S == 1) {  // the unit lies in this cluster's range alone
-        splitk_merge_pushed<RB>(p, P, rank, b, kvh, recv_o, recv_ms, wtab, out_s, lane);
+        splitk_merge_pushed<RB>(p, P, rank, b, kvh, recv_o, recv_ms, wtab, out_s, lane, nq);
         return;
     }
     // Scratch slot of (cluster c, unit u): 2c, or 2c + 1 for the second unit
@@ -368,22 +369,22 @@ __device__ __noinline__ void splitk_merge_pushed_sk(const DecodeParams& p, int P
     const float c = p.scale_log2e;
     const int64_t mine = slot(cluster);
     float* const my_o = p.chunk_o + (mine * P + rank) * BW * RB;
-    // This chunk: weights over the cluster's ranks, then the band.
+    // This chunk: weights over the cluster's pushed partials, then the band.
     for (int r = lane; r < RB; r += 32) {
         float gmax = -INFINITY;
-        for (int q = 0; q < P; ++q) {
+        for (int q = 0; q < nq; ++q) {
             const float2 ms = recv_ms[q * RB + r];
             if (ms.y > 0.f) gmax = fmaxf(gmax, ms.x);
         }
         float gsum = 0.f;
-        for (int q = 0; q < P; ++q) {
+        for (int q = 0; q < nq; ++q) {
             const float2 ms = recv_ms[q * RB + r];
             const float w = ms.y > 0.f ? ms.y * ex2_approx((ms.x - gmax) * c) : 0.f;
             wtab[q * RB + r] = w;
             gsum += w;
         }
         const float inv = gsum > 0.f ? 1.f / gsum : 0.f;
-        for (int q = 0; q < P; ++q) wtab[q * RB + r] *= inv;
+        for (int q = 0; q < nq; ++q) wtab[q * RB + r] *= inv;
         p.chunk_ms[(mine * P + rank) * RB + r] = make_float2(gmax, gsum);
     }
     __syncwarp();
@@ -391,7 +392,7 @@ __device__ __noinline__ void splitk_merge_pushed_sk(const DecodeParams& p, int P
         float o[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) o[r] = 0.f;
-        for (int q = 0; q < P; ++q) {
+        for (int q = 0; q < nq; ++q) {
             const float4* src = reinterpret_cast<const float4*>(recv_o + (q * BW + col) * RB);
 #pragma unroll
             for (int r4 = 0; r4 < RB / 4; ++r4) {
