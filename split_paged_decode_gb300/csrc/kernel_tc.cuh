@@ -205,6 +205,13 @@ __device__ __forceinline__ bool next_unit(const DecodeParams& p, int stride, int
     return false;
 }
 
+// The unit after w: advances w.u by one stride, then as next_unit.
+__device__ __forceinline__ bool next_unit_after(const DecodeParams& p, int stride, int n_units, Unit& w, bool report)
+{
+    w.u += stride;
+    return next_unit(p, stride, n_units, w, report);
+}
+
 // The per-sequence split in one launch (FA4Config page, field
 // dynamic_cluster_dim: the cluster size a sequence uses is chosen at run
 // time). Every cluster has 4 CTAs. The (sequence, kv head) units are ordered
@@ -441,13 +448,16 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         if (t < gc && pslot < p.max_pages) spec_raw = p.page_table[(int64_t)b0 * p.max_pages + pslot];
     }
     if (u_first >= u_end && !idle) return;  // (grids never have more clusters than units or ranges)
-    if (p.auto_split) {
-        // A cluster with no unit in this launch (the per-sequence split gives
-        // its sequences to another launch) leaves at once; the decision is the
-        // same in every CTA of the cluster.
-        Unit first{u_first, 0, 0, 0};
-        if (!next_unit(p, u_step, u_end, first, tid == 0 && rank == 0)) return;
-    }
+    // The cluster's first unit (its sequence length), read by every thread
+    // now: a role that read it later would wait behind the ring's first
+    // copies, which the load warp is about to queue (measured: 6 us on the
+    // MMA warp at the start of a cold launch).
+    Unit first_unit{u_first, 0, 0, 0};
+    const bool have_first = u_first < u_end && next_unit(p, u_step, u_end, first_unit, tid == 0 && rank == 0);
+    // A cluster with no unit in this launch (the per-sequence split gives its
+    // sequences to another launch) leaves at once; the decision is the same in
+    // every CTA of the cluster.
+    if (p.auto_split && !have_first) return;
 
     const uint32_t bar0 = sbase + C::OFF_BAR;
     const uint32_t slot_full = bar0, slot_empty = bar0 + 8 * NSLOT;
@@ -539,8 +549,8 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             int J0 = 0, lu = 0;
             int GT = 0;  // global index of the unit's first tile
             bool ok = true;
-            Unit w{u_first, 0, 0, 0};
-            for (; ok && next_unit(p, u_step, u_end, w, tid == 0 && rank == 0); w.u += u_step, ++lu) {
+            Unit w = first_unit;
+            for (bool on = have_first; ok && on; on = next_unit_after(p, u_step, u_end, w, tid == 0 && rank == 0), ++lu) {
                 int tile_begin, tile_count;
                 rank_tiles(w.u, w.L, tile_begin, tile_count);
                 const int n_items = 2 * tile_count;
@@ -585,7 +595,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                     const bool scaled = FP8 && p.k_scale != nullptr;
                     const int gk = GT + t, kse = scaled ? gk % max(C::KS, 1) : 0;
                     if (scaled && got && k_here && gk >= C::KS)
-                        got = mbar_wait(ks_empty + 8 * kse, ((gk / C::KS) & 1) ^ 1, abort_flag, p.status,
+                        got = mbar_wait(ks_empty + 8 * kse, ((gk / max(C::KS, 1)) & 1) ^ 1, abort_flag, p.status,
                                         p.wait_limit_ns);
                     if (!__all_sync(0xffffffffu, got)) return false;
                     // A K tile of the pass that starts a new block of page entries.
@@ -700,8 +710,8 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             };
             int J0 = 0, gt = 0, lu = 0;
             bool ok = true;
-            Unit w{u_first, 0, 0, 0};
-            for (; ok && next_unit(p, u_step, u_end, w, false); w.u += u_step, ++lu) {
+            Unit w = first_unit;
+            for (bool on = have_first; ok && on; on = next_unit_after(p, u_step, u_end, w, false), ++lu) {
                 int tile_begin, tile_count;
                 rank_tiles(w.u, w.L, tile_begin, tile_count);
                 if (is_s) {
@@ -867,8 +877,8 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             }
         };
 
-        Unit w{u_first, 0, 0, 0};
-        bool have = next_unit(p, u_step, u_end, w, false);
+        Unit w = first_unit;
+        bool have = have_first;
         if (have && lead) {
             uint4 qv[2];
             load_q(w, qv);
@@ -1267,9 +1277,9 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         // the softmax warps work on the next unit.
         bool cluster_waited = false;
         int lu = 0;
-        Unit w{u_first, 0, 0, 0};
+        Unit w = first_unit;
         const uint32_t expect = (uint32_t)pushed_bytes(C::NWG * P, p.band_cols, NRV);
-        for (; next_unit(p, u_step, u_end, w, false); w.u += u_step, ++lu) {
+        for (bool on = have_first; on; on = next_unit_after(p, u_step, u_end, w, false), ++lu) {
             const int rb = lu % C::RECV_BUFS, rk = lu / C::RECV_BUFS;
             if (P > 1 && !cluster_waited) {
                 cluster_wait();  // every rank's barriers are initialised
