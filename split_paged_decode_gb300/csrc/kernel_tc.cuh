@@ -1090,17 +1090,20 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                         *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((((kk >> 3) ^ (r & 7))) << 4) +
                                                           (kk & 7) * 2) = __float2bfloat16_rn(s[r]);
                 } else {
-                    // P <= 16: the operands 16 e4m3(P) and e4m3(16 (P - e4m3(P))), [16 rows][128 keys]
+                    // P <= 16: the operands h = e4m3(16 P) and e4m3(16 P - h), [16 rows][128 keys],
+                    // two rows per packed conversion
                     uint8_t* pb = smem + C::OFF_P + (gi % C::NPB) * C::P_BYTES + (my_lane & 15);
                     const int kc = my_lane >> 4;
 #pragma unroll
-                    for (int r = 0; r < NRV; ++r) {
-                        float h, l;
-                        e4m3_split(s[r], h, l);
-                        const uint32_t hl = e4m3x2(h, l);
-                        const int off = r * 128 + ((kc ^ (r & 7)) << 4);
-                        pb[off] = (uint8_t)(hl & 0xff);
-                        pb[2048 + off] = (uint8_t)(hl >> 8);
+                    for (int r = 0; r < NRV; r += 2) {
+                        uint32_t hc, lc;
+                        e4m3_split2(16.f * s[r], 16.f * s[r + 1], hc, lc);
+                        const int off0 = r * 128 + ((kc ^ (r & 7)) << 4);
+                        const int off1 = (r + 1) * 128 + ((kc ^ ((r + 1) & 7)) << 4);
+                        pb[off0] = (uint8_t)(hc & 0xff);
+                        pb[off1] = (uint8_t)(hc >> 8);
+                        pb[2048 + off0] = (uint8_t)(lc & 0xff);
+                        pb[2048 + off1] = (uint8_t)(lc >> 8);
                     }
                 }
                 // Last tile of the sequence: zero the V rows past L so that unused
