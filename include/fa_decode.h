@@ -261,9 +261,11 @@ int fa_decode_describe(fa_decode_t h, char* buf, int size);
  * streams. A fixed split therefore never takes the stream-K partition (each
  * (sequence, kv head) key range stays on one cluster: on a single long
  * sequence, e.g. 131072 keys over 8 kv heads with split 8, that is 64 CTAs
- * instead of about 120, roughly 25-30 % slower than fa_decode_run), and the
- * per-sequence split (splitk 0) runs its three launches one after another on
- * `stream`. Results agree with fa_decode_run within the rounding tolerance.
+ * instead of about 120, roughly 25-30 % slower than fa_decode_run). The
+ * per-sequence split (splitk 0) runs as one launch on the tensor-core kernel,
+ * as in fa_decode_run; on the FMA and MLA kernels its launches (one per split
+ * size) run one after another on `stream`. Results agree with fa_decode_run
+ * within the rounding tolerance.
  */
 #define FA_NOALLOC_STATUS_SLOTS 64
 int fa_decode_run_noalloc(int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth, int ov_depth,
