@@ -1314,9 +1314,14 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                                          reinterpret_cast<uint16_t*>(smem + C::OFF_OUT), lane, C::NWG * P);
             // Release the buffer to every sender: all lanes' reads of it are
             // complete (their results are in the band); one fence orders them
-            // ahead of the senders' next pushes, then relaxed arrives.
+            // ahead of the senders' next pushes, then relaxed arrives. Only a
+            // unit RECV_BUFS later reuses the buffer: near the end there is
+            // none, and the cluster-scope fence is left out.
+            Unit later = w;
+            bool reused = true;
+            for (int k = 0; reused && k < C::RECV_BUFS; ++k) reused = next_unit_after(p, u_step, u_end, later, false);
             __syncwarp();
-            if (lane == 0) {
+            if (lane == 0 && reused) {
                 if (P > 1) {
                     fence_acq_rel_cluster();
                     for (int q = 0; q < P; ++q) mbar_arrive_cluster_relaxed(map_shared_rank(recv_free + 8 * rb, q));
