@@ -268,6 +268,73 @@ __device__ __forceinline__ void splitk_merge_rows(const DecodeParams& p, int P, 
 // ---------------------------------------------------------------------------
 __host__ __device__ constexpr int pushed_bytes(int P, int BW, int RB) { return P * BW * RB * 4 + P * RB * 8; }
 
+// Row r's weights over `nq` pushed partials (recv_ms [nq][RB]: raw max, sum):
+// Gmax over the partials that saw keys, Gsum, and
+// w_q = sum_q * exp2((max_q - Gmax) * c) / Gsum (0 for an empty partial) into
+// wtab [nq][RB]; returns (Gmax, Gsum). Partials are read four at a time
+// without a guard (the index clamped to nq - 1), so that a round's
+// shared-memory reads are in flight together; the sums keep partial order.
+template <int RB>
+__device__ __forceinline__ float2 partial_weights(const float2* recv_ms, float* wtab, int nq, int r, float c)
+{
+    float gmax = -INFINITY;
+    for (int q0 = 0; q0 < nq; q0 += 4) {
+        float2 m4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m4[j] = recv_ms[min(q0 + j, nq - 1) * RB + r];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (q0 + j < nq && m4[j].y > 0.f) gmax = fmaxf(gmax, m4[j].x);
+    }
+    float gsum = 0.f;
+    for (int q0 = 0; q0 < nq; q0 += 4) {
+        float2 m4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m4[j] = recv_ms[min(q0 + j, nq - 1) * RB + r];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (q0 + j < nq) {
+                const float w = m4[j].y > 0.f ? m4[j].y * ex2_approx((m4[j].x - gmax) * c) : 0.f;
+                wtab[(q0 + j) * RB + r] = w;
+                gsum += w;
+            }
+        }
+    }
+    const float inv = gsum > 0.f ? 1.f / gsum : 0.f;
+    for (int q = 0; q < nq; ++q) wtab[q * RB + r] *= inv;
+    return make_float2(gmax, gsum);
+}
+
+// o[RB] += sum over the nq partials of w_q * (partial q's column `col`)
+// (recv_o [nq][BW][RB]), in partial order, four partials' loads per round.
+template <int RB>
+__device__ __forceinline__ void partial_band(const float* recv_o, const float* wtab, int nq, int BW, int col,
+                                             float (&o)[RB])
+{
+    for (int q0 = 0; q0 < nq; q0 += 4) {
+        float4 v[4][RB / 4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4* src = reinterpret_cast<const float4*>(recv_o + (min(q0 + j, nq - 1) * BW + col) * RB);
+#pragma unroll
+            for (int r4 = 0; r4 < RB / 4; ++r4) v[j][r4] = src[r4];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (q0 + j < nq) {
+                const float* wq = wtab + (q0 + j) * RB;
+#pragma unroll
+                for (int r4 = 0; r4 < RB / 4; ++r4) {
+                    o[4 * r4 + 0] = fmaf(wq[4 * r4 + 0], v[j][r4].x, o[4 * r4 + 0]);
+                    o[4 * r4 + 1] = fmaf(wq[4 * r4 + 1], v[j][r4].y, o[4 * r4 + 1]);
+                    o[4 * r4 + 2] = fmaf(wq[4 * r4 + 2], v[j][r4].z, o[4 * r4 + 2]);
+                    o[4 * r4 + 3] = fmaf(wq[4 * r4 + 3], v[j][r4].w, o[4 * r4 + 3]);
+                }
+            }
+        }
+    }
+}
+
 // Merge by one warp (`lane` 0..31) of the `nq` partials in this rank's
 // receive buffer (one per rank, or one per (rank, softmax warpgroup)), cast,
 // TMA store of the band and lse (rank 0). The caller has waited for the
@@ -286,20 +353,8 @@ __device__ __forceinline__ void splitk_merge_pushed(const DecodeParams& p, int P
     // Per row: Gmax over the partitions that saw keys, Gsum, and the weights
     // w_q = sum_q * exp2((max_q - Gmax) * c) / Gsum (0 for an empty partition).
     for (int r = lane; r < RB; r += 32) {
-        float gmax = -INFINITY;
-        for (int q = 0; q < nq; ++q) {
-            const float2 ms = recv_ms[q * RB + r];
-            if (ms.y > 0.f) gmax = fmaxf(gmax, ms.x);
-        }
-        float gsum = 0.f;
-        for (int q = 0; q < nq; ++q) {
-            const float2 ms = recv_ms[q * RB + r];
-            const float w = ms.y > 0.f ? ms.y * ex2_approx((ms.x - gmax) * c) : 0.f;
-            wtab[q * RB + r] = w;
-            gsum += w;
-        }
-        const float inv = gsum > 0.f ? 1.f / gsum : 0.f;
-        for (int q = 0; q < nq; ++q) wtab[q * RB + r] *= inv;
+        const float2 gm = partial_weights<RB>(recv_ms, wtab, nq, r, c);
+        const float gmax = gm.x, gsum = gm.y;
         if (rank == 0 && r < p.rows && p.lse != nullptr) {
             const int t = r / p.heads_per_cta;
             const int h = kvh * p.group + r % p.heads_per_cta;
@@ -314,17 +369,7 @@ __device__ __forceinline__ void splitk_merge_pushed(const DecodeParams& p, int P
         float o[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) o[r] = 0.f;
-        for (int q = 0; q < nq; ++q) {
-            const float4* src = reinterpret_cast<const float4*>(recv_o + (q * BW + col) * RB);
-#pragma unroll
-            for (int r4 = 0; r4 < RB / 4; ++r4) {
-                const float4 v = src[r4];
-                o[4 * r4 + 0] = fmaf(wtab[q * RB + 4 * r4 + 0], v.x, o[4 * r4 + 0]);
-                o[4 * r4 + 1] = fmaf(wtab[q * RB + 4 * r4 + 1], v.y, o[4 * r4 + 1]);
-                o[4 * r4 + 2] = fmaf(wtab[q * RB + 4 * r4 + 2], v.z, o[4 * r4 + 2]);
-                o[4 * r4 + 3] = fmaf(wtab[q * RB + 4 * r4 + 3], v.w, o[4 * r4 + 3]);
-            }
-        }
+        partial_band<RB>(recv_o, wtab, nq, BW, col, o);
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(out_s) + (col / OC) * RB * OC + col % OC;
 #pragma unroll
         for (int r = 0; r < RB; ++r) dst[r * OC] = __float2bfloat16_rn(o[r]);
@@ -371,20 +416,8 @@ __device__ __noinline__ void splitk_merge_pushed_sk(const DecodeParams& p, int P
     float* const my_o = p.chunk_o + (mine * P + rank) * BW * RB;
     // This chunk: weights over the cluster's pushed partials, then the band.
     for (int r = lane; r < RB; r += 32) {
-        float gmax = -INFINITY;
-        for (int q = 0; q < nq; ++q) {
-            const float2 ms = recv_ms[q * RB + r];
-            if (ms.y > 0.f) gmax = fmaxf(gmax, ms.x);
-        }
-        float gsum = 0.f;
-        for (int q = 0; q < nq; ++q) {
-            const float2 ms = recv_ms[q * RB + r];
-            const float w = ms.y > 0.f ? ms.y * ex2_approx((ms.x - gmax) * c) : 0.f;
-            wtab[q * RB + r] = w;
-            gsum += w;
-        }
-        const float inv = gsum > 0.f ? 1.f / gsum : 0.f;
-        for (int q = 0; q < nq; ++q) wtab[q * RB + r] *= inv;
+        const float2 gm = partial_weights<RB>(recv_ms, wtab, nq, r, c);
+        const float gmax = gm.x, gsum = gm.y;
         p.chunk_ms[(mine * P + rank) * RB + r] = make_float2(gmax, gsum);
     }
     __syncwarp();
@@ -392,17 +425,7 @@ __device__ __noinline__ void splitk_merge_pushed_sk(const DecodeParams& p, int P
         float o[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) o[r] = 0.f;
-        for (int q = 0; q < nq; ++q) {
-            const float4* src = reinterpret_cast<const float4*>(recv_o + (q * BW + col) * RB);
-#pragma unroll
-            for (int r4 = 0; r4 < RB / 4; ++r4) {
-                const float4 v = src[r4];
-                o[4 * r4 + 0] = fmaf(wtab[q * RB + 4 * r4 + 0], v.x, o[4 * r4 + 0]);
-                o[4 * r4 + 1] = fmaf(wtab[q * RB + 4 * r4 + 1], v.y, o[4 * r4 + 1]);
-                o[4 * r4 + 2] = fmaf(wtab[q * RB + 4 * r4 + 2], v.z, o[4 * r4 + 2]);
-                o[4 * r4 + 3] = fmaf(wtab[q * RB + 4 * r4 + 3], v.w, o[4 * r4 + 3]);
-            }
-        }
+        partial_band<RB>(recv_o, wtab, nq, BW, col, o);
         float4* dst = reinterpret_cast<float4*>(my_o + col * RB);
 #pragma unroll
         for (int r4 = 0; r4 < RB / 4; ++r4) dst[r4] = make_float4(o[4 * r4], o[4 * r4 + 1], o[4 * r4 + 2], o[4 * r4 + 3]);
@@ -422,10 +445,15 @@ __device__ __noinline__ void splitk_merge_pushed_sk(const DecodeParams& p, int P
     // flight at once: these reads queue behind the streaming loads.
     if (lane < RB) {
         const int r = lane;
+        // Loads without a guard (chunks past S read chunk S - 1 and are
+        // dropped below), so that all of them are in flight at once.
         float2 ms[kMaxSplit];
 #pragma unroll
         for (int k = 0; k < kMaxSplit; ++k)
-            ms[k] = k < S ? __ldcg(p.chunk_ms + (slot(c_first + k) * P + rank) * RB + r) : make_float2(-INFINITY, 0.f);
+            ms[k] = __ldcg(p.chunk_ms + (slot(c_first + min(k, S - 1)) * P + rank) * RB + r);
+#pragma unroll
+        for (int k = 0; k < kMaxSplit; ++k)
+            if (k >= S) ms[k] = make_float2(-INFINITY, 0.f);
         float gmax = -INFINITY;
 #pragma unroll
         for (int k = 0; k < kMaxSplit; ++k)
@@ -459,21 +487,25 @@ __device__ __noinline__ void splitk_merge_pushed_sk(const DecodeParams& p, int P
     const int OC = p.out_chunk_cols;
     for (int idx = lane; idx < BW * (RB / 4); idx += 32) {
         const int col = idx / (RB / 4), r4 = idx % (RB / 4);
-        float4 v[kMaxSplit];
-#pragma unroll
-        for (int k = 0; k < kMaxSplit; ++k)
-            if (k < S)
-                v[k] = __ldcg(reinterpret_cast<const float4*>(p.chunk_o + ((slot(c_first + k) * P + rank) * BW + col) * RB) +
-                              r4);
+        // Four chunks per round, loaded without a guard (clamped to chunk
+        // S - 1), so a round's loads are in flight at once.
         float o[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k0 = 0; k0 < S; k0 += 4) {
+            float4 v[4];
 #pragma unroll
-        for (int k = 0; k < kMaxSplit; ++k) {
-            if (k < S) {
-                const float* wr = wtab + k * RB + 4 * r4;
-                o[0] = fmaf(wr[0], v[k].x, o[0]);
-                o[1] = fmaf(wr[1], v[k].y, o[1]);
-                o[2] = fmaf(wr[2], v[k].z, o[2]);
-                o[3] = fmaf(wr[3], v[k].w, o[3]);
+            for (int j = 0; j < 4; ++j)
+                v[j] = __ldcg(reinterpret_cast<const float4*>(
+                                  p.chunk_o + ((slot(c_first + min(k0 + j, S - 1)) * P + rank) * BW + col) * RB) +
+                              r4);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (k0 + j < S) {
+                    const float* wr = wtab + (k0 + j) * RB + 4 * r4;
+                    o[0] = fmaf(wr[0], v[j].x, o[0]);
+                    o[1] = fmaf(wr[1], v[j].y, o[1]);
+                    o[2] = fmaf(wr[2], v[j].z, o[2]);
+                    o[3] = fmaf(wr[3], v[j].w, o[3]);
+                }
             }
         }
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(out_s) + (col / OC) * RB * OC + col % OC;
