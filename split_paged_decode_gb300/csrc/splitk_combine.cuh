@@ -75,6 +75,59 @@ __device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, in
     }
 
     const int chunks = BW / 4;
+    if (P <= 4) {
+        // Up to four partitions (the per-sequence split): every partition's
+        // (max, sum) and band values of an item are loaded before any is used,
+        // so the remote reads are in flight together; the sums keep partition
+        // order and skip empty partitions as the general loop below does.
+        for (int it = tid; it < RB * chunks; it += nthreads) {
+            const int r = it / chunks;
+            const int j = (it % chunks) * 4;
+            const uint32_t off = 4u * ((uint32_t)(rank * RB + r) * BW + j);
+            float2 ms[4];
+            float4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int qq = rbase + min(q, P - 1);
+                ms[q] = (P > 1) ? ld_dsmem_f2(map_shared_rank(maxsum_base + 8u * r, qq)) : maxsum_s[r];
+                v[q] = (P > 1) ? ld_dsmem_f4(map_shared_rank(stage_base + off, qq))
+                               : *reinterpret_cast<const float4*>(stage_s + (rank * RB + r) * BW + j);
+            }
+            float gmax = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (q < P && ms[q].y > 0.f) gmax = fmaxf(gmax, ms[q].x);
+            float wq[4];
+            float gsum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                wq[q] = (q < P && ms[q].y > 0.f) ? ms[q].y * ex2_approx((ms[q].x - gmax) * c) : 0.f;
+                gsum += wq[q];
+            }
+            const float inv = gsum > 0.f ? 1.f / gsum : 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (wq[q] > 0.f) {
+                    const float w = wq[q] * inv;
+                    o.x = fmaf(w, v[q].x, o.x);
+                    o.y = fmaf(w, v[q].y, o.y);
+                    o.z = fmaf(w, v[q].z, o.z);
+                    o.w = fmaf(w, v[q].w, o.w);
+                }
+            }
+            uint2 packed = make_uint2(float2_to_bf16x2(o.x, o.y), float2_to_bf16x2(o.z, o.w));
+            const int OC = p.out_chunk_cols;
+            *reinterpret_cast<uint2*>(out_s + ((j / OC) * RB + r) * OC + j % OC) = packed;
+            if (rank == 0 && j == 0 && r < p.rows && p.lse != nullptr) {
+                const int t = r / p.heads_per_cta;
+                const int h = kvh * p.group + row_block * p.heads_per_cta + r % p.heads_per_cta;
+                const float lse = gsum > 0.f ? p.scale * gmax + lg2_approx(gsum) * 0.6931471805599453f
+                                             : -INFINITY;
+                p.lse[((int64_t)b * p.num_q + t) * p.num_q_heads + h] = lse;
+            }
+        }
+    } else
     for (int it = tid; it < RB * chunks; it += nthreads) {
         const int r = it / chunks;
         const int j = (it % chunks) * 4;
