@@ -78,14 +78,39 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and with whitespace collapsed (string
+    literals are kept as they are, apart from whitespace)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif text[i] == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the device-code sources (the host planner's files are excluded)."""
+    """Hash of the device code (the host planner's files are excluded; comments
+    and whitespace do not count, so an edit of comments keeps the stored ncu
+    traffic of the same code)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "split_paged_decode_gb300", "csrc")
     for f in sorted(os.listdir(d)):
         if f.endswith((".cu", ".cuh", ".h")) and f not in ("fa_decode_host.cu", "stream_k_plan.h"):
             h.update(f.encode())
-            h.update(open(os.path.join(d, f), "rb").read())
+            h.update(_code_only(open(os.path.join(d, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

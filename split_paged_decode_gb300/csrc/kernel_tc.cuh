@@ -14,10 +14,11 @@
 // fp8 cache (FA4Config page: qkv_dtype E4M3, scale_dtype_ for the per-token K
 // scale): the E4M3 tiles feed kind::f8f6f4 MMAs straight from the TMA ring
 // (K = 32 per MMA). Q and P are bf16 / fp32 quantities, so each is carried
-// as two E4M3 operands, x ~ 16 h + l with h = e4m3(x) and l = e4m3(16 (x - h))
-// (Q first scaled by a power of two per row so that |16 h| <= 448), both
-// accumulated into the same fp32 accumulator; this keeps about 8 bits of x,
-// as bf16 does. S = acc / (16 sigma_r) times the key's scale, O = acc / 16.
+// as two E4M3 operands whose sum is 16 x to about 2^-8 (fp8.cuh: Q as
+// 16 e4m3(x) + e4m3(16 (x - e4m3(x))) after a power-of-two scale per row;
+// P <= 16 as e4m3(16 P) + e4m3(16 P - e4m3(16 P))), both accumulated into the
+// same fp32 accumulator; this keeps about 8 bits of x, as bf16 does.
+// S = acc / (16 sigma_r) times the key's scale, O = acc / 16.
 // The per-token K scales reach the softmax threads through a small ring of
 // bulk copies (one per page segment) with its own full / empty barriers.
 //
@@ -29,18 +30,21 @@
 //              128-byte-swizzled boxes per page segment, one lane per
 //              segment) into a ring of NSLOT 32 KB slots, in the order the
 //              MMA warps consume them (V lagging K by VLAG tiles, see k_item)
-//   warp 1     MMA S: allocates 256 TMEM columns (S and O, two buffers of four
-//              accumulators each) and issues every S_i = K_i Q^T;
-//   warp 2     MMA O: issues every O_t = V_t^T P_t^T; each MMA warp commits a
-//              tile's products to the softmax warps and to the ring slot it read;
-//   warps 3-6  softmax + correction (thread = TMEM lane = key for S, = value
-//              column for O): online softmax in exp2 form with the running
-//              max in raw score units, P^T to shared memory as bf16, and the
-//              correction O <- O * alpha + O_tile in registers; then the
+//   warp 1     MMA S: allocates 256 TMEM columns (two S buffers of four
+//              accumulators, then one O fragment per softmax warpgroup) and
+//              issues every S_i = K_i Q^T;
+//   warp 2     MMA O: issues every O_t += V_t^T P_t^T into the fragment of the
+//              tile's warpgroup; each MMA warp commits a tile's products to the
+//              softmax warps and to the ring slot it read;
+//   warps 3-6  softmax (and 7-10 for a second warpgroup on alternate tiles;
+//              thread = TMEM lane = key for S, = value column for O): online
+//              softmax in exp2 form with the running max in raw score units,
+//              P^T to shared memory, and the correction O <- O * alpha applied
+//              to the TMEM fragment in place when a row's max moves; then the
 //              split-K epilogue (splitk_combine.cuh): in the shallow-ring
-//              variant they merge themselves, in the deep-ring variant they
-//              push their partial to the band owners and go on;
-//   warp 7     (deep ring) epilogue: merges the pushed partials, stores the band.
+//              variant they merge themselves, in the deep-ring variant each
+//              warpgroup pushes its partial to the band owners and goes on;
+//   last warp  (deep ring) epilogue: merges the pushed partials, stores the band.
 //
 // Geometry and vocabulary follow the FA4Config page (Modular MAX docs):
 // TMEM_S / TMEM_O / TMEM_P column maps, num_kv_stages, GQA fusion (field
@@ -803,12 +807,12 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         }
         __syncwarp();
     } else if (warp < C::EPI) {
-        // ------------------------------------------------- softmax / correction warps
+        // ------------------------------------------------- softmax warps
         // NWG warpgroups; warpgroup g takes the unit's tiles whose index is g
-        // modulo NWG and keeps its own running max, sum and O; at the end of a
-        // unit the second folds its partial into the first, which pushes the
-        // result. Buffers of S, P and O are indexed by the global tile index,
-        // so any warpgroup may consume any buffer; the barrier phases order it.
+        // modulo NWG and keeps its own running max, sum and TMEM O fragment; at
+        // the end of a unit each pushes its own partial. Buffers of S and P are
+        // indexed by the global tile index, so any warpgroup may consume any
+        // buffer; the barrier phases order it.
         const int wg = (warp - C::WG0) >> 2;          // softmax warpgroup
         const int wt = tid - 32 * C::WG0 - 128 * wg;  // 0..127 within it
         const uint32_t wg_bar = 1 + wg;               // its named barrier
@@ -1048,12 +1052,10 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                     s[r] = pr;
                 }
 
-                // P (bf16) -> K-major swizzled B operand of O^T = V^T P^T (rows >= NRV
-                // only feed output columns that are never read). Buffer gi % NPB was
-                // last read by O of global tile gi - NPB, whose completion a
-                // correction has observed: one warpgroup folded it in during its
-                // previous tile, as do two with four buffers; two warpgroups with
-                // two buffers fold it in here, before the store.
+                // P -> K-major swizzled B operand of O^T = V^T P^T (rows >= NRV only
+                // feed output columns that are never read). Buffer gi % NPB was last
+                // read by O of global tile gi - NPB, which must have completed before
+                // the store (and O(gi - 1) before a rescale of the fragment).
                 if constexpr (C::O_BAR_BY_FRAG) {
                     // The fragment's previous O product read the P buffer this tile
                     // reuses, and must finish before a rescale touches the fragment.
