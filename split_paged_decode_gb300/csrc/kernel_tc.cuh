@@ -130,6 +130,10 @@ struct TcCfg {
     // previous one; with two they go by fragment.
     static constexpr bool O_BAR_BY_FRAG = NWG == 2;
     static constexpr int N_OBAR = O_BAR_BY_FRAG ? 2 : NPB;
+    // Two warpgroups with four P buffers also count O products by P buffer
+    // (o_buf), so that writing P(t) waits for O(t - 4), the buffer's previous
+    // reader, and only a rescale waits for the fragment's previous product.
+    static constexpr bool O_BUF_BAR = O_BAR_BY_FRAG && NPB > 2;
     static constexpr int TMEM_S0 = 0, TMEM_O0 = 2 * BUF_COLS;     // S [2], then O [NWG]
     static constexpr int TMEM_COLS = 256;
     // Units with at least this many tiles per rank are issued two items per
@@ -149,8 +153,9 @@ struct TcCfg {
     // p_full[2], o_full[2], o_empty[2], q_full[2], q_empty[2], publish,
     // mma_done, tmem_ready, recv_full[2], recv_free[2], (spare)
     // then (fp8) ks_full[KS], ks_empty[KS], then p_full[NPB], o_full[NPB],
-    // o_empty[NPB] (the pairs above at p_full / o_full / o_empty are unused)
-    static constexpr int NBAR = 2 * NSLOT + 22 + 2 * KS + 3 * NPB;
+    // o_empty[NPB], (O_BUF_BAR) o_buf[NPB] (the pairs above at p_full /
+    // o_full / o_empty are unused)
+    static constexpr int NBAR = 2 * NSLOT + 22 + 2 * KS + 3 * NPB + (O_BUF_BAR ? NPB : 0);
     static constexpr int OFF_ROWS = OFF_BAR + NBAR * 8;          // int [4 tiles][16 segments]
     static constexpr int OFF_MISC = OFF_ROWS + 4 * 16 * 4;       // tmem base, abort, S next item, O next item
     static constexpr int OFF_KS = (OFF_MISC + 16 + 127) / 128 * 128;      // float [KS][BN]
@@ -473,6 +478,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
     const uint32_t ks_full = bar0 + 8 * (2 * NSLOT + 22), ks_empty = ks_full + 8 * C::KS;
     // P / O buffers, by global tile index gi: buffer gi % NPB, phase (gi / NPB) & 1
     const uint32_t p_full = ks_empty + 8 * C::KS, o_full = p_full + 8 * C::NPB, o_empty = o_full + 8 * C::NPB;
+    const uint32_t o_buf = o_empty + 8 * C::NPB;  // O_BUF_BAR: O products by P buffer
     float* ks_s = reinterpret_cast<float*>(smem + C::OFF_KS);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -511,6 +517,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         for (int i = 0; i < C::NPB; ++i) {
             mbar_init(p_full + 8 * i, 4);    // the four softmax warps that wrote P
             mbar_init(o_full + 8 * i, 1);    // the O warp's commit
+            if (C::O_BUF_BAR) mbar_init(o_buf + 8 * i, 1);
             // o_empty[f]: the four warps of warpgroup f, once they have read its fragment at the end of a unit
             mbar_init(o_empty + 8 * i, 4);
         }
@@ -789,7 +796,12 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                                 umma_f8_ss(d + C::ACC_COLS * (ks % C::NACC), a0 + (uint64_t)((ks * 4096) >> 4),
                                            b0 + (uint64_t)((ks * 32) >> 4), id_pv, acc_all || ks >= C::NACC);
                         }
-                        umma_commit(o_full + 8 * (C::O_BAR_BY_FRAG ? frag : (gi % C::NPB)));
+                        // O completion, for the softmax warps: by P buffer (o_buf with two
+                        // warpgroups and four buffers, o_full with one), else by fragment
+                        if constexpr (C::O_BUF_BAR)
+                            umma_commit(o_buf + 8 * (gi % C::NPB));
+                        else
+                            umma_commit(o_full + 8 * (C::O_BAR_BY_FRAG ? frag : (gi % C::NPB)));
                         umma_commit(slot_empty + 8 * slot);  // V_t's slot is free once O_t has completed
                         st_release_u32(o_next, (uint32_t)(t + 1 < tile_count ? J0 + v_item<C::VLAG>(t + 1, tile_count)
                                                                              : J0 + 2 * tile_count));
@@ -1056,9 +1068,33 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 // feed output columns that are never read). Buffer gi % NPB was last
                 // read by O of global tile gi - NPB, which must have completed before
                 // the store (and O(gi - 1) before a rescale of the fragment).
-                if constexpr (C::O_BAR_BY_FRAG) {
-                    // The fragment's previous O product read the P buffer this tile
-                    // reuses, and must finish before a rescale touches the fragment.
+                if constexpr (C::O_BUF_BAR) {
+                    // Four P buffers, O products counted by buffer (o_buf): the
+                    // buffer's previous reader is O(gi - 4), this warpgroup's product
+                    // before its previous one in the unit (earlier units' products
+                    // have all been waited for at the unit's end); a rescale also
+                    // waits for O(gi - 2), the fragment's previous product. Each wait
+                    // is for the phase right after one already waited for on the same
+                    // barrier, so no parity wait can alias.
+                    if (wc_unit > 0) {
+                        if (gi - C::NPB >= gt) {
+                            const int gp = gi - C::NPB;
+                            mbar_wait(o_buf + 8 * (gp % C::NPB), (gp / C::NPB) & 1, abort_flag, p.status,
+                                      p.wait_limit_ns);
+                        }
+                        if (rescale) {
+                            const int gp = gi - 2;
+                            mbar_wait(o_buf + 8 * (gp % C::NPB), (gp / C::NPB) & 1, abort_flag, p.status,
+                                      p.wait_limit_ns);
+                            tc_fence_after_sync();
+                            tmem_scale4<NRV>(tmem + lane_addr + C::TMEM_O0 + C::BUF_COLS * wg, C::PART_COLS, alpha);
+                            tc_fence_before_sync();
+                        }
+                    }
+                } else if constexpr (C::O_BAR_BY_FRAG) {
+                    // Two P buffers: the fragment's previous O product read the buffer
+                    // this tile reuses (and must finish before a rescale touches the
+                    // fragment); waited for on every tile.
                     if (wc_unit > 0) {
                         mbar_wait(o_full + 8 * wg, (wc - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
                         tc_fence_after_sync();
@@ -1068,9 +1104,15 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                         }
                     }
                 } else {
-                    // One warpgroup: a rescale waits for the previous tile's O (and
-                    // with it every earlier one); otherwise only the product that
-                    // read this P buffer, NPB tiles back, has to be complete.
+                    // One warpgroup: the product that read this P buffer, NPB tiles
+                    // back, has to be complete (waited on every tile, which keeps each
+                    // buffer's barrier at most one phase behind); a rescale also waits
+                    // for the previous tile's O, and with it every earlier one.
+                    if (gi >= C::NPB) {
+                        const int gp = gi - C::NPB;
+                        mbar_wait(o_full + 8 * (gp % C::NPB), (gp / C::NPB) & 1, abort_flag, p.status,
+                                  p.wait_limit_ns);
+                    }
                     if (rescale && i > 0) {
                         const int gp = gi - 1;
                         mbar_wait(o_full + 8 * (gp % C::NPB), (gp / C::NPB) & 1, abort_flag, p.status,
@@ -1078,10 +1120,6 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                         tc_fence_after_sync();
                         tmem_scale4<NRV>(tmem + lane_addr + C::TMEM_O0, C::PART_COLS, alpha);
                         tc_fence_before_sync();
-                    } else if (gi >= C::NPB) {
-                        const int gp = gi - C::NPB;
-                        mbar_wait(o_full + 8 * (gp % C::NPB), (gp / C::NPB) & 1, abort_flag, p.status,
-                                  p.wait_limit_ns);
                     }
                 }
                 if constexpr (!FP8) {
@@ -1138,10 +1176,23 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
             }
             // Bounded even after an abort. After an abort the O of the tile
             // that broke the loop was never issued; the wait gives up at once.
-            if (wc_unit > 0) {  // the fragment's last product is complete
-                const int gl = C::O_BAR_BY_FRAG ? wg : (gt + wc_unit - 1) % C::NPB;
-                const int ph = C::O_BAR_BY_FRAG ? (wc - 1) : (gt + wc_unit - 1) / C::NPB;
-                mbar_wait(o_full + 8 * gl, ph & 1, abort_flag, p.status, p.wait_limit_ns);
+            if (wc_unit > 0) {
+                // The fragment's last product is complete. Counted by P buffer,
+                // the warpgroup's last two products are waited for in order, so
+                // that every product of the unit has been waited for on its
+                // barrier before the next unit's first waits.
+                if constexpr (C::O_BAR_BY_FRAG && !C::O_BUF_BAR) {
+                    mbar_wait(o_full + 8 * wg, (wc - 1) & 1, abort_flag, p.status, p.wait_limit_ns);
+                } else {
+                    const int step = C::NWG;  // between a warpgroup's consecutive tiles
+                    const uint32_t bars = C::O_BUF_BAR ? o_buf : o_full;
+                    const int g_last = gt + (C::NWG == 2 ? wg : 0) + C::NWG * (wc_unit - 1);  // its last tile
+                    for (int k = (wc_unit >= 2 ? 1 : 0); k >= 0; --k) {
+                        const int gp = g_last - k * step;
+                        mbar_wait(bars + 8 * (gp % C::NPB), (gp / C::NPB) & 1, abort_flag, p.status,
+                                  p.wait_limit_ns);
+                    }
+                }
                 tc_fence_after_sync();
             }
             if (lead && wt == 0 && lu < kTraceUnits) stamp(unit_slot(lu, 2));
