@@ -123,3 +123,31 @@ def check_against_oracle(call: DeviceCall, rows=None, what=""):
         ref_out, ref_lse = run_oracle(call.inp, rows=rows)
         compare(out[rows[:, 0], rows[:, 1], rows[:, 2]], lse[rows[:, 0], rows[:, 1], rows[:, 2]],
                 ref_out, ref_lse, what)
+
+
+def ramp_keys(inp, alpha: float = 0.01):
+    """Make the running max move on nearly every tile: key j of every sequence
+    becomes alpha * (j + 1) in every component (E4M3 caches: codes of those
+    values with a unit per-token scale) and every query row becomes all ones,
+    so a row's scores rise by 128 * alpha per key, about 20 exp2 units per
+    128-key tile at scale 1/sqrt(128): above both rescale thresholds (2^8,
+    2^4). Rows past a sequence's end keep their garbage (they must stay
+    masked). Returns inp, modified in place."""
+    w = inp.workload
+    ps = w.page_size
+    e4m3 = w.kv_dtype == "e4m3"
+    for b, L in enumerate(inp.seq_lens.tolist()):
+        for pi in range((int(L) + ps - 1) // ps):
+            page = int(inp.page_table[b, pi])
+            n = min(ps, int(L) - pi * ps)
+            vals = alpha * (torch.arange(pi * ps, pi * ps + n, dtype=torch.float32) + 1.0)
+            block = vals[:, None].expand(n, inp.k_pages.shape[3])
+            if e4m3:
+                codes = block.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+                inp.k_pages[page, :, :n, :] = codes
+                if inp.k_scale is not None:
+                    inp.k_scale[page, :, :n] = 1.0
+            else:
+                inp.k_pages[page, :, :n, :] = block.to(inp.k_pages.dtype)
+    inp.q.fill_(1.0)
+    return inp

@@ -14,7 +14,7 @@ import split_paged_decode_gb300 as spd
 from split_paged_decode_gb300.workloads import WORKLOADS, DecodeWorkload, generate
 
 import dominant
-from helpers import DeviceCall, check_against_oracle
+from helpers import DeviceCall, check_against_oracle, ramp_keys
 
 pytestmark = pytest.mark.gpu
 
@@ -151,3 +151,20 @@ def test_workload_full_size(name):
     """The head-dim-128 workloads with an E4M3 cache and per-token K scales."""
     w = WORKLOADS[name].with_(kv_dtype="e4m3", k_scale=True)
     run_and_check(w, what=f"{name} e4m3")
+
+
+@pytest.mark.parametrize("case, kw, path", [
+    ("deep_4rows", dict(batch=2, splitk=4, seq_len_lo=1500, seq_len_hi=2600, seed=980), "auto"),
+    ("multi_unit", dict(batch=7, splitk=2, seq_len_lo=300, seq_len_hi=2600, seed=981), "two_clusters"),
+    ("stream_k_8rows", dict(batch=1, num_q_heads=16, splitk=8, seq_len_lo=9000, seq_len_hi=9000, seed=982), "auto"),
+    ("shallow_16rows", dict(batch=4, num_q=4, splitk=0, seq_len_lo=100, seq_len_hi=3000, seed=983), "auto"),
+])
+def test_running_max_moves_every_tile(case, kw, path):
+    """The fp8 kernel's rescale path on most tiles (threshold 2^4): scores rising
+    along the keys, against the fp8 oracle."""
+    inp = ramp_keys(generate(wl(**kw)))
+    with DeviceCall(inp, path=path) as call:
+        assert "e4m3" in call.describe(), call.describe()
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what=f"fp8 ramp {case}")

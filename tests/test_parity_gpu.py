@@ -12,7 +12,7 @@ import torch
 import split_paged_decode_gb300 as spd
 from split_paged_decode_gb300.workloads import WORKLOADS, DecodeWorkload, generate
 
-from helpers import DeviceCall, check_against_oracle, compare, run_oracle
+from helpers import DeviceCall, check_against_oracle, compare, ramp_keys, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -490,3 +490,28 @@ def test_chained_launches_read_the_previous_output(splitk):
             chained.q = a.out.cpu()
             b.inp = chained
             check_against_oracle(b, what="chain second")
+
+
+RAMP_CASES = {
+    # two softmax warpgroups, 4 rows, one unit per cluster
+    "deep_4rows": (dict(batch=2, splitk=4, seq_len_lo=1500, seq_len_hi=2600, seed=130), "auto"),
+    # 8 rows under the stream-K partition (2 units, fewer than the resident clusters)
+    "stream_k_8rows": (dict(batch=1, num_q_heads=16, splitk=8, seq_len_lo=9000, seq_len_hi=9000, seed=131), "auto"),
+    # two clusters, each working through several units in turn
+    "multi_unit": (dict(batch=5, splitk=2, seq_len_lo=300, seq_len_hi=2600, seed=132), "two_clusters"),
+    # 16 rows (4 tokens x group 4, causal) on the shallow ring, the per-sequence split in one launch
+    "shallow_16rows": (dict(batch=4, num_q=4, splitk=0, seq_len_lo=100, seq_len_hi=3000, seed=133), "auto"),
+}
+
+
+@pytest.mark.parametrize("case", sorted(RAMP_CASES))
+def test_running_max_moves_every_tile(case):
+    """Scores that rise along the keys move every row's running max on nearly
+    every tile, so the in-place rescale of the TMEM O fragment (after the
+    fragment's previous product) runs on most tiles, against the oracle."""
+    kw, path = RAMP_CASES[case]
+    inp = ramp_keys(generate(wl(**kw)))
+    with DeviceCall(inp, path=path) as call:
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what=f"ramp {case}")
