@@ -421,8 +421,12 @@ def measure(spd, torch, w, dev, stream, steps, warmup, flush, clocks, keep=False
     else:
         h = spd.fa_decode_create(w.num_q_heads, w.num_kv_heads, w.qk_depth, w.nope_depth, w.ov_depth,
                                  w.page_size, w.num_q, w.splitk)
-    m.kernel = spd.fa_decode_describe(h).split()[1].split("=", 1)[1]
-    m.launches_per_step = 3 if w.splitk == 0 else 1
+    desc = spd.fa_decode_describe(h)
+    m.kernel = desc.split()[1].split("=", 1)[1]
+    # The per-sequence split (splitk 0) is one launch of 4-CTA clusters on the
+    # tensor-core path, which the description states, for up to 4096
+    # sequences; otherwise one launch per cluster size (1, 2, 4).
+    m.launches_per_step = 1 if w.splitk != 0 or ("one launch" in desc and w.batch <= 4096) else 3
 
     def step():
         if e4m3:

@@ -25,14 +25,17 @@
 //               (thread = TMEM lane = key for S^T, = value column for O^T);
 //               online softmax in exp2 form, P^T to shared memory as bf16,
 //               in-place correction of O^T; then the split-K epilogue
-//               (splitk_combine.cuh) over all 256 softmax threads.
+//               over all 256 softmax threads: each rank pushes the other
+//               bands' columns of its partial O from TMEM into their owners'
+//               drained rings (st.async, distributed shared memory) and
+//               combines its own band from TMEM with what it receives.
 //
 // Geometry follows the FA4Config page (Modular MAX docs): MLA depth split
 // into nope and rope (q_nope / q_rope), one O accumulator for the wide V
 // (single_o), V as the nope prefix of the shared latent row (use_shared_kv),
 // split-K clusters (splitk_partitions).
 #include "fa_decode_internal.h"
-#include "splitk_combine.cuh"
+#include "device_common.cuh"
 #include "tcgen05.cuh"
 
 namespace fad {
@@ -62,20 +65,22 @@ struct MlaCfg {
     static constexpr int OFF_Q = NSLOT * SLOT_BYTES;                 // 9 atoms [64 heads][128 B]
     static constexpr int OFF_P = OFF_Q + Q_BYTES;                    // [P_BUFS][2 atoms][64 heads][128 B]
     static constexpr int OFF_RED = OFF_P + P_BUFS * P_BYTES;         // float [2 warpgroups][4 quadrants][32]
-    static constexpr int OFF_MAXSUM = OFF_RED + 2 * 4 * 32 * 4;      // float2 [64]
     // barriers: slot_full[NSLOT], slot_empty[NSLOT], s_full[2], s_empty[2], p_full[2],
-    // o_full[2], q_full, publish, mma_done, tmem_ready, v_zeroed[4]
-    static constexpr int OFF_BAR = OFF_MAXSUM + ROWS * 8;
-    static constexpr int NBAR = 2 * NSLOT + 16;
+    // o_full[2], q_full, recv_ms, mma_done, tmem_ready, v_zeroed[4], recv_o, ready[kMaxSplit]
+    static constexpr int OFF_BAR = OFF_RED + 2 * 4 * 32 * 4;
+    static constexpr int NBAR = 2 * NSLOT + 17 + kMaxSplit;
     static constexpr int OFF_ROWS = OFF_BAR + NBAR * 8;              // int [4 tiles][16 segments]
     static constexpr int OFF_MISC = OFF_ROWS + 4 * 16 * 4;           // tmem base, abort, S next item, O next item
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-    // Epilogue, once every product has completed: the f32 stage
-    // [P][64][Dv / P] (128 KB) over the drained ring and Q, the bf16 band
-    // [Dv / P / OC][64][OC] (at most 64 KB) after it.
-    static constexpr int OFF_STAGE = 0;
-    static constexpr int OFF_OUT = ROWS * DV * 4;
-    static constexpr int OFF_WTAB = OFF_OUT + ROWS * DV * 2;         // float [P][64] combine weights
+    // Split-K epilogue, once every product of the CTA has completed, over the
+    // drained ring, Q and P: the partials the other ranks push for this
+    // rank's band, f32 [P - 1][BW][64] (at most 15/16 of 128 KB), their rows' (max, sum) float2 [P - 1][64], the bf16 band
+    // [BW / OC][64][OC] (at most 64 KB) and the combine weights float [P][64].
+    static constexpr int OFF_RECV = 0;
+    static constexpr int OFF_RECV_MS = ROWS * DV * 4;
+    static constexpr int OFF_OUT = OFF_RECV_MS + 8192;
+    static constexpr int OFF_WTAB = OFF_OUT + ROWS * DV * 2;
+    static_assert((kMaxSplit - 1) * ROWS * 8 <= OFF_OUT - OFF_RECV_MS, "pushed row statistics fit");
     static_assert(OFF_WTAB + kMaxSplit * ROWS * 4 <= OFF_RED, "epilogue buffers fit below the softmax scratch");
     static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms on 1024 bytes");
     static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
@@ -130,13 +135,16 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
     const uint32_t bar0 = sbase + C::OFF_BAR;
     const uint32_t slot_full = bar0, slot_empty = bar0 + 8 * C::NSLOT;
     const uint32_t s_full = bar0 + 16 * C::NSLOT, s_empty = s_full + 16, p_full = s_full + 32, o_full = s_full + 48;
-    const uint32_t q_full = s_full + 64, publish_bar = s_full + 72, mma_done = s_full + 80, tmem_ready = s_full + 88;
+    const uint32_t q_full = s_full + 64, recv_ms_bar = s_full + 72, mma_done = s_full + 80, tmem_ready = s_full + 88;
     const uint32_t v_zeroed = s_full + 96;  // [4]: the last tile's V items with their rows past L zeroed
+    // Split-K epilogue: the pushed partials' bytes land on recv_o_bar (and
+    // their row statistics on recv_ms_bar); rank q arrives on ready[q] once
+    // its drained ring may take this rank's pushes.
+    const uint32_t recv_o_bar = s_full + 128, ready_bar = s_full + 136;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     const uint32_t s_next = sbase + C::OFF_MISC + 8, o_next = sbase + C::OFF_MISC + 12;
     float* red_s = reinterpret_cast<float*>(smem + C::OFF_RED);
-    float2* maxsum_s = reinterpret_cast<float2*>(smem + C::OFF_MAXSUM);
 
     if (tid == 0) {
         for (int s = 0; s < C::NSLOT; ++s) {
@@ -150,7 +158,9 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
             mbar_init(o_full + 8 * i, 1);
         }
         mbar_init(q_full, 8);
-        mbar_init(publish_bar, P);
+        mbar_init(recv_ms_bar, 1);
+        mbar_init(recv_o_bar, 1);
+        for (int q = 0; q < kMaxSplit; ++q) mbar_init(ready_bar + 8 * q, 1);
         mbar_init(mma_done, 2);
         mbar_init(tmem_ready, 1);
         for (int e = 0; e < C::VITEMS; ++e) mbar_init(v_zeroed + 8 * e, 8);
@@ -571,40 +581,157 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
             red_w[quad * 32 + row] = v[0];
             named_barrier_sync(wg_bar, 128);
         }
-        float inv[32];
+        // Row col_wg + wt's (max, sum) in mm, ll for threads wt < 32.
+        float mm = -INFINITY, ll = 0.f;
+        if (wt < 32) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const float l = red_w[r] + red_w[32 + r] + red_w[64 + r] + red_w[96 + r];
-            if (wt == 0) maxsum_s[col_wg + r] = make_float2(m_run[r], l);
-            inv[r] = l > 0.f ? __frcp_rn(l) : 0.f;
+            for (int r = 0; r < 32; ++r)
+                if (r == wt) mm = m_run[r];
+            ll = red_w[wt] + red_w[32 + wt] + red_w[64 + wt] + red_w[96 + wt];
         }
-        // Both warpgroups' products are complete before the stage overwrites
-        // the ring and Q.
-        named_barrier_sync(3, 256);
-        float* stage_s = reinterpret_cast<float*>(smem + C::OFF_STAGE);
-        const int BW = p.band_cols;
+        // Split-K epilogue (push). Rank q merges band q of the value columns,
+        // [q BW, (q + 1) BW). Every rank pushes, straight from TMEM, its
+        // unnormalised partial O for the columns of each other band, and each
+        // row's (max, sum), into that band owner's shared memory with
+        // st.async; the owner combines its own band from TMEM with what it
+        // received. The receive area is this CTA's drained ring, so a rank
+        // pushes to q only once q has announced (ready[q]) that all of its
+        // own products are complete. Received partial of source s (the
+        // source ranks other than q in order), column c, rows 4k .. 4k + 3 at
+        // float ((s BW + c) 64 + 4 (k ^ (c & 7))): the XOR spreads a warp's 32
+        // consecutive columns over every bank.
+        const int BW = p.band_cols, OC = p.out_chunk_cols;
+        const uint32_t recv_o = sbase + C::OFF_RECV, recv_ms = sbase + C::OFF_RECV_MS;
+        if (P > 1) {
+            cluster_wait();  // every rank's barriers are initialised
+            if (wt == 0 && wg == 0 && !*abort_flag) {
+                // Both warpgroups waited for the last O product, which follows
+                // every product and every read of the ring, Q and P.
+                mbar_arrive_expect_tx(recv_ms_bar, (uint32_t)((P - 1) * C::ROWS * 8));
+                mbar_arrive_expect_tx(recv_o_bar, (uint32_t)((P - 1) * C::ROWS * BW * 4));
+                for (int q = 0; q < P; ++q)
+                    if (q != rank) mbar_arrive_cluster(map_shared_rank(ready_bar + 8 * rank, q));
+            }
+            if (wt < 32) {
+                for (int q = 0; q < P; ++q) {
+                    if (q == rank) continue;
+                    if (!mbar_wait<true>(ready_bar + 8 * q, 0, abort_flag, p.status, p.wait_limit_ns)) break;
+                    const int src = rank < q ? rank : rank - 1;
+                    st_async_f2(map_shared_rank(recv_ms + 8u * (uint32_t)(src * C::ROWS + col_wg + wt), q), mm, ll,
+                                map_shared_rank(recv_ms_bar, q));
+                }
+            }
+#pragma unroll 1
+            for (int blk = 0; blk < 4; ++blk) {
+                const int dv = 128 * blk + my_lane;
+                const int q = dv / BW;
+                if (q == rank) continue;
+                if (!mbar_wait<true>(ready_bar + 8 * q, 0, abort_flag, p.status, p.wait_limit_ns)) break;
+                float o[32];
+                tmem_ld_32x32b_x32(tmem + lane_addr + C::TMEM_O0 + 64 * blk + col_wg, o);
+                if (tile_count == 0) {  // no product was issued: the accumulator holds nothing of ours
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) o[r] = 0.f;
+                }
+                const int c = dv - q * BW, src = rank < q ? rank : rank - 1;
+                const uint32_t dst = map_shared_rank(recv_o + 4u * (uint32_t)((src * BW + c) * C::ROWS), q);
+                const uint32_t bar_q = map_shared_rank(recv_o_bar, q);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int k = (int)(col_wg >> 2) + i;
+                    st_async_f4(dst + 16u * (uint32_t)(k ^ (c & 7)), o[4 * i], o[4 * i + 1], o[4 * i + 2],
+                                o[4 * i + 3], bar_q);
+                }
+            }
+        }
+        if (wt == 0 && wg == 0) stamp(8);  // unit 0: partials pushed
+        // Combine weights of row rr = col_wg + wt (threads wt < 32): Gmax over
+        // the partials that saw keys, Gsum = sum_q sum_q 2^((max_q - Gmax) c),
+        // and w_q = 2^((max_q - Gmax) c) / Gsum on each unnormalised partial
+        // O_q (0 for a partial that saw no key), so O = sum_q w_q O_q.
+        float* wtab = reinterpret_cast<float*>(smem + C::OFF_WTAB);  // [P][64]
+        if (wt < 32) {
+            const float2* ms_in = reinterpret_cast<const float2*>(smem + C::OFF_RECV_MS);
+            const int rr = col_wg + wt;
+            if (P > 1) mbar_wait<true>(recv_ms_bar, 0, abort_flag, p.status, p.wait_limit_ns);
+            float gmax = ll > 0.f ? mm : -INFINITY;
+            for (int s = 0; s < P - 1; ++s) {
+                const float2 v = ms_in[s * C::ROWS + rr];
+                if (v.y > 0.f) gmax = fmaxf(gmax, v.x);
+            }
+            const float e_own = ll > 0.f ? ex2_approx((mm - gmax) * c2) : 0.f;
+            float gsum = ll * e_own;
+            for (int s = 0; s < P - 1; ++s) {
+                const float2 v = ms_in[s * C::ROWS + rr];
+                gsum += v.y > 0.f ? v.y * ex2_approx((v.x - gmax) * c2) : 0.f;
+            }
+            const float ginv = gsum > 0.f ? 1.f / gsum : 0.f;
+            wtab[rank * C::ROWS + rr] = e_own * ginv;
+            for (int s = 0; s < P - 1; ++s) {
+                const float2 v = ms_in[s * C::ROWS + rr];
+                wtab[(s < rank ? s : s + 1) * C::ROWS + rr] = v.y > 0.f ? ex2_approx((v.x - gmax) * c2) * ginv : 0.f;
+            }
+            if (rank == 0 && rr < p.rows && p.lse != nullptr) {
+                const int t = rr / p.heads_per_cta;
+                const int h = kvh * p.group + row_block * p.heads_per_cta + rr % p.heads_per_cta;
+                // natural-log LSE of the scaled scores: scale * Gmax + ln(Gsum)
+                p.lse[((int64_t)b * p.num_q + t) * p.num_q_heads + h] =
+                    gsum > 0.f ? p.scale * gmax + lg2_approx(gsum) * 0.6931471805599453f : -INFINITY;
+            }
+        }
+        named_barrier_sync(wg_bar, 128);  // this warpgroup's rows' weights
+        if (P > 1) mbar_wait<true>(recv_o_bar, 0, abort_flag, p.status, p.wait_limit_ns);
+        uint16_t* out_s = reinterpret_cast<uint16_t*>(smem + C::OFF_OUT);  // [BW / OC][64][OC]
+        const float* recv_f = reinterpret_cast<const float*>(smem + C::OFF_RECV);
 #pragma unroll 1
         for (int blk = 0; blk < 4; ++blk) {
+            const int dv = 128 * blk + my_lane;
+            if (dv / BW != rank) continue;
+            const int c = dv - rank * BW;
             float o[32];
             tmem_ld_32x32b_x32(tmem + lane_addr + C::TMEM_O0 + 64 * blk + col_wg, o);
-            if (tile_count == 0) {  // no product was issued: the accumulator holds nothing of ours
+            if (tile_count == 0) {
 #pragma unroll
                 for (int r = 0; r < 32; ++r) o[r] = 0.f;
             }
-            const int dv = 128 * blk + my_lane;
-            const int q = dv / BW, jc = dv % BW;
+            const float* w_own = wtab + rank * C::ROWS + col_wg;
 #pragma unroll
-            for (int r = 0; r < 32; ++r) stage_s[(q * C::ROWS + col_wg + r) * BW + jc] = o[r] * inv[r];
+            for (int i = 0; i < 8; ++i) {
+                const float4 w = *reinterpret_cast<const float4*>(w_own + 4 * i);
+                o[4 * i] *= w.x;
+                o[4 * i + 1] *= w.y;
+                o[4 * i + 2] *= w.z;
+                o[4 * i + 3] *= w.w;
+            }
+            for (int s = 0; s < P - 1; ++s) {
+                const float* src = recv_f + (s * BW + c) * C::ROWS;
+                const float* w_s = wtab + (s < rank ? s : s + 1) * C::ROWS + col_wg;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int k = (int)(col_wg >> 2) + i;
+                    const float4 v = *reinterpret_cast<const float4*>(src + 4 * (k ^ (c & 7)));
+                    const float4 w = *reinterpret_cast<const float4*>(w_s + 4 * i);
+                    o[4 * i] = fmaf(w.x, v.x, o[4 * i]);
+                    o[4 * i + 1] = fmaf(w.y, v.y, o[4 * i + 1]);
+                    o[4 * i + 2] = fmaf(w.z, v.z, o[4 * i + 2]);
+                    o[4 * i + 3] = fmaf(w.w, v.w, o[4 * i + 3]);
+                }
+            }
+            uint16_t* dst = out_s + ((c / OC) * C::ROWS + col_wg) * OC + c % OC;
+#pragma unroll
+            for (int r = 0; r < 32; ++r) dst[r * OC] = __bfloat16_as_ushort(__float2bfloat16_rn(o[r]));
         }
         tc_fence_before_sync();
+        fence_proxy_async_smem();
         named_barrier_sync(3, 256);
-        if (P > 1) cluster_wait();  // every rank's publish barrier is initialised
-        if (wt == 0 && wg == 0) stamp(8);  // unit 0: merge started
-        splitk_merge_rows<C::ROWS>(p, P, rank, b, kvh, row_block, stage_s, maxsum_s,
-                                   reinterpret_cast<uint16_t*>(smem + C::OFF_OUT),
-                                   reinterpret_cast<float*>(smem + C::OFF_WTAB), publish_bar, abort_flag,
-                                   tid - 32 * C::WG0, 256, 3);
-        if (wt == 0 && wg == 0) stamp(9);  // unit 0: merge done
+        if (wt == 0 && wg == 0) {
+            for (int c0 = 0; c0 < BW; c0 += OC)
+                tma_store_3d(&p.tm_out, smem_addr(out_s + (c0 / OC) * C::ROWS * OC), rank * BW + c0,
+                             kvh * p.group + row_block * p.heads_per_cta, b * p.num_q);
+            tma_store_commit();
+            tma_store_wait_read();
+            stamp(9);  // unit 0: band stored
+        }
     }
 
     __syncthreads();
@@ -619,7 +746,7 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
     }
     if (P > 1 && warp < C::WG0) cluster_wait();  // pairs with the early arrive
     __syncwarp();
-    if (P > 1) cluster_sync_all();  // peers may still read this CTA's staged bands until here
+    if (P > 1) cluster_sync_all();  // after a timed-out wait a peer may still push into this CTA until here
     if (tid == 0) stamp(3);
 }
 
@@ -633,7 +760,7 @@ bool mla_tc_geometry(int qk, int ov, int nope, int heads_per_kv, int num_q, Kern
     g->stages = MlaCfg::NSLOT;
     g->rows_capacity = MlaCfg::ROWS;
     g->smem_bytes = MlaCfg::SMEM_BYTES;
-    g->name = "mla_tc_d576_v512_bn128_n64_slots3";
+    g->name = "mla_tc_d576_v512_bn128_n64_slots4";
     return true;
 }
 

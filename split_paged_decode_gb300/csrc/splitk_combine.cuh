@@ -1,7 +1,7 @@
-// splitk_combine.cuh -- the cluster split-K epilogue shared by every decode
-// kernel: publish this CTA's partial result, merge all partitions' results
-// for this CTA's band of output columns over distributed shared memory, cast
-// to bf16 and TMA-store the band.
+// splitk_combine.cuh -- the cluster split-K epilogue of the SIMT kernels and
+// the GQA tcgen05 kernel: publish this CTA's partial result, merge all
+// partitions' results for this CTA's band of output columns over distributed
+// shared memory, cast to bf16 and TMA-store the band.
 //
 // Follows the fa4_splitk_combine_write page (Modular MAX docs): pass 2 is a
 // reduce-scatter in which cluster rank p owns the output column band
@@ -191,115 +191,6 @@ __device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, in
                          kvh * p.group + row_block * p.heads_per_cta, b * p.num_q);
         tma_store_commit();
         tma_store_wait_read();  // the band's shared memory may be released once read
-    }
-}
-
-// Variant of splitk_merge_and_store for many rows per CTA (the same layouts,
-// publish protocol and result): each row's combine weights are formed once
-// into `wtab` (float [P][RB] of scratch) instead of for every column chunk,
-// and each thread then merges four column chunks at a time with every
-// rank's remote loads for them in flight together, so the merge costs a few
-// distributed-shared-memory round trips rather than one per rank per chunk.
-template <int RB>
-__device__ __forceinline__ void splitk_merge_rows(const DecodeParams& p, int P, int rank, int b, int kvh,
-                                                  int row_block, const float* stage_s, const float2* maxsum_s,
-                                                  uint16_t* out_s, float* wtab, uint32_t publish_bar,
-                                                  volatile int* abort_flag, int tid, int nthreads, uint32_t bar_id)
-{
-    const int BW = p.band_cols;
-    const float c = p.scale_log2e;
-    const uint32_t stage_base = smem_addr(stage_s);
-    const uint32_t maxsum_base = smem_addr(maxsum_s);
-    if (P > 1) {
-        if (tid == 0)
-            for (int q = 0; q < P; ++q) mbar_arrive_cluster(map_shared_rank(publish_bar, q));
-        mbar_wait<true>(publish_bar, 0, abort_flag, p.status, p.wait_limit_ns);
-    }
-    for (int r = tid; r < RB; r += nthreads) {
-        float2 ms[kMaxSplit];
-#pragma unroll
-        for (int q = 0; q < kMaxSplit; ++q)  // own rank from local shared memory: no cluster traffic
-            if (q < P) ms[q] = q != rank ? ld_dsmem_f2(map_shared_rank(maxsum_base + 8u * r, q)) : maxsum_s[r];
-        float gmax = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < kMaxSplit; ++q)
-            if (q < P && ms[q].y > 0.f) gmax = fmaxf(gmax, ms[q].x);
-        float gsum = 0.f;
-#pragma unroll
-        for (int q = 0; q < kMaxSplit; ++q) {
-            if (q < P) {
-                ms[q].y = ms[q].y > 0.f ? ms[q].y * ex2_approx((ms[q].x - gmax) * c) : 0.f;
-                gsum += ms[q].y;
-            }
-        }
-        const float inv = gsum > 0.f ? 1.f / gsum : 0.f;
-#pragma unroll
-        for (int q = 0; q < kMaxSplit; ++q)
-            if (q < P) wtab[q * RB + r] = ms[q].y * inv;
-        if (rank == 0 && r < p.rows && p.lse != nullptr) {
-            const int t = r / p.heads_per_cta;
-            const int h = kvh * p.group + row_block * p.heads_per_cta + r % p.heads_per_cta;
-            // natural-log LSE of the scaled scores: scale * Gmax + ln(Gsum)
-            p.lse[((int64_t)b * p.num_q + t) * p.num_q_heads + h] =
-                gsum > 0.f ? p.scale * gmax + lg2_approx(gsum) * 0.6931471805599453f : -INFINITY;
-        }
-    }
-    named_barrier_sync(bar_id, nthreads);
-    const int chunks = BW / 4;
-    const int items = RB * chunks;
-    const int OC = p.out_chunk_cols;
-    for (int it0 = tid; it0 < items; it0 += 4 * nthreads) {
-        float4 o[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q0 = 0; q0 < P; q0 += 4) {  // ranks in groups of four: 16 loads in flight
-            float4 v[4][4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int it = it0 + u * nthreads;
-                const int r = it / chunks, j = (it % chunks) * 4;
-                const uint32_t off = 4u * ((uint32_t)(rank * RB + r) * BW + j);
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq)
-                    if (it < items && q0 + qq < P)
-                        v[u][qq] = q0 + qq != rank
-                                       ? ld_dsmem_f4(map_shared_rank(stage_base + off, q0 + qq))
-                                       : *reinterpret_cast<const float4*>(stage_s + (rank * RB + r) * BW + j);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int it = it0 + u * nthreads;
-                const int r = it / chunks;
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    if (it < items && q0 + qq < P) {
-                        const float w = wtab[(q0 + qq) * RB + r];
-                        o[u].x = fmaf(w, v[u][qq].x, o[u].x);
-                        o[u].y = fmaf(w, v[u][qq].y, o[u].y);
-                        o[u].z = fmaf(w, v[u][qq].z, o[u].z);
-                        o[u].w = fmaf(w, v[u][qq].w, o[u].w);
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int it = it0 + u * nthreads;
-            if (it < items) {
-                const int r = it / chunks, j = (it % chunks) * 4;
-                const uint2 packed = make_uint2(float2_to_bf16x2(o[u].x, o[u].y), float2_to_bf16x2(o[u].z, o[u].w));
-                *reinterpret_cast<uint2*>(out_s + ((j / OC) * RB + r) * OC + j % OC) = packed;
-            }
-        }
-    }
-    fence_proxy_async_smem();
-    named_barrier_sync(bar_id, nthreads);
-    if (tid == 0) {
-        for (int c0 = 0; c0 < BW; c0 += OC)
-            tma_store_3d(&p.tm_out, smem_addr(out_s + (c0 / OC) * RB * OC), rank * BW + c0,
-                         kvh * p.group + row_block * p.heads_per_cta, b * p.num_q);
-        tma_store_commit();
-        tma_store_wait_read();
     }
 }
 
