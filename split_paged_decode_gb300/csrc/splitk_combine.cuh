@@ -212,70 +212,99 @@ __device__ __forceinline__ void splitk_merge_and_store(const DecodeParams& p, in
 // ---------------------------------------------------------------------------
 __host__ __device__ constexpr int pushed_bytes(int P, int BW, int RB) { return P * BW * RB * 4 + P * RB * 8; }
 
-// Row r's weights over `nq` pushed partials (recv_ms [nq][RB]: raw max, sum):
-// Gmax over the partials that saw keys, Gsum, and
-// w_q = sum_q * exp2((max_q - Gmax) * c) / Gsum (0 for an empty partial) into
-// wtab [nq][RB]; returns (Gmax, Gsum). Partials are read four at a time
-// without a guard (the index clamped to nq - 1), so that a round's
-// shared-memory reads are in flight together; the sums keep partial order.
+// Row weights over the `nq` pushed partials (recv_ms [nq][RB]: raw max,
+// sum; nq <= 2 kMaxSplit) by the whole warp: lane (row r = lane % RB, group
+// g = lane / RB) takes partials g, g + G, ... (G = 32 / RB lanes per row),
+// all its loads in flight together, and xor shuffles over the row's G lanes
+// reduce Gmax (over the partials that saw keys) and Gsum. Writes
+// w_q = sum_q * exp2((max_q - Gmax) * c) / Gsum (0 for an empty partial)
+// into wtab [nq][RB]; every lane of row r returns (Gmax, Gsum).
 template <int RB>
-__device__ __forceinline__ float2 partial_weights(const float2* recv_ms, float* wtab, int nq, int r, float c)
+__device__ __forceinline__ float2 partial_weights(const float2* recv_ms, float* wtab, int nq, int lane, float c)
 {
+    static_assert(32 % RB == 0, "a row's lanes tile the warp");
+    constexpr int G = 32 / RB;
+    constexpr int K = (2 * kMaxSplit + G - 1) / G;  // partials per lane at most
+    const int r = lane % RB, g = lane / RB;
+    float2 m[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int q = g + G * k;
+        m[k] = q < nq ? recv_ms[q * RB + r] : make_float2(-INFINITY, 0.f);
+    }
     float gmax = -INFINITY;
-    for (int q0 = 0; q0 < nq; q0 += 4) {
-        float2 m4[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) m4[j] = recv_ms[min(q0 + j, nq - 1) * RB + r];
+    for (int k = 0; k < K; ++k)
+        if (m[k].y > 0.f) gmax = fmaxf(gmax, m[k].x);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (q0 + j < nq && m4[j].y > 0.f) gmax = fmaxf(gmax, m4[j].x);
-    }
+    for (int sh = RB; sh < 32; sh <<= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, sh));
     float gsum = 0.f;
-    for (int q0 = 0; q0 < nq; q0 += 4) {
-        float2 m4[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) m4[j] = recv_ms[min(q0 + j, nq - 1) * RB + r];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (q0 + j < nq) {
-                const float w = m4[j].y > 0.f ? m4[j].y * ex2_approx((m4[j].x - gmax) * c) : 0.f;
-                wtab[(q0 + j) * RB + r] = w;
-                gsum += w;
-            }
-        }
+    for (int k = 0; k < K; ++k) {
+        m[k].y = m[k].y > 0.f ? m[k].y * ex2_approx((m[k].x - gmax) * c) : 0.f;
+        gsum += m[k].y;
     }
+#pragma unroll
+    for (int sh = RB; sh < 32; sh <<= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, sh);
     const float inv = gsum > 0.f ? 1.f / gsum : 0.f;
-    for (int q = 0; q < nq; ++q) wtab[q * RB + r] *= inv;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int q = g + G * k;
+        if (q < nq) wtab[q * RB + r] = m[k].y * inv;
+    }
     return make_float2(gmax, gsum);
 }
 
-// o[RB] += sum over the nq partials of w_q * (partial q's column `col`)
-// (recv_o [nq][BW][RB]), in partial order, four partials' loads per round.
+// Lanes of a band of BW columns (a power of two): PG = 32 / BW lanes per
+// column when BW < 32 (each takes every PG-th partial), else one; lane's
+// first column, column step and partial group.
+struct BandLanes {
+    int col0, step, pg, PG;
+};
+__device__ __forceinline__ BandLanes band_lanes(int BW, int lane)
+{
+    const int PG = BW < 32 ? 32 / BW : 1, per = 32 / PG;
+    return BandLanes{lane % per, per, lane / per, PG};
+}
+
+// o[RB] = sum over the nq partials of w_q * (partial q's column `col`)
+// (recv_o [nq][BW][RB]; weights wtab [nq][RB]), the partials pg, pg + PG,
+// ... on this lane, four per round with their loads in flight together; with
+// PG > 1 xor shuffles add the column's PG lanes, so each of them ends with
+// the total. Every lane of the warp calls it the same number of times.
 template <int RB>
 __device__ __forceinline__ void partial_band(const float* recv_o, const float* wtab, int nq, int BW, int col,
-                                             float (&o)[RB])
+                                             const BandLanes& bl, float (&o)[RB])
 {
-    for (int q0 = 0; q0 < nq; q0 += 4) {
+#pragma unroll
+    for (int r = 0; r < RB; ++r) o[r] = 0.f;
+    for (int q0 = bl.pg; q0 < nq; q0 += 4 * bl.PG) {
         float4 v[4][RB / 4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float4* src = reinterpret_cast<const float4*>(recv_o + (min(q0 + j, nq - 1) * BW + col) * RB);
+            const float4* src =
+                reinterpret_cast<const float4*>(recv_o + (min(q0 + j * bl.PG, nq - 1) * BW + col) * RB);
 #pragma unroll
             for (int r4 = 0; r4 < RB / 4; ++r4) v[j][r4] = src[r4];
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            if (q0 + j < nq) {
-                const float* wq = wtab + (q0 + j) * RB;
+            if (q0 + j * bl.PG < nq) {
+                const float4* wq = reinterpret_cast<const float4*>(wtab + (q0 + j * bl.PG) * RB);
 #pragma unroll
                 for (int r4 = 0; r4 < RB / 4; ++r4) {
-                    o[4 * r4 + 0] = fmaf(wq[4 * r4 + 0], v[j][r4].x, o[4 * r4 + 0]);
-                    o[4 * r4 + 1] = fmaf(wq[4 * r4 + 1], v[j][r4].y, o[4 * r4 + 1]);
-                    o[4 * r4 + 2] = fmaf(wq[4 * r4 + 2], v[j][r4].z, o[4 * r4 + 2]);
-                    o[4 * r4 + 3] = fmaf(wq[4 * r4 + 3], v[j][r4].w, o[4 * r4 + 3]);
+                    const float4 w = wq[r4];
+                    o[4 * r4 + 0] = fmaf(w.x, v[j][r4].x, o[4 * r4 + 0]);
+                    o[4 * r4 + 1] = fmaf(w.y, v[j][r4].y, o[4 * r4 + 1]);
+                    o[4 * r4 + 2] = fmaf(w.z, v[j][r4].z, o[4 * r4 + 2]);
+                    o[4 * r4 + 3] = fmaf(w.w, v[j][r4].w, o[4 * r4 + 3]);
                 }
             }
         }
+    }
+    for (int sh = 32 / bl.PG; sh < 32; sh <<= 1) {
+#pragma unroll
+        for (int r = 0; r < RB; ++r) o[r] += __shfl_xor_sync(0xffffffffu, o[r], sh);
     }
 }
 
@@ -296,10 +325,11 @@ __device__ __forceinline__ void splitk_merge_pushed(const DecodeParams& p, int P
     __syncwarp();
     // Per row: Gmax over the partitions that saw keys, Gsum, and the weights
     // w_q = sum_q * exp2((max_q - Gmax) * c) / Gsum (0 for an empty partition).
-    for (int r = lane; r < RB; r += 32) {
-        const float2 gm = partial_weights<RB>(recv_ms, wtab, nq, r, c);
+    {
+        const float2 gm = partial_weights<RB>(recv_ms, wtab, nq, lane, c);
         const float gmax = gm.x, gsum = gm.y;
-        if (rank == 0 && r < p.rows && p.lse != nullptr) {
+        const int r = lane;  // lanes 0 .. RB - 1 hold rows 0 .. RB - 1
+        if (lane < RB && rank == 0 && r < p.rows && p.lse != nullptr) {
             const int t = r / p.heads_per_cta;
             const int h = kvh * p.group + r % p.heads_per_cta;
             // natural-log LSE of the scaled scores: scale * Gmax + ln(Gsum)
@@ -309,14 +339,15 @@ __device__ __forceinline__ void splitk_merge_pushed(const DecodeParams& p, int P
     }
     __syncwarp();
     const int OC = p.out_chunk_cols;
-    for (int col = lane; col < BW; col += 32) {
+    const BandLanes bl = band_lanes(BW, lane);
+    for (int col = bl.col0; col < BW; col += bl.step) {
         float o[RB];
+        partial_band<RB>(recv_o, wtab, nq, BW, col, bl, o);
+        if (bl.pg == 0) {
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(out_s) + (col / OC) * RB * OC + col % OC;
 #pragma unroll
-        for (int r = 0; r < RB; ++r) o[r] = 0.f;
-        partial_band<RB>(recv_o, wtab, nq, BW, col, o);
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(out_s) + (col / OC) * RB * OC + col % OC;
-#pragma unroll
-        for (int r = 0; r < RB; ++r) dst[r * OC] = __float2bfloat16_rn(o[r]);
+            for (int r = 0; r < RB; ++r) dst[r * OC] = __float2bfloat16_rn(o[r]);
+        }
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -359,20 +390,21 @@ __device__ __noinline__ void splitk_merge_pushed_sk(const DecodeParams& p, int P
     const int64_t mine = slot(cluster);
     float* const my_o = p.chunk_o + (mine * P + rank) * BW * RB;
     // This chunk: weights over the cluster's pushed partials, then the band.
-    for (int r = lane; r < RB; r += 32) {
-        const float2 gm = partial_weights<RB>(recv_ms, wtab, nq, r, c);
-        const float gmax = gm.x, gsum = gm.y;
-        p.chunk_ms[(mine * P + rank) * RB + r] = make_float2(gmax, gsum);
+    {
+        const float2 gm = partial_weights<RB>(recv_ms, wtab, nq, lane, c);
+        if (lane < RB) p.chunk_ms[(mine * P + rank) * RB + lane] = gm;
     }
     __syncwarp();
-    for (int col = lane; col < BW; col += 32) {
+    const BandLanes bl = band_lanes(BW, lane);
+    for (int col = bl.col0; col < BW; col += bl.step) {
         float o[RB];
+        partial_band<RB>(recv_o, wtab, nq, BW, col, bl, o);
+        if (bl.pg == 0) {
+            float4* dst = reinterpret_cast<float4*>(my_o + col * RB);
 #pragma unroll
-        for (int r = 0; r < RB; ++r) o[r] = 0.f;
-        partial_band<RB>(recv_o, wtab, nq, BW, col, o);
-        float4* dst = reinterpret_cast<float4*>(my_o + col * RB);
-#pragma unroll
-        for (int r4 = 0; r4 < RB / 4; ++r4) dst[r4] = make_float4(o[4 * r4], o[4 * r4 + 1], o[4 * r4 + 2], o[4 * r4 + 3]);
+            for (int r4 = 0; r4 < RB / 4; ++r4)
+                dst[r4] = make_float4(o[4 * r4], o[4 * r4 + 1], o[4 * r4 + 2], o[4 * r4 + 3]);
+        }
     }
     // Publish this chunk's band (every lane's writes, then one count); the
     // cluster that completes the count reads every chunk's band.
@@ -385,6 +417,21 @@ __device__ __noinline__ void splitk_merge_pushed_sk(const DecodeParams& p, int P
     if (lane == 0) last = atomicAdd(count, 1u) == (unsigned int)(S - 1) ? 1u : 0u;
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
     __threadfence();
+    // The band below: lane takes (column, 4-row group) items. Its first
+    // item's first four chunks are loaded now, in flight together with the
+    // (max, sum) reads of the weights.
+    const int items = BW * (RB / 4);
+    auto chunk_item = [&](int k, int idx) -> float4 {
+        const int col = idx / (RB / 4), r4 = idx % (RB / 4);
+        return __ldcg(reinterpret_cast<const float4*>(
+                          p.chunk_o + ((slot(c_first + min(k, S - 1)) * P + rank) * BW + col) * RB) +
+                      r4);
+    };
+    float4 first[4];
+    if (lane < items) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) first[j] = chunk_item(j, lane);
+    }
     // Chunk weights per row (lane r < RB <= 16), every chunk's (max, sum) in
     // flight at once: these reads queue behind the streaming loads.
     if (lane < RB) {
@@ -429,7 +476,7 @@ __device__ __noinline__ void splitk_merge_pushed_sk(const DecodeParams& p, int P
     // The band: lane takes (column, 4-row group) pairs, every chunk's values
     // of a pair in flight at once.
     const int OC = p.out_chunk_cols;
-    for (int idx = lane; idx < BW * (RB / 4); idx += 32) {
+    for (int idx = lane; idx < items; idx += 32) {
         const int col = idx / (RB / 4), r4 = idx % (RB / 4);
         // Four chunks per round, loaded without a guard (clamped to chunk
         // S - 1), so a round's loads are in flight at once.
@@ -437,18 +484,15 @@ __device__ __noinline__ void splitk_merge_pushed_sk(const DecodeParams& p, int P
         for (int k0 = 0; k0 < S; k0 += 4) {
             float4 v[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                v[j] = __ldcg(reinterpret_cast<const float4*>(
-                                  p.chunk_o + ((slot(c_first + min(k0 + j, S - 1)) * P + rank) * BW + col) * RB) +
-                              r4);
+            for (int j = 0; j < 4; ++j) v[j] = (idx == lane && k0 == 0) ? first[j] : chunk_item(k0 + j, idx);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (k0 + j < S) {
-                    const float* wr = wtab + (k0 + j) * RB + 4 * r4;
-                    o[0] = fmaf(wr[0], v[j].x, o[0]);
-                    o[1] = fmaf(wr[1], v[j].y, o[1]);
-                    o[2] = fmaf(wr[2], v[j].z, o[2]);
-                    o[3] = fmaf(wr[3], v[j].w, o[3]);
+                    const float4 w = *reinterpret_cast<const float4*>(wtab + (k0 + j) * RB + 4 * r4);
+                    o[0] = fmaf(w.x, v[j].x, o[0]);
+                    o[1] = fmaf(w.y, v[j].y, o[1]);
+                    o[2] = fmaf(w.z, v[j].z, o[2]);
+                    o[3] = fmaf(w.w, v[j].w, o[3]);
                 }
             }
         }
