@@ -923,8 +923,8 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 if (trace) trace[unit_slot(lu, 6)] = (unsigned long long)tile_count;
             }
             // The next unit of this cluster: its Q rows are fetched now and
-            // stored once the S warp has left the buffer's previous unit (after
-            // this warpgroup's first tile of the unit), so the S warp runs
+            // stored once the S warp has left the buffer's previous unit (at
+            // this warpgroup's second tile of the unit), so the S warp runs
             // straight on into it.
             Unit nx = w;
             nx.u += u_step;
@@ -1161,7 +1161,10 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                         }
                     }
                 }
-                const bool q_now = q_pending;  // uniform: this warpgroup's first tile of the unit
+                // Uniform: this warpgroup's second tile of the unit (its first when it
+                // has one only), so that the next unit's Q rows, fetched at the unit's
+                // start, have a tile's time to arrive.
+                const bool q_now = q_pending && (i > i0 || i + C::NWG >= tile_count);
                 if (q_now) put_next_q();
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -1169,7 +1172,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                     mbar_arrive(p_full + 8 * (gi % C::NPB));
                     if (q_now) mbar_arrive(q_full + 8 * ((lu + 1) & 1));
                 }
-                q_pending = false;
+                q_pending = q_pending && !q_now;
 
                 ++wc;
                 ++wc_unit;
