@@ -848,10 +848,13 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 }
             }
         };
-        auto store_q = [&](int buf, const uint4 (&v)[2]) {
+        // all_rows false: rows >= p.rows of the buffer hold zeros from its first
+        // use, and warps whose two rows are both such rows skip them.
+        auto store_q = [&](int buf, const uint4 (&v)[2], bool all_rows) {
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const int idx = wt + 128 * k, r = idx >> 4, u = idx & 15;
+                if (!all_rows && (((wt & ~31) + 128 * k) >> 4) >= p.rows) continue;  // uniform over the warp
                 if constexpr (!FP8) {
                     *reinterpret_cast<uint4*>(smem + C::OFF_Q + buf * C::Q_BYTES + (u >> 3) * 2048 + r * 128 +
                                               (((u & 7) ^ (r & 7)) << 4)) = v[k];
@@ -898,7 +901,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
         if (have && lead) {
             uint4 qv[2];
             load_q(w, qv);
-            store_q(0, qv);
+            store_q(0, qv, true);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(q_full);
@@ -936,7 +939,7 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
                 if (lu >= 1)
                     mbar_wait(q_empty + 8 * ((lu + 1) & 1), ((lu - 1) >> 1) & 1, abort_flag, p.status,
                               p.wait_limit_ns);
-                store_q((lu + 1) & 1, qn);
+                store_q((lu + 1) & 1, qn, lu == 0);
             };
 #pragma unroll
             for (int r = 0; r < NRV; ++r) {
