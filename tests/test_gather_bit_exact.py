@@ -130,7 +130,7 @@ def mla(**kw):
     return wl(**base)
 
 
-@pytest.mark.parametrize("P", [1, 2, 4, 8])
+@pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("ps", [32, 64, 128])
 def test_mla_tensor_core(P, ps):
     run_dominant(mla(splitk=P, page_size=ps, seed=770 + P + ps), seq_lens=[700, 129, 2000, 1], salt=P + ps,

@@ -101,7 +101,7 @@ def test_mla_tensor_core_path_is_selected():
 
 
 @pytest.mark.parametrize("path", PATHS)
-@pytest.mark.parametrize("P", [1, 2, 4, 8])
+@pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
 def test_mla_splits(P, path):
     """MLA latent layout, 128 heads (two 64-head blocks), ragged lengths across tiles."""
     run_and_check(mla_wl(splitk=P, seed=150 + P), seq_lens=[700, 129, 2000], what=f"mla P{P} {path}", path=path)
