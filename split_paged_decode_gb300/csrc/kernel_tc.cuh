@@ -78,7 +78,9 @@ struct TcCfg {
     static constexpr int NSLOT = FP8 ? 2 * NS32 - (MULTI ? 1 : 0) : NS32;
     // V tiles are issued VLAG tiles after their K (<= 3: rows_s ring). A lag
     // of 2 was measured slower than 1 on the deep ring: K tiles then wait in
-    // the ring for an S buffer instead.
+    // the ring for an S buffer instead. A lag of 0 (V right behind its K) was
+    // slower still (long_context 103 -> 111 us): the next tile's K then
+    // queues behind a V that waits for its P anyway.
     static constexpr int VLAG = 1;
     static constexpr int D = 128;       // qk_depth == ov_depth
     static constexpr int BN = 128;      // keys per tile (M of S^T)
