@@ -216,7 +216,8 @@ int fa_decode_set_debug(fa_decode_t h, uint32_t flags, int64_t wait_limit_ns);
  * the buffer (device memory, 8-byte aligned) and clears it; buf NULL turns
  * tracing off. The MLA tcgen05 kernel (one unit per CTA) records [0]-[3],
  * and for its unit [4] the softmax warps' tile loop done, [5] first S,
- * [6] last O complete, [8] / [9] merge start / end, [10] tiles.
+ * [6] last O complete, [8] partials pushed to the band owners, [9] band
+ * stored, [10] tiles.
  * The FMA kernel records nothing.
  */
 #define FA_TRACE_WORDS_PER_CTA 64
