@@ -1000,9 +1000,15 @@ __global__ void __launch_bounds__(TcCfg<NS32, NRV, FP8>::THREADS, TcCfg<NS32, NR
 
                 const int key0 = (tile_begin + i) * C::BN;
                 const int key = key0 + my_lane;
-                const int r_min = key < vis0 ? 0 : (key >= L ? NRV : (key - vis0 + 1) * p.heads_per_cta);
+                // Causal and length mask; with 16 rows per thread, nothing to do
+                // (uniformly) when every key of the tile is seen by every row and no
+                // row is padding (measured: ragged_speculative_e4m3 199.7 -> 193.1 us;
+                // with 4 or 8 rows the skip was no faster, long_context_e4m3 slower).
+                if (NRV < 16 || key0 + C::BN > vis0 || p.rows < NRV) {
+                    const int r_min = key < vis0 ? 0 : (key >= L ? NRV : (key - vis0 + 1) * p.heads_per_cta);
 #pragma unroll
-                for (int r = 0; r < NRV; ++r) s[r] = ((r >= r_min) & (r < p.rows)) ? s[r] : -INFINITY;
+                    for (int r = 0; r < NRV; ++r) s[r] = ((r >= r_min) & (r < p.rows)) ? s[r] : -INFINITY;
+                }
 
                 // Lazy rescale: a row's running max moves only when some score
                 // exceeds it by more than the threshold. In the common case a single
