@@ -126,6 +126,20 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
     grid_dependency_launch();
 
     int L = p.seq_lens[b];
+    // The load warp's first block of page-table entries, read while the
+    // length is in flight, guessing that the sequence fills its row (checked
+    // once the length is known): the two reads overlap instead of following
+    // one another. spec_raw -2: this lane read nothing.
+    int spec_begin = -1, spec_count = 0, spec_raw = -2;
+    if (warp == 0 && p.max_pages <= INT32_MAX / C::BN / p.page_size) {
+        const int ntg = (p.max_pages * p.page_size + C::BN - 1) / C::BN;
+        spec_begin = rank * (ntg / P) + min(rank, ntg % P);
+        spec_count = ntg / P + (rank < ntg % P ? 1 : 0);
+        const int segs = C::BN / p.box_rows;
+        const int t = lane / segs;
+        const int pslot = ((spec_begin + t) * C::BN + (lane % segs) * p.box_rows) / p.page_size;
+        if (t < spec_count && pslot < p.max_pages) spec_raw = p.page_table[(int64_t)b * p.max_pages + pslot];
+    }
     if (L < 0) {
         if (tid == 0 && rank == 0) atomicOr(p.status, FA_STATUS_BAD_PAGE);
         L = 0;
@@ -208,16 +222,20 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
             const int tpb = 32 / segs;                         // tiles per block of page entries
             int32_t* rows_s = reinterpret_cast<int32_t*>(smem + C::OFF_ROWS);
             constexpr int kNoSegment = INT32_MIN, kPastSequence = INT32_MIN + 1;
-            auto block_entry = [&](int tb) -> int {
+            // raw >= -1: this lane's entry, already read
+            auto block_entry = [&](int tb, int raw = -2) -> int {
                 const int t = tb + lane / segs;
                 if (t >= tile_count) return kNoSegment;
                 const int key = (tile_begin + t) * C::BN + (lane % segs) * p.box_rows;
                 if (key >= L) return kPastSequence;
                 const int pslot = key / p.page_size;
                 if (pslot >= p.max_pages) return -1;
-                return p.page_table[(int64_t)b * p.max_pages + pslot];
+                return raw >= -1 ? raw : p.page_table[(int64_t)b * p.max_pages + pslot];
             };
-            int blk_cur = block_entry(0), blk_next = block_entry(tpb);
+            // The guess holds when this rank's tiles start where it assumed (every
+            // entry the first block needs was then read, at the same page slot).
+            const bool guessed = tile_begin == spec_begin && tile_count <= spec_count;
+            int blk_cur = block_entry(0, guessed ? spec_raw : -2), blk_next = block_entry(tpb);
             int jj = 0;
             bool ok = true;
             for (int g = 0; ok && g < 2 * tile_count; ++g) {
