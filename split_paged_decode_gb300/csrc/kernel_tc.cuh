@@ -126,7 +126,7 @@ struct TcCfg {
     // TMEM_O fragments of the fa4_lse_combine_write page): the O MMA
     // accumulates a warpgroup's tiles straight into its fragment, a moved max
     // rescales the fragment in place, and the unit epilogue reads it once
-    // (two warpgroups: each combines both fragments for half of the rows).
+    // (two warpgroups: each pushes its own fragment as a partial of the unit).
     // With one warpgroup the O barriers go by P buffer, so that writing P
     // waits only for the product two tiles back, and a rescale for the
     // previous one; with two they go by fragment.
