@@ -409,6 +409,25 @@ def test_bounded_wait_times_out_and_context_survives():
         check_against_oracle(call, what="after timeout")
 
 
+@pytest.mark.parametrize("P", [2, 4])
+def test_mla_bounded_wait_times_out_and_context_survives(P):
+    """The MLA kernel with loads suppressed: the first waits run out, a CTA
+    that has given up announces nothing to its peers and their waits for it
+    (ready, pushed partials) give up too; the status says timeout, and the next
+    run on the same handle matches the oracle."""
+    inp = generate(mla_wl(splitk=P, seed=180 + P))
+    with DeviceCall(inp) as call:
+        assert "mla_tc" in call.describe()
+        spd.fa_decode_set_debug(call.h, spd.FA_DEBUG_SKIP_LOADS, 20_000_000)  # 20 ms
+        call.run()
+        st = spd.fa_decode_check(call.h)
+        assert st & spd.FA_STATUS_TIMEOUT
+        spd.fa_decode_set_debug(call.h, 0, 0)
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what=f"mla P{P} after timeout")
+
+
 def test_run_rejects_misaligned_pointer():
     inp = generate(wl(seed=82))
     with DeviceCall(inp) as call:
