@@ -38,7 +38,7 @@ __host__ __device__ inline int sk_cluster_of(int64_t total, int clusters, int64_
 struct DecodeParams {
     CUtensorMap tm_k;    // K rows: [num_pages*Hkv*PS][Dk] bf16, box {64, box_rows}, 128B swizzle
     CUtensorMap tm_v;    // V rows: [num_pages*Hkv*PS][Dv] (unused for the latent layout)
-    CUtensorMap tm_out;  // out: 3-D {Dv, Hq, B*T} bf16, box {band_cols, heads_per_cta, tokens_per_cta}
+    CUtensorMap tm_out;  // out: 3-D {Dv, Hq, B*T} bf16, box {out_chunk_cols, heads_per_cta, tokens_per_cta}
     const uint16_t* q;   // bf16 bits [B][T][Hq][Dk]
     const int32_t* page_table;
     const int32_t* seq_lens;
@@ -55,7 +55,7 @@ struct DecodeParams {
     int dyn_split;       // 1: per-sequence split in one launch of 4-CTA clusters (tcgen05 shallow ring)
     int box_rows;        // key rows per K/V TMA box: min(page_size, keys per tile)
     int band_cols;       // output columns owned by one cluster rank: Dv / P
-    int out_chunk_cols;  // columns per output TMA store box: min(band_cols, 256)
+    int out_chunk_cols;  // columns per output TMA store box: min(band_cols, 256); Dv / 4 under dyn_split
     int32_t oob_row;     // a row coordinate past the end of the cache views (zero fill)
     float scale, scale_log2e;
     uint32_t debug_flags;
