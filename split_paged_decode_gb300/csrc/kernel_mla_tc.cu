@@ -623,8 +623,9 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
         if (P > 1) {
             cluster_wait();  // every rank's barriers are initialised
             if (wt == 0 && wg == 0 && !*abort_flag) {
-                // Both warpgroups waited for the last O product, which follows
-                // every product and every read of the ring, Q and P.
+                // This warpgroup has waited for the last O product, which
+                // follows every product, every read of the ring, Q and P, and
+                // the zeroing of the last tile's V rows.
                 mbar_arrive_expect_tx(recv_ms_bar, (uint32_t)((P - 1) * C::ROWS * 8));
                 mbar_arrive_expect_tx(recv_o_bar, (uint32_t)((P - 1) * C::ROWS * BW * 4));
                 for (int q = 0; q < P; ++q)
