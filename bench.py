@@ -39,16 +39,19 @@ sys.path.insert(0, ROOT)
 METRIC = "decode attention KV HBM GB/s"
 FALLBACK_HBM_GBS = 6800.0
 WORKLOAD_NAMES = ["tiny", "batched_gqa", "long_context", "ragged_speculative", "mla"]
-# The head-dim-128 workloads again over an fp8 (E4M3) cache with per-token K scales.
+# The workloads again over an fp8 (E4M3) cache with per-token K scales; the
+# MLA latent rows keep their rope part in a bf16 cache of its own.
 FP8_WORKLOADS = {"batched_gqa_e4m3": "batched_gqa", "long_context_e4m3": "long_context",
-                 "ragged_speculative_e4m3": "ragged_speculative"}
+                 "ragged_speculative_e4m3": "ragged_speculative", "mla_e4m3": "mla"}
 
 
 def workload(name: str):
     from split_paged_decode_gb300.workloads import WORKLOADS
 
     if name in FP8_WORKLOADS:
-        return WORKLOADS[FP8_WORKLOADS[name]].with_(name=name, kv_dtype="e4m3", k_scale=True)
+        base = WORKLOADS[FP8_WORKLOADS[name]]
+        rope = base.qk_depth - base.nope_depth if base.latent else 0
+        return base.with_(name=name, kv_dtype="e4m3", k_scale=True, rope_depth=rope)
     return WORKLOADS[name]
 
 
@@ -416,6 +419,7 @@ def measure(spd, torch, w, dev, stream, steps, warmup, flush, clocks, keep=False
     e4m3 = w.kv_dtype == "e4m3"
     if e4m3:
         ks = None if inp.k_scale is None else inp.k_scale.to(dev)
+        rope = None if inp.k_rope is None else inp.k_rope.to(dev)
         h = spd.fa_decode_create_kv(w.num_q_heads, w.num_kv_heads, w.qk_depth, w.nope_depth, w.ov_depth,
                                     w.page_size, w.num_q, w.splitk, spd.FA_KV_E4M3, w.rope_depth)
     else:
@@ -430,7 +434,7 @@ def measure(spd, torch, w, dev, stream, steps, warmup, flush, clocks, keep=False
 
     def step():
         if e4m3:
-            spd.fa_decode_run_kv(h, q, k, v, None, ks, pt, lens, inp.scale, out, lse, stream=stream)
+            spd.fa_decode_run_kv(h, q, k, v, rope, ks, pt, lens, inp.scale, out, lse, stream=stream)
         else:
             spd.fa_decode_run(h, q, k, v, pt, lens, inp.scale, out, lse, stream=stream)
 
@@ -460,6 +464,7 @@ def measure(spd, torch, w, dev, stream, steps, warmup, flush, clocks, keep=False
         m.h, m.step = h, step
         m.dev_tensors = (q, k, v, pt, lens, out, lse)
         m.dev_scale = ks if e4m3 else None
+        m.dev_rope = rope if e4m3 else None
     else:
         spd.fa_decode_destroy(h)
     return m
@@ -525,9 +530,10 @@ def run_gpu(args, world, rank, local):
     hq, hk, hv, hpt, hlens = pin(inp.q), pin(inp.k_pages), pin(inp.v_pages), pin(inp.page_table), \
         pin(inp.seq_lens)
     hks, ks = pin(inp.k_scale), head.dev_scale
+    hrope, rope = pin(inp.k_rope), head.dev_rope
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hpt, hlens, hks) if t is not None)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hpt, hlens, hks, hrope) if t is not None)
     d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
     e2e_steps = max(3, min(args.steps, 20))
 
@@ -540,6 +546,8 @@ def run_gpu(args, world, rank, local):
         lens.copy_(hlens, non_blocking=True)
         if ks is not None:
             ks.copy_(hks, non_blocking=True)
+        if rope is not None:
+            rope.copy_(hrope, non_blocking=True)
         head.step()
         hout.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)

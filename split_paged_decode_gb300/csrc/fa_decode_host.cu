@@ -141,7 +141,8 @@ struct fa_decode {
     fad::KernelGeometry geo_tc_big;  // tcgen05 kernel, 6-slot ring (one CTA per SM, several units per cluster)
     fad::KernelGeometry geo_tc_sk;   // the same under the stream-K partition
     fad::KernelGeometry geo_mla;     // tcgen05 kernel of the MLA latent layout (64 heads per CTA)
-    bool has_simt, has_latent, has_tc, has_mla;
+    fad::KernelGeometry geo_latent8; // SIMT kernel, E4M3 latent cache with a bf16 rope cache
+    bool has_simt, has_latent, has_tc, has_mla, has_latent8;
     int sm_count;
     int tc_big_clusters;             // clusters of geo_tc_big (fixed split) resident at once
     unsigned int* d_status;
@@ -157,7 +158,7 @@ struct fa_decode {
     uint64_t wait_limit_ns;
     uint64_t* trace;
     int64_t trace_words;
-    MapCache k_map, v_map, out_map[3];
+    MapCache k_map, v_map, rope_map, out_map[3];
     // Per-sequence split: the launches of the 2- and 4-CTA clusters run on two
     // side streams forked from the caller's stream (their sequences are
     // disjoint), so no launch waits for another's last wave. Owned by the
@@ -341,16 +342,22 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
         return fail(FA_ERR_UNSUPPORTED, "page_size %d is not a multiple of 8", page_size);
     auto page_fits = [&](int bn) { return page_size % bn == 0 || bn % page_size == 0; };
     if (kv_format == FA_KV_E4M3) {
-        // The E4M3 cache: the tcgen05 GQA kernel (head dim 128, <= 16 rows per CTA).
+        // The E4M3 cache: the tcgen05 GQA kernel (head dim 128, <= 16 rows per
+        // CTA, separate V), or the SIMT kernel of the MLA latent layout with a
+        // bf16 rope cache (16 heads per CTA).
         const auto geo = fad::tc_fp8_geometry;
         tmp.has_tc = tmp.row_blocks == 1 && rope_depth == 0 &&
                      geo(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsShared, false, &tmp.geo_tc) &&
                      geo(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsAlone, false, &tmp.geo_tc_big) &&
                      geo(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsAlone, true, &tmp.geo_tc_sk) &&
                      page_fits(tmp.geo_tc.keys_per_tile);
-        if (!tmp.has_tc)
+        tmp.has_latent8 = fad::simt_fp8_latent_geometry(qk_depth, ov_depth, rope_depth, tmp.rows_capacity,
+                                                        &tmp.geo_latent8) &&
+                          page_fits(tmp.geo_latent8.keys_per_tile);
+        if (!tmp.has_tc && !tmp.has_latent8)
             return fail(FA_ERR_UNSUPPORTED, "no E4M3-cache kernel for (qk %d, ov %d, rope %d), %d rows per CTA and "
-                                            "page_size %d (built: qk = ov = 128, rope 0, <= 16 rows per CTA)",
+                                            "page_size %d (built: qk = ov = 128, rope 0, <= 16 rows per CTA; "
+                                            "latent qk 576 = 512 + rope 64, ov 512, 16 rows per CTA)",
                         qk_depth, ov_depth, rope_depth, tmp.rows, page_size);
     } else {
         tmp.has_simt = fad::simt_geometry(qk_depth, ov_depth, false, tmp.rows_capacity, &tmp.geo) &&
@@ -397,6 +404,7 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
     if (tmp.has_tc && (rc = prepare_kernel(&tmp, tmp.geo_tc_big))) return rc;
     if (tmp.has_tc && splitk > 0 && (rc = prepare_kernel(&tmp, tmp.geo_tc_sk))) return rc;
     if (tmp.has_mla && (rc = prepare_kernel(&tmp, tmp.geo_mla))) return rc;
+    if (tmp.has_latent8 && (rc = prepare_kernel(&tmp, tmp.geo_latent8))) return rc;
     if (tmp.has_tc && splitk > 0 && (rc = resident_clusters(&tmp, tmp.geo_tc_big, splitk, &tmp.tc_big_clusters)))
         return rc;
     return FA_OK;
@@ -567,7 +575,9 @@ int fa_decode_describe(fa_decode_t h, char* buf, int size)
     // the shallow-ring one for the per-sequence split, else the SIMT kernel.
     const bool tc = h->has_mla || h->has_tc;
     const fad::KernelGeometry& g =
-        h->has_mla ? h->geo_mla : (h->has_tc ? (h->splitk > 0 ? h->geo_tc_big : h->geo_tc) : h->geo);
+        h->has_mla ? h->geo_mla
+                   : (h->has_tc ? (h->splitk > 0 ? h->geo_tc_big : h->geo_tc)
+                                : (h->has_latent8 ? h->geo_latent8 : h->geo));
     const int rows = h->has_mla ? 64 : h->rows, row_blocks = h->has_mla ? h->group / 64 : h->row_blocks;
     const char* per_seq = h->splitk != 0 ? "" : (h->has_tc && !h->has_mla ? "(per sequence: 1/2/4, one launch)"
                                                                          : "(per sequence: 1/2/4)");
@@ -575,7 +585,7 @@ int fa_decode_describe(fa_decode_t h, char* buf, int size)
              "path=%s kernel=%s simt_kernel=%s latent_kernel=%s splitk=%d%s threads=%d keys_per_tile=%d "
              "stages=%d rows=%d rows_capacity=%d row_blocks=%d smem=%d resident_clusters=%d",
              tc ? "tcgen05" : "simt", g.name, h->has_simt ? h->geo.name : "none",
-             h->has_latent ? h->geo_latent.name : "none", h->splitk, per_seq,
+             h->has_latent ? h->geo_latent.name : (h->has_latent8 ? h->geo_latent8.name : "none"), h->splitk, per_seq,
              g.threads, g.keys_per_tile, g.stages, rows, h->has_mla ? 64 : h->rows_capacity, row_blocks, g.smem_bytes,
              h->tc_big_clusters);
     return FA_OK;
@@ -599,9 +609,12 @@ int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const vo
     const bool e4m3 = h->kv_format == FA_KV_E4M3;
     if (!e4m3 && (k_rope_pages || k_scale))
         return fail(FA_ERR_INVALID_ARG, "k_rope_pages and k_scale apply to an E4M3 cache only");
-    if (e4m3 && k_rope_pages)
-        return fail(FA_ERR_UNSUPPORTED, "a separate bf16 rope cache is not built for this shape");
+    if (e4m3 && (k_rope_pages != nullptr) != (h->rope_depth > 0))
+        return fail(FA_ERR_INVALID_ARG, "k_rope_pages must be given exactly when rope_depth > 0 (rope_depth %d)",
+                    h->rope_depth);
     if (k_scale && !is_aligned(k_scale, 16)) return fail(FA_ERR_INVALID_ARG, "k_scale must be 16-byte aligned");
+    if (k_rope_pages && !is_aligned(k_rope_pages, 16))
+        return fail(FA_ERR_INVALID_ARG, "k_rope_pages must be 16-byte aligned");
     if (batch < 0) return fail(FA_ERR_INVALID_ARG, "batch must be >= 0 (got %d)", batch);
     if (batch == 0) return FA_OK;
     if (!q || !k_pages || !page_table || !seq_lens || !out)
@@ -621,8 +634,10 @@ int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const vo
                     (long long)cache_rows);
 
     const bool latent = (v_pages == nullptr || v_pages == k_pages);
-    if (e4m3 && latent)
-        return fail(FA_ERR_UNSUPPORTED, "the E4M3 cache is built with a separate V cache only");
+    if (e4m3 && latent && !h->has_latent8)
+        return fail(FA_ERR_UNSUPPORTED, "the E4M3 latent layout is built for qk 576 = 512 + rope 64, ov 512");
+    if (e4m3 && !latent && !h->has_tc)
+        return fail(FA_ERR_UNSUPPORTED, "this E4M3 handle reads the latent layout only (v_pages NULL)");
     if (latent && h->dv > h->dk)
         return fail(FA_ERR_INVALID_ARG, "latent layout (v_pages NULL or == k_pages) needs ov_depth <= qk_depth");
     // Kernel choice: for the MLA latent cache the MLA tcgen05 kernel (64 heads
@@ -630,7 +645,7 @@ int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const vo
     // the tcgen05 kernel where it applies, else the SIMT kernel.
     const bool force_simt = (h->debug_flags & FA_DEBUG_FORCE_SIMT) != 0;
     const bool use_mla = latent && h->has_mla && !(force_simt && h->has_latent);
-    const bool use_latent = latent && !use_mla && h->has_latent;
+    const bool use_latent = latent && !use_mla && (e4m3 ? h->has_latent8 : h->has_latent);
     const bool use_tc = !use_mla && !use_latent && h->has_tc && !(force_simt && h->has_simt);
     if (!use_mla && !use_latent && !use_tc && !h->has_simt)
         return fail(FA_ERR_UNSUPPORTED, "no kernel for this call (latent layout %d)", (int)latent);
@@ -668,7 +683,7 @@ int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const vo
         }
     }
     const fad::KernelGeometry& g = use_mla ? h->geo_mla
-                                   : use_latent ? h->geo_latent
+                                   : use_latent ? (e4m3 ? h->geo_latent8 : h->geo_latent)
                                                 : (use_tc ? (tc_big ? (sk_tiles > 0 ? h->geo_tc_sk : h->geo_tc_big)
                                                                     : h->geo_tc)
                                                           : h->geo);
@@ -679,8 +694,12 @@ int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const vo
     const int box_rows = h->page_size < bn ? h->page_size : bn;
 
     const int elem = e4m3 ? 1 : 2;
-    int rc = encode_cache_map(h->k_map, k_pages, h->dk, cache_rows, box_rows, elem);
+    // An E4M3 key row holds the codes only; its rope columns come from their own cache.
+    int rc = encode_cache_map(h->k_map, k_pages, h->dk - (e4m3 ? h->rope_depth : 0), cache_rows, box_rows, elem);
     if (rc) return rc;
+    if (e4m3 && h->rope_depth > 0 &&
+        (rc = encode_cache_map(h->rope_map, k_rope_pages, h->rope_depth, cache_rows, box_rows)))
+        return rc;
     if (latent && !use_latent && !use_mla) {
         // V = K row prefix through a separate-V kernel (e.g. qk == ov): same rows, V width.
         rc = encode_cache_map(h->v_map, k_pages, h->dk, cache_rows, box_rows);
@@ -693,6 +712,7 @@ int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const vo
     std::memset(&p, 0, sizeof p);
     p.tm_k = h->k_map.map;
     if (!use_latent && !use_mla) p.tm_v = h->v_map.map;
+    if (e4m3 && h->rope_depth > 0) p.tm_rope = h->rope_map.map;
     p.q = static_cast<const uint16_t*>(q);
     p.page_table = page_table;
     p.seq_lens = seq_lens;

@@ -39,6 +39,7 @@ struct DecodeParams {
     CUtensorMap tm_k;    // K rows: [num_pages*Hkv*PS][Dk] bf16, box {64, box_rows}, 128B swizzle
     CUtensorMap tm_v;    // V rows: [num_pages*Hkv*PS][Dv] (unused for the latent layout)
     CUtensorMap tm_out;  // out: 3-D {Dv, Hq, B*T} bf16, box {out_chunk_cols, heads_per_cta, tokens_per_cta}
+    CUtensorMap tm_rope; // E4M3 latent cache: the bf16 rope rows [num_pages*Hkv*PS][rope], box {64, box_rows}
     const uint16_t* q;   // bf16 bits [B][T][Hq][Dk]
     const int32_t* page_table;
     const int32_t* seq_lens;
@@ -97,6 +98,10 @@ struct KernelGeometry {
 // Kernel variants of the SIMT (warp-level FMA) path. Returns false when no
 // variant exists for (qk, ov, latent, rows_capacity).
 bool simt_geometry(int qk_depth, int ov_depth, bool latent, int rows_capacity, KernelGeometry* g);
+// The SIMT kernel over an E4M3 latent cache (V = the first ov dequantized
+// codes of the key row) whose last rope_depth key columns come from a bf16
+// cache of their own. Returns false when no variant exists.
+bool simt_fp8_latent_geometry(int qk_depth, int ov_depth, int rope_depth, int rows_capacity, KernelGeometry* g);
 
 // Kernel variants of the tcgen05 path (head dim 128, <= 16 rows per CTA) with
 // a ring of `nslot` 32 KB K/V tile slots; stream_k selects the variant of the

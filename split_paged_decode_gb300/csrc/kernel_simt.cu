@@ -19,20 +19,31 @@
 // the latent layout K_nope and V sharing one shared-memory stage (field
 // use_shared_kv, method shared_kv_cols).
 #include "fa_decode_internal.h"
+#include "fp8.cuh"
 #include "splitk_combine.cuh"
 
 namespace fad {
 
-template <int DK, int DV, int BN, int STAGES, int RB, bool LATENT>
+// FP8: the E4M3 cache in the latent layout (FA4Config page: qkv_dtype E4M3,
+// scale_dtype_ for the per-token K scale, rope_dtype_ for a bf16 rope part):
+// a key row is D8 = DK - ROPE E4M3 codes (scaled by the key's K scale)
+// followed by ROPE bf16 rope values (unscaled) from a cache of their own, and
+// V is the first DV dequantized codes of the same row.
+template <int DK, int DV, int BN, int STAGES, int RB, bool LATENT, bool FP8 = false, int ROPE = 0>
 struct SimtCfg {
     static constexpr int NCW = 4;                   // compute warps
     static constexpr int NCT = NCW * 32;            // compute threads
     static constexpr int THREADS = NCT + 32;        // + one load warp
-    static constexpr int KBOX = DK / 64;            // 64-column TMA boxes per K row
+    static constexpr int D8 = FP8 ? DK - ROPE : 0;  // E4M3 columns of a key row
+    static constexpr int K8BOX = D8 / 128;          // their 128-column (128-byte) TMA boxes
+    static constexpr int RBOX = ROPE / 64;          // 64-column bf16 boxes of the rope part
+    static constexpr int KBOX = FP8 ? K8BOX + RBOX : DK / 64;  // TMA boxes per K row
     static constexpr int VBOX = DV / 64;
     static constexpr int K_BYTES = KBOX * BN * 128;
     static constexpr int V_BYTES = LATENT ? 0 : VBOX * BN * 128;
-    static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
+    static constexpr int TILE_BYTES = K_BYTES + V_BYTES;  // bytes a stage's TMA boxes bring
+    static constexpr int SC_BYTES = FP8 ? BN * 4 : 0;     // FP8: the tile's per-key K scales, after the boxes
+    static constexpr int STAGE_BYTES = (TILE_BYTES + SC_BYTES + 1023) / 1024 * 1024;
     // Region offsets. Every region starts on 128 bytes; those a TMA copy
     // touches (the K/V ring and the bf16 output band) start on 1024 bytes.
     static constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -62,6 +73,8 @@ struct SimtCfg {
     static_assert(NCT % BN == 0 && BN % 32 == 0, "tile of keys must divide the compute threads");
     static_assert(NCH % NCT == 0 || NCT % NCH == 0, "column chunks must tile the threads");
     static_assert(!LATENT || DV <= DK, "latent V is a prefix of the K row");
+    static_assert(!FP8 || (LATENT && D8 % 128 == 0 && ROPE % 64 == 0 && DV <= D8 && DV % 128 == 0),
+                  "E4M3: the latent layout, whole 128-column code boxes, V inside the codes");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 };
 
@@ -74,11 +87,28 @@ __device__ __forceinline__ uint32_t swz_offset(int row, int col, int bn)
     return (uint32_t)((box * bn + row) * 128 + ((unit ^ (row & 7)) << 4) + (col & 7) * 2);
 }
 
-template <int DK, int DV, int BN, int STAGES, int RB, bool LATENT>
-__global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREADS, 1)
+// The same for one-byte (E4M3) elements: 128-column boxes.
+__device__ __forceinline__ uint32_t swz8_offset(int row, int col, int bn)
+{
+    const int box = col >> 7;
+    const int unit = (col & 127) >> 4;
+    return (uint32_t)((box * bn + row) * 128 + ((unit ^ (row & 7)) << 4) + (col & 15));
+}
+
+// Four E4M3 codes, in memory order, as four floats (exact: every E4M3 value
+// is a half value).
+__device__ __forceinline__ float4 e4m3x4_to_float4(uint32_t w)
+{
+    const float2 a = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3)));
+    const float2 b = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3)));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <int DK, int DV, int BN, int STAGES, int RB, bool LATENT, bool FP8 = false, int ROPE = 0>
+__global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT, FP8, ROPE>::THREADS, 1)
     simt_decode_kernel(const __grid_constant__ DecodeParams p)
 {
-    using C = SimtCfg<DK, DV, BN, STAGES, RB, LATENT>;
+    using C = SimtCfg<DK, DV, BN, STAGES, RB, LATENT, FP8, ROPE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_addr(smem);
@@ -183,13 +213,13 @@ __global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREA
                 if (i >= STAGES &&
                     !mbar_wait(empty_bar + 8 * s, ((i / STAGES) & 1) ^ 1, abort_flag, p.status, p.wait_limit_ns))
                     break;
-                mbar_arrive_expect_tx(full_bar + 8 * s, C::STAGE_BYTES);
-                issued = i + 1;
                 const int key0 = (tile_begin + i) * BN;
                 const uint32_t dst = sbase + s * C::STAGE_BYTES;
-                for (int seg = 0; seg < segs; ++seg) {
+                // Cache row of page segment seg of this tile (the zero-fill row
+                // past the sequence or on a bad page, which is flagged).
+                auto seg_row = [&](int seg) -> int32_t {
                     const int key = key0 + seg * p.box_rows;
-                    int32_t row = p.oob_row;  // zero fill past the sequence or on a bad page
+                    int32_t row = p.oob_row;
                     if (key < L) {
                         const int slot = key / p.page_size;
                         const int phys = slot < p.max_pages ? p.page_table[(int64_t)b * p.max_pages + slot] : -1;
@@ -198,15 +228,58 @@ __global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREA
                         else
                             atomicOr(p.status, FA_STATUS_BAD_PAGE);
                     }
-                    const uint32_t seg_off = seg * p.box_rows * 128;
+                    return row;
+                };
+                if constexpr (FP8) {
+                    // The E4M3 boxes, the bf16 rope boxes and, with K scales, one
+                    // bulk copy of each segment's scales (zeros, written before the
+                    // arrive that publishes them, for a zero-fill segment).
+                    int32_t rows[BN / 8];  // segs <= BN / 8: page_size is a multiple of 8
+                    uint32_t sc_bytes = 0;
+                    float* sc_s = reinterpret_cast<float*>(smem + s * C::STAGE_BYTES + C::TILE_BYTES);
+                    for (int seg = 0; seg < segs; ++seg) {
+                        rows[seg] = seg_row(seg);
+                        if (p.k_scale != nullptr) {
+                            if (rows[seg] != p.oob_row)
+                                sc_bytes += (uint32_t)(p.box_rows * 4);
+                            else
+                                for (int r = 0; r < p.box_rows; ++r) sc_s[seg * p.box_rows + r] = 0.f;
+                        }
+                    }
+                    // Zeros written here may later be overwritten by a bulk copy into this stage.
+                    if (p.k_scale != nullptr) fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(full_bar + 8 * s, (uint32_t)C::TILE_BYTES + sc_bytes);
+                    issued = i + 1;
+                    for (int seg = 0; seg < segs; ++seg) {
+                        const int32_t row = rows[seg];
+                        const uint32_t seg_off = seg * p.box_rows * 128;
 #pragma unroll
-                    for (int c = 0; c < C::KBOX; ++c)
-                        tma_load_2d(dst + c * BN * 128 + seg_off, &p.tm_k, c * 64, row, full_bar + 8 * s, policy);
-                    if (!LATENT) {
+                        for (int c = 0; c < C::K8BOX; ++c)
+                            tma_load_2d(dst + c * BN * 128 + seg_off, &p.tm_k, c * 128, row, full_bar + 8 * s,
+                                        policy);
 #pragma unroll
-                        for (int c = 0; c < C::VBOX; ++c)
-                            tma_load_2d(dst + C::K_BYTES + c * BN * 128 + seg_off, &p.tm_v, c * 64, row,
+                        for (int c = 0; c < C::RBOX; ++c)
+                            tma_load_2d(dst + (C::K8BOX + c) * BN * 128 + seg_off, &p.tm_rope, c * 64, row,
                                         full_bar + 8 * s, policy);
+                        if (p.k_scale != nullptr && row != p.oob_row)
+                            bulk_load(dst + C::TILE_BYTES + seg * p.box_rows * 4, p.k_scale + row,
+                                      (uint32_t)(p.box_rows * 4), full_bar + 8 * s);
+                    }
+                } else {
+                    mbar_arrive_expect_tx(full_bar + 8 * s, C::TILE_BYTES);
+                    issued = i + 1;
+                    for (int seg = 0; seg < segs; ++seg) {
+                        const int32_t row = seg_row(seg);
+                        const uint32_t seg_off = seg * p.box_rows * 128;
+#pragma unroll
+                        for (int c = 0; c < C::KBOX; ++c)
+                            tma_load_2d(dst + c * BN * 128 + seg_off, &p.tm_k, c * 64, row, full_bar + 8 * s, policy);
+                        if (!LATENT) {
+#pragma unroll
+                            for (int c = 0; c < C::VBOX; ++c)
+                                tma_load_2d(dst + C::K_BYTES + c * BN * 128 + seg_off, &p.tm_v, c * 64, row,
+                                            full_bar + 8 * s, policy);
+                        }
                     }
                 }
             }
@@ -228,6 +301,8 @@ __global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREA
             if (tid == 0) *consumed_s = i + 1;
             const uint8_t* kt = smem + s * C::STAGE_BYTES;
             const uint8_t* vt = LATENT ? kt : kt + C::K_BYTES;
+            const float* sc_s = reinterpret_cast<const float*>(kt + C::TILE_BYTES);  // FP8: per-key K scales
+            const bool scaled = FP8 && p.k_scale != nullptr;
             const int key0 = (tile_begin + i) * BN;
 
             // ---- S = Q K^T for key kk, rows rg + QK_GROUPS * k (raw units, masked)
@@ -235,17 +310,60 @@ __global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREA
                 float sacc[C::QK_ROWS];
 #pragma unroll
                 for (int k = 0; k < C::QK_ROWS; ++k) sacc[k] = 0.f;
+                if constexpr (FP8) {
+                    // E4M3 part (16 codes per 16-byte unit), times the key's scale
 #pragma unroll 2
-                for (int cc = 0; cc < DK / 8; ++cc) {
-                    const uint4 kw = *reinterpret_cast<const uint4*>(kt + swz_offset(kk, cc * 8, BN));
+                    for (int cc = 0; cc < C::D8 / 16; ++cc) {
+                        const uint4 kw = *reinterpret_cast<const uint4*>(kt + swz8_offset(kk, cc * 16, BN));
+                        const float4 k0 = e4m3x4_to_float4(kw.x), k1 = e4m3x4_to_float4(kw.y);
+                        const float4 k2 = e4m3x4_to_float4(kw.z), k3 = e4m3x4_to_float4(kw.w);
+#pragma unroll
+                        for (int k = 0; k < C::QK_ROWS; ++k) {
+                            const int r = rg + C::QK_GROUPS * k;
+                            if (C::QK_ROWS * C::QK_GROUPS > RB && r >= RB) continue;
+                            const float4* qv = reinterpret_cast<const float4*>(q_s + r * DK + cc * 16);
+                            const float4 qa = qv[0], qb = qv[1], qc = qv[2], qd = qv[3];
+                            float a = sacc[k];
+                            a = fmaf(qa.x, k0.x, a);
+                            a = fmaf(qa.y, k0.y, a);
+                            a = fmaf(qa.z, k0.z, a);
+                            a = fmaf(qa.w, k0.w, a);
+                            a = fmaf(qb.x, k1.x, a);
+                            a = fmaf(qb.y, k1.y, a);
+                            a = fmaf(qb.z, k1.z, a);
+                            a = fmaf(qb.w, k1.w, a);
+                            a = fmaf(qc.x, k2.x, a);
+                            a = fmaf(qc.y, k2.y, a);
+                            a = fmaf(qc.z, k2.z, a);
+                            a = fmaf(qc.w, k2.w, a);
+                            a = fmaf(qd.x, k3.x, a);
+                            a = fmaf(qd.y, k3.y, a);
+                            a = fmaf(qd.z, k3.z, a);
+                            a = fmaf(qd.w, k3.w, a);
+                            sacc[k] = a;
+                        }
+                    }
+                    if (scaled) {
+                        const float ks = sc_s[kk];
+#pragma unroll
+                        for (int k = 0; k < C::QK_ROWS; ++k) sacc[k] *= ks;
+                    }
+                }
+                // bf16 columns: the whole row, or (FP8) the rope part after the codes
+                constexpr int BF_COLS = FP8 ? ROPE : DK;
+                constexpr int BF_Q0 = FP8 ? C::D8 : 0;        // its first column in Q
+                constexpr int BF_OFF = FP8 ? C::K8BOX * BN * 128 : 0;  // its first box in the stage
+#pragma unroll 2
+                for (int cc = 0; cc < BF_COLS / 8; ++cc) {
+                    const uint4 kw = *reinterpret_cast<const uint4*>(kt + BF_OFF + swz_offset(kk, cc * 8, BN));
                     const float2 k01 = bf16x2_to_float2(kw.x), k23 = bf16x2_to_float2(kw.y);
                     const float2 k45 = bf16x2_to_float2(kw.z), k67 = bf16x2_to_float2(kw.w);
 #pragma unroll
                     for (int k = 0; k < C::QK_ROWS; ++k) {
                         const int r = rg + C::QK_GROUPS * k;
                         if (C::QK_ROWS * C::QK_GROUPS > RB && r >= RB) continue;
-                        const float4 qa = *reinterpret_cast<const float4*>(q_s + r * DK + cc * 8);
-                        const float4 qb = *reinterpret_cast<const float4*>(q_s + r * DK + cc * 8 + 4);
+                        const float4 qa = *reinterpret_cast<const float4*>(q_s + r * DK + BF_Q0 + cc * 8);
+                        const float4 qb = *reinterpret_cast<const float4*>(q_s + r * DK + BF_Q0 + cc * 8 + 4);
                         float a = sacc[k];
                         a = fmaf(qa.x, k01.x, a);
                         a = fmaf(qa.y, k01.y, a);
@@ -321,16 +439,25 @@ __global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREA
 #pragma unroll 2
             for (int j = 0; j < j_end; ++j) {
                 float pr[C::PV_ROWS];
+                const float vs = scaled ? sc_s[j] : 1.f;  // FP8 latent V: the key's scale, on P
 #pragma unroll
                 for (int k = 0; k < C::PV_ROWS; ++k) {
                     const int r = pv_row0 + C::PV_ROW_LANES * k;
-                    pr[k] = (r < RB) ? s_s[r * BN + j] : 0.f;
+                    pr[k] = (r < RB) ? s_s[r * BN + j] * vs : 0.f;
                 }
 #pragma unroll
                 for (int ch = 0; ch < C::PV_CHUNKS; ++ch) {
                     const int col = (pv_lane + ch * C::NCT) * 4;
-                    const uint2 vw = *reinterpret_cast<const uint2*>(vt + swz_offset(j, col, BN));
-                    const float2 v01 = bf16x2_to_float2(vw.x), v23 = bf16x2_to_float2(vw.y);
+                    float2 v01, v23;
+                    if constexpr (FP8) {
+                        const float4 v = e4m3x4_to_float4(*reinterpret_cast<const uint32_t*>(vt + swz8_offset(j, col, BN)));
+                        v01 = make_float2(v.x, v.y);
+                        v23 = make_float2(v.z, v.w);
+                    } else {
+                        const uint2 vw = *reinterpret_cast<const uint2*>(vt + swz_offset(j, col, BN));
+                        v01 = bf16x2_to_float2(vw.x);
+                        v23 = bf16x2_to_float2(vw.y);
+                    }
 #pragma unroll
                     for (int k = 0; k < C::PV_ROWS; ++k) {
                         acc[k][ch][0] = fmaf(pr[k], v01.x, acc[k][ch][0]);
@@ -391,11 +518,11 @@ __global__ void __launch_bounds__(SimtCfg<DK, DV, BN, STAGES, RB, LATENT>::THREA
 // ---------------------------------------------------------------------------
 // Variants and their geometry
 // ---------------------------------------------------------------------------
-template <int DK, int DV, int BN, int STAGES, int RB, bool LATENT>
+template <int DK, int DV, int BN, int STAGES, int RB, bool LATENT, bool FP8 = false, int ROPE = 0>
 static bool fill_geometry(KernelGeometry* g, const char* name)
 {
-    using C = SimtCfg<DK, DV, BN, STAGES, RB, LATENT>;
-    g->func = reinterpret_cast<const void*>(&simt_decode_kernel<DK, DV, BN, STAGES, RB, LATENT>);
+    using C = SimtCfg<DK, DV, BN, STAGES, RB, LATENT, FP8, ROPE>;
+    g->func = reinterpret_cast<const void*>(&simt_decode_kernel<DK, DV, BN, STAGES, RB, LATENT, FP8, ROPE>);
     g->threads = C::THREADS;
     g->keys_per_tile = BN;
     g->stages = STAGES;
@@ -420,6 +547,14 @@ bool simt_geometry(int qk, int ov, bool latent, int rb, KernelGeometry* g)
     FAD_SIMT(576, 512, 32, 3, 16, true, "_latent")
     FAD_SIMT(576, 512, 32, 2, 16, false, "")
 #undef FAD_SIMT
+    return false;
+}
+
+bool simt_fp8_latent_geometry(int qk, int ov, int rope, int rb, KernelGeometry* g)
+{
+    // MLA: 512 E4M3 latent columns (V = all of them) and a 64-column bf16 rope.
+    if (qk == 576 && ov == 512 && rope == 64 && rb == 16)
+        return fill_geometry<576, 512, 32, 4, 16, true, true, 64>(g, "simt_e4m3_d576_r64_v512_bn32_s4_r16_latent");
     return false;
 }
 

@@ -168,3 +168,66 @@ def test_running_max_moves_every_tile(case, kw, path):
         call.run()
         assert call.status() == 0
         check_against_oracle(call, what=f"fp8 ramp {case}")
+
+
+# --- the MLA latent layout over an E4M3 cache with a bf16 rope cache ---------
+# K_j = [k_scale_j * e4m3(k8_j[0:512]), bf16 rope_j[0:64]] and V_j =
+# k_scale_j * e4m3(k8_j[0:512]): the FA4Config page's separate rope dtype and
+# per-token K scale (SIMT kernel, 16 heads per CTA).
+
+def mla_wl(**kw):
+    base = dict(name="fp8_mla", batch=3, num_q=1, num_q_heads=32, num_kv_heads=1, qk_depth=576, nope_depth=512,
+                ov_depth=512, page_size=64, splitk=2, seq_len_lo=1, seq_len_hi=700, latent=True,
+                scale=1.0 / 24.0, seed=1100, kv_dtype="e4m3", k_scale=True, rope_depth=64)
+    base.update(kw)
+    return DecodeWorkload(**base)
+
+
+@pytest.mark.parametrize("scaled", [True, False])
+@pytest.mark.parametrize("P", [1, 2, 4, 16])
+def test_mla_latent_rope_splits(P, scaled):
+    w = mla_wl(splitk=P, k_scale=scaled, seed=1100 + P)
+    run_and_check(w, seq_lens=[1, 333, 700], what=f"fp8 mla P{P} scale {scaled}")
+
+
+@pytest.mark.parametrize("ps", [8, 32, 128])
+def test_mla_latent_rope_page_sizes(ps):
+    run_and_check(mla_wl(page_size=ps, splitk=4, seed=1120 + ps), seq_lens=[65, 1000, 257],
+                  what=f"fp8 mla ps{ps}")
+
+
+def test_mla_latent_rope_per_sequence_split_and_short():
+    w = mla_wl(batch=8, num_q_heads=16, splitk=0, seed=1130)
+    run_and_check(w, seq_lens=[0, 1, 31, 32, 33, 1100, 4097, 9000], what="fp8 mla auto split")
+
+
+def test_mla_latent_rope_nonfinite_tails_do_not_leak():
+    w = mla_wl(batch=3, splitk=2, seed=1140)
+    lens = [70, 200, 129]
+    inp = generate(w, seq_lens=lens)
+    for b, L in enumerate(lens):
+        last = int(inp.page_table[b, (L - 1) // 64])
+        inp.k_pages[last, :, L % 64:, :] = 0x7F   # NaN code
+        inp.k_rope[last, :, L % 64:, :] = float("nan")
+        inp.k_scale[last, :, L % 64:] = float("nan")
+    with DeviceCall(inp) as call:
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what="fp8 mla non-finite tails")
+
+
+def test_mla_latent_rope_full_size():
+    """The mla workload (32 seqs x 128 heads, L8192, split 2) over the E4M3 latent cache."""
+    w = WORKLOADS["mla"].with_(kv_dtype="e4m3", k_scale=True, rope_depth=64)
+    run_and_check(w, what="mla e4m3")
+
+
+def test_mla_latent_rope_argument_checks():
+    inp = generate(mla_wl(seed=1150))
+    with DeviceCall(inp) as call:
+        # no rope cache; a separate V cache (a copy: the same pointer would read as the latent layout)
+        for rope, v, code in [(None, None, spd.FA_ERR_INVALID_ARG), (call.rope, call.k.clone(), spd.FA_ERR_UNSUPPORTED)]:
+            with pytest.raises(spd.FaDecodeError) as e:
+                spd.fa_decode_run_kv(call.h, call.q, call.k, v, rope, call.ks, call.pt, call.lens, inp.scale,
+                                     call.out, call.lse)
+            assert e.value.code == code, e.value
