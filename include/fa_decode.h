@@ -132,8 +132,12 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
  * mantissa bits; no infinity; largest finite value 448), read as
  *   K_j = k_scale_j * e4m3(k_pages row j)   (k_scale_j = 1 without scales)
  *   V_j = e4m3(v_pages row j)                (V carries no scale)
- * with Q, out and lse as for a bf16 cache. It halves the cache bytes that
- * every decode step reads.
+ * with Q, out and lse as for a bf16 cache. In the latent layout (v_pages
+ * NULL) with rope_depth R, a k_pages row holds qk_depth - R codes and the
+ * key row ends in R bf16 values from their own cache (unscaled):
+ *   K_j = [k_scale_j * e4m3(k_pages row j), k_rope_pages row j]
+ *   V_j = k_scale_j * e4m3(k_pages row j)[0 : ov_depth]
+ * It halves the cache bytes that every decode step reads.
  */
 #define FA_KV_BF16 0
 #define FA_KV_E4M3 1
@@ -146,8 +150,10 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
  *               rope dtype, for a latent cache); 0 for FA_KV_BF16
  * Built for E4M3: qk_depth == ov_depth == 128 with a separate V cache,
  * rope_depth 0, T * g <= 16 rows per CTA (the tcgen05 GQA kernel, every
- * split). Other E4M3 shapes return FA_ERR_UNSUPPORTED. Allocates as
- * fa_decode_create does.
+ * split); and the MLA latent layout qk_depth 576 (512 codes + rope_depth
+ * 64), ov_depth 512, with T * g == 16 or num_q == 1 and g a multiple of 16
+ * (the FMA kernel, 16 heads per CTA, every split). Other E4M3 shapes return
+ * FA_ERR_UNSUPPORTED. Allocates as fa_decode_create does.
  */
 int fa_decode_create_kv(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth,
                         int ov_depth, int page_size, int num_q, int splitk, int kv_format, int rope_depth);
@@ -156,10 +162,12 @@ int fa_decode_create_kv(fa_decode_t* out, int num_q_heads, int num_kv_heads, int
  * Enqueue one decode forward over the handle's cache format. Arguments as for
  * fa_decode_run, plus:
  *   k_pages / v_pages  for FA_KV_E4M3: uint8 E4M3 codes [num_pages][num_kv_heads]
- *                      [page_size][depth], 16-byte aligned; v_pages must be a
- *                      separate cache
- *   k_rope_pages       bf16 [num_pages][num_kv_heads][page_size][rope_depth], or
- *                      NULL; must be NULL while rope_depth is 0
+ *                      [page_size][depth], 16-byte aligned (depth qk_depth -
+ *                      rope_depth for K); v_pages a separate cache, or NULL (or
+ *                      k_pages) for the latent layout where the plan has it
+ *   k_rope_pages       bf16 [num_pages][num_kv_heads][page_size][rope_depth],
+ *                      16-byte aligned: given exactly when rope_depth > 0
+ *                      (FA_ERR_INVALID_ARG otherwise)
  *   k_scale            fp32 [num_pages][num_kv_heads][page_size] per-token K
  *                      scales, 16-byte aligned, or NULL for unit scales; NULL
  *                      for a bf16 cache
