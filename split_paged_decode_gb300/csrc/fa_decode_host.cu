@@ -343,8 +343,8 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
     auto page_fits = [&](int bn) { return page_size % bn == 0 || bn % page_size == 0; };
     if (kv_format == FA_KV_E4M3) {
         // The E4M3 cache: the tcgen05 GQA kernel (head dim 128, <= 16 rows per
-        // CTA, separate V), or the SIMT kernel of the MLA latent layout with a
-        // bf16 rope cache (16 heads per CTA).
+        // CTA, separate V); for the MLA latent layout with a bf16 rope cache the
+        // tcgen05 MLA kernel (64 heads per CTA) and the SIMT kernel (16).
         const auto geo = fad::tc_fp8_geometry;
         tmp.has_tc = tmp.row_blocks == 1 && rope_depth == 0 &&
                      geo(qk_depth, ov_depth, tmp.rows, fad::kTcSlotsShared, false, &tmp.geo_tc) &&
@@ -354,7 +354,10 @@ static int plan_decode(fa_decode& tmp, int num_q_heads, int num_kv_heads, int qk
         tmp.has_latent8 = fad::simt_fp8_latent_geometry(qk_depth, ov_depth, rope_depth, tmp.rows_capacity,
                                                         &tmp.geo_latent8) &&
                           page_fits(tmp.geo_latent8.keys_per_tile);
-        if (!tmp.has_tc && !tmp.has_latent8)
+        tmp.has_mla = fad::mla_tc_fp8_geometry(qk_depth, ov_depth, tmp.nope, rope_depth, tmp.group, num_q,
+                                               &tmp.geo_mla) &&
+                      page_fits(tmp.geo_mla.keys_per_tile);
+        if (!tmp.has_tc && !tmp.has_latent8 && !tmp.has_mla)
             return fail(FA_ERR_UNSUPPORTED, "no E4M3-cache kernel for (qk %d, ov %d, rope %d), %d rows per CTA and "
                                             "page_size %d (built: qk = ov = 128, rope 0, <= 16 rows per CTA; "
                                             "latent qk 576 = 512 + rope 64, ov 512, 16 rows per CTA)",
@@ -634,7 +637,7 @@ int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const vo
                     (long long)cache_rows);
 
     const bool latent = (v_pages == nullptr || v_pages == k_pages);
-    if (e4m3 && latent && !h->has_latent8)
+    if (e4m3 && latent && !h->has_latent8 && !h->has_mla)
         return fail(FA_ERR_UNSUPPORTED, "the E4M3 latent layout is built for qk 576 = 512 + rope 64, ov 512");
     if (e4m3 && !latent && !h->has_tc)
         return fail(FA_ERR_UNSUPPORTED, "this E4M3 handle reads the latent layout only (v_pages NULL)");
@@ -644,7 +647,7 @@ int fa_decode_run_kv(fa_decode_t h, const void* q, const void* k_pages, const vo
     // per CTA) where it applies, else the latent-layout SIMT kernel; otherwise
     // the tcgen05 kernel where it applies, else the SIMT kernel.
     const bool force_simt = (h->debug_flags & FA_DEBUG_FORCE_SIMT) != 0;
-    const bool use_mla = latent && h->has_mla && !(force_simt && h->has_latent);
+    const bool use_mla = latent && h->has_mla && !(force_simt && (e4m3 ? h->has_latent8 : h->has_latent));
     const bool use_latent = latent && !use_mla && (e4m3 ? h->has_latent8 : h->has_latent);
     const bool use_tc = !use_mla && !use_latent && h->has_tc && !(force_simt && h->has_simt);
     if (!use_mla && !use_latent && !use_tc && !h->has_simt)

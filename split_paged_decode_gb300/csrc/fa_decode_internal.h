@@ -114,6 +114,10 @@ bool tc_fp8_geometry(int qk_depth, int ov_depth, int rows, int nslot, bool strea
 // ov 512, V = the latent rows' first 512 columns) for num_q == 1 and a
 // multiple of 64 heads per kv head: 64 heads per CTA.
 bool mla_tc_geometry(int qk_depth, int ov_depth, int nope_depth, int heads_per_kv, int num_q, KernelGeometry* g);
+// The same kernel over the E4M3 latent cache: 512 codes per row with a
+// per-token K scale, the 64 rope columns from a bf16 cache of their own.
+bool mla_tc_fp8_geometry(int qk_depth, int ov_depth, int nope_depth, int rope_depth, int heads_per_kv, int num_q,
+                         KernelGeometry* g);
 // The stream-K partition is used only while every cluster rank keeps at
 // least this many 128-key tiles of its range.
 constexpr int kChunkMinTilesPerRank = 4;

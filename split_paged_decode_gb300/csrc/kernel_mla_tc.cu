@@ -34,13 +34,31 @@
 // into nope and rope (q_nope / q_rope), one O accumulator for the wide V
 // (single_o), V as the nope prefix of the shared latent row (use_shared_kv),
 // split-K clusters (splitk_partitions).
+//
+// FP8: the E4M3 latent cache (FA4Config page: qkv_dtype E4M3, scale_dtype_
+// for the per-token K scale, rope_dtype_ for the bf16 rope part). A key row
+// is 512 codes, scaled by the key's K scale, followed by 64 bf16 rope values
+// from a cache of their own; V is the 512 scaled codes. The code part of S^T
+// is a kind::f8f6f4 product against Q^T carried as two E4M3 operands (16 h
+// and l, fp8.cuh; each head scaled by a power of two sigma_h first) into one
+// accumulator, the rope part a kind::f16 product into the other:
+//   S = acc_codes / (16 sigma_h) * k_scale_j + acc_rope.
+// O^T += V^T P'^T takes the codes as they are and P' = P k_scale_j / Sigma as
+// two E4M3 operands (16 P' = h + l), where Sigma is a power of two that bounds
+// every K scale seen so far (raised, with O corrected like a moved max, when
+// a tile brings a larger scale), so P' <= P and the O partial is
+// acc Sigma / 16. The ring items carry twice the columns of a bf16 item: K as
+// two 256-code items plus the rope item, V as two items; the per-token
+// scales come in a ring of their own.
 #include "fa_decode_internal.h"
 #include "device_common.cuh"
+#include "fp8.cuh"
 #include "tcgen05.cuh"
 
 namespace fad {
 
-struct MlaCfg {
+template <bool FP8>
+struct MlaCfgT {
     static constexpr int ROWS = 64;                 // heads per CTA (N of both MMAs)
     static constexpr int BN = 128;                  // keys per tile (M of S^T)
     static constexpr int DK = 576, DV = 512;
@@ -49,9 +67,15 @@ struct MlaCfg {
     static constexpr int P_BUFS = 1;
     static constexpr int ATOM_BYTES = BN * 128;     // 16 KB: 64 columns of a tile
     static constexpr int SLOT_BYTES = 2 * ATOM_BYTES;
-    static constexpr int KITEMS = 5;                // K: 4 x 128 columns + the 64-column rope
-    static constexpr int VITEMS = 4;                // V: 4 x 128 columns
-    static constexpr int Q_ATOM = ROWS * 128;       // 8 KB: 64 depth columns of the 64 heads
+    // K: 4 x 128 columns + the 64-column rope (FP8: 2 x 256 codes + the rope);
+    // V: 4 x 128 columns (FP8: 2 x 256 codes). An item is two 128-byte boxes
+    // (one for the rope item).
+    static constexpr int KITEMS = FP8 ? 3 : 5;
+    static constexpr int VITEMS = FP8 ? 2 : 4;
+    static constexpr int ITEM_COLS = FP8 ? 256 : 128;  // cache columns of a two-box item
+    static constexpr float RESCALE = FP8 ? 4.0f : 8.0f;  // lazy rescale: P <= 2^RESCALE (FP8: 16 P' <= 448)
+    static constexpr int KS = FP8 ? 4 : 0;          // FP8: per-token K scale ring entries (one tile each)
+    static constexpr int Q_ATOM = ROWS * 128;       // 8 KB: 64 depth columns of the 64 heads (FP8: 128 codes)
     static constexpr int Q_BYTES = 9 * Q_ATOM;      // 72 KB
     static constexpr int P_ATOM = ROWS * 128;       // 8 KB: 64 keys of P^T
     static constexpr int P_BYTES = 2 * P_ATOM;      // 16 KB
@@ -66,12 +90,17 @@ struct MlaCfg {
     static constexpr int OFF_P = OFF_Q + Q_BYTES;                    // [P_BUFS][2 atoms][64 heads][128 B]
     static constexpr int OFF_RED = OFF_P + P_BUFS * P_BYTES;         // float [2 warpgroups][4 quadrants][32]
     // barriers: slot_full[NSLOT], slot_empty[NSLOT], s_full[2], s_empty[2], p_full[2],
-    // o_full[2], q_full, recv_ms, mma_done, tmem_ready, v_zeroed[4], recv_o, ready[kMaxSplit]
+    // o_full[2], q_full, recv_ms, mma_done, tmem_ready, v_zeroed[4], recv_o, ready[kMaxSplit],
+    // (FP8) ks_full[KS], ks_empty[KS]
     static constexpr int OFF_BAR = OFF_RED + 2 * 4 * 32 * 4;
-    static constexpr int NBAR = 2 * NSLOT + 17 + kMaxSplit;
+    static constexpr int NBAR = 2 * NSLOT + 17 + kMaxSplit + 2 * KS;
     static constexpr int OFF_ROWS = OFF_BAR + NBAR * 8;              // int [4 tiles][16 segments]
     static constexpr int OFF_MISC = OFF_ROWS + 4 * 16 * 4;           // tmem base, abort, S next item, O next item
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    // FP8: K scales float [KS][BN], 1 / (16 sigma_h) float [64], tile scale maxima float [2][4]
+    static constexpr int OFF_KS = (OFF_MISC + 16 + 127) / 128 * 128;  // bulk copy destinations: 16-byte aligned
+    static constexpr int OFF_QINV = OFF_KS + KS * BN * 4;
+    static constexpr int OFF_SIG = OFF_QINV + (FP8 ? ROWS * 4 : 0);
+    static constexpr int SMEM_BYTES = OFF_SIG + (FP8 ? 32 : 0) + 1024;
     // Split-K epilogue, once every product of the CTA has completed, over the
     // drained ring, Q and P: the partials the other ranks push for this
     // rank's band, f32 [P - 1][BW][64] (at most 15/16 of 128 KB), their rows' (max, sum) float2 [P - 1][64], the bf16 band
@@ -83,6 +112,7 @@ struct MlaCfg {
     static_assert((kMaxSplit - 1) * ROWS * 8 <= OFF_OUT - OFF_RECV_MS, "pushed row statistics fit");
     static_assert(OFF_WTAB + kMaxSplit * ROWS * 4 <= OFF_RED, "epilogue buffers fit below the softmax scratch");
     static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms on 1024 bytes");
+    static_assert(OFF_KS % 16 == 0 && OFF_QINV % 16 == 0, "K scale copies and float4 reads");
     static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
 };
 
@@ -92,15 +122,17 @@ struct MlaCfg {
 // first item of the group at position g.
 __device__ __forceinline__ int mla_k_group(int i) { return i == 0 ? 0 : 2 * i - 1; }
 __device__ __forceinline__ int mla_v_group(int t, int n) { return t == n - 1 ? 2 * n - 1 : 2 * t + 2; }
+template <bool FP8>
 __device__ __forceinline__ int mla_group_item(int g, int n)
 {
     const int nk = g == 0 ? 0 : min(n, (g + 2) / 2);  // K groups before position g
-    return MlaCfg::KITEMS * nk + MlaCfg::VITEMS * (g - nk);
+    return MlaCfgT<FP8>::KITEMS * nk + MlaCfgT<FP8>::VITEMS * (g - nk);
 }
 
-__global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const __grid_constant__ DecodeParams p)
+template <bool FP8>
+__global__ void __launch_bounds__(MlaCfgT<FP8>::THREADS, 1) mla_tc_decode_kernel(const __grid_constant__ DecodeParams p)
 {
-    using C = MlaCfg;
+    using C = MlaCfgT<FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_addr(smem);
@@ -155,6 +187,10 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
     // their row statistics on recv_ms_bar); rank q arrives on ready[q] once
     // its drained ring may take this rank's pushes.
     const uint32_t recv_o_bar = s_full + 128, ready_bar = s_full + 136;
+    // FP8 K scale ring: tile t's scales in entry t % KS (full: the copies landed;
+    // empty: every softmax warp has read them).
+    const uint32_t ks_full = s_full + 8 * (17 + kMaxSplit), ks_empty = ks_full + 8 * C::KS;
+    const bool scaled = FP8 && p.k_scale != nullptr;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     const uint32_t s_next = sbase + C::OFF_MISC + 8, o_next = sbase + C::OFF_MISC + 12;
@@ -178,6 +214,10 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
         mbar_init(mma_done, 2);
         mbar_init(tmem_ready, 1);
         for (int e = 0; e < C::VITEMS; ++e) mbar_init(v_zeroed + 8 * e, 8);
+        for (int e = 0; e < C::KS; ++e) {
+            mbar_init(ks_full + 8 * e, 1);
+            mbar_init(ks_empty + 8 * e, 8);
+        }
         *abort_flag = 0;
         // Next item of each kind to be consumed: K starts at item 0, V at the
         // first item of V(0) (no earlier item is a V item, and with 5-item K
@@ -186,10 +226,13 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
         const int tc0 = nt / P + (rank < nt % P ? 1 : 0);
         *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 8) = 0;
         *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 12) =
-            tc0 > 0 ? (uint32_t)mla_group_item(mla_v_group(0, tc0), tc0) : 0xffffffffu;
+            tc0 > 0 ? (uint32_t)mla_group_item<FP8>(mla_v_group(0, tc0), tc0) : 0xffffffffu;
         fence_mbarrier_init_cluster();
     }
-    if (warp == 0 && lane == 0) tma_prefetch_map(&p.tm_k);
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&p.tm_k);
+        if (FP8) tma_prefetch_map(&p.tm_rope);
+    }
     __syncthreads();
     if (P > 1) cluster_arrive_relaxed();
     uint32_t tmem = 0;
@@ -211,6 +254,7 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
     const bool v_tail = tile_count > 0 && (tile_begin + tile_count) * C::BN > L;
 
     int issued = 0;
+    int ks_issued = 0;  // FP8: tiles whose K scale copies were issued
     // Softmax state of this thread's 32 heads.
     float m_run[32], l_part[32];
 
@@ -259,6 +303,37 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                         }
                     }
                     if (lane < 16) rows_s[(t & 3) * 16 + lane] = row;
+                    if (scaled) {
+                        // Tile t's K scales, one bulk copy per page segment in the cache
+                        // (none for a zero-filled segment: the softmax masks those keys).
+                        const int kse = t % C::KS;
+                        if (t >= C::KS) {
+                            const bool got = mbar_wait(ks_empty + 8 * kse, ((t / C::KS) & 1) ^ 1, abort_flag,
+                                                       p.status, p.wait_limit_ns);
+                            if (!__all_sync(0xffffffffu, got)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        const bool copy = lane < segs && row != p.oob_row;
+                        // Zeros for a zero-filled segment's keys (a bad page), written
+                        // before the arrive that publishes the entry; a later copy into
+                        // the entry follows the proxy fence.
+                        float* ks_w = reinterpret_cast<float*>(smem + C::OFF_KS) + kse * C::BN;
+                        for (int sg = 0; sg < segs; ++sg) {
+                            const int32_t r_sg = __shfl_sync(0xffffffffu, row, sg);
+                            if (lane == 0 && r_sg == p.oob_row)
+                                for (int k = 0; k < p.box_rows; ++k) ks_w[sg * p.box_rows + k] = 0.f;
+                        }
+                        if (lane == 0) fence_proxy_async_smem();
+                        const uint32_t n = __popc(__ballot_sync(0xffffffffu, copy));
+                        if (lane == 0) mbar_arrive_expect_tx(ks_full + 8 * kse, n * (uint32_t)p.box_rows * 4u);
+                        __syncwarp();
+                        if (copy)
+                            bulk_load(sbase + C::OFF_KS + (uint32_t)((kse * C::BN + lane * p.box_rows) * 4),
+                                      p.k_scale + row, (uint32_t)p.box_rows * 4u, ks_full + 8 * kse);
+                        ks_issued = t + 1;
+                    }
                 } else {
                     row = lane < 16 ? rows_s[(t & 3) * 16 + lane] : p.oob_row;
                 }
@@ -274,15 +349,23 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                         }
                     }
                     const bool rope = !is_v && e == C::KITEMS - 1;
-                    const int col = rope ? C::DV : 128 * e;
                     if (lane == 0) mbar_arrive_expect_tx(slot_full + 8 * slot, rope ? C::ATOM_BYTES : C::SLOT_BYTES);
                     __syncwarp();
                     issued = jj + 1;
                     if (jj == 0 && lane == 0) stamp(1);
                     if (lane < segs) {
                         const uint32_t dst = sbase + C::OFF_RING + slot * C::SLOT_BYTES + lane * p.box_rows * 128;
-                        tma_load_2d(dst, &p.tm_k, col, row, slot_full + 8 * slot, policy);
-                        if (!rope) tma_load_2d(dst + C::ATOM_BYTES, &p.tm_k, col + 64, row, slot_full + 8 * slot, policy);
+                        if (rope && FP8) {
+                            tma_load_2d(dst, &p.tm_rope, 0, row, slot_full + 8 * slot, policy);
+                        } else if (rope) {
+                            tma_load_2d(dst, &p.tm_k, C::DV, row, slot_full + 8 * slot, policy);
+                        } else {
+                            // two 128-byte boxes: 64 bf16 columns or 128 codes each
+                            const int col = C::ITEM_COLS * e;
+                            tma_load_2d(dst, &p.tm_k, col, row, slot_full + 8 * slot, policy);
+                            tma_load_2d(dst + C::ATOM_BYTES, &p.tm_k, col + C::ITEM_COLS / 2, row,
+                                        slot_full + 8 * slot, policy);
+                        }
                     }
                 }
             }
@@ -302,11 +385,12 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
             bool ok = true;
             if (is_s) {
                 const uint32_t id_s = umma_idesc_bf16_f32(128, C::ROWS, false, false);
+                const uint32_t id_s8 = umma_idesc_e4m3_f32(128, C::ROWS, false, false);
                 const uint64_t q_desc0 = umma_smem_desc(sbase + C::OFF_Q, 16, 1024, kLayoutSwizzle128);
                 const uint64_t k_desc0 = umma_smem_desc(sbase + C::OFF_RING, 16, 1024, kLayoutSwizzle128);
                 ok = mbar_wait(q_full, 0, abort_flag, p.status, p.wait_limit_ns);
                 for (int i = 0; ok && i < tile_count; ++i) {
-                    const int j0 = mla_group_item(mla_k_group(i), tile_count);
+                    const int j0 = mla_group_item<FP8>(mla_k_group(i), tile_count);
                     const uint32_t d0 = tmem + C::TMEM_S0 + C::S_BUF * (i & 1);
                     for (int e = 0; ok && e < C::KITEMS; ++e) {
                         const int j = j0 + e, slot = j % C::NSLOT;
@@ -319,25 +403,42 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                         if (!ok) break;
                         tc_fence_after_sync();
                         const uint64_t a0 = k_desc0 + (uint64_t)((slot * C::SLOT_BYTES) >> 4);
-                        const int steps = e == C::KITEMS - 1 ? 4 : 8;
-                        for (int ks = 0; ks < steps; ++ks) {
-                            const int gk = 8 * e + ks;  // K-step over the 576 depth columns
-                            umma_f16_ss(d0 + C::S_ACC * (gk & 1),
-                                        a0 + (uint64_t)(((ks >> 2) * C::ATOM_BYTES + (ks & 3) * 32) >> 4),
-                                        q_desc0 + (uint64_t)(((gk >> 2) * C::Q_ATOM + (gk & 3) * 32) >> 4), id_s,
-                                        gk >= 2);
+                        if constexpr (!FP8) {
+                            const int steps = e == C::KITEMS - 1 ? 4 : 8;
+                            for (int ks = 0; ks < steps; ++ks) {
+                                const int gk = 8 * e + ks;  // K-step over the 576 depth columns
+                                umma_f16_ss(d0 + C::S_ACC * (gk & 1),
+                                            a0 + (uint64_t)(((ks >> 2) * C::ATOM_BYTES + (ks & 3) * 32) >> 4),
+                                            q_desc0 + (uint64_t)(((gk >> 2) * C::Q_ATOM + (gk & 3) * 32) >> 4),
+                                            id_s, gk >= 2);
+                            }
+                        } else if (e < C::KITEMS - 1) {
+                            // codes: eight K-steps of 32 against Q_hi (16 h) and Q_lo (l), accumulator 0
+                            for (int ks = 0; ks < 8; ++ks) {
+                                const int gk = 8 * e + ks;  // K-step over the 512 codes
+                                const uint64_t a = a0 + (uint64_t)(((ks >> 2) * C::ATOM_BYTES + (ks & 3) * 32) >> 4);
+                                const uint64_t qh = q_desc0 + (uint64_t)(((gk >> 2) * C::Q_ATOM + (gk & 3) * 32) >> 4);
+                                umma_f8_ss(d0, a, qh, id_s8, gk > 0);
+                                umma_f8_ss(d0, a, qh + (uint64_t)((4 * C::Q_ATOM) >> 4), id_s8, 1);
+                            }
+                        } else {
+                            // rope: four bf16 K-steps of 16, accumulator 1
+                            for (int ks = 0; ks < 4; ++ks)
+                                umma_f16_ss(d0 + C::S_ACC, a0 + (uint64_t)((ks * 32) >> 4),
+                                            q_desc0 + (uint64_t)((8 * C::Q_ATOM + ks * 32) >> 4), id_s, ks > 0);
                         }
                         umma_commit(slot_empty + 8 * slot);  // the item's slot is free once these complete
                         st_release_u32(s_next, (uint32_t)(e + 1 < C::KITEMS
                                                               ? j + 1
                                                               : (i + 1 < tile_count
-                                                                     ? mla_group_item(mla_k_group(i + 1), tile_count)
+                                                                     ? mla_group_item<FP8>(mla_k_group(i + 1), tile_count)
                                                                      : 0xffffffffu)));
                     }
                     if (ok) umma_commit(s_full + 8 * (i & 1));
                 }
             } else {
-                const uint32_t id_pv = umma_idesc_bf16_f32(128, C::ROWS, true, false);
+                const uint32_t id_pv = FP8 ? umma_idesc_e4m3_f32(128, C::ROWS, true, false)
+                                           : umma_idesc_bf16_f32(128, C::ROWS, true, false);
                 // A = V^T, MN-major: two 64-column atoms one atom apart (LBO), 8-key groups 1024 B apart (SBO)
                 const uint64_t v_desc0 = umma_smem_desc(sbase + C::OFF_RING, C::ATOM_BYTES, 1024, kLayoutSwizzle128);
                 // B = P^T, K-major: 64-key atoms of 64 heads x 128 B
@@ -346,7 +447,7 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                 tc_fence_after_sync();
                 tmem = *tmem_slot;
                 for (int t = 0; ok && t < tile_count; ++t) {
-                    const int j0 = mla_group_item(mla_v_group(t, tile_count), tile_count);
+                    const int j0 = mla_group_item<FP8>(mla_v_group(t, tile_count), tile_count);
                     ok = mbar_wait(p_full + 8 * (t & 1), (t >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
                     for (int e = 0; ok && e < C::VITEMS; ++e) {
                         const int j = j0 + e, slot = j % C::NSLOT;
@@ -359,18 +460,34 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                         tc_fence_after_sync();
                         const uint64_t a0 = v_desc0 + (uint64_t)((slot * C::SLOT_BYTES) >> 4);
                         const uint64_t b0 = p_desc0 + (uint64_t)(((t % C::P_BUFS) * C::P_BYTES) >> 4);
-                        const uint32_t d = tmem + C::TMEM_O0 + 64 * e;  // dv block e
+                        if constexpr (!FP8) {
+                            const uint32_t d = tmem + C::TMEM_O0 + 64 * e;  // dv block e
 #pragma unroll
-                        for (int ks = 0; ks < C::BN / 16; ++ks)
-                            umma_f16_ss(d, a0 + (uint64_t)((ks * 2048) >> 4),
-                                        b0 + (uint64_t)(((ks >> 2) * C::P_ATOM + (ks & 3) * 32) >> 4), id_pv,
-                                        t > 0 || ks > 0);
+                            for (int ks = 0; ks < C::BN / 16; ++ks)
+                                umma_f16_ss(d, a0 + (uint64_t)((ks * 2048) >> 4),
+                                            b0 + (uint64_t)(((ks >> 2) * C::P_ATOM + (ks & 3) * 32) >> 4), id_pv,
+                                            t > 0 || ks > 0);
+                        } else {
+                            // dv blocks 2e, 2e + 1 (one box each); four K-steps of 32 keys
+                            // (four 8-key groups of V^T) against P'_hi and P'_lo
+#pragma unroll
+                            for (int bb = 0; bb < 2; ++bb) {
+                                const uint32_t d = tmem + C::TMEM_O0 + 64 * (2 * e + bb);
+#pragma unroll
+                                for (int ks = 0; ks < 4; ++ks) {
+                                    const uint64_t a = a0 + (uint64_t)((bb * C::ATOM_BYTES + ks * 4096) >> 4);
+                                    const uint64_t ph = b0 + (uint64_t)((ks * 32) >> 4);
+                                    umma_f8_ss(d, a, ph, id_pv, t > 0 || ks > 0);
+                                    umma_f8_ss(d, a, ph + (uint64_t)(C::P_ATOM >> 4), id_pv, 1);
+                                }
+                            }
+                        }
                         umma_commit(slot_empty + 8 * slot);
                         st_release_u32(o_next,
                                        (uint32_t)(e + 1 < C::VITEMS
                                                       ? j + 1
                                                       : (t + 1 < tile_count
-                                                             ? mla_group_item(mla_v_group(t + 1, tile_count), tile_count)
+                                                             ? mla_group_item<FP8>(mla_v_group(t + 1, tile_count), tile_count)
                                                              : 0xffffffffu)));
                     }
                     if (ok) umma_commit(o_full + 8 * (t & 1));
@@ -395,7 +512,65 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
 
         // Q rows -> nine K-major 128-byte-swizzled atoms. Every load is issued
         // before the first store, so the 18 chunks of a thread arrive together.
-        {
+        if constexpr (FP8) {
+            // Four threads per head: codes [128 part, 128 part + 128) of the nope
+            // part (one 128-byte row of atom `part`) and rope chunks 2 part, 2 part
+            // + 1. The head is scaled by sigma_h, a power of two with max |q_nope|
+            // sigma_h <= 28, and split into 16 e4m3(x) (atoms 0-3) and
+            // e4m3(16 (x - e4m3(x))) (atoms 4-7); the rope stays bf16 (atom 8).
+            const int T = wt + 128 * wg, hh = T >> 2, part = T & 3;
+            const uint4* qg = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.num_q_heads + h0 + hh) * C::DK);
+            uint4 qv[16], qr[2];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) qv[k] = __ldg(qg + 16 * part + k);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) qr[k] = __ldg(qg + 64 + 2 * part + k);
+            float amax = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const uint32_t w4[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = bf16x2_to_float2(w4[e]);
+                    amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+                }
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const float sig = e4m3_split_scale(amax, 28.f);
+            uint8_t* qa = smem + C::OFF_Q + part * C::Q_ATOM + hh * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {  // 16 codes of chunks 2u, 2u + 1
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const uint32_t w4[4] = {qv[2 * u + c].x, qv[2 * u + c].y, qv[2 * u + c].z, qv[2 * u + c].w};
+                    uint32_t hp[4], lp[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = bf16x2_to_float2(w4[e]);
+                        float h0, l0, h1, l1;
+                        e4m3_split(f.x * sig, h0, l0);
+                        e4m3_split(f.y * sig, h1, l1);
+                        hp[e] = e4m3x2(h0, h1);
+                        lp[e] = e4m3x2(l0, l1);
+                    }
+                    hw[2 * c] = hp[0] | (hp[1] << 16);
+                    hw[2 * c + 1] = hp[2] | (hp[3] << 16);
+                    lw[2 * c] = lp[0] | (lp[1] << 16);
+                    lw[2 * c + 1] = lp[2] | (lp[3] << 16);
+                }
+                const int off = (u ^ (hh & 7)) << 4;
+                *reinterpret_cast<uint4*>(qa + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(qa + 4 * C::Q_ATOM + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int c = 2 * part + k;
+                *reinterpret_cast<uint4*>(smem + C::OFF_Q + 8 * C::Q_ATOM + hh * 128 + ((c ^ (hh & 7)) << 4)) = qr[k];
+            }
+            if (part == 0) reinterpret_cast<float*>(smem + C::OFF_QINV)[hh] = 0.0625f / sig;
+        } else {
             constexpr int kChunks = C::ROWS * (C::DK / 8) / 256;  // 16-byte chunks per thread
             static_assert(kChunks * 256 == C::ROWS * (C::DK / 8), "Q chunks split evenly");
             uint4 qv[kChunks];
@@ -413,6 +588,7 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(q_full);
+        if (FP8) named_barrier_sync(3, 256);  // every head's 1 / (16 sigma_h) is written
         mbar_wait(tmem_ready, 0, abort_flag, p.status, p.wait_limit_ns);
         tc_fence_after_sync();
         tmem = *tmem_slot;
@@ -425,6 +601,11 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
         const uint32_t col_wg = 32 * wg;  // this warpgroup's columns in every S^T / O^T accumulator
         float* red_w = red_s + wg * 4 * 32;
         bool seen_abort = false;
+        // FP8: Sigma, the power of two that bounds every K scale this warpgroup
+        // has folded into P (0 before the first); O^T holds 16 / Sigma times the
+        // scaled partial.
+        float sig_run = 0.f;
+        float* sig_w = reinterpret_cast<float*>(smem + C::OFF_SIG) + 4 * wg;
         for (int i = 0; i < tile_count; ++i) {
             mbar_wait(s_full + 8 * (i & 1), (i >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
             if (i == 0 && wt == 0 && wg == 0) {
@@ -433,15 +614,42 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
             }
             tc_fence_after_sync();
             float s[32];
-            tmem_ld2_sum_x32(tmem + lane_addr + C::TMEM_S0 + C::S_BUF * (i & 1) + col_wg, C::S_ACC, s);
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_empty + 8 * (i & 1));
+            float ksc = 1.f;  // FP8: this key's K scale (0 past the sequence)
+            if constexpr (!FP8) {
+                tmem_ld2_sum_x32(tmem + lane_addr + C::TMEM_S0 + C::S_BUF * (i & 1) + col_wg, C::S_ACC, s);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_empty + 8 * (i & 1));
+            } else {
+                float sr[32];
+                tmem_ld2_x32(tmem + lane_addr + C::TMEM_S0 + C::S_BUF * (i & 1) + col_wg, C::S_ACC, s, sr);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_empty + 8 * (i & 1));
+                if (scaled) {
+                    const int kse = i % C::KS;
+                    mbar_wait(ks_full + 8 * kse, (i / C::KS) & 1, abort_flag, p.status, p.wait_limit_ns);
+                    ksc = reinterpret_cast<const float*>(smem + C::OFF_KS)[kse * C::BN + my_lane];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ks_empty + 8 * kse);
+                }
+                // raw score: codes / (16 sigma_h) times the key's K scale, plus the rope part
+                const float4* qinv = reinterpret_cast<const float4*>(smem + C::OFF_QINV) + (col_wg >> 2);
+#pragma unroll
+                for (int r4 = 0; r4 < 8; ++r4) {
+                    const float4 qm = qinv[r4];
+                    s[4 * r4 + 0] = fmaf(s[4 * r4 + 0], qm.x * ksc, sr[4 * r4 + 0]);
+                    s[4 * r4 + 1] = fmaf(s[4 * r4 + 1], qm.y * ksc, sr[4 * r4 + 1]);
+                    s[4 * r4 + 2] = fmaf(s[4 * r4 + 2], qm.z * ksc, sr[4 * r4 + 2]);
+                    s[4 * r4 + 3] = fmaf(s[4 * r4 + 3], qm.w * ksc, sr[4 * r4 + 3]);
+                }
+            }
 
             const int key = (tile_begin + i) * C::BN + my_lane;
             if (key >= L) {
 #pragma unroll
                 for (int r = 0; r < 32; ++r) s[r] = -INFINITY;
+                ksc = 0.f;
             }
             // Without short-circuit branches (one per head otherwise): a finite
             // score over an empty row, or one more than the threshold above the
@@ -450,8 +658,15 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
                 const bool first = (m_run[r] == -INFINITY) & (s[r] != -INFINITY);
-                const bool over = (s[r] - m_run[r]) * c2 > 8.0f;
+                const bool over = (s[r] - m_run[r]) * c2 > C::RESCALE;
                 need = need | first | over;
+            }
+            if constexpr (FP8) {
+                // a K scale above the bound, or a warp whose keys' scales all lie
+                // more than 16x below it (the bound then follows them down, so
+                // that P' keeps its precision)
+                const bool low = __all_sync(0xffffffffu, ksc < sig_run * 0.0625f) && __any_sync(0xffffffffu, ksc > 0.f);
+                need = need | (ksc > sig_run) | low;
             }
             seen_abort |= (*abort_flag != 0);
             if (named_barrier_or(wg_bar, 128, need || seen_abort)) {
@@ -475,20 +690,45 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                     }
                     red_w[quad * 32 + row] = v[0];
                 }
+                if constexpr (FP8) {
+                    float km = ksc;
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, o));
+                    if (lane == 0) sig_w[quad] = km;
+                }
                 seen_abort |= (*abort_flag != 0);
                 if (named_barrier_or(wg_bar, 128, seen_abort)) break;
                 bool moved = false;
+                // FP8: a K scale above Sigma, or a tile whose largest scale km lies
+                // more than 16x below it, sets Sigma to the power of two above km,
+                // and O^T, which holds 16 / Sigma times its partial, is corrected by
+                // Sigma_old / Sigma_new (nothing to correct before the first).
+                float sig_ratio = 1.f;
+                if constexpr (FP8) {
+                    const float km = fmaxf(fmaxf(sig_w[0], sig_w[1]), fmaxf(sig_w[2], sig_w[3]));
+                    if (km > sig_run || (km > 0.f && km < sig_run * 0.0625f)) {
+                        int ex = 0;
+                        frexpf(km, &ex);
+                        const float sig_new = ldexpf(1.f, ex);
+                        if (sig_run > 0.f) {
+                            sig_ratio = sig_run / sig_new;
+                            moved = true;
+                        }
+                        sig_run = sig_new;
+                    }
+                }
                 float alpha[32];
 #pragma unroll
                 for (int r = 0; r < 32; ++r) {
                     const float tmax = fmaxf(fmaxf(red_w[r], red_w[32 + r]), fmaxf(red_w[64 + r], red_w[96 + r]));
                     const bool move = (m_run[r] == -INFINITY) ? (tmax != -INFINITY)
-                                                              : ((tmax - m_run[r]) * c2 > 8.0f);
-                    alpha[r] = 1.f;
+                                                              : ((tmax - m_run[r]) * c2 > C::RESCALE);
+                    alpha[r] = sig_ratio;  // O^T's correction: the max's and (FP8) Sigma's
                     if (move) {
-                        alpha[r] = (m_run[r] == -INFINITY) ? 0.f : ex2_approx((m_run[r] - tmax) * c2);
+                        const float a_m = (m_run[r] == -INFINITY) ? 0.f : ex2_approx((m_run[r] - tmax) * c2);
                         m_run[r] = tmax;
-                        l_part[r] *= alpha[r];
+                        l_part[r] *= a_m;
+                        alpha[r] = a_m * sig_ratio;
                         moved = true;  // uniform: every thread sees the same maxima
                     }
                 }
@@ -526,7 +766,7 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                 const int tp = i - C::P_BUFS;
                 mbar_wait(o_full + 8 * (tp & 1), (tp >> 1) & 1, abort_flag, p.status, p.wait_limit_ns);
             }
-            {
+            if constexpr (!FP8) {
                 uint8_t* pb = smem + C::OFF_P + (i % C::P_BUFS) * C::P_BYTES + (my_lane >> 6) * C::P_ATOM;
                 const int kk = my_lane & 63;
 #pragma unroll
@@ -534,6 +774,24 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                     const int hr = col_wg + r;  // head row of P^T
                     *reinterpret_cast<__nv_bfloat16*>(pb + hr * 128 + (((kk >> 3) ^ (hr & 7)) << 4) + (kk & 7) * 2) =
                         __float2bfloat16_rn(s[r]);
+                }
+            } else {
+                // 16 P' = 16 P k_scale / Sigma <= 256 as two E4M3 codes (h + l): P'_hi
+                // in one atom [64 heads][128 keys], P'_lo in the next.
+                uint8_t* pb = smem + C::OFF_P + (i % C::P_BUFS) * C::P_BYTES;
+                const float f = sig_run > 0.f ? 16.f * ksc / sig_run : 0.f;
+                const int kb = my_lane >> 4, kw = my_lane & 15;
+#pragma unroll
+                for (int r = 0; r < 32; r += 2) {
+                    uint32_t hi, lo;
+                    e4m3_split2(s[r] * f, s[r + 1] * f, hi, lo);
+                    const int h0r = col_wg + r, h1r = h0r + 1;
+                    const int o0 = h0r * 128 + ((kb ^ (h0r & 7)) << 4) + kw;
+                    const int o1 = h1r * 128 + ((kb ^ (h1r & 7)) << 4) + kw;
+                    pb[o0] = (uint8_t)(hi & 0xffu);
+                    pb[o1] = (uint8_t)((hi >> 8) & 0xffu);
+                    pb[C::P_ATOM + o0] = (uint8_t)(lo & 0xffu);
+                    pb[C::P_ATOM + o1] = (uint8_t)((lo >> 8) & 0xffu);
                 }
             }
             fence_proxy_async_smem();
@@ -548,7 +806,7 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
         // before has been consumed (both MMA warps' published progress).
         if (v_tail && !seen_abort) {
             const int t = tile_count - 1;
-            const int j0 = mla_group_item(mla_v_group(t, tile_count), tile_count);
+            const int j0 = mla_group_item<FP8>(mla_v_group(t, tile_count), tile_count);
             const bool past = (tile_begin + t) * C::BN + my_lane >= L;
             for (int e = 0; e < C::VITEMS; ++e) {
                 const int j = j0 + e, slot = j % C::NSLOT;
@@ -620,6 +878,7 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
         // consecutive columns over every bank.
         const int BW = p.band_cols, OC = p.out_chunk_cols;
         const uint32_t recv_o = sbase + C::OFF_RECV, recv_ms = sbase + C::OFF_RECV_MS;
+        const float o_unit = sig_run * 0.0625f;  // FP8: O^T holds 16 / Sigma times the partial
         if (P > 1) {
             cluster_wait();  // every rank's barriers are initialised
             if (wt == 0 && wg == 0 && !*abort_flag) {
@@ -651,6 +910,10 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
                 if (tile_count == 0) {  // no product was issued: the accumulator holds nothing of ours
 #pragma unroll
                     for (int r = 0; r < 32; ++r) o[r] = 0.f;
+                }
+                if constexpr (FP8) {
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) o[r] *= o_unit;
                 }
                 const int c = dv - q * BW, src = rank < q ? rank : rank - 1;
                 const uint32_t dst = map_shared_rank(recv_o + 4u * (uint32_t)((src * BW + c) * C::ROWS), q);
@@ -713,6 +976,10 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
 #pragma unroll
                 for (int r = 0; r < 32; ++r) o[r] = 0.f;
             }
+            if constexpr (FP8) {
+#pragma unroll
+                for (int r = 0; r < 32; ++r) o[r] *= o_unit;
+            }
             const float* w_own = wtab + rank * C::ROWS + col_wg;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -762,6 +1029,8 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
         volatile int keep_waiting = 0;
         for (int j = issued > C::NSLOT ? issued - C::NSLOT : 0; j < issued; ++j)
             mbar_wait(slot_full + 8 * (j % C::NSLOT), (j / C::NSLOT) & 1, &keep_waiting, p.status, p.wait_limit_ns);
+        for (int t = ks_issued > C::KS ? ks_issued - C::KS : 0; t < ks_issued; ++t)
+            mbar_wait(ks_full + 8 * (t % C::KS), (t / C::KS) & 1, &keep_waiting, p.status, p.wait_limit_ns);
     }
     if (P > 1 && warp < C::WG0) cluster_wait();  // pairs with the early arrive
     __syncwarp();
@@ -769,17 +1038,34 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1) mla_tc_decode_kernel(const
     if (tid == 0) stamp(3);
 }
 
+template <bool FP8>
+static void mla_fill_geometry(KernelGeometry* g, const char* name)
+{
+    using C = MlaCfgT<FP8>;
+    g->func = reinterpret_cast<const void*>(&mla_tc_decode_kernel<FP8>);
+    g->threads = C::THREADS;
+    g->keys_per_tile = C::BN;
+    g->stages = C::NSLOT;
+    g->rows_capacity = C::ROWS;
+    g->smem_bytes = C::SMEM_BYTES;
+    g->name = name;
+}
+
 bool mla_tc_geometry(int qk, int ov, int nope, int heads_per_kv, int num_q, KernelGeometry* g)
 {
-    if (qk != MlaCfg::DK || ov != MlaCfg::DV || nope != MlaCfg::DV || num_q != 1 || heads_per_kv % MlaCfg::ROWS)
+    using C = MlaCfgT<false>;
+    if (qk != C::DK || ov != C::DV || nope != C::DV || num_q != 1 || heads_per_kv % C::ROWS) return false;
+    mla_fill_geometry<false>(g, "mla_tc_d576_v512_bn128_n64_slots4");
+    return true;
+}
+
+bool mla_tc_fp8_geometry(int qk, int ov, int nope, int rope, int heads_per_kv, int num_q, KernelGeometry* g)
+{
+    using C = MlaCfgT<true>;
+    if (qk != C::DK || ov != C::DV || nope != C::DV || rope != C::DK - C::DV || num_q != 1 ||
+        heads_per_kv % C::ROWS)
         return false;
-    g->func = reinterpret_cast<const void*>(&mla_tc_decode_kernel);
-    g->threads = MlaCfg::THREADS;
-    g->keys_per_tile = MlaCfg::BN;
-    g->stages = MlaCfg::NSLOT;
-    g->rows_capacity = MlaCfg::ROWS;
-    g->smem_bytes = MlaCfg::SMEM_BYTES;
-    g->name = "mla_tc_d576_v512_bn128_n64_slots4";
+    mla_fill_geometry<true>(g, "mla_tc_e4m3_d576_r64_v512_bn128_n64_slots4");
     return true;
 }
 

@@ -173,36 +173,59 @@ def test_running_max_moves_every_tile(case, kw, path):
 # --- the MLA latent layout over an E4M3 cache with a bf16 rope cache ---------
 # K_j = [k_scale_j * e4m3(k8_j[0:512]), bf16 rope_j[0:64]] and V_j =
 # k_scale_j * e4m3(k8_j[0:512]): the FA4Config page's separate rope dtype and
-# per-token K scale (SIMT kernel, 16 heads per CTA).
+# per-token K scale. A multiple of 64 heads per kv head takes the tcgen05 MLA
+# kernel (64 heads per CTA), fewer the FMA kernel (16 heads per CTA).
 
 def mla_wl(**kw):
-    base = dict(name="fp8_mla", batch=3, num_q=1, num_q_heads=32, num_kv_heads=1, qk_depth=576, nope_depth=512,
+    base = dict(name="fp8_mla", batch=3, num_q=1, num_q_heads=64, num_kv_heads=1, qk_depth=576, nope_depth=512,
                 ov_depth=512, page_size=64, splitk=2, seq_len_lo=1, seq_len_hi=700, latent=True,
                 scale=1.0 / 24.0, seed=1100, kv_dtype="e4m3", k_scale=True, rope_depth=64)
     base.update(kw)
     return DecodeWorkload(**base)
 
 
+def expect_kernel(call, heads_per_kv, path="auto"):
+    """The description names the default kernel; a forced FMA run needs its latent kernel."""
+    d = call.describe()
+    if path == "simt":
+        assert "latent_kernel=simt_e4m3" in d, d
+    else:
+        assert ("kernel=mla_tc_e4m3" in d) == (heads_per_kv % 64 == 0), d
+
+
+@pytest.mark.parametrize("heads", [32, 64, 128])
 @pytest.mark.parametrize("scaled", [True, False])
 @pytest.mark.parametrize("P", [1, 2, 4, 16])
-def test_mla_latent_rope_splits(P, scaled):
-    w = mla_wl(splitk=P, k_scale=scaled, seed=1100 + P)
-    run_and_check(w, seq_lens=[1, 333, 700], what=f"fp8 mla P{P} scale {scaled}")
+def test_mla_latent_rope_splits(P, scaled, heads):
+    w = mla_wl(splitk=P, k_scale=scaled, num_q_heads=heads, seed=1100 + P + heads)
+    inp = generate(w, seq_lens=[1, 333, 700])
+    with DeviceCall(inp) as call:
+        expect_kernel(call, heads)
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what=f"fp8 mla P{P} scale {scaled} heads {heads}")
 
 
+@pytest.mark.parametrize("path", ["auto", "simt"])
 @pytest.mark.parametrize("ps", [8, 32, 128])
-def test_mla_latent_rope_page_sizes(ps):
-    run_and_check(mla_wl(page_size=ps, splitk=4, seed=1120 + ps), seq_lens=[65, 1000, 257],
-                  what=f"fp8 mla ps{ps}")
+def test_mla_latent_rope_page_sizes(ps, path):
+    inp = generate(mla_wl(page_size=ps, splitk=4, seed=1120 + ps), seq_lens=[65, 1000, 257])
+    with DeviceCall(inp, path=path) as call:
+        expect_kernel(call, 64, path)
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what=f"fp8 mla ps{ps} {path}")
 
 
-def test_mla_latent_rope_per_sequence_split_and_short():
-    w = mla_wl(batch=8, num_q_heads=16, splitk=0, seed=1130)
-    run_and_check(w, seq_lens=[0, 1, 31, 32, 33, 1100, 4097, 9000], what="fp8 mla auto split")
+@pytest.mark.parametrize("heads", [16, 64])
+def test_mla_latent_rope_per_sequence_split_and_short(heads):
+    w = mla_wl(batch=8, num_q_heads=heads, splitk=0, seed=1130 + heads)
+    run_and_check(w, seq_lens=[0, 1, 31, 32, 33, 1100, 4097, 9000], what=f"fp8 mla auto split heads {heads}")
 
 
-def test_mla_latent_rope_nonfinite_tails_do_not_leak():
-    w = mla_wl(batch=3, splitk=2, seed=1140)
+@pytest.mark.parametrize("heads", [32, 64])
+def test_mla_latent_rope_nonfinite_tails_do_not_leak(heads):
+    w = mla_wl(batch=3, splitk=2, num_q_heads=heads, seed=1140 + heads)
     lens = [70, 200, 129]
     inp = generate(w, seq_lens=lens)
     for b, L in enumerate(lens):
@@ -213,13 +236,55 @@ def test_mla_latent_rope_nonfinite_tails_do_not_leak():
     with DeviceCall(inp) as call:
         call.run()
         assert call.status() == 0
-        check_against_oracle(call, what="fp8 mla non-finite tails")
+        check_against_oracle(call, what=f"fp8 mla non-finite tails heads {heads}")
 
 
-def test_mla_latent_rope_full_size():
+@pytest.mark.parametrize("P", [1, 4])
+def test_mla_latent_rope_scale_bound_moves(P):
+    """K scales that change along the sequence (x2 every 128 keys, up to x32,
+    then back to x1) with the codes divided by the same factor, so the keys
+    keep their magnitudes: the tcgen05 kernel moves its bound on the scales
+    folded into P up and down mid-sequence and corrects O, against the oracle."""
+    w = mla_wl(batch=2, splitk=P, seed=1160 + P)
+    lens = [1500, 2300]
+    inp = generate(w, seq_lens=lens)
+    ps = w.page_size
+    for b, L in enumerate(lens):
+        for key in range(L):
+            page, row = int(inp.page_table[b, key // ps]), key % ps
+            f = float(2 ** ((key // 128) % 6))
+            inp.k_scale[page, :, row] *= f
+            codes = inp.k_pages[page, :, row, :].view(torch.float8_e4m3fn).float() / f
+            inp.k_pages[page, :, row, :] = codes.to(torch.float8_e4m3fn).view(torch.uint8)
+    with DeviceCall(inp) as call:
+        expect_kernel(call, 64)
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what=f"fp8 mla changing scales P{P}")
+
+
+@pytest.mark.parametrize("P", [2, 4])
+def test_mla_latent_rope_running_max_moves_every_tile(P):
+    """Scores rising along the keys: the rescale path (threshold 2^4 for the
+    E4M3 P split) on most tiles."""
+    inp = ramp_keys(generate(mla_wl(batch=2, splitk=P, seed=1170 + P), seq_lens=[1800, 2600]))
+    with DeviceCall(inp) as call:
+        expect_kernel(call, 64)
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what=f"fp8 mla ramp P{P}")
+
+
+@pytest.mark.parametrize("path", ["auto", "simt"])
+def test_mla_latent_rope_full_size(path):
     """The mla workload (32 seqs x 128 heads, L8192, split 2) over the E4M3 latent cache."""
     w = WORKLOADS["mla"].with_(kv_dtype="e4m3", k_scale=True, rope_depth=64)
-    run_and_check(w, what="mla e4m3")
+    inp = generate(w)
+    with DeviceCall(inp, path=path) as call:
+        expect_kernel(call, 128, path)
+        call.run()
+        assert call.status() == 0
+        check_against_oracle(call, what=f"mla e4m3 {path}")
 
 
 def test_mla_latent_rope_argument_checks():
