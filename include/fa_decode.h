@@ -151,9 +151,10 @@ int fa_decode_run(fa_decode_t h, const void* q, const void* k_pages, const void*
  * Built for E4M3: qk_depth == ov_depth == 128 with a separate V cache,
  * rope_depth 0, T * g <= 16 rows per CTA (the tcgen05 GQA kernel, every
  * split); and the MLA latent layout qk_depth 576 (512 codes + rope_depth
- * 64), ov_depth 512, with T * g == 16 or num_q == 1 and g a multiple of 16
- * (the FMA kernel, 16 heads per CTA, every split). Other E4M3 shapes return
- * FA_ERR_UNSUPPORTED. Allocates as fa_decode_create does.
+ * 64), nope_depth 512, ov_depth 512: num_q == 1 with g a multiple of 64 (the
+ * MLA tcgen05 kernel, 64 heads per CTA), or T * g == 16 or num_q == 1 with g
+ * a multiple of 16 (the FMA kernel, 16 heads per CTA), every split. Other
+ * E4M3 shapes return FA_ERR_UNSUPPORTED. Allocates as fa_decode_create does.
  */
 int fa_decode_create_kv(fa_decode_t* out, int num_q_heads, int num_kv_heads, int qk_depth, int nope_depth,
                         int ov_depth, int page_size, int num_q, int splitk, int kv_format, int rope_depth);
