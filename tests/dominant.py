@@ -78,7 +78,9 @@ def choose_positions(w, lens, splitk_of=None, salt: int = 0) -> dict:
 def plant(inp, positions: dict, alpha: float = 64.0):
     """Modify `inp` in place (q and the K cache) so that each chosen key dominates.
     An E4M3 cache gets the code of 448 in the dominant columns and, with
-    per-token scales, the scale 0.25 (key value 112) for the chosen row."""
+    per-token scales, the scale 0.25 (key value 112) for the chosen row; an
+    E4M3 latent cache with a bf16 rope cache gets `alpha` in the chosen row's
+    rope values (the dominant columns) and the scale 0.25."""
     w = inp.workload
     cols = dom_cols(w)
     q = inp.q.float()
@@ -87,7 +89,12 @@ def plant(inp, positions: dict, alpha: float = 64.0):
     ps = w.page_size
     for (b, k), j in positions.items():
         page = int(inp.page_table[b, j // ps])
-        if w.kv_dtype == "e4m3":
+        if w.kv_dtype == "e4m3" and inp.k_rope is not None:
+            # latent E4M3 cache: the dominant columns are the bf16 rope part
+            inp.k_rope[page, k, j % ps, :] = alpha
+            if inp.k_scale is not None:
+                inp.k_scale[page, k, j % ps] = 0.25
+        elif w.kv_dtype == "e4m3":
             inp.k_pages[page, k, j % ps, cols] = 0x7E
             if inp.k_scale is not None:
                 inp.k_scale[page, k, j % ps] = 0.25
@@ -101,10 +108,19 @@ def _e4m3(codes: torch.Tensor, dtype) -> torch.Tensor:
 
 
 def value_row(inp, b: int, k: int, j: int) -> torch.Tensor:
-    """V_j as bf16 (an E4M3 value row widened exactly)."""
+    """V_j as bf16 (an E4M3 value row widened exactly; in the latent layout
+    the K scale times the row's first ov_depth codes, exact for the planted
+    scale 0.25)."""
     w = inp.workload
     ps = w.page_size
     page = int(inp.page_table[b, j // ps])
+    if w.kv_dtype == "e4m3" and inp.v_pages is None:
+        v = _e4m3(inp.k_pages[page, k, j % ps, :w.ov_depth], torch.float64)
+        if inp.k_scale is not None:
+            v = v * float(inp.k_scale[page, k, j % ps])
+        vb = v.to(torch.bfloat16)
+        assert bool((vb.double() == v).all()), "planted V row is not exact in bf16"
+        return vb
     if w.kv_dtype == "e4m3":
         return _e4m3(inp.v_pages[page, k, j % ps, :], torch.bfloat16)
     if inp.v_pages is None:
@@ -121,6 +137,8 @@ def _gather_keys(inp, b: int, k: int, L: int) -> torch.Tensor:
         kk = _e4m3(inp.k_pages[pages, k, j % ps, :], torch.float64)
         if inp.k_scale is not None:
             kk = kk * inp.k_scale[pages, k, j % ps].double().unsqueeze(1)
+        if inp.k_rope is not None:
+            kk = torch.cat([kk, inp.k_rope[pages, k, j % ps, :].double()], dim=1)
         return kk
     return inp.k_pages[pages, k, j % ps, :].double()
 

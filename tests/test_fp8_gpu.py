@@ -287,6 +287,26 @@ def test_mla_latent_rope_full_size(path):
         check_against_oracle(call, what=f"mla e4m3 {path}")
 
 
+@pytest.mark.parametrize("heads,P,ps,path", [(64, 1, 64, "auto"), (64, 2, 16, "auto"), (128, 4, 128, "auto"),
+                                         (64, 16, 64, "auto"), (64, 4, 32, "simt"), (32, 2, 64, "auto")])
+def test_mla_latent_rope_gather_bit_exact(heads, P, ps, path):
+    """Dominant keys (the bf16 rope part of the chosen row, K scale 0.25):
+    every output row that sees its key equals 0.25 * codes[:512] of that row
+    bit for bit, on the tcgen05 E4M3 mode and on the FMA kernel."""
+    w = mla_wl(batch=6, splitk=P, page_size=ps, num_q_heads=heads, seed=1180 + P + ps + heads)
+    inp = generate(w, seq_lens=[1, 130, 700, 2000, 129, 4097])
+    pos = dominant.choose_positions(w, inp.seq_lens.tolist(), salt=P + ps)
+    dominant.plant(inp, pos)
+    dominant.check_margin(inp, pos)
+    with DeviceCall(inp, path=path) as call:
+        expect_kernel(call, heads, path)
+        call.run()
+        assert call.status() == 0
+        n = dominant.check_bit_exact(call.out, inp, pos, what=f"fp8 mla gather heads {heads} P{P} ps{ps} {path}")
+        assert n > 0
+        check_against_oracle(call, what=f"fp8 mla gather heads {heads} P{P} ps{ps} {path} oracle")
+
+
 def test_mla_latent_rope_argument_checks():
     inp = generate(mla_wl(seed=1150))
     with DeviceCall(inp) as call:
