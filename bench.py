@@ -27,6 +27,7 @@ import ctypes
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -104,28 +105,59 @@ def _code_only(text: str) -> str:
     return " ".join("".join(out).split())
 
 
-def kernel_source_hash() -> str:
-    """Hash of the device code (the host planner's files are excluded; comments
-    and whitespace do not count, so an edit of comments keeps the stored ncu
-    traffic of the same code)."""
+# Translation units of each kernel family (by the kernel's name in an ncu capture).
+KERNEL_UNITS = (("mla_tc_decode_kernel", ("kernel_mla_tc.cu",)),
+                ("simt_decode_kernel", ("kernel_simt.cu",)),
+                ("tc_decode_kernel", ("kernel_tc.cu", "kernel_tc_fp8.cu")))
+
+
+def kernel_units(kernel_name: str):
+    for key, units in KERNEL_UNITS:
+        if key in kernel_name:
+            return units
+    return None
+
+
+def kernel_source_files(units) -> dict:
+    """The sources a kernel family is built from: its translation units and
+    every local header they include, transitively (name -> text)."""
+    dirs = [os.path.join(ROOT, "split_paged_decode_gb300", "csrc"), os.path.join(ROOT, "include")]
+    seen, stack = {}, list(units)
+    while stack:
+        name = stack.pop()
+        if name in seen:
+            continue
+        path = next((os.path.join(d, name) for d in dirs if os.path.isfile(os.path.join(d, name))), None)
+        if path is None:
+            continue
+        text = open(path, encoding="utf-8").read()
+        seen[name] = text
+        stack += re.findall(r'^\s*#\s*include\s+"([^"]+)"', text, flags=re.M)
+    return seen
+
+
+def kernel_source_hash(units) -> str:
+    """Hash of a kernel family's sources (comments and whitespace do not
+    count, so an edit of comments keeps the stored ncu traffic of the same
+    code)."""
+    seen = kernel_source_files(units)
     h = hashlib.sha256()
-    d = os.path.join(ROOT, "split_paged_decode_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")) and f not in ("fa_decode_host.cu", "stream_k_plan.h"):
-            h.update(f.encode())
-            h.update(_code_only(open(os.path.join(d, f), encoding="utf-8").read()).encode())
+    for name in sorted(seen):
+        h.update(name.encode())
+        h.update(_code_only(seen[name]).encode())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current sources of its kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             doc = json.load(f)
         ent = doc[workload]
-        if ent.get("kernel_source_hash") != kernel_source_hash():
+        units = kernel_units(ent["kernel"])
+        if units is None or ent.get("kernel_source_hash") != kernel_source_hash(units):
             return None
         return float(ent["bytes_per_launch"])
     except Exception:
