@@ -264,8 +264,8 @@ int fa_decode_describe(fa_decode_t h, char* buf, int size);
  *                bits in *status_out and returns FA_ERR_DEVICE if any is set.
  *
  * The first call on each device looks up the array's device address there
- * (cudaGetSymbolAddress); make that first call before any stream capture.
- * The call itself makes no device allocation and frees nothing.
+ * (cudaGetSymbolAddress). The call makes no device allocation and frees
+ * nothing.
  *
  * Schedule: this call has no handle, hence no stream-K scratch and no side
  * streams. A fixed split therefore never takes the stream-K partition (each
