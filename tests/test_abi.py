@@ -127,3 +127,43 @@ def test_trace_hook_rejects_null_handle(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(FileNotFoundError):
         spd.load_library(str(tmp_path / "libfa_decode.so"))
+
+
+def _create_kv(lib, *args):
+    h = ctypes.c_void_p()
+    rc = lib.fa_decode_create_kv(ctypes.byref(h), *args)
+    return rc, h
+
+
+@pytest.mark.parametrize("args, code", [
+    ((32, 8, 128, -1, 128, 128, 1, 4, 2, 0), "FA_ERR_INVALID_ARG"),                  # unknown cache format
+    ((32, 8, 128, -1, 128, 128, 1, 4, spd.FA_KV_BF16, 16), "FA_ERR_INVALID_ARG"),    # rope apart on a bf16 cache
+    ((32, 8, 128, -1, 128, 128, 1, 4, spd.FA_KV_E4M3, 128), "FA_ERR_INVALID_ARG"),   # rope as wide as the row
+    ((32, 8, 64, -1, 64, 64, 1, 2, spd.FA_KV_E4M3, 0), "FA_ERR_UNSUPPORTED"),        # E4M3 head dim 64
+    ((128, 1, 576, 512, 512, 64, 1, 2, spd.FA_KV_E4M3, 32), "FA_ERR_UNSUPPORTED"),   # latent rope of 32
+    ((8, 1, 576, 512, 512, 64, 1, 2, spd.FA_KV_E4M3, 64), "FA_ERR_UNSUPPORTED"),     # 8 heads: neither MLA kernel
+])
+def test_create_kv_rejects_on_the_host(lib, args, code):
+    """Cache-format arguments and E4M3 shapes without a kernel are refused
+    before any device query."""
+    rc, h = _create_kv(lib, *args)
+    assert rc == getattr(spd, code), lib.fa_decode_last_error()
+    assert not h.value
+
+
+@pytest.mark.parametrize("args", [
+    (32, 8, 128, -1, 128, 128, 1, 4, spd.FA_KV_E4M3, 0),      # the GQA tcgen05 kernel
+    (128, 1, 576, 512, 512, 64, 1, 2, spd.FA_KV_E4M3, 64),    # the MLA tcgen05 kernel, E4M3 mode
+    (32, 1, 576, 512, 512, 64, 1, 2, spd.FA_KV_E4M3, 64),     # the FMA kernel, E4M3 latent mode
+])
+def test_create_kv_planned_shapes_reach_the_device_query(lib, args):
+    """Shapes with an E4M3 kernel pass the host checks; without a GB300 the
+    plan then fails at the device query."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc, h = _create_kv(lib, *args)
+    assert rc in (spd.FA_ERR_CUDA, spd.FA_ERR_UNSUPPORTED)
+    assert "compute capability" in lib.fa_decode_last_error().decode() or rc == spd.FA_ERR_CUDA
+    assert not h.value
