@@ -170,8 +170,8 @@ int fa_decode_create_kv(fa_decode_t* out, int num_q_heads, int num_kv_heads, int
  *                      16-byte aligned: given exactly when rope_depth > 0
  *                      (FA_ERR_INVALID_ARG otherwise)
  *   k_scale            fp32 [num_pages][num_kv_heads][page_size] per-token K
- *                      scales, 16-byte aligned, or NULL for unit scales; NULL
- *                      for a bf16 cache
+ *                      scales (finite, >= 0: magnitudes), 16-byte aligned, or
+ *                      NULL for unit scales; NULL for a bf16 cache
  * fa_decode_run on an E4M3 handle returns FA_ERR_INVALID_ARG. Rows past L_b
  * and unused pages may hold any codes and scales; they are never used.
  */
