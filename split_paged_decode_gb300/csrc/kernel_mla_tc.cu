@@ -44,10 +44,11 @@
 // accumulator, the rope part a kind::f16 product into the other:
 //   S = acc_codes / (16 sigma_h) * k_scale_j + acc_rope.
 // O^T += V^T P'^T takes the codes as they are and P' = P k_scale_j / Sigma as
-// two E4M3 operands (16 P' = h + l), where Sigma is a power of two that bounds
-// every K scale seen so far (raised, with O corrected like a moved max, when
-// a tile brings a larger scale), so P' <= P and the O partial is
-// acc Sigma / 16. The ring items carry twice the columns of a bf16 item: K as
+// two E4M3 operands (16 P' = h + l), where Sigma is a power of two above
+// every K scale of the current tile (raised when a tile brings a larger
+// scale, lowered when a tile's scales all lie 16x below it, with O corrected
+// like a moved max; the scales are non-negative), so P' <= P and the O partial
+// is acc Sigma / 16. The ring items carry twice the columns of a bf16 item: K as
 // two 256-code items plus the rope item, V as two items; the per-token
 // scales come in a ring of their own.
 #include "fa_decode_internal.h"
